@@ -1,0 +1,439 @@
+"""KDA prefill / decode benchmark on GB300.
+
+One step = one kda_chunk_fwd over the prefill workload B=4, H=16, T=8192,
+dk=dv=128, chunk=64, with the final state and every chunk-boundary snapshot
+written (inputs larger than L2).  The decode step (512 x 32 resident states,
+dk=dv=128, 1000 chained steps) is measured in the same run and reported as
+its own object.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+build) on the host cores, on a bounded sample of the same workload.
+Under torchrun each rank runs its own replica (weak scaling, no collective
+on the data path); timing is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s and decode steps/s on 1 GB300; % of TC / HBM roofline"
+UNIT = "tokens/s"
+WORKLOAD = "mid"
+
+# Algorithmic traffic and work per token-head at chunk 64 (bf16 in/out, fp32 states):
+#   q, k, z (dk each), v, o (dv each) in bf16 plus beta: 2 (3 dk + 2 dv) + 2 bytes;
+#   chunk-boundary snapshots: 4 dk dv / 64 bytes;
+#   flops: 6 dk dv + 64 (3 dk + 2 dv) + 64^2 / 3 (causal halves once, masked tiles not counted).
+
+
+def prefill_bytes(token_heads, seq_heads, dk, dv, snapshots=True, s0=False, s_final=True):
+    b = token_heads * (2 * (3 * dk + 2 * dv) + 2)
+    if snapshots:
+        b += token_heads * 4 * dk * dv // 64
+    b += seq_heads * 4 * dk * dv * (int(s0) + int(s_final))
+    return b
+
+
+def prefill_flops(token_heads, dk, dv):
+    return token_heads * (6 * dk * dv + 64 * (3 * dk + 2 * dv) + 64 * 64 / 3)
+
+
+def decode_bytes(n_states, dk, dv):
+    # state read + write, q, k, z, v, o in bf16, beta
+    return n_states * (8 * dk * dv + 2 * (3 * dk + 2 * dv) + 2)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get(
+            "bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    """Rank info; under torchrun each rank gets its own GPU (no data collective)."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus and world > 1:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    return rank, world, local
+
+
+def reduce_max(value, world):
+    """Maximum of a float over ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def init_pg(world):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+
+
+# --- reference arm: the fp64 oracle on the host cores --------------------------------------
+
+def oracle_sample(x, n_tokens):
+    """Host fp64 copies of the first n_tokens of every sequence, all heads."""
+    import numpy as np
+    import torch
+    import kda_inputs
+    cu = x["cu_seqlens"].cpu().numpy()
+    parts = {n: [] for n in ("q", "k", "v", "z", "beta")}
+    lens = []
+    for s in range(len(cu) - 1):
+        a, L = int(cu[s]), min(n_tokens, int(cu[s + 1] - cu[s]))
+        lens.append(L)
+        for n in parts:
+            parts[n].append(kda_inputs.to_f64(x[n][a:a + L]))
+    cat = {n: np.concatenate(parts[n]) for n in parts}
+    cat["A"] = kda_inputs.to_f64(x["A"])
+    cat["cu"] = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    del torch
+    return cat, int(sum(lens))
+
+
+def time_oracle(cat, steps):
+    import oracle
+    dts = []
+    for _ in range(steps):
+        t = time.perf_counter()
+        oracle.prefill(cat["q"], cat["k"], cat["v"], cat["z"], cat["beta"], cat["A"],
+                       cu_seqlens=cat["cu"], snapshots=True)
+        dts.append(time.perf_counter() - t)
+    return dts
+
+
+def run_reference(args, rank, world):
+    import kda_inputs
+    import oracle
+    if rank != 0:
+        return
+    w = kda_inputs.WORKLOADS[WORKLOAD]
+    x = kda_inputs.make_workload_prefill(WORKLOAD, device="cpu")
+    cat, n_tok = oracle_sample(x, args.ref_tokens)
+    H = w["H"]
+    time_oracle(cat, args.warmup)
+    dts = time_oracle(cat, args.steps)
+    total = sum(dts)
+    value = n_tok * args.steps / total  # tokens (all H heads) per second
+    cores = oracle.num_threads()
+    sample = (f"first {args.ref_tokens} tokens of each of the {w['B']} sequences, all {H} heads "
+              f"({n_tok * H} token-heads per step), snapshots on")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": f"kda prefill B={w['B']} H={w['H']} T={w['T']} dk={w['dk']} "
+                        f"dv={w['dv']} chunk={w['chunk']}, final state + chunk snapshots",
+            "global_batch": w["B"], "seq_len": w["T"], "heads": w["H"],
+            "l2": "inputs larger than L2 (~1.2 GB of HBM traffic per step), no flush"}
+
+
+# --- our arm ------------------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import kda_inputs
+    import linear_attention_serving_chunk_gb300 as kda
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kda.build()
+    kda.lib()
+    hbm_peak, tc_peak, tc_sus, peak_src = load_peaks()
+    w = kda_inputs.WORKLOADS[WORKLOAD]
+    B, H, T, dk, dv = w["B"], w["H"], w["T"], w["dk"], w["dv"]
+    x = kda_inputs.make_workload_prefill(WORKLOAD, device=dev)
+    offs = kda.snapshot_offsets(x["lengths"], device=dev)
+    snaps = torch.empty((int(offs[-1]), H, dk, dv), dtype=torch.float32, device=dev)
+    S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    o = torch.empty((B * T, H, dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                      cu_seqlens=x["cu_seqlens"], o=o, S_final=S_final, snaps=snaps,
+                      snap_offsets=offs, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if kda.device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid).replace("GPU-", "")
+    except Exception:
+        gpu_id = local
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = reduce_max(t0.elapsed_time(t1), world)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+
+    token_heads = B * T * H
+    value = B * T * args.steps * world / (elapsed_ms / 1e3)
+    alg_bytes = prefill_bytes(token_heads, B * H, dk, dv)
+    alg_flops = prefill_flops(token_heads, dk, dv)
+    achieved = alg_bytes / avg_launch_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": args.traffic,
+                "kernel": "kda_chunk_fwd (one launch per step)",
+                "peak_source": peak_src,
+                "tensor": {"achieved_tflops": alg_flops / avg_launch_s / 1e12,
+                           "peak_tflops": tc_peak,
+                           "frac": alg_flops / avg_launch_s / 1e12 / tc_peak}}
+
+    # end to end: pinned host inputs -> device -> kda_chunk_fwd -> host outputs
+    host_in = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "z", "beta", "A",
+                                                     "cu_seqlens")}
+    host_out = {"o": torch.empty_like(o, device="cpu").pin_memory(),
+                "S_final": torch.empty_like(S_final, device="cpu").pin_memory(),
+                "snaps": torch.empty_like(snaps, device="cpu").pin_memory()}
+    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        kda.chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["z"], dev_in["beta"],
+                      dev_in["A"], cu_seqlens=dev_in["cu_seqlens"], o=o, S_final=S_final,
+                      snaps=snaps, snap_offsets=offs, stream=stream)
+        host_out["o"].copy_(o, non_blocking=True)
+        host_out["S_final"].copy_(S_final, non_blocking=True)
+        host_out["snaps"].copy_(snaps, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(a.elapsed_time(b), world)
+    e2e = {"value": B * T * e2e_steps * world / (e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del host_in, host_out, dev_in
+
+    decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak, peak_src, world)
+
+    cpu_baseline = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        cat, n_tok = oracle_sample(x, args.ref_tokens)
+        dts = time_oracle(cat, 1)
+        cpu_baseline = {"value": n_tok / dts[0], "unit": UNIT, "cores": oracle.num_threads(),
+                        "kind": "oracle",
+                        "sample": f"first {args.ref_tokens} tokens of each of the {B} sequences,"
+                                  f" all {H} heads ({n_tok * H} token-heads), snapshots on"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": kda_dtype(),
+                "data": "synthetic", "config": workload_config(w),
+                "clocks": clocks.summary(), "roofline": roofline, "cpu_baseline": cpu_baseline,
+                "e2e": e2e, "gpu_launches": args.steps, "decode": decode}
+        print(json.dumps(line), flush=True)
+
+
+def kda_dtype():
+    import linear_attention_serving_chunk_gb300 as kda
+    return getattr(kda, "PREFILL_COMPUTE_DTYPE", "f32")
+
+
+def run_decode(args, dev, stream, hbm_peak, peak_src, world):
+    """1000 chained decode steps (512 x 32 states, dk=dv=128) with fresh inputs."""
+    import torch
+
+    import kda_inputs
+    import linear_attention_serving_chunk_gb300 as kda
+    w = kda_inputs.WORKLOADS["decode"]
+    Bd, H, dk, dv, n_steps = w["batch"], w["H"], w["dk"], w["dv"], args.decode_steps
+    pool, A = kda_inputs.make_decode_state(Bd, H, dk, dv, w["seed"], device=dev,
+                                           std=w["state_std"])
+    toks = [kda_inputs.make_decode_token(Bd, H, dk, dv, w["seed"], s, device=dev)
+            for s in range(n_steps)]
+    o = torch.empty((Bd, H, dv), dtype=torch.bfloat16, device=dev)
+
+    def one(s):
+        t = toks[s]
+        kda.decode_step(t["q"], t["k"], t["v"], t["z"], t["beta"], A, pool, o=o, stream=stream)
+
+    for s in range(3):
+        one(s)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_steps)]
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for s in range(n_steps):
+        evs[s][0].record(stream)
+        one(s)
+        evs[s][1].record(stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    total_ms = reduce_max(a.elapsed_time(b), world)
+    per = statistics.mean(x.elapsed_time(y) for x, y in evs) / 1e3
+    nbytes = decode_bytes(Bd * H, dk, dv)
+    achieved = nbytes / per / 1e9
+    return {"value": n_steps * world / (total_ms / 1e3), "unit": "steps/s",
+            "tokens_per_s": Bd * n_steps * world / (total_ms / 1e3),
+            "workload": f"kda decode {Bd} sequences x H={H}, dk=dv={dk}, fp32 state in place, "
+                        f"{n_steps} chained steps with fresh inputs",
+            "gpu_launches": n_steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None,
+                         "kernel": "kda_decode_step", "peak_source": peak_src}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=2048,
+                    help="tokens per sequence in the oracle's bounded sample")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu DRAM bytes per prefill launch, when measured for this kernel")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    rank, world, local = dist_setup(args.gpus)
+    init_pg(world)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

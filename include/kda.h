@@ -1,0 +1,149 @@
+/*
+ * kda.h - C ABI of the GB300 (sm_103a) Kimi Delta Attention (KDA) library.
+ *
+ * KDA is the gated delta rule with a channel-wise, lower-bounded decay.  Per
+ * sequence and head, with a dk x dv fp32 state S (row = key channel i,
+ * column = value channel j):
+ *
+ *   g_t = gmin * sigmoid(exp(A_h) * z_t)                (vector over dk, gmin = -5)
+ *   S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *   o_t = S_t^T q_t
+ *
+ * Sources: "Kimi K3 Technical Report - Open Frontier Intelligence", Key
+ * claims and Method (sec. 2.1 chunkwise-parallel form; sec. 2.1.1 and Fig. 3,
+ * the scaled-sigmoid log-decay bounded below at gmin = -5 with a learnable
+ * per-head A; sec. 2.1.2, channel-wise gating), and "How a Frontier Model Gets
+ * Built, Read from the Kimi K3 Report", Technical Details (a fixed-size
+ * running state replaces the KV cache).  The update itself is not printed on
+ * those pages; the recurrence above is the reading this library implements.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers of the current CUDA device,
+ *    row-major (C order), 16-byte aligned.  bf16 tensors are passed as raw
+ *    16-bit patterns (kda_bf16).
+ *  - The caller owns all memory.  The library allocates nothing, frees
+ *    nothing and never synchronises: work is enqueued on `stream` (a
+ *    cudaStream_t; NULL = the legacy default stream) and the call returns.
+ *  - Arguments the host can check are checked before anything is launched;
+ *    a rejected call returns a non-zero kda_status and enqueues nothing.
+ *    A launch failure returns KDA_ERR_CUDA.  Nothing aborts, traps or throws.
+ *  - Supported sizes: dk, dv in {64, 128}; chunk = 64; -5.5 <= gmin <= 0.
+ *    The chunkwise prefill rescales 16-token sub-tiles by factors up to
+ *    exp(-16 * gmin); the bound keeps them inside the bf16/fp32 range
+ *    (sec. 2.1.1, Fig. 3 of the report page).
+ *
+ * Layouts (total = sum of sequence lengths; n = sequences or decode rows):
+ *   q, k, z       [total, H, dk] bf16        v, o   [total, H, dv] bf16
+ *   beta          [total, H] bf16            A      [H] fp32 (per head)
+ *   states        [n, H, dk, dv] fp32 (dv contiguous)
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kda_bf16;                 /* raw bfloat16 bit pattern */
+typedef struct CUstream_st *kda_stream_t;  /* same type as cudaStream_t */
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_NULL = 1,        /* a required pointer is NULL */
+  KDA_ERR_SHAPE = 2,       /* inconsistent or negative sizes */
+  KDA_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+  KDA_ERR_UNSUPPORTED = 4, /* dk/dv/chunk/gmin outside the supported set */
+  KDA_ERR_WORKSPACE = 5,   /* workspace missing or too small */
+  KDA_ERR_CUDA = 6,        /* a CUDA launch or runtime call failed */
+  KDA_ERR_TIMEOUT = 7      /* a bounded in-kernel wait gave up (device status) */
+} kda_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *kda_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int kda_version(void);
+
+/*
+ * Workspace bytes kda_chunk_fwd needs for these sizes (may be 0).  Pure
+ * host arithmetic; returns 0 for unsupported sizes as well.
+ */
+size_t kda_chunk_fwd_workspace_bytes(int n_seq, int64_t total_tokens, int H, int dk, int dv,
+                                     int chunk);
+
+/*
+ * kda_chunk_fwd - chunkwise-parallel KDA prefill over a batch of sequences
+ * (report page, sec. 2.1: chunkwise-parallel form; sec. 2.1.1/Fig. 3: every
+ * causal tile, diagonal and off-diagonal, as a dense matmul).
+ *
+ *   q, k, v, z, beta, A  inputs in the layouts above; gmin = -5 for KDA.
+ *   cu_seqlens  device int32 [n_seq + 1], token offsets of packed sequences
+ *               (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[n_seq] =
+ *               total_tokens); NULL = n_seq sequences of equal length
+ *               total_tokens / n_seq (must divide).  Chunks restart at each
+ *               sequence start; a sequence's last chunk may be partial.
+ *   S0          initial states [n_seq, H, dk, dv] fp32, or NULL for zero.
+ *   o           output [total, H, dv] bf16 (round to nearest even).
+ *   S_final     final states [n_seq, H, dk, dv] fp32, or NULL.
+ *   snaps       chunk-boundary states for prefix caching, or NULL: the state
+ *               after the first 64*j tokens of sequence s (j = 1 ..
+ *               floor(L_s / 64)) is written to row snap_offsets[s] + j - 1 of
+ *               a [rows, H, dk, dv] fp32 array.  S0 itself is not a snapshot.
+ *   snap_offsets device int64 [n_seq + 1], prefix sums of floor(L_s / 64);
+ *               may be NULL only when cu_seqlens is NULL (rows s * (T / 64)).
+ *   workspace   device scratch of kda_chunk_fwd_workspace_bytes() bytes
+ *               (NULL allowed when that is 0); contents need not be zeroed.
+ *   Errors: KDA_ERR_NULL, _SHAPE, _ALIGN, _UNSUPPORTED, _WORKSPACE, _CUDA.
+ */
+int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                  const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                  const int32_t *cu_seqlens, int n_seq, int64_t total_tokens, int H,
+                  int dk, int dv, int chunk, const float *S0, kda_bf16 *o, float *S_final,
+                  float *snaps, const int64_t *snap_offsets, void *workspace,
+                  size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_decode_step - one token of the recurrence for n sequences on resident
+ * fp32 states, updated in place (the fixed-size running state of "How a
+ * Frontier Model Gets Built, Read from the Kimi K3 Report", Technical
+ * Details).  Row b of q, k, v, z, beta ([n, H, ...]) is applied to state slot
+ * slots[b] of state_pool [n_slots, H, dk, dv]; slots is a device int32 [n]
+ * array, or NULL for slot b.  Slots must be distinct (two rows writing one
+ * slot race).  o [n, H, dv] bf16 receives S_t^T q_t (the updated state).
+ *   Errors: KDA_ERR_NULL, _SHAPE, _ALIGN, _UNSUPPORTED, _CUDA.
+ */
+int kda_decode_step(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                    const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                    float *state_pool, const int32_t *slots, int n, int H, int dk, int dv,
+                    kda_bf16 *o, kda_stream_t stream);
+
+/*
+ * kda_state_snapshot - restore chunk-boundary states for prefix caching
+ * ("state-aware prefix caching", report page, Key claims / Infrastructure):
+ * for b in [0, n) copy the H x dk x dv fp32 block at row src_idx[b] of snaps
+ * ([rows, H, dk, dv], as written by kda_chunk_fwd) to slot dst_slots[b] of
+ * state_pool ([n_slots, H, dk, dv]).  src_idx: device int64 [n]; dst_slots:
+ * device int32 [n]; destinations must be distinct.  After it, the slot is a
+ * valid S0 for kda_chunk_fwd on the suffix or a state for kda_decode_step.
+ *   Errors: KDA_ERR_NULL, _SHAPE, _ALIGN, _UNSUPPORTED, _CUDA.
+ */
+int kda_state_snapshot(const float *snaps, const int64_t *src_idx, float *state_pool,
+                       const int32_t *dst_slots, int n, int H, int dk, int dv,
+                       kda_stream_t stream);
+
+/*
+ * kda_device_status - read (and with reset != 0, clear) the library's
+ * device-side status word on the current device.  Kernels with bounded waits
+ * record KDA_ERR_TIMEOUT there instead of hanging.  This call synchronises
+ * the device.  Returns KDA_OK, KDA_ERR_TIMEOUT or KDA_ERR_CUDA.
+ */
+int kda_device_status(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,137 @@
+// Single-token recurrent decode step on resident fp32 states, in place.
+//
+// Per (sequence, head): a = exp(g), S' = Diag(a) S, p = S'^T k, u = S'^T q,
+// delta = beta (v - p), S'' = S' + k delta^T, o = S''^T q = u + (k.q) delta.
+// This equals S_t = (I - beta k k^T) Diag(exp(g)) S_{t-1} + beta k v^T and
+// o_t = S_t^T q_t (the fixed-size running state of "How a Frontier Model Gets
+// Built, Read from the Kimi K3 Report", Technical Details; gate from "Kimi K3
+// Technical Report - Open Frontier Intelligence", sec. 2.1.1).
+//
+// The step is bound by HBM: each state (dk*dv*4 bytes) is read once and
+// written once.  One 256-thread CTA owns one state; every thread keeps a
+// (dk / row_groups) x 4 block of it in registers between the read and the
+// write, so the state crosses HBM exactly twice.  Rows of S are read and
+// written as 16-byte vectors, one 512-byte row per warp instruction (dv=128).
+#include "kda_common.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int kDecodeThreads = 256;
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kDecodeThreads)
+decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ k,
+                   const kda_bf16 *__restrict__ v, const kda_bf16 *__restrict__ z,
+                   const kda_bf16 *__restrict__ beta, const float *__restrict__ A,
+                   float gmin, float *__restrict__ pool, const int32_t *__restrict__ slots,
+                   int H, kda_bf16 *__restrict__ o) {
+  constexpr int TPR = DV / 4;                // threads across one row (4 columns each)
+  constexpr int RG = kDecodeThreads / TPR;   // row groups
+  constexpr int RPT = DK / RG;               // rows per thread
+  static_assert(RPT * RG == DK && TPR * RG == kDecodeThreads, "decode tiling");
+
+  __shared__ float s_a[DK], s_k[DK], s_q[DK];
+  __shared__ float s_red_p[RG][DV], s_red_u[RG][DV];
+  __shared__ float s_delta[DV];
+  __shared__ float s_kq_part[DK / 32];
+
+  const int row = blockIdx.x;  // b * H + h
+  const int b = row / H, h = row - b * H;
+  const int tid = threadIdx.x;
+  const int cg = tid % TPR, rg = tid / TPR;
+  const int slot = slots ? slots[b] : b;
+  float *S = pool + (static_cast<size_t>(slot) * H + h) * (DK * DV);
+
+  // Issue the whole state read first; the gate below overlaps its latency.
+  float4 s[RPT];
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr)
+    s[rr] = __ldcs(reinterpret_cast<const float4 *>(S + (rg * RPT + rr) * DV) + cg);
+
+  if (tid < DK) {
+    const size_t x = static_cast<size_t>(row) * DK + tid;
+    const float kv = bf2f(k[x]), qv = bf2f(q[x]);
+    s_a[tid] = decay_factor(gmin, expf(A[h]), bf2f(z[x]));
+    s_k[tid] = kv;
+    s_q[tid] = qv;
+    float kq = kv * qv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+    if ((tid & 31) == 0) s_kq_part[tid >> 5] = kq;
+  }
+  __syncthreads();
+
+  float p[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr) {
+    const int i = rg * RPT + rr;
+    const float a = s_a[i], kv = s_k[i], qv = s_q[i];
+    s[rr].x *= a; s[rr].y *= a; s[rr].z *= a; s[rr].w *= a;
+    p[0] += s[rr].x * kv; p[1] += s[rr].y * kv; p[2] += s[rr].z * kv; p[3] += s[rr].w * kv;
+    u[0] += s[rr].x * qv; u[1] += s[rr].y * qv; u[2] += s[rr].z * qv; u[3] += s[rr].w * qv;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    s_red_p[rg][cg * 4 + c] = p[c];
+    s_red_u[rg][cg * 4 + c] = u[c];
+  }
+  __syncthreads();
+
+  if (tid < DV) {
+    float pj = 0.f, uj = 0.f;
+#pragma unroll
+    for (int g = 0; g < RG; ++g) {
+      pj += s_red_p[g][tid];
+      uj += s_red_u[g][tid];
+    }
+    float kq = 0.f;
+#pragma unroll
+    for (int w = 0; w < DK / 32; ++w) kq += s_kq_part[w];
+    const size_t xv = static_cast<size_t>(row) * DV + tid;
+    const float delta = bf2f(beta[row]) * (bf2f(v[xv]) - pj);
+    s_delta[tid] = delta;
+    o[xv] = f2bf(uj + kq * delta);
+  }
+  __syncthreads();
+
+  const float d0 = s_delta[cg * 4 + 0], d1 = s_delta[cg * 4 + 1];
+  const float d2 = s_delta[cg * 4 + 2], d3 = s_delta[cg * 4 + 3];
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr) {
+    const float kv = s_k[rg * RPT + rr];
+    s[rr].x += kv * d0; s[rr].y += kv * d1; s[rr].z += kv * d2; s[rr].w += kv * d3;
+    __stcs(reinterpret_cast<float4 *>(S + (rg * RPT + rr) * DV) + cg, s[rr]);
+  }
+}
+
+template <int DK, int DV>
+cudaError_t launch_decode(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                          const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                          float *pool, const int32_t *slots, int n, int H, kda_bf16 *o,
+                          cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(n) * H;
+  decode_step_kernel<DK, DV><<<static_cast<unsigned>(rows), kDecodeThreads, 0, stream>>>(
+      q, k, v, z, beta, A, gmin, pool, slots, H, o);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t decode_step_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                               const kda_bf16 *z, const kda_bf16 *beta, const float *A,
+                               float gmin, float *pool, const int32_t *slots, int n, int H,
+                               int dk, int dv, kda_bf16 *o, cudaStream_t stream) {
+  if (dk == 128 && dv == 128)
+    return launch_decode<128, 128>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, stream);
+  if (dk == 64 && dv == 64)
+    return launch_decode<64, 64>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, stream);
+  if (dk == 128 && dv == 64)
+    return launch_decode<128, 64>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, stream);
+  if (dk == 64 && dv == 128)
+    return launch_decode<64, 128>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

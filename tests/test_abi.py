@@ -1,0 +1,100 @@
+"""Host-side checks of the C ABI: the library loads, exports every function
+declared in include/kda.h, and rejects bad arguments before launching
+anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_serving_chunk_gb300 as kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    kda.build()
+    return kda.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for fn in ("kda_chunk_fwd", "kda_decode_step", "kda_state_snapshot"):
+        assert fn in names
+    assert set(names) == set(kda.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} is declared in kda.h but not exported"
+
+
+def test_status_strings_and_version(L):
+    assert L.kda_version() >= 100
+    for s in range(8):
+        assert L.kda_status_string(s)
+    assert L.kda_status_string(99) == b"unknown status"
+
+
+def _chunk_args(**kw):
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: every call below is rejected first
+    args = dict(q=fake, k=fake, v=fake, z=fake, beta=fake, A=fake, gmin=-5.0, cu=None, n_seq=1,
+                total=128, H=2, dk=64, dv=64, chunk=64, S0=None, o=fake, S_final=None,
+                snaps=None, snap_offsets=None, ws=None, ws_bytes=0, stream=None)
+    args.update(kw)
+    return list(args.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=96), 4), (dict(dv=32), 4), (dict(chunk=32), 4), (dict(gmin=-8.0), 4),
+    (dict(gmin=0.5), 4), (dict(gmin=float("nan")), 4), (dict(H=0), 2), (dict(n_seq=-1), 2),
+    (dict(total=-5), 2), (dict(n_seq=3, total=128), 2), (dict(q=None), 1), (dict(A=None), 1),
+    (dict(o=None), 1), (dict(q=ctypes.c_void_p(0x10008)), 3),
+    (dict(snaps=ctypes.c_void_p(0x20000), cu=ctypes.c_void_p(0x30000)), 1),
+    (dict(n_seq=0, total=0), 0),
+])
+def test_chunk_fwd_rejects_before_launch(L, kw, status):
+    assert L.kda_chunk_fwd(*_chunk_args(**kw)) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=48), 4), (dict(gmin=-7.0), 4), (dict(n=-1), 2), (dict(H=0), 2), (dict(q=None), 1),
+    (dict(pool=None), 1), (dict(o=ctypes.c_void_p(0x10004)), 3), (dict(n=0), 0),
+])
+def test_decode_step_rejects_before_launch(L, kw, status):
+    fake = ctypes.c_void_p(0x10000)
+    a = dict(q=fake, k=fake, v=fake, z=fake, beta=fake, A=fake, gmin=-5.0, pool=fake, slots=None,
+             n=4, H=2, dk=64, dv=64, o=fake, stream=None)
+    a.update(kw)
+    assert L.kda_decode_step(*a.values()) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=32), 4), (dict(n=-2), 2), (dict(snaps=None), 1), (dict(dst=None), 1),
+    (dict(src=ctypes.c_void_p(0x10002)), 3), (dict(n=0), 0),
+])
+def test_state_snapshot_rejects_before_launch(L, kw, status):
+    fake = ctypes.c_void_p(0x10000)
+    a = dict(snaps=fake, src=fake, pool=fake, dst=fake, n=2, H=2, dk=64, dv=64, stream=None)
+    a.update(kw)
+    assert L.kda_state_snapshot(*a.values()) == status
+
+
+def test_workspace_query_is_pure_host(L):
+    assert L.kda_chunk_fwd_workspace_bytes(4, 4 * 8192, 16, 128, 128, 64) >= 0
+
+
+def test_python_binding_fails_loudly_without_cuda_tensors(L):
+    import torch
+    x = torch.zeros(64, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kda.chunk_fwd(x, x, x, x, torch.zeros(64, 1, dtype=torch.bfloat16),
+                      torch.zeros(1, dtype=torch.float32))

@@ -1,0 +1,316 @@
+"""GPU parity: the CUDA library (through the C ABI) against the fp64 oracle on
+the same seeded inputs.
+
+Tolerances: outputs max|o - o_ref| <= 2e-2 * RMS(o_ref); states (final and
+snapshots) relative Frobenius error <= 1e-2; decode state trajectories
+relative Frobenius error <= 1e-4 per state.  The oracle never sees a value
+produced by the CUDA path: its inputs are the generated inputs, copied to the
+host, and it carries its own state between segments.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 2e-2
+S_TOL = 1e-2
+DECODE_TOL = 1e-4
+
+f64 = kda_inputs.to_f64
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import linear_attention_serving_chunk_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+def o_err(o_gpu, o_ref):
+    """max |o - o_ref| / RMS(o_ref)."""
+    return float(np.max(np.abs(o_gpu - o_ref)) / max(np.sqrt(np.mean(o_ref ** 2)), 1e-30))
+
+
+def s_err(S_gpu, S_ref):
+    """Relative Frobenius error."""
+    return float(np.linalg.norm(S_gpu - S_ref) / max(np.linalg.norm(S_ref), 1e-30))
+
+
+def run_prefill(kda, x, snapshots=True, S0=True):
+    n_seq = len(x["lengths"])
+    total, H, dk = x["k"].shape
+    dv = x["v"].shape[2]
+    dev = x["k"].device
+    offs = kda.snapshot_offsets(x["lengths"], device=dev)
+    snaps = (torch.full((max(int(offs[-1]), 1), H, dk, dv), float("nan"), device=dev)
+             if snapshots else None)
+    S_final = torch.full((n_seq, H, dk, dv), float("nan"), device=dev)
+    o = torch.full((total, H, dv), float("nan"), dtype=torch.bfloat16, device=dev)
+    kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], cu_seqlens=x["cu_seqlens"],
+                  S0=x["S0"] if S0 else None, o=o, S_final=S_final, snaps=snaps,
+                  snap_offsets=offs if snapshots else None)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    return o, S_final, snaps, offs
+
+
+def oracle_subset(x, seqs, heads, t_limit=None, snapshots=True):
+    """Oracle on sequences ``seqs`` and heads ``heads`` (optionally only the
+    first t_limit tokens of each sequence).  Inputs are gathered on the host."""
+    cu = x["cu_seqlens"].cpu().numpy().astype(np.int64)
+    hs = torch.tensor(heads, device=x["k"].device)
+    parts = {n: [] for n in ("q", "k", "v", "z", "beta")}
+    lens = []
+    for s in seqs:
+        a = int(cu[s])
+        L = int(cu[s + 1] - cu[s]) if t_limit is None else min(t_limit, int(cu[s + 1] - cu[s]))
+        lens.append(L)
+        for n in parts:
+            parts[n].append(f64(x[n][a:a + L].index_select(1, hs)))
+    cat = {n: np.concatenate(parts[n], axis=0) for n in parts}
+    S0 = None
+    if x["S0"] is not None:
+        S0 = f64(x["S0"][torch.tensor(seqs, device=x["k"].device)].index_select(1, hs))
+    ref = oracle.prefill(cat["q"], cat["k"], cat["v"], cat["z"], cat["beta"],
+                         f64(x["A"])[heads], cu_seqlens=np.concatenate([[0], np.cumsum(lens)]),
+                         S0=S0, snapshots=snapshots)
+    ref["lens"] = lens
+    return ref
+
+
+def gather_gpu(x, o, S_final, snaps, offs, seqs, heads, t_limit=None):
+    cu = x["cu_seqlens"].cpu().numpy().astype(np.int64)
+    offs_h = offs.cpu().numpy()
+    hs = torch.tensor(heads, device=o.device)
+    oo, ss, sn = [], [], []
+    for s in seqs:
+        a = int(cu[s])
+        L = int(cu[s + 1] - cu[s]) if t_limit is None else min(t_limit, int(cu[s + 1] - cu[s]))
+        oo.append(f64(o[a:a + L].index_select(1, hs)))
+        ss.append(f64(S_final[s].index_select(0, hs)))
+        if snaps is not None:
+            nsn = L // 64
+            sn.append(f64(snaps[int(offs_h[s]):int(offs_h[s]) + nsn].index_select(1, hs)))
+    return (np.concatenate(oo), np.stack(ss),
+            np.concatenate(sn) if sn else None)
+
+
+def check_all(x, kda, seqs=None, heads=None, t_limit=None):
+    o, S_final, snaps, offs = run_prefill(kda, x)
+    n_seq = len(x["lengths"])
+    H = x["k"].shape[1]
+    seqs = list(range(n_seq)) if seqs is None else seqs
+    heads = list(range(H)) if heads is None else heads
+    ref = oracle_subset(x, seqs, heads, t_limit)
+    go, gs, gsn = gather_gpu(x, o, S_final, snaps, offs, seqs, heads, t_limit)
+    e_o = o_err(go, ref["o"])
+    assert np.all(np.isfinite(go)), "non-finite outputs"
+    assert e_o <= O_TOL, f"output error {e_o:.3e}"
+    if ref["snaps"] is not None and ref["snaps"].shape[0]:
+        e_sn = s_err(gsn, ref["snaps"])
+        assert e_sn <= S_TOL, f"snapshot error {e_sn:.3e}"
+    if t_limit is None:
+        e_s = s_err(gs, ref["S_final"])
+        assert e_s <= S_TOL, f"final state error {e_s:.3e}"
+    return o, S_final, snaps, offs, ref
+
+
+# --- the workloads ---------------------------------------------------------------------------
+
+def test_tiny_full(kda):
+    x = kda_inputs.make_workload_prefill("tiny", device="cuda")
+    check_all(x, kda)
+
+
+def test_mid_full(kda):
+    """B=4, H=16, T=8192, dk=dv=128: every output, final state and snapshot."""
+    x = kda_inputs.make_workload_prefill("mid", device="cuda")
+    check_all(x, kda)
+
+
+def test_varlen_64_sequences(kda):
+    """64 packed sequences, lengths U[512, 32768], H=32, S0 ~ N(0, 0.02^2):
+    the GPU runs everything; all 64 sequences are checked on 4 seeded heads."""
+    x = kda_inputs.make_workload_prefill("varlen", device="cuda")
+    heads = sorted(np.random.default_rng(2024).choice(32, size=4, replace=False).tolist())
+    check_all(x, kda, heads=heads)
+
+
+def test_long_context(kda):
+    """T = 1,048,576, H = 16: heads 0 and 1 are checked over the first 65,536
+    tokens (outputs and 1024 snapshots) and over the whole length (outputs
+    and final state), the oracle running segment by segment on its own state."""
+    x = kda_inputs.make_workload_prefill("long", device="cuda")
+    o, S_final, snaps, offs, _ = check_all(x, kda, seqs=[0], heads=[0, 1], t_limit=65536)
+    heads = [0, 1]
+    hs = torch.tensor(heads, device="cuda")
+    T = x["k"].shape[0]
+    seg = 1 << 17
+    S = None
+    worst = 0.0
+    for a in range(0, T, seg):
+        sl = slice(a, a + seg)
+        ref = oracle.prefill(*(f64(x[n][sl].index_select(1, hs)) for n in ("q", "k", "v", "z",
+                                                                            "beta")),
+                             f64(x["A"])[heads], S0=S)
+        S = ref["S_final"]
+        worst = max(worst, o_err(f64(o[sl].index_select(1, hs)), ref["o"]))
+    assert worst <= O_TOL, f"output error {worst:.3e}"
+    e_s = s_err(f64(S_final[0].index_select(0, hs)), S[0])
+    assert e_s <= S_TOL, f"final state error {e_s:.3e}"
+    last = f64(snaps[int(offs[1]) - 1].index_select(0, hs))
+    assert s_err(last, S[0]) <= S_TOL, "last snapshot is not the final state"
+
+
+def test_decode_1000_steps(kda):
+    """512 x 32 resident states, 1000 chained steps with fresh inputs: all
+    states are checked after steps 1 and 10, 256 seeded (sequence, head)
+    pairs after steps 1, 10, 100 and 1000, 16 of them after every step."""
+    w = kda_inputs.WORKLOADS["decode"]
+    B, H, dk, dv = w["batch"], w["H"], w["dk"], w["dv"]
+    pool, A = kda_inputs.make_decode_state(B, H, dk, dv, w["seed"], device="cuda",
+                                           std=w["state_std"])
+    rng = np.random.default_rng(77)
+    pairs = rng.choice(B * H, size=256, replace=False)
+    every = pairs[:16]
+    pb, ph = torch.tensor(pairs // H, device="cuda"), torch.tensor(pairs % H, device="cuda")
+    eb, eh = torch.tensor(every // H, device="cuda"), torch.tensor(every % H, device="cuda")
+    Af = f64(A)
+    full = np.ascontiguousarray(f64(pool))
+    sub = np.ascontiguousarray(f64(pool[pb, ph]))[:, None]  # [256, 1, dk, dv]
+    worst_every, worst_o = 0.0, 0.0
+    for step in range(w["steps"]):
+        t = kda_inputs.make_decode_token(B, H, dk, dv, w["seed"], step, device="cuda")
+        o = kda.decode_step(t["q"], t["k"], t["v"], t["z"], t["beta"], A, pool)
+        # oracle on the 256-pair subset (one sequence per pair, its own head's A)
+        ins = {n: f64(t[n][pb, ph])[:, None] for n in ("q", "k", "v", "z", "beta")}
+        o_ref = np.empty((256, dv))
+        for hh in np.unique(pairs % H):
+            m = (pairs % H) == hh
+            st = np.ascontiguousarray(sub[m])
+            o_ref[m] = oracle.decode_step(ins["q"][m], ins["k"][m], ins["v"][m], ins["z"][m],
+                                          ins["beta"][m], Af[hh:hh + 1], st)[:, 0]
+            sub[m] = st
+        worst_o = max(worst_o, o_err(f64(o[pb, ph]), o_ref))
+        if step < 10:
+            oracle.decode_step(f64(t["q"]), f64(t["k"]), f64(t["v"]), f64(t["z"]),
+                               f64(t["beta"]), Af, full)
+        n = step + 1
+        g_every = f64(pool[eb, eh])
+        for a, i in enumerate(range(16)):
+            worst_every = max(worst_every, s_err(g_every[a], sub[i, 0]))
+        if n in (1, 10, 100, 1000):
+            g_sub = f64(pool[pb, ph])
+            e = max(s_err(g_sub[i], sub[i, 0]) for i in range(256))
+            assert e <= DECODE_TOL, f"step {n}: subset state error {e:.3e}"
+        if n in (1, 10):
+            g_full = f64(pool).reshape(B * H, dk, dv)
+            e = max(s_err(g_full[i], full.reshape(B * H, dk, dv)[i]) for i in range(B * H))
+            assert e <= DECODE_TOL, f"step {n}: state error {e:.3e}"
+    assert worst_every <= DECODE_TOL, f"per-step trajectory error {worst_every:.3e}"
+    assert worst_o <= O_TOL, f"decode output error {worst_o:.3e}"
+
+
+# --- edge cases --------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (128, 64), (64, 128)])
+def test_ragged_lengths(kda, dk, dv):
+    """Empty, single-token, sub-chunk, exact-chunk and ragged sequences."""
+    lengths = [0, 1, 63, 64, 65, 127, 128, 200, 331]
+    x = kda_inputs.make_prefill(3, dk, dv, lengths, seed=11, device="cuda", S0_std=0.02)
+    o, S_final, snaps, offs, ref = check_all(x, kda)
+    # the empty sequence keeps its initial state exactly
+    assert torch.equal(S_final[0], x["S0"][0])
+
+
+def test_zero_initial_state_and_no_optional_outputs(kda):
+    x = kda_inputs.make_prefill(2, 64, 64, [150, 77], seed=12, device="cuda")
+    o = kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                      cu_seqlens=x["cu_seqlens"])
+    ref = oracle_subset(x, [0, 1], [0, 1], snapshots=False)
+    assert o_err(f64(o), ref["o"]) <= O_TOL
+
+
+def test_equal_length_batch_without_cu_seqlens(kda):
+    x = kda_inputs.make_prefill(2, 128, 128, [192, 192, 192], seed=13, device="cuda",
+                                S0_std=0.02)
+    n_seq = 3
+    S_final = torch.empty((n_seq, 2, 128, 128), device="cuda")
+    snaps = torch.empty((9, 2, 128, 128), device="cuda")
+    o = kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], n_seq=n_seq, S0=x["S0"],
+                      S_final=S_final, snaps=snaps)
+    ref = oracle_subset(x, [0, 1, 2], [0, 1])
+    assert o_err(f64(o), ref["o"]) <= O_TOL
+    assert s_err(f64(S_final), ref["S_final"]) <= S_TOL
+    assert s_err(f64(snaps), ref["snaps"]) <= S_TOL
+
+
+@pytest.mark.parametrize("zval", [float("inf"), float("-inf"), 40.0])
+def test_extreme_gates(kda, zval):
+    """z = +inf gives g = -5 in every channel (the strongest decay the bound
+    allows: a rescaling factor of e^80 per 16-token sub-tile); the output must
+    stay finite and match.  z = -inf gives no decay at all."""
+    x = kda_inputs.make_prefill(2, 128, 128, [256, 100], seed=14, device="cuda", S0_std=0.02)
+    x["z"].fill_(zval)
+    o, S_final, snaps, offs, ref = check_all(x, kda)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(S_final).all()
+
+
+def test_prefix_cache_roundtrip(kda):
+    """Prefill a sequence, restore the snapshot after 3 chunks into a state
+    slot, prefill the suffix from that slot and decode one token from another
+    restored slot: both match the oracle run on the whole sequence."""
+    L, H, d = 300, 2, 128
+    x = kda_inputs.make_prefill(H, d, d, [L], seed=15, device="cuda", S0_std=0.02)
+    o, S_final, snaps, offs = run_prefill(kda, x)
+    pool = torch.zeros((4, H, d, d), device="cuda")
+    kda.state_snapshot(snaps, torch.tensor([2, 1], dtype=torch.int64, device="cuda"), pool,
+                       torch.tensor([3, 0], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(pool[3], snaps[2]) and torch.equal(pool[0], snaps[1])
+    cut = 192
+    o_suf = kda.chunk_fwd(*(x[n][cut:].contiguous() for n in ("q", "k", "v", "z", "beta")), x["A"],
+                          S0=pool[3:4].contiguous())
+    ref = oracle_subset(x, [0], [0, 1])
+    assert o_err(f64(o_suf), ref["o"][cut:]) <= O_TOL
+    # decode the token at position 128 from the snapshot after 2 chunks (slot 0)
+    t = {n: x[n][128:129].contiguous() for n in ("q", "k", "v", "z", "beta")}
+    od = kda.decode_step(t["q"], t["k"], t["v"], t["z"], t["beta"], x["A"], pool,
+                         slots=torch.tensor([0], dtype=torch.int32, device="cuda"))
+    assert o_err(f64(od)[0], ref["o"][128]) <= O_TOL
+
+
+def test_decode_slots_and_prefill_agreement(kda):
+    """Decode through a slot permutation equals decode in place; n decode
+    steps reproduce the oracle's n-token prefill."""
+    n, H, d, steps = 6, 2, 64, 20
+    x = kda_inputs.make_prefill(H, d, d, [steps] * n, seed=16, device="cuda", S0_std=0.02)
+    perm = torch.tensor([3, 0, 5, 1, 4, 2], dtype=torch.int32, device="cuda")
+    pool_a = x["S0"].clone()
+    pool_b = torch.empty_like(pool_a)
+    pool_b[perm.long()] = x["S0"]
+    for t in range(steps):
+        rows = torch.arange(n, device="cuda") * steps + t
+        tok = {nm: x[nm][rows].contiguous() for nm in ("q", "k", "v", "z", "beta")}
+        oa = kda.decode_step(tok["q"], tok["k"], tok["v"], tok["z"], tok["beta"], x["A"], pool_a)
+        ob = kda.decode_step(tok["q"], tok["k"], tok["v"], tok["z"], tok["beta"], x["A"], pool_b,
+                             slots=perm)
+        assert torch.equal(oa, ob)
+    assert torch.equal(pool_b[perm.long()], pool_a)
+    ref = oracle_subset(x, list(range(n)), [0, 1], snapshots=False)
+    assert s_err(f64(pool_a), ref["S_final"]) <= DECODE_TOL
+
+
+def test_runs_on_a_side_stream(kda):
+    x = kda_inputs.make_prefill(2, 64, 64, [130], seed=17, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o = kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"])
+    s.synchronize()
+    ref = oracle_subset(x, [0], [0, 1], snapshots=False)
+    assert o_err(f64(o), ref["o"]) <= O_TOL

@@ -1,9 +1,12 @@
 """GPU parity: the CUDA library (through the C ABI) against the fp64 oracle on
 the same seeded inputs.
 
-Tolerances: outputs max|o - o_ref| <= 2e-2 * RMS(o_ref); states (final and
-snapshots) relative Frobenius error <= 1e-2; decode state trajectories
-relative Frobenius error <= 1e-4 per state.  The oracle never sees a value
+Tolerances: outputs |o - o_ref| <= 2e-2 * RMS(o_ref) + 2^-8 |o_ref| per
+element (the stated 2e-2 RMS bound on the computation plus one bf16 ulp of
+the exact value for the output cast: the outputs are heavy-tailed, max|o| is
+about 12 RMS, so rounding the exact result to bf16 alone reaches 2.7e-2 RMS);
+states (final and snapshots) relative Frobenius error <= 1e-2; decode state
+trajectories relative Frobenius error <= 1e-4 per state.  The oracle never sees a value
 produced by the CUDA path: its inputs are the generated inputs, copied to the
 host, and it carries its own state between segments.
 """
@@ -31,9 +34,14 @@ def kda():
     return m
 
 
+BF16_ULP = 2.0 ** -8
+
+
 def o_err(o_gpu, o_ref):
-    """max |o - o_ref| / RMS(o_ref)."""
-    return float(np.max(np.abs(o_gpu - o_ref)) / max(np.sqrt(np.mean(o_ref ** 2)), 1e-30))
+    """max over elements of (|o - o_ref| - 2^-8 |o_ref|) / RMS(o_ref): the
+    output error beyond one bf16 ulp of the exact value, in units of RMS."""
+    excess = np.abs(o_gpu - o_ref) - BF16_ULP * np.abs(o_ref)
+    return float(np.max(excess) / max(np.sqrt(np.mean(o_ref ** 2)), 1e-30))
 
 
 def s_err(S_gpu, S_ref):

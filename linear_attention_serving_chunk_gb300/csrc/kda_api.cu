@@ -26,7 +26,20 @@ cudaError_t prefill_simt_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_
                                 kda_bf16 *o, float *S_final, float *snaps,
                                 const int64_t *snap_offsets, cudaStream_t stream);
 
+bool prefill_tc_supported(int dk, int dv, int64_t total_tokens);
+cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                              const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                              const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
+                              int64_t fixed_len, int H, const float *S0, kda_bf16 *o,
+                              float *S_final, float *snaps, const int64_t *snap_offsets,
+                              int *status, cudaStream_t stream);
+
 namespace {
+
+int *status_word() {
+  void *p = nullptr;
+  return cudaGetSymbolAddress(&p, g_status) == cudaSuccess ? static_cast<int *>(p) : nullptr;
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -91,9 +104,17 @@ int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const
     if (p && !aligned16(p)) return KDA_ERR_ALIGN;
   const size_t need = kda_chunk_fwd_workspace_bytes(n_seq, total_tokens, H, dk, dv, chunk);
   if (need > 0 && (!workspace || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
-  const cudaError_t err =
-      prefill_simt_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, fixed_len, H, dk, dv, S0,
-                          o, S_final, snaps, snap_offsets, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (prefill_tc_supported(dk, dv, total_tokens)) {
+    int *status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    err = prefill_tc_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, total_tokens, fixed_len,
+                            H, S0, o, S_final, snaps, snap_offsets, status, st);
+  } else {
+    err = prefill_simt_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, fixed_len, H, dk, dv,
+                              S0, o, S_final, snaps, snap_offsets, st);
+  }
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -1,0 +1,753 @@
+// Chunkwise-parallel KDA prefill on the sm_103a tensor cores (tcgen05 + TMEM,
+// operands staged by TMA), dk = dv = 128, chunk C = 64.
+//
+// Algebra ("Kimi K3 Technical Report - Open Frontier Intelligence", sec. 2.1
+// chunkwise-parallel form, sec. 2.1.1 / Fig. 3 bounded decay): for one chunk
+// with inclusive cumulative log-decay G_r and chunk-start state S,
+//
+//   A_kk = strict_lower(diag(beta) (K e^G)(K e^-G)^T),  T = (I + A_kk)^{-1}
+//   T'   = T diag(beta),   Wk = T' (K e^G),   U = T' V,   W = U - Wk S
+//   P    = tril((Q e^G)(K e^-G)^T),  O = (Q e^G) S + P W
+//   S'   = Diag(e^{G_last}) S + (K e^{G_last - G})^T W
+//
+// Every causal tile of A_kk and P, the diagonal ones included, is one dense
+// MMA.  The chunk is split into four 16-row sub-tiles; for the rows of
+// sub-tile R the reference is the cumulative decay just before R, so the row
+// factor e^{G_r - G_ref} is <= 1 and the column factor e^{G_ref - G_i} is at
+// most e^{-16 gmin} = e^80: the lower bound gmin = -5 is what keeps these
+// reciprocal factors inside the 8-bit-exponent (bf16 / fp32) range.  The
+// transposed products D[i, r] = Khat_R[i] . [K_R e^{G - G_ref}; Q_R e^{G - G_ref}][r]
+// are issued two sub-tiles per M = 128 MMA.
+//
+// Operand precision: the A_kk / P products need the 8-bit exponent range
+// (factors up to e^80) and more than bf16's 8-bit mantissa (outputs are
+// heavy-tailed and P feeds them directly), so they run as kind::tf32
+// (10-bit mantissa).  T' K~ and T' V use bf16 (V arrives as bf16).  The
+// state-dependent products use fp16 operands (11-bit mantissa; |S|, |W|,
+// |Wk| stay far below 65504 for unit keys and beta in [0, 1]).
+//
+// Per chunk (one CTA per (sequence, head), 256 threads, chunks in order):
+//   TMA     q -> A3 lower half, z -> ZB, k -> KB, v -> VB (next chunk's q/z
+//           double-buffered, k/v refilled as soon as their MMAs finish)
+//   SIMT    gate exp(g), per-sub-tile running products, then every scaled
+//           operand in place: k -> K e^G, q -> -(Q e^G), z -> K e^{G_last-G}
+//   MMA     A_kk and P (2 x M128 N64 K128, tf32), T on the CUDA cores (blocked
+//           16x16 forward substitution, fp32), Wk = T' K~ and U = T' V
+//           (M128 N128 K64; U lands in the output accumulator D1)
+//   serial  D1 += [-Wk; -Q~] S_fp16  (W in rows 0..63, -Q~S in rows 64..127)
+//           S_tm = e^{G_last} S_tm + K'^T W   (fp32 state kept in TMEM)
+//           D1 += [0; -P] W                   (-O in rows 64..127)
+//
+// Sizes: shared memory 226 KB (1 CTA / SM), TMEM 384 of 512 columns.
+// Every mbarrier wait is bounded; a wait that gives up records
+// KDA_ERR_TIMEOUT in the status word and the CTA stops cleanly.
+#include "kda_common.cuh"
+#include "kda_sm100.cuh"
+
+namespace kda {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int TC_THREADS = 256;
+constexpr int TD = 128;  // dk = dv handled by this kernel
+constexpr uint32_t KiB = 1024;
+
+// Shared-memory map, byte offsets from the (1024-aligned) dynamic base.
+constexpr uint32_t SM_A3 = 0;                     // 2 x 32 KiB: [-Wk ; q -> -Q~], K-major
+constexpr uint32_t SM_ZB = 64 * KiB;              // 2 x 16 KiB: z -> K'   [tok x dk]
+constexpr uint32_t SM_KB = 96 * KiB;              // 16 KiB: k -> K~       [tok x dk]
+constexpr uint32_t SM_VB = 112 * KiB;             // 16 KiB: v             [tok x dv]
+constexpr uint32_t SM_AP = 128 * KiB;             // 96 KiB work region
+constexpr uint32_t SM_APA = SM_AP;                // tf32 [Khat_2p ; Khat_2p+1]   128 x 128
+constexpr uint32_t SM_APB = SM_AP + 64 * KiB;     // tf32 [KE_2p; QE_2p; KE_2p+1; QE_2p+1] 64 x 128
+constexpr uint32_t SM_AKK = SM_AP;                // fp32 [64][65] A_kk (after the AP MMAs)
+constexpr uint32_t SM_TF = SM_AP + 64 * 65 * 4;   // fp32 [64][65] T
+constexpr uint32_t SM_TY = SM_AP + 34 * KiB;      // fp32 [3][16][17] block products
+constexpr uint32_t SM_SBF = SM_AP;                // [dk x dv] S in fp16, MN-major (after T')
+constexpr uint32_t SM_A5 = SM_AP + 48 * KiB;      // [128 x 64] K-major: [0 ; -P]
+constexpr uint32_t SM_TP = SM_AP + 64 * KiB;      // [128 x 64] K-major: [T diag(beta) ; 0]
+constexpr uint32_t SM_WBF = SM_AP + 64 * KiB;     // [tok x dv] W in fp16 (after T' is used)
+constexpr uint32_t SM_MISC = 224 * KiB;
+constexpr uint32_t MS_BAR_QZ = SM_MISC + 0;       // 2 mbarriers
+constexpr uint32_t MS_BAR_KV = SM_MISC + 16;
+constexpr uint32_t MS_BAR_MMA = SM_MISC + 24;
+constexpr uint32_t MS_TMEM = SM_MISC + 32;
+constexpr uint32_t MS_BETA = SM_MISC + 64;        // 64 fp32
+constexpr uint32_t MS_LAM = SM_MISC + 320;        // [4][128] fp32 sub-tile decay totals
+constexpr uint32_t TC_SMEM_BYTES = MS_LAM + 4 * TD * 4;
+static_assert(SM_TF + 64 * 65 * 4 <= SM_TY, "T scratch overlaps");
+static_assert(SM_TY + 3 * 16 * 17 * 4 <= SM_A5, "block scratch overlaps A5");
+static_assert(TC_SMEM_BYTES <= 232448, "shared memory budget");
+
+constexpr uint32_t A3_BYTES = 32 * KiB;
+constexpr uint32_t TILE_BYTES = 16 * KiB;   // a [64 tok x 128] bf16 tile
+constexpr uint32_t REG64 = 8 * KiB;         // one 64-column region of a 64-row tile
+constexpr uint32_t REG128 = 16 * KiB;       // one 64-column region of a 128-row tile
+// tf32 tiles: 32-column regions of 128-byte rows
+constexpr uint32_t APA_REG = 128 * 128;     // 128 rows
+constexpr uint32_t APB_REG = 64 * 128;      // 64 rows
+
+// TMEM columns.
+constexpr uint32_t TM_AP = 0;     // A_kk / P products, later Wk
+constexpr uint32_t TM_D1 = 128;   // U -> W (rows 0..63), -O (rows 64..127)
+constexpr uint32_t TM_S = 256;    // fp32 state S (row = key channel)
+constexpr uint32_t TM_COLS = 512;
+
+constexpr uint32_t kWaitPolls = 1u << 24;
+
+// Instruction descriptors (fp32 accumulation).
+constexpr uint32_t ID_AP = idesc_mma(128, 64, kFmtTF32, kFmtTF32, 0, 0);      // A_kk / P
+constexpr uint32_t ID_TPROD = idesc_mma(128, 128, kFmtBF16, kFmtBF16, 0, 1);  // T' K~, T' V
+constexpr uint32_t ID_KMN = idesc_mma(128, 128, kFmtF16, kFmtF16, 0, 1);      // K-major x MN
+constexpr uint32_t ID_MNMN = idesc_mma(128, 128, kFmtF16, kFmtF16, 1, 1);     // MN x MN
+
+struct TcParams {
+  const kda_bf16 *beta;
+  const float *A;
+  float gmin;
+  const int32_t *cu_seqlens;
+  int64_t fixed_len;
+  int H;
+  const float *S0;
+  kda_bf16 *o;
+  float *S_final;
+  float *snaps;
+  const int64_t *snap_offsets;
+  int *status;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void sts64(uint32_t a, uint32_t x, uint32_t y) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z,
+                                       uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z),
+               "r"(w)
+               : "memory");
+}
+
+__device__ __forceinline__ float ldsf(uint32_t a) { return __uint_as_float(lds32(a)); }
+
+__device__ __forceinline__ void stsf(uint32_t a, float v) { sts32(a, __float_as_uint(v)); }
+
+// Fast per-step decay exp(gmin * sigmoid(eA * z)).
+__device__ __forceinline__ float fast_decay(float gmin, float eA, float z) {
+  const float sig = __frcp_rn(1.0f + __expf(-eA * z));
+  return __expf(gmin * sig);
+}
+
+// Write 64 fp32 values (columns [64*half, 64*half + 64) of `row`) as one
+// swizzled 128-byte fp16 row of a tile whose regions are `region` bytes apart.
+__device__ __forceinline__ void store_row_f16(uint32_t tile, int row, int half, uint32_t region,
+                                              const float (&v)[64], float scale) {
+  const uint32_t base = tile + static_cast<uint32_t>(half) * region + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t pos = static_cast<uint32_t>(j ^ (row & 7)) << 4;
+    sts128(base + pos, pack_f16x2(scale * v[8 * j + 0], scale * v[8 * j + 1]),
+           pack_f16x2(scale * v[8 * j + 2], scale * v[8 * j + 3]),
+           pack_f16x2(scale * v[8 * j + 4], scale * v[8 * j + 5]),
+           pack_f16x2(scale * v[8 * j + 6], scale * v[8 * j + 7]));
+  }
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  float a[32], b[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = a[i];
+    v[32 + i] = b[i];
+  }
+}
+
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const float (&v)[64]) {
+  float a[32], b[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    a[i] = v[i];
+    b[i] = v[32 + i];
+  }
+  tmem_st32(taddr, a);
+  tmem_st32(taddr + 32, b);
+  tmem_wait_st();
+}
+
+// Issue the MMAs of one product: K-steps of 16 elements.
+// A K-major: start advances 32 B per step inside a 64-column region and jumps
+// a_region per 64 columns; MN-major: start advances 2048 B (16 rows) per step.
+// (For tf32 the same byte strides hold: a K-step is 8 elements = 32 bytes and
+// a region is 32 columns.)
+__device__ __forceinline__ void issue_mma(uint32_t d_tmem, uint32_t a_base, bool a_mn,
+                                          uint32_t a_region, uint32_t b_base, bool b_mn,
+                                          uint32_t b_region, int ksteps, uint32_t idesc,
+                                          uint32_t accumulate, bool tf32 = false) {
+  for (int ks = 0; ks < ksteps; ++ks) {
+    const uint32_t a_addr = a_mn ? a_base + static_cast<uint32_t>(ks) * 2048u
+                                 : a_base + static_cast<uint32_t>(ks >> 2) * a_region +
+                                       static_cast<uint32_t>(ks & 3) * 32u;
+    const uint32_t b_addr = b_mn ? b_base + static_cast<uint32_t>(ks) * 2048u
+                                 : b_base + static_cast<uint32_t>(ks >> 2) * b_region +
+                                       static_cast<uint32_t>(ks & 3) * 32u;
+    const uint64_t ad = sw128_desc(a_addr, a_mn ? a_region : 16u, 1024u);
+    const uint64_t bd = sw128_desc(b_addr, b_mn ? b_region : 16u, 1024u);
+    if (tf32)
+      mma_tf32(d_tmem, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
+    else
+      mma_f16(d_tmem, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
+  }
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
+                  const TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x, s = blockIdx.y;
+  const int H = p.H;
+
+  if ((sb & 1023u) != 0) {  // the swizzled layouts need 1024-byte alignment
+    if (tid == 0) atomicOr(p.status, KDA_ERR_UNSUPPORTED);
+    return;
+  }
+
+  int64_t t_begin, t_end;
+  if (p.cu_seqlens) {
+    t_begin = p.cu_seqlens[s];
+    t_end = p.cu_seqlens[s + 1];
+  } else {
+    t_begin = static_cast<int64_t>(s) * p.fixed_len;
+    t_end = t_begin + p.fixed_len;
+  }
+  const int n_chunks = static_cast<int>((t_end - t_begin + 63) / 64);
+  int64_t snap_row = 0;
+  if (p.snaps)
+    snap_row = p.snap_offsets ? p.snap_offsets[s] : static_cast<int64_t>(s) * (p.fixed_len / 64);
+  const float eA = __expf(p.A[h]);
+  const float gmin = p.gmin;
+  const size_t state_off = (static_cast<size_t>(s) * H + h) * TD * TD;
+
+  const uint32_t bar_qz0 = sb + MS_BAR_QZ, bar_kv = sb + MS_BAR_KV, bar_mma = sb + MS_BAR_MMA;
+  if (tid == 0) {
+    mbar_init(bar_qz0, 1);
+    mbar_init(bar_qz0 + 8, 1);
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_z);
+    prefetch_tensormap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + MS_TMEM, TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + MS_TMEM);
+
+  // Lane quadrant and column half each warp owns in TMEM read-outs.
+  const int quad = warp & 3, half = warp >> 2;
+  const int trow = quad * 32 + lane;  // TMEM lane = matrix row
+  const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+
+  // Initial state -> TMEM (row trow, columns [64 half, 64 half + 64)).
+  {
+    float v[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+      v[j] = p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + 64 * half + j] : 0.f;
+    tmem_st64(t_lane + TM_S + 64 * half, v);
+  }
+
+  auto issue_qz = [&](int n) {  // q -> A3[n&1] lower half, z -> ZB[n&1]
+    const int par = n & 1;
+    const int t0 = static_cast<int>(t_begin + 64LL * n);
+    const uint32_t bar = bar_qz0 + 8 * par;
+    mbar_expect_tx(bar, 2 * TILE_BYTES);
+    const uint32_t a3 = sb + SM_A3 + par * A3_BYTES;
+    tma_load_3d(a3 + 64 * 128, &tm_q, 0, h, t0, bar);
+    tma_load_3d(a3 + REG128 + 64 * 128, &tm_q, 64, h, t0, bar);
+    const uint32_t zb = sb + SM_ZB + par * TILE_BYTES;
+    tma_load_3d(zb, &tm_z, 0, h, t0, bar);
+    tma_load_3d(zb + REG64, &tm_z, 64, h, t0, bar);
+  };
+  auto issue_kv = [&](int n) {
+    const int t0 = static_cast<int>(t_begin + 64LL * n);
+    mbar_expect_tx(bar_kv, 2 * TILE_BYTES);
+    tma_load_3d(sb + SM_KB, &tm_k, 0, h, t0, bar_kv);
+    tma_load_3d(sb + SM_KB + REG64, &tm_k, 64, h, t0, bar_kv);
+    tma_load_3d(sb + SM_VB, &tm_v, 0, h, t0, bar_kv);
+    tma_load_3d(sb + SM_VB + REG64, &tm_v, 64, h, t0, bar_kv);
+  };
+
+  bool qz_pending[2] = {false, false}, kv_pending = false, mma_pending = false;
+  uint32_t mma_phase = 0;
+  bool aborted = false;
+
+  // Wait helper: every thread polls; the CTA agrees on the outcome.
+  auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+    const bool ok = mbar_wait_bounded(bar, parity, kWaitPolls);
+    const int bad = __syncthreads_or(ok ? 0 : 1);
+    if (bad) {
+      if (tid == 0) atomicOr(p.status, KDA_ERR_TIMEOUT);
+      return false;
+    }
+    return true;
+  };
+  auto wait_mma = [&]() -> bool {
+    const bool ok = wait_all(bar_mma, mma_phase);
+    if (ok) {
+      mma_phase ^= 1u;
+      mma_pending = false;
+    }
+    tc_fence_after();
+    return ok;
+  };
+
+  if (tid == 0 && n_chunks > 0) {
+    issue_qz(0);
+    issue_kv(0);
+  }
+  qz_pending[0] = kv_pending = (n_chunks > 0);
+
+  // SIMT mapping of the element phase: channel pair cp, sub-tile R.
+  const int cp = tid & 63, R = tid >> 6;
+  const int c0 = 2 * cp;
+
+  for (int n = 0; n < n_chunks && !aborted; ++n) {
+    const int par = n & 1;
+    const int64_t t0 = t_begin + 64LL * n;
+    const int L = static_cast<int>(min(static_cast<int64_t>(64), t_end - t0));
+    const uint32_t a3 = sb + SM_A3 + par * A3_BYTES;
+    const uint32_t zb = sb + SM_ZB + par * TILE_BYTES;
+
+    // Prefetch the next chunk's q and z into the other parity buffers.
+    if (tid == 0 && n + 1 < n_chunks) {
+      fence_proxy_async();
+      issue_qz(n + 1);
+    }
+    if (n + 1 < n_chunks) qz_pending[par ^ 1] = true;
+    if (tid < 64)
+      stsf(sb + MS_BETA + 4 * tid,
+           tid < L ? bf2f(p.beta[static_cast<size_t>(t0 + tid) * H + h]) : 0.f);
+    if (!wait_all(bar_qz0 + 8 * par, (n >> 1) & 1)) { aborted = true; break; }
+    qz_pending[par] = false;
+
+    // ---- element phase A: decay factors and running products in registers --------------
+    float ef0[16], ef1[16], eb0[16], eb1[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int r = 16 * R + j;
+      if (r < L) {
+        const float2 zz = unpack_bf16x2(lds32(zb + sw128_off(r, c0, REG64)));
+        ef0[j] = fast_decay(gmin, eA, zz.x);
+        ef1[j] = fast_decay(gmin, eA, zz.y);
+      } else {
+        ef0[j] = 1.f;
+        ef1[j] = 1.f;
+      }
+    }
+    eb0[15] = 1.f;
+    eb1[15] = 1.f;
+#pragma unroll
+    for (int j = 14; j >= 0; --j) {
+      eb0[j] = eb0[j + 1] * ef0[j + 1];
+      eb1[j] = eb1[j + 1] * ef1[j + 1];
+    }
+#pragma unroll
+    for (int j = 1; j < 16; ++j) {
+      ef0[j] *= ef0[j - 1];
+      ef1[j] *= ef1[j - 1];
+    }
+    stsf(sb + MS_LAM + 4 * (R * TD + c0), ef0[15]);
+    stsf(sb + MS_LAM + 4 * (R * TD + c0 + 1), ef1[15]);
+    if (!wait_all(bar_kv, n & 1)) { aborted = true; break; }  // also orders the Lam table
+    kv_pending = false;
+
+    // ---- element phase B: scaled operands, one row-block pair at a time -----------------
+    // Pass pp builds the tf32 operands of sub-tiles {2pp, 2pp+1} and runs their
+    // M128 x N64 x K128 MMA; the second pass also rewrites k, q, z in place.
+    {
+      float l0[4], l1[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        l0[m] = ldsf(sb + MS_LAM + 4 * (m * TD + c0));
+        l1[m] = ldsf(sb + MS_LAM + 4 * (m * TD + c0 + 1));
+      }
+      float x0 = 1.f, x1 = 1.f, y0 = 1.f, y1 = 1.f;  // prod_{M<R} Lam, prod_{M>R} Lam
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        if (m < R) { x0 *= l0[m]; x1 *= l1[m]; }
+        if (m > R) { y0 *= l0[m]; y1 *= l1[m]; }
+      }
+      // column factors of Khat_{R'} for R' >= R (this thread's rows are sub-tile R)
+      float f0[4], f1[4];
+#pragma unroll
+      for (int rp = 0; rp < 4; ++rp) {
+        float a = 1.f, b = 1.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          if (m > R && m < rp) { a *= l0[m]; b *= l1[m]; }
+        f0[rp] = (rp == R) ? __frcp_rn(l0[R]) : a;
+        f1[rp] = (rp == R) ? __frcp_rn(l1[R]) : b;
+      }
+      for (int pp = 0; pp < 2; ++pp) {
+        if (2 * pp + 1 >= R) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = 16 * R + j;
+            float2 kk = unpack_bf16x2(lds32(sb + SM_KB + sw128_off(r, c0, REG64)));
+            float2 qq = unpack_bf16x2(lds32(a3 + sw128_off(64 + r, c0, REG128)));
+            if (r >= L) {
+              kk = make_float2(0.f, 0.f);
+              qq = make_float2(0.f, 0.f);
+            }
+            const float ke0 = kk.x * ef0[j], ke1 = kk.y * ef1[j];
+            const float qe0 = qq.x * ef0[j], qe1 = qq.y * ef1[j];
+            const float kb0 = kk.x * eb0[j], kb1 = kk.y * eb1[j];
+            if ((R >> 1) == pp) {
+              const int lb = R - 2 * pp;
+              sts64(sb + SM_APB + sw128_off32(32 * lb + j, c0, APB_REG), to_tf32(ke0), to_tf32(ke1));
+              sts64(sb + SM_APB + sw128_off32(32 * lb + 16 + j, c0, APB_REG), to_tf32(qe0),
+                    to_tf32(qe1));
+            }
+#pragma unroll
+            for (int rl = 0; rl < 2; ++rl) {
+              const int rp = 2 * pp + rl;
+              if (rp >= R)
+                sts64(sb + SM_APA + sw128_off32(64 * rl + r, c0, APA_REG),
+                      to_tf32(kb0 * f0[rp]), to_tf32(kb1 * f1[rp]));
+            }
+            if (pp == 1) {
+              sts32(sb + SM_KB + sw128_off(r, c0, REG64), pack_bf16x2(ke0 * x0, ke1 * x1));
+              sts32(a3 + sw128_off(64 + r, c0, REG128), pack_f16x2(-qe0 * x0, -qe1 * x1));
+              sts32(zb + sw128_off(r, c0, REG64), pack_f16x2(kb0 * y0, kb1 * y1));
+            }
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+          tc_fence_after();
+          issue_mma(tmem + TM_AP + 64 * pp, sb + SM_APA, false, APA_REG, sb + SM_APB, false,
+                    APB_REG, 16, ID_AP, 0, true);
+          mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        if (!wait_mma()) break;
+      }
+      if (mma_pending) { aborted = true; break; }
+    }
+
+    // zero A5 (its upper block stays zero; -P fills the lower block)
+    for (int x = tid; x < 1024; x += TC_THREADS) sts128(sb + SM_A5 + 16 * x, 0, 0, 0, 0);
+    __syncthreads();
+    {
+      // lane trow of pair `half`: rows < 64 read columns [0, 32), rows >= 64 [32, 64)
+      float v[32];
+      tmem_ld32(t_lane + TM_AP + 64 * half + (quad >= 2 ? 32 : 0), v);
+      tmem_wait_ld();
+      const int i = trow & 63;
+      const int Rb = 2 * half + (quad >= 2 ? 1 : 0);  // sub-tile of the rows r
+      if (i < 16 * Rb + 16) {
+#pragma unroll
+        for (int nn = 0; nn < 16; ++nn) {
+          const int r = 16 * Rb + nn;
+          if (i < r)
+            stsf(sb + SM_AKK + 4 * (r * 65 + i), ldsf(sb + MS_BETA + 4 * r) * v[nn]);
+          if (i <= r) {
+            const uint32_t a = sb + SM_A5 + sw128_off(64 + r, i, REG128);
+            // 2-byte store of -P[r][i] (fp16)
+            __half hv = __float2half_rn(-v[16 + nn]);
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(a),
+                         "h"(*reinterpret_cast<unsigned short *>(&hv))
+                         : "memory");
+          }
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- T = (I + A_kk)^{-1}: diagonal 16x16 blocks, then off-diagonal by distance ------
+    if (tid < 64) {
+      const int Rd = tid >> 4, jc = tid & 15, o = 16 * Rd;
+      float col[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float acc = (r == jc) ? 1.f : 0.f;
+        if (r > jc) {
+          acc = 0.f;
+#pragma unroll
+          for (int m = 0; m < 16; ++m)
+            if (m >= jc && m < r) acc -= ldsf(sb + SM_AKK + 4 * ((o + r) * 65 + o + m)) * col[m];
+        }
+        col[r] = acc;
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) stsf(sb + SM_TF + 4 * ((o + r) * 65 + o + jc), col[r]);
+    }
+    __syncthreads();
+    for (int d = 1; d < 4; ++d) {
+      const int nb = 4 - d;  // blocks (Rr, Rr - d), Rr = d..3
+      // Y = sum_{M=J}^{Rr-1} A[Rr][M] T[M][J]
+      for (int x = tid; x < nb * 256; x += TC_THREADS) {
+        const int b = x >> 8, e = x & 255, rr = e >> 4, cc = e & 15;
+        const int Rr = d + b, J = Rr - d;
+        float acc = 0.f;
+        for (int M = J; M < Rr; ++M)
+#pragma unroll
+          for (int m = 0; m < 16; ++m)
+            acc += ldsf(sb + SM_AKK + 4 * ((16 * Rr + rr) * 65 + 16 * M + m)) *
+                   ldsf(sb + SM_TF + 4 * ((16 * M + m) * 65 + 16 * J + cc));
+        stsf(sb + SM_TY + 4 * ((b * 16 + rr) * 17 + cc), acc);
+      }
+      __syncthreads();
+      // T[Rr][J] = -T[Rr][Rr] Y
+      for (int x = tid; x < nb * 256; x += TC_THREADS) {
+        const int b = x >> 8, e = x & 255, rr = e >> 4, cc = e & 15;
+        const int Rr = d + b, J = Rr - d;
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          acc -= ldsf(sb + SM_TF + 4 * ((16 * Rr + rr) * 65 + 16 * Rr + m)) *
+                 ldsf(sb + SM_TY + 4 * ((b * 16 + m) * 17 + cc));
+        stsf(sb + SM_TF + 4 * ((16 * Rr + rr) * 65 + 16 * J + cc), acc);
+      }
+      __syncthreads();
+    }
+    // T' = T diag(beta) in bf16, K-major [128 rows x 64]; rows >= 64 and the upper triangle zero.
+    for (int x = tid; x < 128 * 8; x += TC_THREADS) {
+      const int row = x >> 3, ch = x & 7;
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      if (row < 64) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i0 = 8 * ch + 2 * e;
+          const float t0v = (i0 <= row) ? ldsf(sb + SM_TF + 4 * (row * 65 + i0)) *
+                                              ldsf(sb + MS_BETA + 4 * i0) : 0.f;
+          const float t1v = (i0 + 1 <= row) ? ldsf(sb + SM_TF + 4 * (row * 65 + i0 + 1)) *
+                                                  ldsf(sb + MS_BETA + 4 * (i0 + 1)) : 0.f;
+          w[e] = pack_bf16x2(t0v, t1v);
+        }
+      }
+      sts128(sb + SM_TP + row * 128 + (static_cast<uint32_t>(ch ^ (row & 7)) << 4), w[0], w[1],
+             w[2], w[3]);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- Wk = T' K~ -> TM_AP,  U = T' V -> D1 ---------------------------------------------
+    if (tid == 0) {
+      tc_fence_after();
+      issue_mma(tmem + TM_AP, sb + SM_TP, false, REG128, sb + SM_KB, true, REG64, 4, ID_TPROD, 0);
+      issue_mma(tmem + TM_D1, sb + SM_TP, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD, 0);
+      mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    if (!wait_mma()) { aborted = true; break; }
+    if (tid == 0 && n + 1 < n_chunks) {  // k and v of the next chunk
+      fence_proxy_async();
+      issue_kv(n + 1);
+    }
+    if (n + 1 < n_chunks) kv_pending = true;
+
+    // -Wk -> A3 rows 0..63;  S (fp32, TMEM) -> fp16 S for the MMA, then S *= e^{G_last}.
+    {
+      float v[64];
+      if (quad < 2) {
+        tmem_ld64(t_lane + TM_AP + 64 * half, v);
+        store_row_f16(a3, trow, half, REG128, v, -1.f);
+      }
+      tmem_ld64(t_lane + TM_S + 64 * half, v);
+      store_row_f16(sb + SM_SBF, trow, half, REG128, v, 1.f);
+      float gam = 1.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) gam *= ldsf(sb + MS_LAM + 4 * (m * TD + trow));
+#pragma unroll
+      for (int j = 0; j < 64; ++j) v[j] *= gam;
+      tmem_st64(t_lane + TM_S + 64 * half, v);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- D1 += [-Wk; -Q~] S: W (rows 0..63), -Q~ S (rows 64..127) --------------------------
+    if (tid == 0) {
+      tc_fence_after();
+      issue_mma(tmem + TM_D1, a3, false, REG128, sb + SM_SBF, true, REG128, 8, ID_KMN, 1);
+      mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    if (!wait_mma()) { aborted = true; break; }
+    if (quad < 2) {
+      float v[64];
+      tmem_ld64(t_lane + TM_D1 + 64 * half, v);
+      store_row_f16(sb + SM_WBF, trow, half, REG64, v, 1.f);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- S += K'^T W;  D1 += [0; -P] W -------------------------------------------------------
+    if (tid == 0) {
+      tc_fence_after();
+      issue_mma(tmem + TM_S, zb, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
+      issue_mma(tmem + TM_D1, sb + SM_A5, false, REG128, sb + SM_WBF, true, REG64, 4, ID_KMN, 1);
+      mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    if (!wait_mma()) { aborted = true; break; }
+
+    // ---- outputs: o = -D1 rows 64..127; snapshot of the new state ----------------------------
+    if (quad >= 2) {
+      const int r = trow - 64;
+      float v[64];
+      tmem_ld64(t_lane + TM_D1 + 64 * half, v);
+      if (r < L) {
+        uint4 *dst = reinterpret_cast<uint4 *>(
+            p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + 64 * half);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_uint4(pack_bf16x2(-v[8 * j + 0], -v[8 * j + 1]),
+                              pack_bf16x2(-v[8 * j + 2], -v[8 * j + 3]),
+                              pack_bf16x2(-v[8 * j + 4], -v[8 * j + 5]),
+                              pack_bf16x2(-v[8 * j + 6], -v[8 * j + 7]));
+      }
+    }
+    if (p.snaps && L == 64) {
+      float v[64];
+      tmem_ld64(t_lane + TM_S + 64 * half, v);
+      float4 *dst = reinterpret_cast<float4 *>(
+          p.snaps + (static_cast<size_t>(snap_row) * H + h) * TD * TD +
+          static_cast<size_t>(trow) * TD + 64 * half);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+    }
+    if (L == 64) ++snap_row;
+    tc_fence_before();
+    __syncthreads();
+  }
+
+  if (!aborted && p.S_final) {
+    float v[64];
+    tmem_ld64(t_lane + TM_S + 64 * half, v);
+    float4 *dst = reinterpret_cast<float4 *>(p.S_final + state_off +
+                                             static_cast<size_t>(trow) * TD + 64 * half);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  }
+
+  // Drain anything still in flight (bounded) before TMEM is released.
+  if (aborted && tid == 0) {
+    if (mma_pending) mbar_wait_bounded(bar_mma, mma_phase, kWaitPolls);
+    for (int b = 0; b < 2; ++b)
+      if (qz_pending[b]) mbar_wait_bounded(bar_qz0 + 8 * b, 0, kWaitPolls) ||
+                             mbar_wait_bounded(bar_qz0 + 8 * b, 1, kWaitPolls);
+    if (kv_pending) mbar_wait_bounded(bar_kv, 0, kWaitPolls) || mbar_wait_bounded(bar_kv, 1, kWaitPolls);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TM_COLS);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 3-D map over a [total, H, d] bf16 tensor: box = 64 channels x 1 head x 64 tokens.
+bool make_map(CUtensorMap *m, const void *base, int64_t total, int H, int d) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(total)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(d) * 2 * H};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int dk, int dv, int64_t total_tokens) {
+  return dk == TD && dv == TD && total_tokens > 0 && total_tokens < (1LL << 31);
+}
+
+cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                              const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                              const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
+                              int64_t fixed_len, int H, const float *S0, kda_bf16 *o,
+                              float *S_final, float *snaps, const int64_t *snap_offsets,
+                              int *status, cudaStream_t stream) {
+  CUtensorMap mq, mk, mz, mv;
+  if (!make_map(&mq, q, total_tokens, H, TD) || !make_map(&mk, k, total_tokens, H, TD) ||
+      !make_map(&mz, z, total_tokens, H, TD) || !make_map(&mv, v, total_tokens, H, TD))
+    return cudaErrorInvalidValue;
+  cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(TC_SMEM_BYTES));
+  if (err != cudaSuccess) return err;
+  TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, H, S0, o, S_final, snaps, snap_offsets,
+               status};
+  const dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(n_seq));
+  prefill_tc_kernel<<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(mq, mk, mz, mv, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

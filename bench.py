@@ -242,9 +242,11 @@ def run_ours(args, rank, world, local):
     kda.build()
     kda.lib()
     hbm_peak, tc_peak, tc_sus, peak_src = load_peaks()
-    w = kda_inputs.WORKLOADS[WORKLOAD]
+    w = dict(kda_inputs.WORKLOADS[WORKLOAD])
+    if args.seq_len:
+        w["T"] = args.seq_len
     B, H, T, dk, dv = w["B"], w["H"], w["T"], w["dk"], w["dv"]
-    x = kda_inputs.make_workload_prefill(WORKLOAD, device=dev)
+    x = kda_inputs.make_workload_prefill(WORKLOAD, device=dev, T=T)
     offs = kda.snapshot_offsets(x["lengths"], device=dev)
     snaps = torch.empty((int(offs[-1]), H, dk, dv), dtype=torch.float32, device=dev)
     S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
@@ -298,7 +300,38 @@ def run_ours(args, rank, world, local):
                            "peak_tflops": tc_peak,
                            "frac": alg_flops / avg_launch_s / 1e12 / tc_peak}}
 
-    # end to end: pinned host inputs -> device -> kda_chunk_fwd -> host outputs
+    e2e = None if args.no_e2e else run_e2e(args, x, o, S_final, snaps, offs, stream, world, B, T)
+    decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak, peak_src, world)
+
+    cpu_baseline = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        cat, n_tok = oracle_sample(x, args.ref_tokens)
+        dts = time_oracle(cat, 1)
+        cpu_baseline = {"value": n_tok / dts[0], "unit": UNIT, "cores": oracle.num_threads(),
+                        "kind": "oracle",
+                        "sample": f"first {args.ref_tokens} tokens of each of the {B} sequences,"
+                                  f" all {H} heads ({n_tok * H} token-heads), snapshots on"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": kda_dtype(),
+                "data": "synthetic", "config": workload_config(w),
+                "clocks": clocks.summary(), "roofline": roofline, "cpu_baseline": cpu_baseline,
+                "e2e": e2e, "gpu_launches": args.steps, "decode": decode}
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, x, o, S_final, snaps, offs, stream, world, B, T):
+    """The same step through the public API with host buffers: pinned host
+    inputs -> device -> kda_chunk_fwd -> host outputs, all inside the timed
+    region."""
+    import torch
+
+    import linear_attention_serving_chunk_gb300 as kda
+    dev = o.device
     host_in = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "z", "beta", "A",
                                                      "cu_seqlens")}
     host_out = {"o": torch.empty_like(o, device="cpu").pin_memory(),
@@ -333,28 +366,8 @@ def run_ours(args, rank, world, local):
     e2e = {"value": B * T * e2e_steps * world / (e2e_ms / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     del host_in, host_out, dev_in
+    return e2e
 
-    decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak, peak_src, world)
-
-    cpu_baseline = None
-    if rank == 0 and not args.no_cpu_baseline:
-        import oracle
-        cat, n_tok = oracle_sample(x, args.ref_tokens)
-        dts = time_oracle(cat, 1)
-        cpu_baseline = {"value": n_tok / dts[0], "unit": UNIT, "cores": oracle.num_threads(),
-                        "kind": "oracle",
-                        "sample": f"first {args.ref_tokens} tokens of each of the {B} sequences,"
-                                  f" all {H} heads ({n_tok * H} token-heads), snapshots on"}
-
-    if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": kda_dtype(),
-                "data": "synthetic", "config": workload_config(w),
-                "clocks": clocks.summary(), "roofline": roofline, "cpu_baseline": cpu_baseline,
-                "e2e": e2e, "gpu_launches": args.steps, "decode": decode}
-        print(json.dumps(line), flush=True)
 
 
 def kda_dtype():
@@ -412,7 +425,7 @@ def run_decode(args, dev, stream, hbm_peak, peak_src, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--decode-steps", type=int, default=1000)
@@ -422,6 +435,9 @@ def main(argv=None):
                     help="tokens per sequence in the oracle's bounded sample")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per prefill launch, when measured for this kernel")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override T of the prefill workload (small cases for profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     rank, world, local = dist_setup(args.gpus)

@@ -19,6 +19,9 @@ from .build import LIB_PATH, build  # noqa: F401  (re-exported)
 
 GMIN = -5.0   # "Kimi K3 Technical Report - Open Frontier Intelligence", sec. 2.1.1
 CHUNK = 64
+# Arithmetic of the dk = dv = 128 prefill: bf16 in/out with tf32 / bf16 / fp16
+# tensor-core operands, fp32 accumulation and fp32 state.
+PREFILL_COMPUTE_DTYPE = "bf16"
 
 KDA_OK = 0
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_ALIGN",

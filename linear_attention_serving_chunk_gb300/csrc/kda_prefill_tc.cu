@@ -22,11 +22,12 @@
 // Operand precision: the A_kk / P products need the 8-bit exponent range
 // (factors up to e^80) and more than bf16's 8-bit mantissa (outputs are
 // heavy-tailed and P feeds them directly), so they run as kind::tf32
-// (10-bit mantissa).  T' K~ and T' V use bf16 (V arrives as bf16).  The
+// (10-bit mantissa, operands rounded to nearest).  T' K~ and T' V use bf16
+// (V arrives as bf16).  The
 // state-dependent products use fp16 operands (11-bit mantissa; |S|, |W|,
 // |Wk| stay far below 65504 for unit keys and beta in [0, 1]).
 //
-// Per chunk (one CTA per (sequence, head), 256 threads, chunks in order):
+// Per chunk (one CTA per (sequence, head), 512 threads, chunks in order):
 //   TMA     q -> A3 lower half, z -> ZB, k -> KB, v -> VB (next chunk's q/z
 //           double-buffered, k/v refilled as soon as their MMAs finish)
 //   SIMT    gate exp(g), per-sub-tile running products, then every scaled
@@ -50,7 +51,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int TC_THREADS = 256;
+constexpr int TC_THREADS = 512;
 constexpr int TD = 128;  // dk = dv handled by this kernel
 constexpr uint32_t KiB = 1024;
 
@@ -132,81 +133,69 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
+// Shared memory seen by the threads: plain C++ accesses (so the compiler can
+// schedule and overlap them) addressed by the same 32-bit shared-window
+// addresses the descriptors and TMA use.
+struct Smem {
+  uint8_t *base;
+  uint32_t sb;
+  __device__ __forceinline__ uint8_t *ptr(uint32_t a) const { return base + (a - sb); }
+  __device__ __forceinline__ uint32_t &u32(uint32_t a) const {
+    return *reinterpret_cast<uint32_t *>(ptr(a));
+  }
+  __device__ __forceinline__ float &f32(uint32_t a) const {
+    return *reinterpret_cast<float *>(ptr(a));
+  }
+  __device__ __forceinline__ uint2 &u64(uint32_t a) const {
+    return *reinterpret_cast<uint2 *>(ptr(a));
+  }
+  __device__ __forceinline__ uint4 &u128(uint32_t a) const {
+    return *reinterpret_cast<uint4 *>(ptr(a));
+  }
+  __device__ __forceinline__ unsigned short &u16(uint32_t a) const {
+    return *reinterpret_cast<unsigned short *>(ptr(a));
+  }
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-__device__ __forceinline__ void sts64(uint32_t a, uint32_t x, uint32_t y) {
-  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+// Per-step decay exp(gmin * sigmoid(eA * z)) with the base-2 constants folded
+// in: c1 = -eA log2(e), c2 = gmin log2(e).  z = +inf gives e^gmin, z = -inf 1.
+__device__ __forceinline__ float fast_decay2(float c1, float c2, float z) {
+  return ex2_approx(c2 * rcp_approx(1.0f + ex2_approx(c1 * z)));
 }
 
-__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z,
-                                       uint32_t w) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z),
-               "r"(w)
-               : "memory");
-}
-
-__device__ __forceinline__ float ldsf(uint32_t a) { return __uint_as_float(lds32(a)); }
-
-__device__ __forceinline__ void stsf(uint32_t a, float v) { sts32(a, __float_as_uint(v)); }
-
-// Fast per-step decay exp(gmin * sigmoid(eA * z)).
-__device__ __forceinline__ float fast_decay(float gmin, float eA, float z) {
-  const float sig = __frcp_rn(1.0f + __expf(-eA * z));
-  return __expf(gmin * sig);
-}
-
-// Write 64 fp32 values (columns [64*half, 64*half + 64) of `row`) as one
-// swizzled 128-byte fp16 row of a tile whose regions are `region` bytes apart.
-__device__ __forceinline__ void store_row_f16(uint32_t tile, int row, int half, uint32_t region,
-                                              const float (&v)[64], float scale) {
-  const uint32_t base = tile + static_cast<uint32_t>(half) * region + static_cast<uint32_t>(row) * 128u;
+// Write 32 fp32 values (columns [32 q4, 32 q4 + 32) of `row`) as fp16 into a
+// 128-byte-swizzled tile whose 64-column regions are `region` bytes apart.
+__device__ __forceinline__ void store_row32_f16(const Smem &S, uint32_t tile, int row, int q4,
+                                                uint32_t region, const float (&v)[32],
+                                                float scale) {
+  const uint32_t base =
+      tile + static_cast<uint32_t>(q4 >> 1) * region + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t pos = static_cast<uint32_t>(j ^ (row & 7)) << 4;
-    sts128(base + pos, pack_f16x2(scale * v[8 * j + 0], scale * v[8 * j + 1]),
-           pack_f16x2(scale * v[8 * j + 2], scale * v[8 * j + 3]),
-           pack_f16x2(scale * v[8 * j + 4], scale * v[8 * j + 5]),
-           pack_f16x2(scale * v[8 * j + 6], scale * v[8 * j + 7]));
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t pos = static_cast<uint32_t>((4 * (q4 & 1) + j) ^ (row & 7)) << 4;
+    S.u128(base + pos) = make_uint4(pack_f16x2(scale * v[8 * j + 0], scale * v[8 * j + 1]),
+                                    pack_f16x2(scale * v[8 * j + 2], scale * v[8 * j + 3]),
+                                    pack_f16x2(scale * v[8 * j + 4], scale * v[8 * j + 5]),
+                                    pack_f16x2(scale * v[8 * j + 6], scale * v[8 * j + 7]));
   }
 }
 
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  float a[32], b[32];
-  tmem_ld32(taddr, a);
-  tmem_ld32(taddr + 32, b);
-  tmem_wait_ld();
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    v[i] = a[i];
-    v[32 + i] = b[i];
-  }
-}
-
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const float (&v)[64]) {
-  float a[32], b[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    a[i] = v[i];
-    b[i] = v[32 + i];
-  }
-  tmem_st32(taddr, a);
-  tmem_st32(taddr + 32, b);
-  tmem_wait_st();
-}
-
-// Issue the MMAs of one product: K-steps of 16 elements.
-// A K-major: start advances 32 B per step inside a 64-column region and jumps
-// a_region per 64 columns; MN-major: start advances 2048 B (16 rows) per step.
-// (For tf32 the same byte strides hold: a K-step is 8 elements = 32 bytes and
-// a region is 32 columns.)
+// Issue the MMAs of one product: K-steps of 16 elements (8 for tf32, the same
+// 32 bytes).  K-major operands advance 32 bytes per step inside a 128-byte
+// row and jump one region per 4 steps; MN-major operands advance 2048 bytes
+// (16 rows) per step and find their 64-element MN blocks `region` apart.
 __device__ __forceinline__ void issue_mma(uint32_t d_tmem, uint32_t a_base, bool a_mn,
                                           uint32_t a_region, uint32_t b_base, bool b_mn,
                                           uint32_t b_region, int ksteps, uint32_t idesc,
@@ -233,6 +222,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
+  const Smem S{smem, sb};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, s = blockIdx.y;
   const int H = p.H;
@@ -254,8 +244,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   int64_t snap_row = 0;
   if (p.snaps)
     snap_row = p.snap_offsets ? p.snap_offsets[s] : static_cast<int64_t>(s) * (p.fixed_len / 64);
-  const float eA = __expf(p.A[h]);
-  const float gmin = p.gmin;
+  const float kLog2e = 1.4426950408889634f;
+  const float dc1 = -__expf(p.A[h]) * kLog2e, dc2 = p.gmin * kLog2e;
   const size_t state_off = (static_cast<size_t>(s) * H + h) * TD * TD;
 
   const uint32_t bar_qz0 = sb + MS_BAR_QZ, bar_kv = sb + MS_BAR_KV, bar_mma = sb + MS_BAR_MMA;
@@ -279,18 +269,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + MS_TMEM);
 
-  // Lane quadrant and column half each warp owns in TMEM read-outs.
-  const int quad = warp & 3, half = warp >> 2;
+  // TMEM read-outs: a warp reaches the 32 lanes of its quadrant; the 16 warps
+  // split the columns in quarters.
+  const int quad = warp & 3, q4 = warp >> 2;
   const int trow = quad * 32 + lane;  // TMEM lane = matrix row
   const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
 
-  // Initial state -> TMEM (row trow, columns [64 half, 64 half + 64)).
+  // Initial state -> TMEM (row trow, columns [32 q4, 32 q4 + 32)).
   {
-    float v[64];
+    float v[32];
 #pragma unroll
-    for (int j = 0; j < 64; ++j)
-      v[j] = p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + 64 * half + j] : 0.f;
-    tmem_st64(t_lane + TM_S + 64 * half, v);
+    for (int j = 0; j < 32; ++j)
+      v[j] = p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + 32 * q4 + j] : 0.f;
+    tmem_st32(t_lane + TM_S + 32 * q4, v);
+    tmem_wait_st();
   }
 
   auto issue_qz = [&](int n) {  // q -> A3[n&1] lower half, z -> ZB[n&1]
@@ -344,9 +336,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   qz_pending[0] = kv_pending = (n_chunks > 0);
 
-  // SIMT mapping of the element phase: channel pair cp, sub-tile R.
-  const int cp = tid & 63, R = tid >> 6;
+  // Element-phase mapping: channel pair cp (channels c0, c0 + 1), sub-tile R,
+  // and half hf of the sub-tile's rows.  Thread rows, in order, are
+  //   r(j) = 16 R + 4 hf + (j & 3) + 8 (j >> 2),  j = 0..7,
+  // i.e. the two 4-row segments hf and 2 + hf of the sub-tile; the partner
+  // holding the other two segments is lane ^ 16.  A row's swizzle phase is
+  // 4 hf + (j & 3), so the two half-warps touch disjoint banks.
+  const int hf = lane >> 4;
+  const int cp = (warp & 3) * 16 + (lane & 15), R = warp >> 2;
   const int c0 = 2 * cp;
+  uint32_t sw16[4], sw32[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int ph = 4 * hf + t;
+    sw16[t] = (static_cast<uint32_t>(((c0 >> 3) & 7) ^ ph) << 4) + static_cast<uint32_t>(c0 & 7) * 2u;
+    sw32[t] = (static_cast<uint32_t>(((c0 >> 2) & 7) ^ ph) << 4) + static_cast<uint32_t>(c0 & 3) * 4u;
+  }
+  const uint32_t rg16_64 = static_cast<uint32_t>(c0 >> 6) * REG64;    // 64-row 2-byte tiles
+  const uint32_t rg16_128 = static_cast<uint32_t>(c0 >> 6) * REG128;  // 128-row 2-byte tiles
+  const uint32_t rg32_a = static_cast<uint32_t>(c0 >> 5) * APA_REG;   // tf32 APA
+  const uint32_t rg32_b = static_cast<uint32_t>(c0 >> 5) * APB_REG;   // tf32 APB
+  const int rbase = 16 * R + 4 * hf;
 
   for (int n = 0; n < n_chunks && !aborted; ++n) {
     const int par = n & 1;
@@ -362,51 +372,87 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     if (n + 1 < n_chunks) qz_pending[par ^ 1] = true;
     if (tid < 64)
-      stsf(sb + MS_BETA + 4 * tid,
-           tid < L ? bf2f(p.beta[static_cast<size_t>(t0 + tid) * H + h]) : 0.f);
+      S.f32(sb + MS_BETA + 4 * tid) =
+          tid < L ? bf2f(p.beta[static_cast<size_t>(t0 + tid) * H + h]) : 0.f;
     if (!wait_all(bar_qz0 + 8 * par, (n >> 1) & 1)) { aborted = true; break; }
     qz_pending[par] = false;
 
-    // ---- element phase A: decay factors and running products in registers --------------
-    float ef0[16], ef1[16], eb0[16], eb1[16];
+    // ---- element phase A: decay factors and their running products ---------------------
+    float ef0[8], ef1[8], eb0[8], eb1[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int r = 16 * R + j;
+    for (int j = 0; j < 8; ++j) {
+      const int r = rbase + (j & 3) + 8 * (j >> 2);
       if (r < L) {
-        const float2 zz = unpack_bf16x2(lds32(zb + sw128_off(r, c0, REG64)));
-        ef0[j] = fast_decay(gmin, eA, zz.x);
-        ef1[j] = fast_decay(gmin, eA, zz.y);
+        const float2 zz =
+            unpack_bf16x2(S.u32(zb + rg16_64 + static_cast<uint32_t>(r) * 128u + sw16[j & 3]));
+        ef0[j] = fast_decay2(dc1, dc2, zz.x);
+        ef1[j] = fast_decay2(dc1, dc2, zz.y);
       } else {
         ef0[j] = 1.f;
         ef1[j] = 1.f;
       }
     }
-    eb0[15] = 1.f;
-    eb1[15] = 1.f;
+    // segment-local backward products (rows after j inside its 4-row segment)
 #pragma unroll
-    for (int j = 14; j >= 0; --j) {
-      eb0[j] = eb0[j + 1] * ef0[j + 1];
-      eb1[j] = eb1[j + 1] * ef1[j + 1];
-    }
+    for (int sg = 0; sg < 2; ++sg) {
+      eb0[4 * sg + 3] = 1.f;
+      eb1[4 * sg + 3] = 1.f;
 #pragma unroll
-    for (int j = 1; j < 16; ++j) {
-      ef0[j] *= ef0[j - 1];
-      ef1[j] *= ef1[j - 1];
+      for (int j = 2; j >= 0; --j) {
+        eb0[4 * sg + j] = eb0[4 * sg + j + 1] * ef0[4 * sg + j + 1];
+        eb1[4 * sg + j] = eb1[4 * sg + j + 1] * ef1[4 * sg + j + 1];
+      }
+#pragma unroll
+      for (int j = 1; j < 4; ++j) {
+        ef0[4 * sg + j] *= ef0[4 * sg + j - 1];
+        ef1[4 * sg + j] *= ef1[4 * sg + j - 1];
+      }
     }
-    stsf(sb + MS_LAM + 4 * (R * TD + c0), ef0[15]);
-    stsf(sb + MS_LAM + 4 * (R * TD + c0 + 1), ef1[15]);
+    {
+      // Segment totals of the whole sub-tile: T_hf, T_2+hf here, the others at lane ^ 16.
+      const float ta0 = ef0[3], tb0 = ef0[7], ta1 = ef1[3], tb1 = ef1[7];
+      const float pa0 = __shfl_xor_sync(0xffffffffu, ta0, 16);
+      const float pb0 = __shfl_xor_sync(0xffffffffu, tb0, 16);
+      const float pa1 = __shfl_xor_sync(0xffffffffu, ta1, 16);
+      const float pb1 = __shfl_xor_sync(0xffffffffu, tb1, 16);
+      // segments in row order: s0 = (hf0, A), s1 = (hf1, A), s2 = (hf0, B), s3 = (hf1, B)
+      const float s00 = hf ? pa0 : ta0, s10 = hf ? ta0 : pa0, s20 = hf ? pb0 : tb0, s30 = hf ? tb0 : pb0;
+      const float s01 = hf ? pa1 : ta1, s11 = hf ? ta1 : pa1, s21 = hf ? pb1 : tb1, s31 = hf ? tb1 : pb1;
+      // prefix before and suffix after each of this thread's segments
+      const float preA0 = hf ? s00 : 1.f, preB0 = hf ? s00 * s10 * s20 : s00 * s10;
+      const float preA1 = hf ? s01 : 1.f, preB1 = hf ? s01 * s11 * s21 : s01 * s11;
+      const float sufA0 = hf ? s20 * s30 : s10 * s20 * s30, sufB0 = hf ? 1.f : s30;
+      const float sufA1 = hf ? s21 * s31 : s11 * s21 * s31, sufB1 = hf ? 1.f : s31;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        ef0[j] *= preA0;
+        ef1[j] *= preA1;
+        eb0[j] *= sufA0;
+        eb1[j] *= sufA1;
+        ef0[4 + j] *= preB0;
+        ef1[4 + j] *= preB1;
+        eb0[4 + j] *= sufB0;
+        eb1[4 + j] *= sufB1;
+      }
+      if (hf == 0) {
+        S.f32(sb + MS_LAM + 4 * (R * TD + c0)) = s00 * s10 * s20 * s30;
+        S.f32(sb + MS_LAM + 4 * (R * TD + c0 + 1)) = s01 * s11 * s21 * s31;
+      }
+    }
     if (!wait_all(bar_kv, n & 1)) { aborted = true; break; }  // also orders the Lam table
     kv_pending = false;
 
     // ---- element phase B: scaled operands, one row-block pair at a time -----------------
     // Pass pp builds the tf32 operands of sub-tiles {2pp, 2pp+1} and runs their
     // M128 x N64 x K128 MMA; the second pass also rewrites k, q, z in place.
+    // The tf32 operands are rounded to nearest (truncation would bias the
+    // 128-term sums).
     {
       float l0[4], l1[4];
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        l0[m] = ldsf(sb + MS_LAM + 4 * (m * TD + c0));
-        l1[m] = ldsf(sb + MS_LAM + 4 * (m * TD + c0 + 1));
+        l0[m] = S.f32(sb + MS_LAM + 4 * (m * TD + c0));
+        l1[m] = S.f32(sb + MS_LAM + 4 * (m * TD + c0 + 1));
       }
       float x0 = 1.f, x1 = 1.f, y0 = 1.f, y1 = 1.f;  // prod_{M<R} Lam, prod_{M>R} Lam
 #pragma unroll
@@ -422,16 +468,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           if (m > R && m < rp) { a *= l0[m]; b *= l1[m]; }
-        f0[rp] = (rp == R) ? __frcp_rn(l0[R]) : a;
-        f1[rp] = (rp == R) ? __frcp_rn(l1[R]) : b;
+        f0[rp] = (rp == R) ? rcp_approx(l0[R]) : a;
+        f1[rp] = (rp == R) ? rcp_approx(l1[R]) : b;
       }
       for (int pp = 0; pp < 2; ++pp) {
         if (2 * pp + 1 >= R) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = 16 * R + j;
-            float2 kk = unpack_bf16x2(lds32(sb + SM_KB + sw128_off(r, c0, REG64)));
-            float2 qq = unpack_bf16x2(lds32(a3 + sw128_off(64 + r, c0, REG128)));
+          for (int j = 0; j < 8; ++j) {
+            const int r = rbase + (j & 3) + 8 * (j >> 2);
+            const uint32_t ro = static_cast<uint32_t>(r) * 128u;
+            const uint32_t o16 = ro + sw16[j & 3];
+            const uint32_t o32 = ro + sw32[j & 3];
+            const uint32_t a_kb = sb + SM_KB + rg16_64 + o16;
+            const uint32_t a_q = a3 + rg16_128 + 64 * 128 + o16;
+            const uint32_t a_z = zb + rg16_64 + o16;
+            float2 kk = unpack_bf16x2(S.u32(a_kb));
+            float2 qq = unpack_bf16x2(S.u32(a_q));
             if (r >= L) {
               kk = make_float2(0.f, 0.f);
               qq = make_float2(0.f, 0.f);
@@ -440,22 +492,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float qe0 = qq.x * ef0[j], qe1 = qq.y * ef1[j];
             const float kb0 = kk.x * eb0[j], kb1 = kk.y * eb1[j];
             if ((R >> 1) == pp) {
-              const int lb = R - 2 * pp;
-              sts64(sb + SM_APB + sw128_off32(32 * lb + j, c0, APB_REG), to_tf32(ke0), to_tf32(ke1));
-              sts64(sb + SM_APB + sw128_off32(32 * lb + 16 + j, c0, APB_REG), to_tf32(qe0),
-                    to_tf32(qe1));
+              // rows 32 lb + (r - 16R) (KE) and +16 (QE), lb = R - 2pp:
+              // byte offset r * 128 + 2048 R - 8192 pp, same swizzle phase as r
+              const uint32_t ab = sb + SM_APB + rg32_b + o32 + 2048u * R - 8192u * pp;
+              S.u64(ab) = make_uint2(to_tf32(ke0), to_tf32(ke1));
+              S.u64(ab + 16 * 128) = make_uint2(to_tf32(qe0), to_tf32(qe1));
             }
 #pragma unroll
             for (int rl = 0; rl < 2; ++rl) {
               const int rp = 2 * pp + rl;
               if (rp >= R)
-                sts64(sb + SM_APA + sw128_off32(64 * rl + r, c0, APA_REG),
-                      to_tf32(kb0 * f0[rp]), to_tf32(kb1 * f1[rp]));
+                S.u64(sb + SM_APA + rg32_a + 64 * 128 * rl + o32) =
+                    make_uint2(to_tf32(kb0 * f0[rp]), to_tf32(kb1 * f1[rp]));
             }
             if (pp == 1) {
-              sts32(sb + SM_KB + sw128_off(r, c0, REG64), pack_bf16x2(ke0 * x0, ke1 * x1));
-              sts32(a3 + sw128_off(64 + r, c0, REG128), pack_f16x2(-qe0 * x0, -qe1 * x1));
-              sts32(zb + sw128_off(r, c0, REG64), pack_f16x2(kb0 * y0, kb1 * y1));
+              S.u32(a_kb) = pack_bf16x2(ke0 * x0, ke1 * x1);
+              S.u32(a_q) = pack_f16x2(-qe0 * x0, -qe1 * x1);
+              S.u32(a_z) = pack_f16x2(kb0 * y0, kb1 * y1);
             }
           }
         }
@@ -475,28 +528,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 
     // zero A5 (its upper block stays zero; -P fills the lower block)
-    for (int x = tid; x < 1024; x += TC_THREADS) sts128(sb + SM_A5 + 16 * x, 0, 0, 0, 0);
+    for (int x = tid; x < 1024; x += TC_THREADS) S.u128(sb + SM_A5 + 16 * x) = make_uint4(0, 0, 0, 0);
     __syncthreads();
     {
-      // lane trow of pair `half`: rows < 64 read columns [0, 32), rows >= 64 [32, 64)
-      float v[32];
-      tmem_ld32(t_lane + TM_AP + 64 * half + (quad >= 2 ? 32 : 0), v);
+      // Pair q4 >> 1 of the products: lanes < 64 (rows i of Khat_2pair) hold
+      // columns [0, 32), lanes >= 64 (Khat_2pair+1) columns [32, 64); the
+      // first 16 of them are A_kk / beta, the next 16 P.  q4 & 1 picks which.
+      const int pair = q4 >> 1, sub = q4 & 1;
+      float v[16];
+      tmem_ld16(t_lane + TM_AP + 64 * pair + (quad >= 2 ? 32 : 0) + 16 * sub, v);
       tmem_wait_ld();
       const int i = trow & 63;
-      const int Rb = 2 * half + (quad >= 2 ? 1 : 0);  // sub-tile of the rows r
+      const int Rb = 2 * pair + (quad >= 2 ? 1 : 0);  // sub-tile of the rows r
       if (i < 16 * Rb + 16) {
 #pragma unroll
         for (int nn = 0; nn < 16; ++nn) {
           const int r = 16 * Rb + nn;
-          if (i < r)
-            stsf(sb + SM_AKK + 4 * (r * 65 + i), ldsf(sb + MS_BETA + 4 * r) * v[nn]);
-          if (i <= r) {
-            const uint32_t a = sb + SM_A5 + sw128_off(64 + r, i, REG128);
-            // 2-byte store of -P[r][i] (fp16)
-            __half hv = __float2half_rn(-v[16 + nn]);
-            asm volatile("st.shared.b16 [%0], %1;" ::"r"(a),
-                         "h"(*reinterpret_cast<unsigned short *>(&hv))
-                         : "memory");
+          if (sub == 0) {
+            if (i < r) S.f32(sb + SM_AKK + 4 * (r * 65 + i)) = S.f32(sb + MS_BETA + 4 * r) * v[nn];
+          } else if (i <= r) {
+            __half hv = __float2half_rn(-v[nn]);  // -P[r][i] in fp16
+            S.u16(sb + SM_A5 + sw128_off(64 + r, i, REG128)) = *reinterpret_cast<unsigned short *>(&hv);
           }
         }
       }
@@ -505,21 +557,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     // ---- T = (I + A_kk)^{-1}: diagonal 16x16 blocks, then off-diagonal by distance ------
     if (tid < 64) {
+      // column jc of the inverse of diagonal block Rd, by column updates: once
+      // x[m] is final, subtract A[r][m] x[m] from every later row r.
       const int Rd = tid >> 4, jc = tid & 15, o = 16 * Rd;
-      float col[16];
+      float x[16];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float acc = (r == jc) ? 1.f : 0.f;
-        if (r > jc) {
-          acc = 0.f;
+      for (int r = 0; r < 16; ++r) x[r] = (r == jc) ? 1.f : 0.f;
 #pragma unroll
-          for (int m = 0; m < 16; ++m)
-            if (m >= jc && m < r) acc -= ldsf(sb + SM_AKK + 4 * ((o + r) * 65 + o + m)) * col[m];
-        }
-        col[r] = acc;
+      for (int m = 0; m < 15; ++m) {
+#pragma unroll
+        for (int r = m + 1; r < 16; ++r)
+          x[r] -= S.f32(sb + SM_AKK + 4 * ((o + r) * 65 + o + m)) * x[m];
       }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) stsf(sb + SM_TF + 4 * ((o + r) * 65 + o + jc), col[r]);
+      for (int r = 0; r < 16; ++r) S.f32(sb + SM_TF + 4 * ((o + r) * 65 + o + jc)) = x[r];
     }
     __syncthreads();
     for (int d = 1; d < 4; ++d) {
@@ -532,9 +583,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int M = J; M < Rr; ++M)
 #pragma unroll
           for (int m = 0; m < 16; ++m)
-            acc += ldsf(sb + SM_AKK + 4 * ((16 * Rr + rr) * 65 + 16 * M + m)) *
-                   ldsf(sb + SM_TF + 4 * ((16 * M + m) * 65 + 16 * J + cc));
-        stsf(sb + SM_TY + 4 * ((b * 16 + rr) * 17 + cc), acc);
+            acc += S.f32(sb + SM_AKK + 4 * ((16 * Rr + rr) * 65 + 16 * M + m)) *
+                   S.f32(sb + SM_TF + 4 * ((16 * M + m) * 65 + 16 * J + cc));
+        S.f32(sb + SM_TY + 4 * ((b * 16 + rr) * 17 + cc)) = acc;
       }
       __syncthreads();
       // T[Rr][J] = -T[Rr][Rr] Y
@@ -544,9 +595,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float acc = 0.f;
 #pragma unroll
         for (int m = 0; m < 16; ++m)
-          acc -= ldsf(sb + SM_TF + 4 * ((16 * Rr + rr) * 65 + 16 * Rr + m)) *
-                 ldsf(sb + SM_TY + 4 * ((b * 16 + m) * 17 + cc));
-        stsf(sb + SM_TF + 4 * ((16 * Rr + rr) * 65 + 16 * J + cc), acc);
+          acc -= S.f32(sb + SM_TF + 4 * ((16 * Rr + rr) * 65 + 16 * Rr + m)) *
+                 S.f32(sb + SM_TY + 4 * ((b * 16 + m) * 17 + cc));
+        S.f32(sb + SM_TF + 4 * ((16 * Rr + rr) * 65 + 16 * J + cc)) = acc;
       }
       __syncthreads();
     }
@@ -558,15 +609,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i0 = 8 * ch + 2 * e;
-          const float t0v = (i0 <= row) ? ldsf(sb + SM_TF + 4 * (row * 65 + i0)) *
-                                              ldsf(sb + MS_BETA + 4 * i0) : 0.f;
-          const float t1v = (i0 + 1 <= row) ? ldsf(sb + SM_TF + 4 * (row * 65 + i0 + 1)) *
-                                                  ldsf(sb + MS_BETA + 4 * (i0 + 1)) : 0.f;
+          const float t0v = (i0 <= row) ? S.f32(sb + SM_TF + 4 * (row * 65 + i0)) *
+                                              S.f32(sb + MS_BETA + 4 * i0) : 0.f;
+          const float t1v = (i0 + 1 <= row) ? S.f32(sb + SM_TF + 4 * (row * 65 + i0 + 1)) *
+                                                  S.f32(sb + MS_BETA + 4 * (i0 + 1)) : 0.f;
           w[e] = pack_bf16x2(t0v, t1v);
         }
       }
-      sts128(sb + SM_TP + row * 128 + (static_cast<uint32_t>(ch ^ (row & 7)) << 4), w[0], w[1],
-             w[2], w[3]);
+      S.u128(sb + SM_TP + row * 128 + (static_cast<uint32_t>(ch ^ (row & 7)) << 4)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -589,19 +640,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     // -Wk -> A3 rows 0..63;  S (fp32, TMEM) -> fp16 S for the MMA, then S *= e^{G_last}.
     {
-      float v[64];
+      float v[32];
       if (quad < 2) {
-        tmem_ld64(t_lane + TM_AP + 64 * half, v);
-        store_row_f16(a3, trow, half, REG128, v, -1.f);
+        tmem_ld32(t_lane + TM_AP + 32 * q4, v);
+        tmem_wait_ld();
+        store_row32_f16(S, a3, trow, q4, REG128, v, -1.f);
       }
-      tmem_ld64(t_lane + TM_S + 64 * half, v);
-      store_row_f16(sb + SM_SBF, trow, half, REG128, v, 1.f);
+      tmem_ld32(t_lane + TM_S + 32 * q4, v);
+      tmem_wait_ld();
+      store_row32_f16(S, sb + SM_SBF, trow, q4, REG128, v, 1.f);
       float gam = 1.f;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) gam *= ldsf(sb + MS_LAM + 4 * (m * TD + trow));
+      for (int m = 0; m < 4; ++m) gam *= S.f32(sb + MS_LAM + 4 * (m * TD + trow));
 #pragma unroll
-      for (int j = 0; j < 64; ++j) v[j] *= gam;
-      tmem_st64(t_lane + TM_S + 64 * half, v);
+      for (int j = 0; j < 32; ++j) v[j] *= gam;
+      tmem_st32(t_lane + TM_S + 32 * q4, v);
+      tmem_wait_st();
     }
     fence_proxy_async();
     tc_fence_before();
@@ -616,9 +670,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mma_pending = true;
     if (!wait_mma()) { aborted = true; break; }
     if (quad < 2) {
-      float v[64];
-      tmem_ld64(t_lane + TM_D1 + 64 * half, v);
-      store_row_f16(sb + SM_WBF, trow, half, REG64, v, 1.f);
+      float v[32];
+      tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
+      tmem_wait_ld();
+      store_row32_f16(S, sb + SM_WBF, trow, q4, REG64, v, 1.f);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -637,13 +692,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // ---- outputs: o = -D1 rows 64..127; snapshot of the new state ----------------------------
     if (quad >= 2) {
       const int r = trow - 64;
-      float v[64];
-      tmem_ld64(t_lane + TM_D1 + 64 * half, v);
+      float v[32];
+      tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
+      tmem_wait_ld();
       if (r < L) {
         uint4 *dst = reinterpret_cast<uint4 *>(
-            p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + 64 * half);
+            p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + 32 * q4);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < 4; ++j)
           dst[j] = make_uint4(pack_bf16x2(-v[8 * j + 0], -v[8 * j + 1]),
                               pack_bf16x2(-v[8 * j + 2], -v[8 * j + 3]),
                               pack_bf16x2(-v[8 * j + 4], -v[8 * j + 5]),
@@ -651,13 +707,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     if (p.snaps && L == 64) {
-      float v[64];
-      tmem_ld64(t_lane + TM_S + 64 * half, v);
+      float v[32];
+      tmem_ld32(t_lane + TM_S + 32 * q4, v);
+      tmem_wait_ld();
       float4 *dst = reinterpret_cast<float4 *>(
           p.snaps + (static_cast<size_t>(snap_row) * H + h) * TD * TD +
-          static_cast<size_t>(trow) * TD + 64 * half);
+          static_cast<size_t>(trow) * TD + 32 * q4);
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
+      for (int j = 0; j < 8; ++j)
         __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
     }
     if (L == 64) ++snap_row;
@@ -666,12 +723,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
 
   if (!aborted && p.S_final) {
-    float v[64];
-    tmem_ld64(t_lane + TM_S + 64 * half, v);
+    float v[32];
+    tmem_ld32(t_lane + TM_S + 32 * q4, v);
+    tmem_wait_ld();
     float4 *dst = reinterpret_cast<float4 *>(p.S_final + state_off +
-                                             static_cast<size_t>(trow) * TD + 64 * half);
+                                             static_cast<size_t>(trow) * TD + 32 * q4);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
   }
 
   // Drain anything still in flight (bounded) before TMEM is released.

@@ -69,7 +69,14 @@ int kda_version(void);
 
 /*
  * Workspace bytes kda_chunk_fwd needs for these sizes (may be 0).  Pure
- * host arithmetic; returns 0 for unsupported sizes as well.
+ * host arithmetic; returns 0 for unsupported sizes as well.  It is non-zero
+ * only for equal-length batches (cu_seqlens NULL) with dk = dv = 128 whose
+ * (sequence, head) chains would fill under a quarter of the GPU (n_seq * H
+ * <= 38) and whose sequences are long: those run as a segment-parallel scan
+ * (each segment's zero-start state N and transition M, an fp32 chain
+ * S_start[g+1] = M_g S_start[g] + N_g, then a pass from the true segment
+ * starts), which keeps three [n_seq * n_segs, H, 128, 128] fp32 arrays in the
+ * workspace.  Calls with cu_seqlens need no workspace.
  */
 size_t kda_chunk_fwd_workspace_bytes(int n_seq, int64_t total_tokens, int H, int dk, int dv,
                                      int chunk);
@@ -95,7 +102,9 @@ size_t kda_chunk_fwd_workspace_bytes(int n_seq, int64_t total_tokens, int H, int
  *   snap_offsets device int64 [n_seq + 1], prefix sums of floor(L_s / 64);
  *               may be NULL only when cu_seqlens is NULL (rows s * (T / 64)).
  *   workspace   device scratch of kda_chunk_fwd_workspace_bytes() bytes
- *               (NULL allowed when that is 0); contents need not be zeroed.
+ *               (NULL allowed when that is 0), 16-byte aligned; contents need
+ *               not be zeroed and are garbage afterwards.  Calls sharing one
+ *               workspace must not overlap on the GPU.
  *   Errors: KDA_ERR_NULL, _SHAPE, _ALIGN, _UNSUPPORTED, _WORKSPACE, _CUDA.
  */
 int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,

@@ -142,7 +142,7 @@ def chunk_fwd(q, k, v, z, beta, A, gmin=GMIN, cu_seqlens=None, n_seq=None, S0=No
     if o is None:
         o = torch.empty((total, H, dv), dtype=torch.bfloat16, device=k.device)
     _check(o, "o", torch.bfloat16, (total, H, dv))
-    need = workspace_bytes(n_seq, total, H, dk, dv, chunk)
+    need = 0 if cu_seqlens is not None else workspace_bytes(n_seq, total, H, dk, dv, chunk)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=k.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -32,9 +32,47 @@ cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
                               const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
                               int64_t fixed_len, int H, const float *S0, kda_bf16 *o,
                               float *S_final, float *snaps, const int64_t *snap_offsets,
-                              int *status, cudaStream_t stream);
+                              int *status, int zero_v, int s0_identity, cudaStream_t stream);
+cudaError_t segment_combine_launch(const float *M, const float *N, const float *S0,
+                                   float *S_start, float *S_final, int n_seq, int n_segs, int H,
+                                   cudaStream_t stream);
 
 namespace {
+
+// Segment-parallel scan plan for equal-length sequences with few (sequence,
+// head) chains: split each sequence into n_segs segments of seg_len tokens so
+// that about kScanTargetChains segment chains run at once.  Without the scan
+// a chain walks its chunks one after another and most SMs sit idle.
+constexpr int kSMs = 152;
+constexpr int kScanTargetChains = 4 * kSMs;
+constexpr int64_t kScanMinSegment = 4096;
+struct ScanPlan {
+  int n_segs;
+  int64_t seg_len;
+};
+
+bool plan_scan(int n_seq, int64_t total_tokens, int H, int dk, int dv, ScanPlan *plan) {
+  if (dk != 128 || dv != 128 || n_seq <= 0 || total_tokens <= 0) return false;
+  if (total_tokens % n_seq != 0) return false;
+  const int64_t T = total_tokens / n_seq;
+  const int64_t chains = static_cast<int64_t>(n_seq) * H;
+  // The scan does about three times the work of one sequential pass, so it
+  // pays only when the sequential pass would fill less than a quarter of the SMs.
+  if (chains * 4 > kSMs) return false;
+  int n_segs = 1;
+  while (chains * n_segs < kScanTargetChains && T % (2 * n_segs) == 0 &&
+         (T / (2 * n_segs)) % 64 == 0 && T / (2 * n_segs) >= kScanMinSegment)
+    n_segs *= 2;
+  if (n_segs < 4) return false;
+  plan->n_segs = n_segs;
+  plan->seg_len = T / n_segs;
+  return true;
+}
+
+size_t scan_workspace_bytes(int n_seq, int H, const ScanPlan &plan) {
+  // M, N and the segment start states: three [n_seq * n_segs, H, 128, 128] fp32 arrays
+  return 3 * static_cast<size_t>(n_seq) * plan.n_segs * H * 128 * 128 * sizeof(float);
+}
 
 int *status_word() {
   void *p = nullptr;
@@ -75,8 +113,9 @@ int kda_version(void) { return 100; }
 
 size_t kda_chunk_fwd_workspace_bytes(int n_seq, int64_t total_tokens, int H, int dk, int dv,
                                      int chunk) {
-  (void)n_seq; (void)total_tokens; (void)H; (void)dk; (void)dv; (void)chunk;
-  return 0;
+  ScanPlan plan;
+  if (chunk != kChunk || H <= 0 || !plan_scan(n_seq, total_tokens, H, dk, dv, &plan)) return 0;
+  return scan_workspace_bytes(n_seq, H, plan);
 }
 
 int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *z,
@@ -102,15 +141,42 @@ int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const
   const void *ptrs[] = {q, k, v, z, beta, A, S0, o, S_final, snaps, snap_offsets, cu_seqlens};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_ALIGN;
-  const size_t need = kda_chunk_fwd_workspace_bytes(n_seq, total_tokens, H, dk, dv, chunk);
-  if (need > 0 && (!workspace || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ScanPlan plan;
+  const bool scan = !cu_seqlens && !(snaps && snap_offsets) &&
+                    prefill_tc_supported(dk, dv, total_tokens) &&
+                    plan_scan(n_seq, total_tokens, H, dk, dv, &plan);
+  if (scan) {
+    const size_t need = scan_workspace_bytes(n_seq, H, plan);
+    if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return KDA_ERR_ALIGN;
+    int *status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    const int n2 = n_seq * plan.n_segs;
+    const size_t arr = static_cast<size_t>(n2) * H * 128 * 128;
+    float *Mb = static_cast<float *>(workspace), *Nb = Mb + arr, *Ss = Nb + arr;
+    // 1. every segment from a zero state (N) and its transition from S0 = I with v = 0 (M)
+    cudaError_t err = prefill_tc_launch(q, k, v, z, beta, A, gmin, nullptr, n2, total_tokens,
+                                        plan.seg_len, H, nullptr, nullptr, Nb, nullptr, nullptr,
+                                        status, 0, 0, st);
+    if (err == cudaSuccess)
+      err = prefill_tc_launch(q, k, v, z, beta, A, gmin, nullptr, n2, total_tokens, plan.seg_len,
+                              H, nullptr, nullptr, Mb, nullptr, nullptr, status, 1, 1, st);
+    // 2. chain the segments: start states and the final state
+    if (err == cudaSuccess)
+      err = segment_combine_launch(Mb, Nb, S0, Ss, S_final, n_seq, plan.n_segs, H, st);
+    // 3. outputs and snapshots from the true start state of every segment
+    if (err == cudaSuccess)
+      err = prefill_tc_launch(q, k, v, z, beta, A, gmin, nullptr, n2, total_tokens, plan.seg_len,
+                              H, Ss, o, nullptr, snaps, nullptr, status, 0, 0, st);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  }
   cudaError_t err;
   if (prefill_tc_supported(dk, dv, total_tokens)) {
     int *status = status_word();
     if (!status) return KDA_ERR_CUDA;
     err = prefill_tc_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, total_tokens, fixed_len,
-                            H, S0, o, S_final, snaps, snap_offsets, status, st);
+                            H, S0, o, S_final, snaps, snap_offsets, status, 0, 0, st);
   } else {
     err = prefill_simt_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, fixed_len, H, dk, dv,
                               S0, o, S_final, snaps, snap_offsets, st);

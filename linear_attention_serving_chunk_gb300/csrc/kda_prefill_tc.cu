@@ -117,6 +117,8 @@ struct TcParams {
   float *snaps;
   const int64_t *snap_offsets;
   int *status;
+  int zero_v;       // 1: treat v as zero (U = 0) and do not read it
+  int s0_identity;  // 1: start every chain from S0 = I (dk = dv) instead of S0
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -173,6 +175,34 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // in: c1 = -eA log2(e), c2 = gmin log2(e).  z = +inf gives e^gmin, z = -inf 1.
 __device__ __forceinline__ float fast_decay2(float c1, float c2, float z) {
   return ex2_approx(c2 * rcp_approx(1.0f + ex2_approx(c1 * z)));
+}
+
+// Warp-level D(16x8) += A(16x8) B(8x8) in tf32 with fp32 accumulation.
+__device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                                 uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One warp: C[16x16] (two 16x8 fragments) += X[16x16] Y[16x16] with X and Y
+// fp32 in shared memory (row strides ldx, ldy floats).
+__device__ __forceinline__ void warp_mma16(const float *X, int ldx, const float *Y, int ldy,
+                                           float (&c)[2][4], int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    const int k0 = 8 * ks;
+    const uint32_t a[4] = {to_tf32(X[g * ldx + k0 + t]), to_tf32(X[(g + 8) * ldx + k0 + t]),
+                           to_tf32(X[g * ldx + k0 + t + 4]),
+                           to_tf32(X[(g + 8) * ldx + k0 + t + 4])};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+      mma_m16n8k8_tf32(c[nt], a, to_tf32(Y[(k0 + t) * ldy + 8 * nt + g]),
+                       to_tf32(Y[(k0 + t + 4) * ldy + 8 * nt + g]));
+  }
 }
 
 // Write 32 fp32 values (columns [32 q4, 32 q4 + 32) of `row`) as fp16 into a
@@ -280,7 +310,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      v[j] = p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + 32 * q4 + j] : 0.f;
+      v[j] = p.s0_identity ? (trow == 32 * q4 + j ? 1.f : 0.f)
+             : p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + 32 * q4 + j] : 0.f;
     tmem_st32(t_lane + TM_S + 32 * q4, v);
     tmem_wait_st();
   }
@@ -299,14 +330,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   };
   auto issue_kv = [&](int n) {
     const int t0 = static_cast<int>(t_begin + 64LL * n);
-    mbar_expect_tx(bar_kv, 2 * TILE_BYTES);
+    mbar_expect_tx(bar_kv, (p.zero_v ? 1 : 2) * TILE_BYTES);
     tma_load_3d(sb + SM_KB, &tm_k, 0, h, t0, bar_kv);
     tma_load_3d(sb + SM_KB + REG64, &tm_k, 64, h, t0, bar_kv);
-    tma_load_3d(sb + SM_VB, &tm_v, 0, h, t0, bar_kv);
-    tma_load_3d(sb + SM_VB + REG64, &tm_v, 64, h, t0, bar_kv);
+    if (!p.zero_v) {
+      tma_load_3d(sb + SM_VB, &tm_v, 0, h, t0, bar_kv);
+      tma_load_3d(sb + SM_VB + REG64, &tm_v, 64, h, t0, bar_kv);
+    }
   };
 
   bool qz_pending[2] = {false, false}, kv_pending = false, mma_pending = false;
+  float beta_next = (tid < 64 && t_begin + tid < t_end)
+                        ? bf2f(p.beta[static_cast<size_t>(t_begin + tid) * H + h])
+                        : 0.f;
+  // A full chunk's snapshot is written from the next chunk's state read-out
+  // (or after the last chunk): the row it goes to, or -1.
+  int64_t snap_pending = -1;
   uint32_t mma_phase = 0;
   bool aborted = false;
 
@@ -371,9 +410,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       issue_qz(n + 1);
     }
     if (n + 1 < n_chunks) qz_pending[par ^ 1] = true;
-    if (tid < 64)
-      S.f32(sb + MS_BETA + 4 * tid) =
-          tid < L ? bf2f(p.beta[static_cast<size_t>(t0 + tid) * H + h]) : 0.f;
+    // beta of this chunk was loaded one chunk ahead; start the next one's load now
+    if (tid < 64) {
+      S.f32(sb + MS_BETA + 4 * tid) = tid < L ? beta_next : 0.f;
+      beta_next = (n + 1 < n_chunks && t0 + 64 + tid < t_end)
+                      ? bf2f(p.beta[static_cast<size_t>(t0 + 64 + tid) * H + h])
+                      : 0.f;
+    }
     if (!wait_all(bar_qz0 + 8 * par, (n >> 1) & 1)) { aborted = true; break; }
     qz_pending[par] = false;
 
@@ -573,34 +616,40 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int r = 0; r < 16; ++r) S.f32(sb + SM_TF + 4 * ((o + r) * 65 + o + jc)) = x[r];
     }
     __syncthreads();
-    for (int d = 1; d < 4; ++d) {
-      const int nb = 4 - d;  // blocks (Rr, Rr - d), Rr = d..3
-      // Y = sum_{M=J}^{Rr-1} A[Rr][M] T[M][J]
-      for (int x = tid; x < nb * 256; x += TC_THREADS) {
-        const int b = x >> 8, e = x & 255, rr = e >> 4, cc = e & 15;
-        const int Rr = d + b, J = Rr - d;
-        float acc = 0.f;
+    // Off-diagonal blocks, one block column J per warp (warps 0..2), top to
+    // bottom: T[R][J] = -T[R][R] sum_{M=J}^{R-1} A[R][M] T[M][J].  Every
+    // operand a warp needs is a diagonal block or one it wrote itself.
+    if (warp < 3) {
+      const int J = warp, g = lane >> 2, t = lane & 3;
+      float *akk = reinterpret_cast<float *>(S.ptr(sb + SM_AKK));
+      float *tf = reinterpret_cast<float *>(S.ptr(sb + SM_TF));
+      float *ty = reinterpret_cast<float *>(S.ptr(sb + SM_TY)) + J * 16 * 17;
+      for (int Rr = J + 1; Rr < 4; ++Rr) {
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         for (int M = J; M < Rr; ++M)
+          warp_mma16(akk + (16 * Rr) * 65 + 16 * M, 65, tf + (16 * M) * 65 + 16 * J, 65, c, lane);
 #pragma unroll
-          for (int m = 0; m < 16; ++m)
-            acc += S.f32(sb + SM_AKK + 4 * ((16 * Rr + rr) * 65 + 16 * M + m)) *
-                   S.f32(sb + SM_TF + 4 * ((16 * M + m) * 65 + 16 * J + cc));
-        S.f32(sb + SM_TY + 4 * ((b * 16 + rr) * 17 + cc)) = acc;
-      }
-      __syncthreads();
-      // T[Rr][J] = -T[Rr][Rr] Y
-      for (int x = tid; x < nb * 256; x += TC_THREADS) {
-        const int b = x >> 8, e = x & 255, rr = e >> 4, cc = e & 15;
-        const int Rr = d + b, J = Rr - d;
-        float acc = 0.f;
+        for (int nt = 0; nt < 2; ++nt) {
+          ty[g * 17 + 8 * nt + 2 * t] = c[nt][0];
+          ty[g * 17 + 8 * nt + 2 * t + 1] = c[nt][1];
+          ty[(g + 8) * 17 + 8 * nt + 2 * t] = c[nt][2];
+          ty[(g + 8) * 17 + 8 * nt + 2 * t + 1] = c[nt][3];
+        }
+        __syncwarp();
+        float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mma16(tf + (16 * Rr) * 65 + 16 * Rr, 65, ty, 17, e, lane);
+        float *dst = tf + (16 * Rr) * 65 + 16 * J;
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
-          acc -= S.f32(sb + SM_TF + 4 * ((16 * Rr + rr) * 65 + 16 * Rr + m)) *
-                 S.f32(sb + SM_TY + 4 * ((b * 16 + m) * 17 + cc));
-        S.f32(sb + SM_TF + 4 * ((16 * Rr + rr) * 65 + 16 * J + cc)) = acc;
+        for (int nt = 0; nt < 2; ++nt) {
+          dst[g * 65 + 8 * nt + 2 * t] = -e[nt][0];
+          dst[g * 65 + 8 * nt + 2 * t + 1] = -e[nt][1];
+          dst[(g + 8) * 65 + 8 * nt + 2 * t] = -e[nt][2];
+          dst[(g + 8) * 65 + 8 * nt + 2 * t + 1] = -e[nt][3];
+        }
+        __syncwarp();
       }
-      __syncthreads();
     }
+    __syncthreads();
     // T' = T diag(beta) in bf16, K-major [128 rows x 64]; rows >= 64 and the upper triangle zero.
     for (int x = tid; x < 128 * 8; x += TC_THREADS) {
       const int row = x >> 3, ch = x & 7;
@@ -627,7 +676,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
       tc_fence_after();
       issue_mma(tmem + TM_AP, sb + SM_TP, false, REG128, sb + SM_KB, true, REG64, 4, ID_TPROD, 0);
-      issue_mma(tmem + TM_D1, sb + SM_TP, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD, 0);
+      if (!p.zero_v)
+        issue_mma(tmem + TM_D1, sb + SM_TP, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD, 0);
       mma_commit(bar_mma);
     }
     mma_pending = true;
@@ -648,6 +698,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       tmem_ld32(t_lane + TM_S + 32 * q4, v);
       tmem_wait_ld();
+      if (snap_pending >= 0) {  // the state after the previous (full) chunk
+        float4 *dst = reinterpret_cast<float4 *>(
+            p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
+            static_cast<size_t>(trow) * TD + 32 * q4);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        snap_pending = -1;
+      }
       store_row32_f16(S, sb + SM_SBF, trow, q4, REG128, v, 1.f);
       float gam = 1.f;
 #pragma unroll
@@ -664,7 +723,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // ---- D1 += [-Wk; -Q~] S: W (rows 0..63), -Q~ S (rows 64..127) --------------------------
     if (tid == 0) {
       tc_fence_after();
-      issue_mma(tmem + TM_D1, a3, false, REG128, sb + SM_SBF, true, REG128, 8, ID_KMN, 1);
+      // with zero v there is no U: this product initialises D1
+      issue_mma(tmem + TM_D1, a3, false, REG128, sb + SM_SBF, true, REG128, 8, ID_KMN,
+                p.zero_v ? 0u : 1u);
       mma_commit(bar_mma);
     }
     mma_pending = true;
@@ -695,7 +756,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float v[32];
       tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
       tmem_wait_ld();
-      if (r < L) {
+      if (r < L && p.o) {
         uint4 *dst = reinterpret_cast<uint4 *>(
             p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + 32 * q4);
 #pragma unroll
@@ -706,30 +767,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                               pack_bf16x2(-v[8 * j + 6], -v[8 * j + 7]));
       }
     }
-    if (p.snaps && L == 64) {
-      float v[32];
-      tmem_ld32(t_lane + TM_S + 32 * q4, v);
-      tmem_wait_ld();
-      float4 *dst = reinterpret_cast<float4 *>(
-          p.snaps + (static_cast<size_t>(snap_row) * H + h) * TD * TD +
-          static_cast<size_t>(trow) * TD + 32 * q4);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-    }
+    if (p.snaps && L == 64) snap_pending = snap_row;
     if (L == 64) ++snap_row;
     tc_fence_before();
     __syncthreads();
   }
 
-  if (!aborted && p.S_final) {
+  if (!aborted && (p.S_final || snap_pending >= 0)) {
     float v[32];
     tmem_ld32(t_lane + TM_S + 32 * q4, v);
     tmem_wait_ld();
-    float4 *dst = reinterpret_cast<float4 *>(p.S_final + state_off +
-                                             static_cast<size_t>(trow) * TD + 32 * q4);
+    if (p.S_final) {
+      float4 *dst = reinterpret_cast<float4 *>(p.S_final + state_off +
+                                               static_cast<size_t>(trow) * TD + 32 * q4);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      for (int j = 0; j < 8; ++j)
+        dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+    if (snap_pending >= 0) {
+      float4 *dst = reinterpret_cast<float4 *>(
+          p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
+          static_cast<size_t>(trow) * TD + 32 * q4);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+    }
   }
 
   // Drain anything still in flight (bounded) before TMEM is released.
@@ -792,17 +854,18 @@ cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
                               const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
                               int64_t fixed_len, int H, const float *S0, kda_bf16 *o,
                               float *S_final, float *snaps, const int64_t *snap_offsets,
-                              int *status, cudaStream_t stream) {
+                              int *status, int zero_v, int s0_identity, cudaStream_t stream) {
   CUtensorMap mq, mk, mz, mv;
   if (!make_map(&mq, q, total_tokens, H, TD) || !make_map(&mk, k, total_tokens, H, TD) ||
-      !make_map(&mz, z, total_tokens, H, TD) || !make_map(&mv, v, total_tokens, H, TD))
+      !make_map(&mz, z, total_tokens, H, TD) ||
+      !make_map(&mv, zero_v ? k : v, total_tokens, H, TD))
     return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(TC_SMEM_BYTES));
   if (err != cudaSuccess) return err;
   TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, H, S0, o, S_final, snaps, snap_offsets,
-               status};
+               status, zero_v, s0_identity};
   const dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(n_seq));
   prefill_tc_kernel<<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(mq, mk, mz, mv, prm);
   return cudaGetLastError();

@@ -175,6 +175,27 @@ def test_long_context(kda):
     assert s_err(last, S[0]) <= S_TOL, "last snapshot is not the final state"
 
 
+@pytest.mark.parametrize("S0_std", [None, 0.02])
+def test_segment_scan_long_sequences(kda, S0_std):
+    """Few chains and long sequences take the segment-parallel scan (2 x 65,536
+    tokens, H = 2: 16 segments of 4096 tokens per chain); every output, the
+    final states and all snapshots are checked against the oracle."""
+    x = kda_inputs.make_prefill(2, 128, 128, [65536, 65536], seed=21, device="cuda",
+                                S0_std=S0_std)
+    assert kda.workspace_bytes(2, 2 * 65536, 2, 128, 128) > 0  # the scan path is taken
+    n_seq, H = 2, 2
+    S_final = torch.full((n_seq, H, 128, 128), float("nan"), device="cuda")
+    snaps = torch.full((2 * 1024, H, 128, 128), float("nan"), device="cuda")
+    o = kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], n_seq=n_seq,
+                      S0=x["S0"], S_final=S_final, snaps=snaps)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    ref = oracle_subset(x, [0, 1], [0, 1])
+    assert o_err(f64(o), ref["o"]) <= O_TOL
+    assert s_err(f64(S_final), ref["S_final"]) <= S_TOL
+    assert s_err(f64(snaps), ref["snaps"]) <= S_TOL
+
+
 def test_decode_1000_steps(kda):
     """512 x 32 resident states, 1000 chained steps with fresh inputs: all
     states are checked after steps 1 and 10, 256 seeded (sequence, head)

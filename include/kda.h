@@ -115,6 +115,31 @@ int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                   size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_noalloc - kda_chunk_fwd for callers that cannot allocate
+ * device memory (no access to an allocator, or no cudaMalloc allowed on their
+ * path because it can synchronise the device).  The pages have no
+ * counterpart: this is a convenience of this library.
+ *
+ * Same arguments as kda_chunk_fwd without the workspace.  When the call needs
+ * a workspace (kda_chunk_fwd_workspace_bytes() > 0 for an equal-length batch:
+ * the segment-parallel scan) it uses a fixed scratch array of
+ * KDA_NOALLOC_WORKSPACE_BYTES in device memory that the library holds on
+ * every GPU that loads it; calls needing more return KDA_ERR_WORKSPACE
+ * before launching anything.  The first call on a device looks up the
+ * array's device address (with that device current); make it before any
+ * stream capture.  All calls share the array: calls that overlap on the GPU
+ * race.  Allocates nothing.
+ */
+#define KDA_NOALLOC_WORKSPACE_BYTES (32u << 20)
+
+int kda_chunk_fwd_noalloc(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                          const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                          const int32_t *cu_seqlens, int n_seq, int64_t total_tokens, int H,
+                          int dk, int dv, int chunk, const float *S0, kda_bf16 *o,
+                          float *S_final, float *snaps, const int64_t *snap_offsets,
+                          kda_stream_t stream);
+
+/*
  * kda_decode_step - one token of the recurrence for n sequences on resident
  * fp32 states, updated in place (the fixed-size running state of "How a
  * Frontier Model Gets Built, Read from the Kimi K3 Report", Technical

@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_
                 7: "KDA_ERR_TIMEOUT"}
 
 EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_bytes",
-            "kda_chunk_fwd", "kda_decode_step", "kda_state_snapshot", "kda_device_status")
+            "kda_chunk_fwd", "kda_decode_step", "kda_state_snapshot", "kda_device_status",
+            "kda_chunk_fwd_noalloc")
 
 _lib = None
 
@@ -61,6 +62,9 @@ def lib():
         L.kda_chunk_fwd.restype = I
         L.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, F, P, I, I64, I, I, I, I, P, P, P, P, P,
                                     P, SZ, P]
+        L.kda_chunk_fwd_noalloc.restype = I
+        L.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, F, P, I, I64, I, I, I, I, P, P, P,
+                                            P, P, P]
         L.kda_decode_step.restype = I
         L.kda_decode_step.argtypes = [P, P, P, P, P, P, F, P, P, I, I, I, I, P, P]
         L.kda_state_snapshot.restype = I

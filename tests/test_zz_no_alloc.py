@@ -1,0 +1,92 @@
+"""kda_chunk_fwd_noalloc: the prefill entry point for callers that cannot
+allocate device memory (no allocator of their own, or no cudaMalloc allowed on
+their path).  Called through the C ABI, it must give the same results as
+kda_chunk_fwd with a caller-allocated workspace, on two calls in a row with
+different inputs (the scratch array keeps the first call's contents), and it
+must refuse sizes beyond its fixed scratch before launching anything.
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test; it also passes when run alone.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 2e-2
+S_TOL = 1e-2
+KDA_ERR_WORKSPACE = 5
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import linear_attention_serving_chunk_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _o_err(a, b):
+    a = a.double().cpu().numpy()
+    b = b.double().cpu().numpy()
+    excess = np.abs(a - b) - 2.0 ** -8 * np.abs(b)
+    return float(np.max(excess) / max(np.sqrt(np.mean(b * b)), 1e-30))
+
+
+def _s_err(a, b):
+    return float(torch.linalg.vector_norm(a.double() - b.double()) /
+                 torch.linalg.vector_norm(b.double()))
+
+
+def _noalloc(kda, x, n_seq, S_final, snaps):
+    total, H, dk = x["k"].shape
+    dv = x["v"].shape[2]
+    o = torch.full((total, H, dv), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = kda.lib().kda_chunk_fwd_noalloc(
+        _ptr(x["q"]), _ptr(x["k"]), _ptr(x["v"]), _ptr(x["z"]), _ptr(x["beta"]), _ptr(x["A"]),
+        -5.0, None, n_seq, total, H, dk, dv, 64, _ptr(x["S0"]), _ptr(o), _ptr(S_final),
+        _ptr(snaps), None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, f"kda_chunk_fwd_noalloc returned {st}"
+    return o
+
+
+def test_noalloc_matches_the_workspace_entry_point_twice(kda):
+    # two sequences of 65,536 tokens, 2 heads: the segment-parallel scan runs
+    # and needs a 12 MiB workspace, inside the fixed scratch.
+    n_seq, H, T = 2, 2, 65536
+    need = kda.workspace_bytes(n_seq, n_seq * T, H, 128, 128)
+    assert 0 < need <= (32 << 20)
+    for seed in (31, 32):  # two calls in a row, different inputs
+        x = kda_inputs.make_prefill(H, 128, 128, [T] * n_seq, seed=seed, device="cuda",
+                                    S0_std=0.02)
+        S_ref = torch.empty((n_seq, H, 128, 128), device="cuda")
+        snaps_ref = torch.empty((n_seq * T // 64, H, 128, 128), device="cuda")
+        o_ref = kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], n_seq=n_seq,
+                              S0=x["S0"], S_final=S_ref, snaps=snaps_ref)
+        S_new = torch.full_like(S_ref, float("nan"))
+        snaps_new = torch.full_like(snaps_ref, float("nan"))
+        o_new = _noalloc(kda, x, n_seq, S_new, snaps_new)
+        torch.cuda.synchronize()
+        assert kda.device_status() == 0
+        assert _o_err(o_new, o_ref) <= O_TOL
+        assert _s_err(S_new, S_ref) <= S_TOL
+        assert _s_err(snaps_new, snaps_ref) <= S_TOL
+
+
+def test_noalloc_refuses_sizes_beyond_its_scratch(kda):
+    # one 2^20-token sequence with 16 heads needs 192 MiB of scan workspace:
+    # refused on the host, before any pointer is touched or kernel launched.
+    fake = ctypes.c_void_p(0x10000)
+    st = kda.lib().kda_chunk_fwd_noalloc(fake, fake, fake, fake, fake, fake, -5.0, None, 1,
+                                         1 << 20, 16, 128, 128, 64, None, fake, None, None,
+                                         None, None)
+    assert st == KDA_ERR_WORKSPACE

@@ -698,14 +698,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       tmem_ld32(t_lane + TM_S + 32 * q4, v);
       tmem_wait_ld();
-      if (snap_pending >= 0) {  // the state after the previous (full) chunk
-        float4 *dst = reinterpret_cast<float4 *>(
-            p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
-            static_cast<size_t>(trow) * TD + 32 * q4);
+      if (snap_pending >= 0) {
+        // The state after the previous (full) chunk.  Each warp stages its
+        // 32 x 32 fp32 tile (4 KiB, float4 slots swizzled by row) in the work
+        // region, then stores it so that every instruction writes four whole
+        // 128-byte rows.  Warps 0..7 use [0, 32 KiB) (not yet the fp16 S),
+        // warps 8..15 [64 KiB, 96 KiB) (T' is consumed, W not yet written).
+        const uint32_t tile = sb + SM_AP + (warp < 8 ? warp : warp + 8) * 4096u;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+          S.u128(tile + lane * 128u + (static_cast<uint32_t>(j ^ (lane & 7)) << 4)) =
+              make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                         __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+        __syncwarp();
+        float *base = p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
+                      static_cast<size_t>(quad * 32) * TD + 32 * q4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3), c = lane & 7;
+          const uint4 w = S.u128(tile + r * 128u + (static_cast<uint32_t>(c ^ (r & 7)) << 4));
+          __stcs(reinterpret_cast<float4 *>(base + static_cast<size_t>(r) * TD) + c,
+                 make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                             __uint_as_float(w.w)));
+        }
         snap_pending = -1;
+        __syncthreads();  // staging tiles are read before the fp16 S overwrites them
       }
       store_row32_f16(S, sb + SM_SBF, trow, q4, REG128, v, 1.f);
       float gam = 1.f;

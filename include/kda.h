@@ -48,6 +48,18 @@ extern "C" {
 #endif
 
 typedef uint16_t kda_bf16;                 /* raw bfloat16 bit pattern */
+
+/* Input pre-ops fused into the kernels (the `pre` flags of kda_chunk_fwd_ex,
+ * kda_decode_step_ex and kda_decode_tokens; 0 = inputs used as given).  The
+ * recurrence expects unit-norm q, k rows and beta in (0, 1); with these flags
+ * the caller passes the projections' raw outputs and the kernels form
+ *   q <- q / ||q||_2, k <- k / ||k||_2   per (token, head) row, in fp32
+ *                                         (an all-zero row stays zero), and
+ *   beta <- 1 / (1 + exp(-beta)),
+ * right after loading them, before any other use.  The tensor-core prefill
+ * rounds the normalised q, k back to bf16 (its operands are bf16). */
+#define KDA_PRE_L2NORM_QK 1u
+#define KDA_PRE_SIGMOID_BETA 2u
 typedef struct CUstream_st *kda_stream_t;  /* same type as cudaStream_t */
 
 typedef enum {
@@ -115,6 +127,20 @@ int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                   size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_ex - kda_chunk_fwd with input pre-ops: `pre` is a set of
+ * KDA_PRE_* flags (other bits: KDA_ERR_UNSUPPORTED).  pre = 0 is exactly
+ * kda_chunk_fwd.  The pre-ops run inside the prefill kernels on every pass
+ * (the scan's segment passes included); no normalised copy of q, k or beta is
+ * written anywhere.
+ */
+int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                     const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                     const int32_t *cu_seqlens, int n_seq, int64_t total_tokens, int H,
+                     int dk, int dv, int chunk, unsigned pre, const float *S0, kda_bf16 *o,
+                     float *S_final, float *snaps, const int64_t *snap_offsets,
+                     void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_noalloc - kda_chunk_fwd for callers that cannot allocate
  * device memory (no access to an allocator, or no cudaMalloc allowed on their
  * path because it can synchronise the device).  The pages have no
@@ -153,6 +179,33 @@ int kda_decode_step(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                     const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
                     float *state_pool, const int32_t *slots, int n, int H, int dk, int dv,
                     kda_bf16 *o, kda_stream_t stream);
+
+/* kda_decode_step_ex - kda_decode_step with KDA_PRE_* input pre-ops (pre = 0
+ * is exactly kda_decode_step). */
+int kda_decode_step_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                       const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                       float *state_pool, const int32_t *slots, int n, int H, int dk, int dv,
+                       unsigned pre, kda_bf16 *o, kda_stream_t stream);
+
+/*
+ * kda_decode_tokens - several tokens per sequence on resident states: the
+ * serving step for multi-token decode and speculative verification (the
+ * chunkwise form of the report page, sec. 2.1, applied to short runs on the
+ * fixed-size running state).  Sequence b's tokens are rows [cu_seqlens[b],
+ * cu_seqlens[b+1]) of q, k, v, z, beta (layouts as kda_chunk_fwd; any
+ * lengths, chunked by 64); its state is slot slots[b] of state_pool
+ * [n_slots, H, dk, dv].  o receives every token's output.  With commit != 0
+ * the state after the last token is written back to the slot (in place);
+ * with commit == 0 the pool is left unchanged (verify without accepting).
+ * Slots must be distinct.  cu_seqlens (int32 [n + 1]) and slots (int32 [n])
+ * are device arrays.  pre: KDA_PRE_* input pre-ops (0 = none).
+ *   Errors: KDA_ERR_NULL, _SHAPE, _ALIGN, _UNSUPPORTED, _CUDA.
+ */
+int kda_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                      const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                      const int32_t *cu_seqlens, int n, int64_t total_tokens, int H, int dk,
+                      int dv, unsigned pre, float *state_pool, const int32_t *slots, int commit,
+                      kda_bf16 *o, kda_stream_t stream);
 
 /*
  * kda_state_snapshot - restore chunk-boundary states for prefix caching

@@ -91,6 +91,29 @@ def make_prefill(H, dk, dv, lengths, seed, device="cpu", S0_std=None):
                 lengths=[int(x) for x in lengths])
 
 
+def make_raw_prefill(H, dk, dv, lengths, seed, device="cpu", S0_std=None):
+    """Inputs as a model's projections give them, before the pre-ops: q, k rows
+    N(0, 1) times a per-row scale U[0.25, 4] (not unit length), beta the raw
+    N(0, 1) logit.  Everything else as make_prefill.  bf16 like the others."""
+    total = int(sum(lengths))
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    q = _randn((total, H, dk), gen, device)
+    k = _randn((total, H, dk), gen, device)
+    q.mul_(torch.rand((total, H, 1), generator=gen, device=device) * 3.75 + 0.25)
+    k.mul_(torch.rand((total, H, 1), generator=gen, device=device) * 3.75 + 0.25)
+    v = _randn((total, H, dv), gen, device).to(torch.bfloat16)
+    z = _randn((total, H, dk), gen, device).to(torch.bfloat16)
+    beta = _randn((total, H), gen, device).to(torch.bfloat16)
+    A = (torch.rand(H, generator=gen, device=device, dtype=torch.float32) * 2.0 - 1.0)
+    S0 = None
+    if S0_std is not None:
+        S0 = _randn((len(lengths), H, dk, dv), gen, device, std=float(S0_std))
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32), device=device)
+    return dict(q=q.to(torch.bfloat16), k=k.to(torch.bfloat16), v=v, z=z, beta=beta, A=A, S0=S0,
+                cu_seqlens=cu, lengths=[int(x) for x in lengths])
+
+
 def make_workload_prefill(name, device="cpu", **override):
     """Inputs of a named prefill workload ('tiny', 'mid', 'varlen', 'long')."""
     w = dict(WORKLOADS[name])

@@ -23,6 +23,10 @@ CHUNK = 64
 # tensor-core operands, fp32 accumulation and fp32 state.
 PREFILL_COMPUTE_DTYPE = "bf16"
 
+# Input pre-ops (KDA_PRE_* in kda.h): L2-normalise q, k rows; sigmoid of beta.
+PRE_L2NORM_QK = 1
+PRE_SIGMOID_BETA = 2
+
 KDA_OK = 0
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_ALIGN",
                 4: "KDA_ERR_UNSUPPORTED", 5: "KDA_ERR_WORKSPACE", 6: "KDA_ERR_CUDA",
@@ -30,7 +34,8 @@ STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_
 
 EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_bytes",
             "kda_chunk_fwd", "kda_decode_step", "kda_state_snapshot", "kda_device_status",
-            "kda_chunk_fwd_noalloc")
+            "kda_chunk_fwd_noalloc", "kda_decode_tokens", "kda_chunk_fwd_ex",
+            "kda_decode_step_ex")
 
 _lib = None
 
@@ -51,8 +56,8 @@ def lib():
             raise ImportError(f"{LIB_PATH} is missing: run "
                               "linear_attention_serving_chunk_gb300.build() first")
         L = ctypes.CDLL(LIB_PATH)
-        P, I, I64, F, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
-                            ctypes.c_size_t)
+        P, I, I64, F, SZ, U = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                               ctypes.c_size_t, ctypes.c_uint)
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_status_string.argtypes = [I]
         L.kda_version.restype = I
@@ -62,11 +67,19 @@ def lib():
         L.kda_chunk_fwd.restype = I
         L.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, F, P, I, I64, I, I, I, I, P, P, P, P, P,
                                     P, SZ, P]
+        L.kda_chunk_fwd_ex.restype = I
+        L.kda_chunk_fwd_ex.argtypes = [P, P, P, P, P, P, F, P, I, I64, I, I, I, I, U, P, P, P,
+                                       P, P, P, SZ, P]
         L.kda_chunk_fwd_noalloc.restype = I
         L.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, F, P, I, I64, I, I, I, I, P, P, P,
                                             P, P, P]
+        L.kda_decode_tokens.restype = I
+        L.kda_decode_tokens.argtypes = [P, P, P, P, P, P, F, P, I, I64, I, I, I, U, P, P, I, P,
+                                        P]
         L.kda_decode_step.restype = I
         L.kda_decode_step.argtypes = [P, P, P, P, P, P, F, P, P, I, I, I, I, P, P]
+        L.kda_decode_step_ex.restype = I
+        L.kda_decode_step_ex.argtypes = [P, P, P, P, P, P, F, P, P, I, I, I, I, U, P, P]
         L.kda_state_snapshot.restype = I
         L.kda_state_snapshot.argtypes = [P, P, P, P, I, I, I, I, P]
         L.kda_device_status.restype = I
@@ -116,13 +129,14 @@ def workspace_bytes(n_seq, total_tokens, H, dk, dv, chunk=CHUNK):
 
 def chunk_fwd(q, k, v, z, beta, A, gmin=GMIN, cu_seqlens=None, n_seq=None, S0=None, o=None,
               S_final=None, snaps=None, snap_offsets=None, workspace=None, chunk=CHUNK,
-              stream=None):
+              pre=0, stream=None):
     """KDA prefill (kda_chunk_fwd).  Shapes: q, k, z [total, H, dk] bf16;
     v [total, H, dv] bf16; beta [total, H] bf16; A [H] fp32; cu_seqlens int32
     [n_seq + 1] or None (then n_seq equal sequences, default 1); S0, S_final
     [n_seq, H, dk, dv] fp32; snaps [rows, H, dk, dv] fp32 with snap_offsets
     int64 [n_seq + 1].  Outputs that are None are allocated (o) or skipped
-    (S_final, snaps).  Returns o."""
+    (S_final, snaps).  pre: PRE_* flags (raw q, k and beta logits; calls
+    kda_chunk_fwd_ex when non-zero).  Returns o."""
     total, H, dk = k.shape
     dv = v.shape[2]
     for t, nm in ((q, "q"), (k, "k"), (z, "z")):
@@ -150,6 +164,14 @@ def chunk_fwd(q, k, v, z, beta, A, gmin=GMIN, cu_seqlens=None, n_seq=None, S0=No
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=k.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if pre:
+        st = lib().kda_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
+                                    float(gmin), _ptr(cu_seqlens), int(n_seq), int(total),
+                                    int(H), int(dk), int(dv), int(chunk), int(pre), _ptr(S0),
+                                    _ptr(o), _ptr(S_final), _ptr(snaps), _ptr(snap_offsets),
+                                    _ptr(workspace), ws_bytes, _stream(stream))
+        _raise_on("kda_chunk_fwd_ex", st)
+        return o
     st = lib().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
                              float(gmin), _ptr(cu_seqlens), int(n_seq), int(total), int(H),
                              int(dk), int(dv), int(chunk), _ptr(S0), _ptr(o), _ptr(S_final),
@@ -159,10 +181,12 @@ def chunk_fwd(q, k, v, z, beta, A, gmin=GMIN, cu_seqlens=None, n_seq=None, S0=No
     return o
 
 
-def decode_step(q, k, v, z, beta, A, state_pool, slots=None, gmin=GMIN, o=None, stream=None):
+def decode_step(q, k, v, z, beta, A, state_pool, slots=None, gmin=GMIN, o=None, pre=0,
+                stream=None):
     """One decode step (kda_decode_step), in place on state_pool
     [n_slots, H, dk, dv] fp32.  q, k, z [n, H, dk]; v [n, H, dv]; beta [n, H]
-    bf16; slots int32 [n] or None.  Returns o [n, H, dv] bf16."""
+    bf16; slots int32 [n] or None; pre: PRE_* flags (kda_decode_step_ex when
+    non-zero).  Returns o [n, H, dv] bf16."""
     n, H, dk = k.shape
     dv = v.shape[2]
     for t, nm in ((q, "q"), (k, "k"), (z, "z")):
@@ -181,10 +205,46 @@ def decode_step(q, k, v, z, beta, A, state_pool, slots=None, gmin=GMIN, o=None, 
     if o is None:
         o = torch.empty((n, H, dv), dtype=torch.bfloat16, device=k.device)
     _check(o, "o", torch.bfloat16, (n, H, dv))
+    if pre:
+        st = lib().kda_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
+                                      float(gmin), _ptr(state_pool), _ptr(slots), int(n), int(H),
+                                      int(dk), int(dv), int(pre), _ptr(o), _stream(stream))
+        _raise_on("kda_decode_step_ex", st)
+        return o
     st = lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
                                float(gmin), _ptr(state_pool), _ptr(slots), int(n), int(H),
                                int(dk), int(dv), _ptr(o), _stream(stream))
     _raise_on("kda_decode_step", st)
+    return o
+
+
+def decode_tokens(q, k, v, z, beta, A, state_pool, slots, cu_seqlens, commit=True, gmin=GMIN,
+                  o=None, pre=0, stream=None):
+    """Several tokens per sequence on resident states (kda_decode_tokens):
+    sequence b's tokens are rows cu_seqlens[b]:cu_seqlens[b+1] of q, k, v, z,
+    beta; its state is state_pool[slots[b]], updated in place when commit.
+    pre: PRE_* flags.  Returns o [total, H, dv] bf16."""
+    total, H, dk = k.shape
+    dv = v.shape[2]
+    for t, nm in ((q, "q"), (k, "k"), (z, "z")):
+        _check(t, nm, torch.bfloat16, (total, H, dk))
+    _check(v, "v", torch.bfloat16, (total, H, dv))
+    _check(beta, "beta", torch.bfloat16, (total, H))
+    _check(A, "A", torch.float32, (H,))
+    _check(cu_seqlens, "cu_seqlens", torch.int32)
+    n = cu_seqlens.numel() - 1
+    _check(slots, "slots", torch.int32, (n,))
+    _check(state_pool, "state_pool", torch.float32)
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, dk, dv):
+        raise ValueError("state_pool must be [n_slots, H, dk, dv]")
+    if o is None:
+        o = torch.empty((total, H, dv), dtype=torch.bfloat16, device=k.device)
+    _check(o, "o", torch.bfloat16, (total, H, dv))
+    st = lib().kda_decode_tokens(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
+                                 float(gmin), _ptr(cu_seqlens), int(n), int(total), int(H),
+                                 int(dk), int(dv), int(pre), _ptr(state_pool), _ptr(slots),
+                                 1 if commit else 0, _ptr(o), _stream(stream))
+    _raise_on("kda_decode_tokens", st)
     return o
 
 

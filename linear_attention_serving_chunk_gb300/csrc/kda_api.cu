@@ -15,7 +15,7 @@ __device__ int g_status = 0;
 cudaError_t decode_step_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                                const kda_bf16 *z, const kda_bf16 *beta, const float *A,
                                float gmin, float *pool, const int32_t *slots, int n, int H,
-                               int dk, int dv, kda_bf16 *o, cudaStream_t stream);
+                               int dk, int dv, kda_bf16 *o, unsigned pre, cudaStream_t stream);
 cudaError_t snapshot_restore_launch(const float *snaps, const int64_t *src_idx, float *pool,
                                     const int32_t *dst_slots, int n, int H, int dk, int dv,
                                     cudaStream_t stream);
@@ -24,7 +24,8 @@ cudaError_t prefill_simt_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_
                                 float gmin, const int32_t *cu_seqlens, int n_seq,
                                 int64_t fixed_len, int H, int dk, int dv, const float *S0,
                                 kda_bf16 *o, float *S_final, float *snaps,
-                                const int64_t *snap_offsets, cudaStream_t stream);
+                                const int64_t *snap_offsets, const int32_t *slots,
+                                unsigned pre, cudaStream_t stream);
 
 bool prefill_tc_supported(int dk, int dv, int64_t total_tokens);
 cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
@@ -32,7 +33,8 @@ cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
                               const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
                               int64_t fixed_len, int H, const float *S0, kda_bf16 *o,
                               float *S_final, float *snaps, const int64_t *snap_offsets,
-                              int *status, int zero_v, int s0_identity, cudaStream_t stream);
+                              int *status, int zero_v, int s0_identity, const int32_t *slots,
+                              unsigned pre, cudaStream_t stream);
 cudaError_t segment_combine_launch(const float *M, const float *N, const float *S0,
                                    float *S_start, float *S_final, int n_seq, int n_segs, int H,
                                    cudaStream_t stream);
@@ -87,6 +89,8 @@ bool dim_ok(int d) { return d == 64 || d == 128; }
 // inside the fp32/bf16 range; the report's value is -5.
 bool gmin_ok(float gmin) { return isfinite(gmin) && gmin <= 0.f && gmin >= -5.5f; }
 
+bool pre_ok(unsigned pre) { return (pre & ~(KDA_PRE_L2NORM_QK | KDA_PRE_SIGMOID_BETA)) == 0; }
+
 }  // namespace
 
 }  // namespace kda
@@ -124,8 +128,19 @@ int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const
                   const float *S0, kda_bf16 *o, float *S_final, float *snaps,
                   const int64_t *snap_offsets, void *workspace, size_t workspace_bytes,
                   kda_stream_t stream) {
+  return kda_chunk_fwd_ex(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, total_tokens, H, dk, dv,
+                          chunk, 0u, S0, o, S_final, snaps, snap_offsets, workspace,
+                          workspace_bytes, stream);
+}
+
+int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *z,
+                     const kda_bf16 *beta, const float *A, float gmin,
+                     const int32_t *cu_seqlens, int n_seq, int64_t total_tokens, int H, int dk,
+                     int dv, int chunk, unsigned pre, const float *S0, kda_bf16 *o,
+                     float *S_final, float *snaps, const int64_t *snap_offsets, void *workspace,
+                     size_t workspace_bytes, kda_stream_t stream) {
   if (n_seq < 0 || total_tokens < 0 || H <= 0 || H > 65535) return KDA_ERR_SHAPE;
-  if (!dim_ok(dk) || !dim_ok(dv) || chunk != kChunk || !gmin_ok(gmin))
+  if (!dim_ok(dk) || !dim_ok(dv) || chunk != kChunk || !gmin_ok(gmin) || !pre_ok(pre))
     return KDA_ERR_UNSUPPORTED;
   if (n_seq == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_SHAPE;
   if (n_seq > 65535) return KDA_ERR_SHAPE;
@@ -158,17 +173,19 @@ int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const
     // 1. every segment from a zero state (N) and its transition from S0 = I with v = 0 (M)
     cudaError_t err = prefill_tc_launch(q, k, v, z, beta, A, gmin, nullptr, n2, total_tokens,
                                         plan.seg_len, H, nullptr, nullptr, Nb, nullptr, nullptr,
-                                        status, 0, 0, st);
+                                        status, 0, 0, nullptr, pre, st);
     if (err == cudaSuccess)
       err = prefill_tc_launch(q, k, v, z, beta, A, gmin, nullptr, n2, total_tokens, plan.seg_len,
-                              H, nullptr, nullptr, Mb, nullptr, nullptr, status, 1, 1, st);
+                              H, nullptr, nullptr, Mb, nullptr, nullptr, status, 1, 1, nullptr,
+                              pre, st);
     // 2. chain the segments: start states and the final state
     if (err == cudaSuccess)
       err = segment_combine_launch(Mb, Nb, S0, Ss, S_final, n_seq, plan.n_segs, H, st);
     // 3. outputs and snapshots from the true start state of every segment
     if (err == cudaSuccess)
       err = prefill_tc_launch(q, k, v, z, beta, A, gmin, nullptr, n2, total_tokens, plan.seg_len,
-                              H, Ss, o, nullptr, snaps, nullptr, status, 0, 0, st);
+                              H, Ss, o, nullptr, snaps, nullptr, status, 0, 0, nullptr, pre,
+                              st);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }
   cudaError_t err;
@@ -176,10 +193,11 @@ int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const
     int *status = status_word();
     if (!status) return KDA_ERR_CUDA;
     err = prefill_tc_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, total_tokens, fixed_len,
-                            H, S0, o, S_final, snaps, snap_offsets, status, 0, 0, st);
+                            H, S0, o, S_final, snaps, snap_offsets, status, 0, 0, nullptr, pre,
+                            st);
   } else {
     err = prefill_simt_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, fixed_len, H, dk, dv,
-                              S0, o, S_final, snaps, snap_offsets, st);
+                              S0, o, S_final, snaps, snap_offsets, nullptr, pre, st);
   }
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -188,8 +206,16 @@ int kda_decode_step(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, con
                     const kda_bf16 *beta, const float *A, float gmin, float *state_pool,
                     const int32_t *slots, int n, int H, int dk, int dv, kda_bf16 *o,
                     kda_stream_t stream) {
+  return kda_decode_step_ex(q, k, v, z, beta, A, gmin, state_pool, slots, n, H, dk, dv, 0u, o,
+                            stream);
+}
+
+int kda_decode_step_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                       const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                       float *state_pool, const int32_t *slots, int n, int H, int dk, int dv,
+                       unsigned pre, kda_bf16 *o, kda_stream_t stream) {
   if (n < 0 || H <= 0) return KDA_ERR_SHAPE;
-  if (!dim_ok(dk) || !dim_ok(dv) || !gmin_ok(gmin)) return KDA_ERR_UNSUPPORTED;
+  if (!dim_ok(dk) || !dim_ok(dv) || !gmin_ok(gmin) || !pre_ok(pre)) return KDA_ERR_UNSUPPORTED;
   if (n == 0) return KDA_OK;
   if (static_cast<int64_t>(n) * H > 0x7fffffffLL) return KDA_ERR_SHAPE;
   if (!q || !k || !v || !z || !beta || !A || !state_pool || !o) return KDA_ERR_NULL;
@@ -197,7 +223,37 @@ int kda_decode_step(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, con
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_ALIGN;
   const cudaError_t err = decode_step_launch(q, k, v, z, beta, A, gmin, state_pool, slots, n, H,
-                                             dk, dv, o, reinterpret_cast<cudaStream_t>(stream));
+                                             dk, dv, o, pre,
+                                             reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                      const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                      const int32_t *cu_seqlens, int n, int64_t total_tokens, int H, int dk,
+                      int dv, unsigned pre, float *state_pool, const int32_t *slots, int commit,
+                      kda_bf16 *o, kda_stream_t stream) {
+  if (n < 0 || total_tokens < 0 || H <= 0 || H > 65535 || n > 65535) return KDA_ERR_SHAPE;
+  if (!dim_ok(dk) || !dim_ok(dv) || !gmin_ok(gmin) || !pre_ok(pre)) return KDA_ERR_UNSUPPORTED;
+  if (n == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_SHAPE;
+  if (!A || !state_pool || !slots || !cu_seqlens) return KDA_ERR_NULL;
+  if (total_tokens > 0 && (!q || !k || !v || !z || !beta || !o)) return KDA_ERR_NULL;
+  const void *ptrs[] = {q, k, v, z, beta, A, state_pool, slots, cu_seqlens, o};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  float *S_final = commit ? state_pool : nullptr;
+  cudaError_t err;
+  if (prefill_tc_supported(dk, dv, total_tokens)) {
+    int *status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    err = prefill_tc_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n, total_tokens, 0, H,
+                            state_pool, o, S_final, nullptr, nullptr, status, 0, 0, slots, pre,
+                            st);
+  } else {
+    err = prefill_simt_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n, 0, H, dk, dv, state_pool,
+                              o, S_final, nullptr, nullptr, slots, pre, st);
+  }
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

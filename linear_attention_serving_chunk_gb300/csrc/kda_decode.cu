@@ -26,7 +26,7 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
                    const kda_bf16 *__restrict__ v, const kda_bf16 *__restrict__ z,
                    const kda_bf16 *__restrict__ beta, const float *__restrict__ A,
                    float gmin, float *__restrict__ pool, const int32_t *__restrict__ slots,
-                   int H, kda_bf16 *__restrict__ o) {
+                   int H, kda_bf16 *__restrict__ o, unsigned pre) {
   constexpr int TPR = DV / 4;                // threads across one row (4 columns each)
   constexpr int RG = kDecodeThreads / TPR;   // row groups
   constexpr int RPT = DK / RG;               // rows per thread
@@ -35,7 +35,7 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
   __shared__ float s_a[DK], s_k[DK], s_q[DK];
   __shared__ float s_red_p[RG][DV], s_red_u[RG][DV];
   __shared__ float s_delta[DV];
-  __shared__ float s_kq_part[DK / 32];
+  __shared__ float s_part[3][DK / 32];  // per-warp sums of k.q, k.k, q.q
 
   const int row = blockIdx.x;  // b * H + h
   const int b = row / H, h = row - b * H;
@@ -56,18 +56,39 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
     s_a[tid] = decay_factor(gmin, expf(A[h]), bf2f(z[x]));
     s_k[tid] = kv;
     s_q[tid] = qv;
-    float kq = kv * qv;
+    float kq = kv * qv, kk = kv * kv, qq = qv * qv;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-    if ((tid & 31) == 0) s_kq_part[tid >> 5] = kq;
+    for (int off = 16; off > 0; off >>= 1) {
+      kq += __shfl_xor_sync(0xffffffffu, kq, off);
+      kk += __shfl_xor_sync(0xffffffffu, kk, off);
+      qq += __shfl_xor_sync(0xffffffffu, qq, off);
+    }
+    if ((tid & 31) == 0) {
+      s_part[0][tid >> 5] = kq;
+      s_part[1][tid >> 5] = kk;
+      s_part[2][tid >> 5] = qq;
+    }
   }
   __syncthreads();
+  // Raw q and k (pre-op flag): every read of k and q below takes the 1 / norm
+  // factors ik, iq; otherwise both are 1.
+  float ik = 1.f, iq = 1.f;
+  if (pre & KDA_PRE_L2NORM_QK) {
+    float kk = 0.f, qq = 0.f;
+#pragma unroll
+    for (int w = 0; w < DK / 32; ++w) {
+      kk += s_part[1][w];
+      qq += s_part[2][w];
+    }
+    ik = kk > 0.f ? rsqrtf(kk) : 0.f;
+    iq = qq > 0.f ? rsqrtf(qq) : 0.f;
+  }
 
   float p[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int rr = 0; rr < RPT; ++rr) {
     const int i = rg * RPT + rr;
-    const float a = s_a[i], kv = s_k[i], qv = s_q[i];
+    const float a = s_a[i], kv = s_k[i] * ik, qv = s_q[i] * iq;
     s[rr].x *= a; s[rr].y *= a; s[rr].z *= a; s[rr].w *= a;
     p[0] += s[rr].x * kv; p[1] += s[rr].y * kv; p[2] += s[rr].z * kv; p[3] += s[rr].w * kv;
     u[0] += s[rr].x * qv; u[1] += s[rr].y * qv; u[2] += s[rr].z * qv; u[3] += s[rr].w * qv;
@@ -88,9 +109,12 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
     }
     float kq = 0.f;
 #pragma unroll
-    for (int w = 0; w < DK / 32; ++w) kq += s_kq_part[w];
+    for (int w = 0; w < DK / 32; ++w) kq += s_part[0][w];
+    kq *= ik * iq;
     const size_t xv = static_cast<size_t>(row) * DV + tid;
-    const float delta = bf2f(beta[row]) * (bf2f(v[xv]) - pj);
+    float bt = bf2f(beta[row]);
+    if (pre & KDA_PRE_SIGMOID_BETA) bt = 1.f / (1.f + __expf(-bt));
+    const float delta = bt * (bf2f(v[xv]) - pj);
     s_delta[tid] = delta;
     o[xv] = f2bf(uj + kq * delta);
   }
@@ -100,7 +124,7 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
   const float d2 = s_delta[cg * 4 + 2], d3 = s_delta[cg * 4 + 3];
 #pragma unroll
   for (int rr = 0; rr < RPT; ++rr) {
-    const float kv = s_k[rg * RPT + rr];
+    const float kv = s_k[rg * RPT + rr] * ik;
     s[rr].x += kv * d0; s[rr].y += kv * d1; s[rr].z += kv * d2; s[rr].w += kv * d3;
     __stcs(reinterpret_cast<float4 *>(S + (rg * RPT + rr) * DV) + cg, s[rr]);
   }
@@ -110,10 +134,10 @@ template <int DK, int DV>
 cudaError_t launch_decode(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                           const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
                           float *pool, const int32_t *slots, int n, int H, kda_bf16 *o,
-                          cudaStream_t stream) {
+                          unsigned pre, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(n) * H;
   decode_step_kernel<DK, DV><<<static_cast<unsigned>(rows), kDecodeThreads, 0, stream>>>(
-      q, k, v, z, beta, A, gmin, pool, slots, H, o);
+      q, k, v, z, beta, A, gmin, pool, slots, H, o, pre);
   return cudaGetLastError();
 }
 
@@ -122,15 +146,16 @@ cudaError_t launch_decode(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *
 cudaError_t decode_step_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                                const kda_bf16 *z, const kda_bf16 *beta, const float *A,
                                float gmin, float *pool, const int32_t *slots, int n, int H,
-                               int dk, int dv, kda_bf16 *o, cudaStream_t stream) {
+                               int dk, int dv, kda_bf16 *o, unsigned pre,
+                               cudaStream_t stream) {
   if (dk == 128 && dv == 128)
-    return launch_decode<128, 128>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, stream);
+    return launch_decode<128, 128>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, pre, stream);
   if (dk == 64 && dv == 64)
-    return launch_decode<64, 64>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, stream);
+    return launch_decode<64, 64>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, pre, stream);
   if (dk == 128 && dv == 64)
-    return launch_decode<128, 64>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, stream);
+    return launch_decode<128, 64>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, pre, stream);
   if (dk == 64 && dv == 128)
-    return launch_decode<64, 128>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, stream);
+    return launch_decode<64, 128>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, pre, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -61,9 +61,10 @@ prefill_simt_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__
                     const kda_bf16 *__restrict__ v, const kda_bf16 *__restrict__ z,
                     const kda_bf16 *__restrict__ beta, const float *__restrict__ A, float gmin,
                     const int32_t *__restrict__ cu_seqlens, int64_t fixed_len, int H, int DV,
-                    const float *__restrict__ S0, kda_bf16 *__restrict__ o,
-                    float *__restrict__ S_final, float *__restrict__ snaps,
-                    const int64_t *__restrict__ snap_offsets) {
+                    const float *S0, kda_bf16 *__restrict__ o,
+                    float *S_final, float *__restrict__ snaps,
+                    const int64_t *__restrict__ snap_offsets,
+                    const int32_t *__restrict__ slots, unsigned pre) {
   static_assert(NS % 4 == 0 && (kChunk * 4) == kThreads, "row-major thread mapping");
   constexpr int JW = NS / 4;  // value columns per thread in the (row, column-group) mapping
   extern __shared__ float4 smem_raw[];
@@ -83,7 +84,8 @@ prefill_simt_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__
   int64_t snap_row = 0;
   if (snaps) snap_row = snap_offsets ? snap_offsets[s] : static_cast<int64_t>(s) * (fixed_len / kChunk);
   const float eA = expf(A[h]);
-  const size_t state_off = (static_cast<size_t>(s) * H + h) * DK * DV;
+  // S0 / S_final rows: the sequence itself, or its slot of a state pool
+  const size_t state_off = (static_cast<size_t>(slots ? slots[s] : s) * H + h) * DK * DV;
 
   for (int x = tid; x < DK * NS; x += kThreads) {
     const int c = x / NS, j = x % NS;
@@ -118,8 +120,32 @@ prefill_simt_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__
       const int r = x / NS, j = x % NS;
       sm.V[r][j] = r < L ? bf2f(v[(static_cast<size_t>(t0 + r) * H + h) * DV + j0 + j]) : 0.f;
     }
-    if (tid < kChunk) sm.beta[tid] = tid < L ? bf2f(beta[static_cast<size_t>(t0 + tid) * H + h]) : 0.f;
+    if (tid < kChunk) {
+      float b = tid < L ? bf2f(beta[static_cast<size_t>(t0 + tid) * H + h]) : 0.f;
+      if ((pre & KDA_PRE_SIGMOID_BETA) && tid < L) b = 1.f / (1.f + __expf(-b));
+      sm.beta[tid] = b;
+    }
     __syncthreads();
+    if (pre & KDA_PRE_L2NORM_QK) {
+      // raw q, k: unit L2 norm per row, four threads per row (DK / 4 channels each)
+      const int r = tid >> 2, c0 = (tid & 3) * (DK / 4);
+      float sk = 0.f, sq = 0.f;
+      for (int c = c0; c < c0 + DK / 4; ++c) {
+        sk += sm.KE[r][c] * sm.KE[r][c];
+        sq += sm.QE[r][c] * sm.QE[r][c];
+      }
+#pragma unroll
+      for (int off = 1; off < 4; off <<= 1) {
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+      }
+      const float ik = sk > 0.f ? rsqrtf(sk) : 0.f, iq = sq > 0.f ? rsqrtf(sq) : 0.f;
+      for (int c = c0; c < c0 + DK / 4; ++c) {
+        sm.KE[r][c] *= ik;
+        sm.QE[r][c] *= iq;
+      }
+      __syncthreads();
+    }
 
     // 2. per (sub-tile R, channel c): backward products Eb[r] = prod_{m=r+1}^{end(R)} a_m
     //    into KP, forward products Ef[r] = prod_{m=start(R)}^{r} a_m in place in KH,
@@ -300,7 +326,8 @@ cudaError_t launch_simt(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                         const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
                         const int32_t *cu_seqlens, int n_seq, int64_t fixed_len, int H, int dv,
                         const float *S0, kda_bf16 *o, float *S_final, float *snaps,
-                        const int64_t *snap_offsets, cudaStream_t stream) {
+                        const int64_t *snap_offsets, const int32_t *slots, unsigned pre,
+                        cudaStream_t stream) {
   const size_t smem = sizeof(SimtSmem<DK, NS>);
   cudaError_t err = cudaFuncSetAttribute(prefill_simt_kernel<DK, NS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -310,7 +337,7 @@ cudaError_t launch_simt(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                   static_cast<unsigned>(n_seq));
   prefill_simt_kernel<DK, NS><<<grid, kThreads, smem, stream>>>(
       q, k, v, z, beta, A, gmin, cu_seqlens, fixed_len, H, dv, S0, o, S_final, snaps,
-      snap_offsets);
+      snap_offsets, slots, pre);
   return cudaGetLastError();
 }
 
@@ -321,13 +348,14 @@ cudaError_t prefill_simt_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_
                                 float gmin, const int32_t *cu_seqlens, int n_seq,
                                 int64_t fixed_len, int H, int dk, int dv, const float *S0,
                                 kda_bf16 *o, float *S_final, float *snaps,
-                                const int64_t *snap_offsets, cudaStream_t stream) {
+                                const int64_t *snap_offsets, const int32_t *slots,
+                                unsigned pre, cudaStream_t stream) {
   if (dk == 128)
     return launch_simt<128, 32>(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, fixed_len, H, dv,
-                                S0, o, S_final, snaps, snap_offsets, stream);
+                                S0, o, S_final, snaps, snap_offsets, slots, pre, stream);
   if (dk == 64)
     return launch_simt<64, 32>(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, fixed_len, H, dv,
-                               S0, o, S_final, snaps, snap_offsets, stream);
+                               S0, o, S_final, snaps, snap_offsets, slots, pre, stream);
   return cudaErrorInvalidValue;
 }
 

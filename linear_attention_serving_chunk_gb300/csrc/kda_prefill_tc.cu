@@ -70,6 +70,7 @@ constexpr uint32_t SM_SBF = SM_AP;                // [dk x dv] S in fp16, MN-maj
 constexpr uint32_t SM_A5 = SM_AP + 48 * KiB;      // [128 x 64] K-major: [0 ; -P]
 constexpr uint32_t SM_TP = SM_AP + 64 * KiB;      // [128 x 64] K-major: [T diag(beta) ; 0]
 constexpr uint32_t SM_WBF = SM_AP + 64 * KiB;     // [tok x dv] W in fp16 (after T' is used)
+
 constexpr uint32_t SM_MISC = 224 * KiB;
 constexpr uint32_t MS_BAR_QZ = SM_MISC + 0;       // 2 mbarriers
 constexpr uint32_t MS_BAR_KV = SM_MISC + 16;
@@ -94,9 +95,13 @@ constexpr uint32_t APB_REG = 64 * 128;      // 64 rows
 constexpr uint32_t TM_AP = 0;     // A_kk / P products, later Wk
 constexpr uint32_t TM_D1 = 128;   // U -> W (rows 0..63), -O (rows 64..127)
 constexpr uint32_t TM_S = 256;    // fp32 state S (row = key channel)
+
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t kWaitPolls = 1u << 24;
+// TMA loads are issued by lane 0 of warp 4 (a warp with no output stores),
+// the MMAs by thread 0.
+constexpr int kTmaThread = 128;
 
 // Instruction descriptors (fp32 accumulation).
 constexpr uint32_t ID_AP = idesc_mma(128, 64, kFmtTF32, kFmtTF32, 0, 0);      // A_kk / P
@@ -117,8 +122,10 @@ struct TcParams {
   float *snaps;
   const int64_t *snap_offsets;
   int *status;
+  const int32_t *slots;  // S0 / S_final row of sequence s: slots[s] (state pool), or s
   int zero_v;       // 1: treat v as zero (U = 0) and do not read it
   int s0_identity;  // 1: start every chain from S0 = I (dk = dv) instead of S0
+  unsigned pre;     // KDA_PRE_* input pre-ops (L2-normalise q, k; sigmoid of beta)
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -133,6 +140,21 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
+// Round fp32 to tf32 (nearest, ties away from zero) on the integer ALU: add
+// half a unit of the 10-bit mantissa, clear the 13 low bits.  (Values here are
+// finite and far below FLT_MAX, so the carry into the exponent is exact.)
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
+}
+
+// bf16 global load kept where it is written (a prefetch the compiler must not
+// sink to its use).
+__device__ __forceinline__ float ldg_bf16_pinned(const kda_bf16 *ptr) {
+  unsigned short raw;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(raw) : "l"(ptr));
+  return __uint_as_float(static_cast<uint32_t>(raw) << 16);
 }
 
 // Shared memory seen by the threads: plain C++ accesses (so the compiler can
@@ -195,13 +217,13 @@ __device__ __forceinline__ void warp_mma16(const float *X, int ldx, const float 
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     const int k0 = 8 * ks;
-    const uint32_t a[4] = {to_tf32(X[g * ldx + k0 + t]), to_tf32(X[(g + 8) * ldx + k0 + t]),
-                           to_tf32(X[g * ldx + k0 + t + 4]),
-                           to_tf32(X[(g + 8) * ldx + k0 + t + 4])};
+    const uint32_t a[4] = {tf32_rna(X[g * ldx + k0 + t]), tf32_rna(X[(g + 8) * ldx + k0 + t]),
+                           tf32_rna(X[g * ldx + k0 + t + 4]),
+                           tf32_rna(X[(g + 8) * ldx + k0 + t + 4])};
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
-      mma_m16n8k8_tf32(c[nt], a, to_tf32(Y[(k0 + t) * ldy + 8 * nt + g]),
-                       to_tf32(Y[(k0 + t + 4) * ldy + 8 * nt + g]));
+      mma_m16n8k8_tf32(c[nt], a, tf32_rna(Y[(k0 + t) * ldy + 8 * nt + g]),
+                       tf32_rna(Y[(k0 + t + 4) * ldy + 8 * nt + g]));
   }
 }
 
@@ -276,7 +298,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     snap_row = p.snap_offsets ? p.snap_offsets[s] : static_cast<int64_t>(s) * (p.fixed_len / 64);
   const float kLog2e = 1.4426950408889634f;
   const float dc1 = -__expf(p.A[h]) * kLog2e, dc2 = p.gmin * kLog2e;
-  const size_t state_off = (static_cast<size_t>(s) * H + h) * TD * TD;
+  const size_t state_off =
+      (static_cast<size_t>(p.slots ? p.slots[s] : s) * H + h) * TD * TD;
 
   const uint32_t bar_qz0 = sb + MS_BAR_QZ, bar_kv = sb + MS_BAR_KV, bar_mma = sb + MS_BAR_MMA;
   if (tid == 0) {
@@ -369,7 +392,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     return ok;
   };
 
-  if (tid == 0 && n_chunks > 0) {
+  if (tid == kTmaThread && n_chunks > 0) {
     issue_qz(0);
     issue_kv(0);
   }
@@ -396,7 +419,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t rg32_a = static_cast<uint32_t>(c0 >> 5) * APA_REG;   // tf32 APA
   const uint32_t rg32_b = static_cast<uint32_t>(c0 >> 5) * APB_REG;   // tf32 APB
   const int rbase = 16 * R + 4 * hf;
-
   for (int n = 0; n < n_chunks && !aborted; ++n) {
     const int par = n & 1;
     const int64_t t0 = t_begin + 64LL * n;
@@ -404,18 +426,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t a3 = sb + SM_A3 + par * A3_BYTES;
     const uint32_t zb = sb + SM_ZB + par * TILE_BYTES;
 
-    // Prefetch the next chunk's q and z into the other parity buffers.
-    if (tid == 0 && n + 1 < n_chunks) {
-      fence_proxy_async();
-      issue_qz(n + 1);
-    }
+    // Prefetch the next chunk's q and z into the other parity buffers.  (The
+    // threads that last wrote those buffers fenced their generic-proxy
+    // writes before the barrier that ended the previous chunk.)
+    if (tid == kTmaThread && n + 1 < n_chunks) issue_qz(n + 1);
     if (n + 1 < n_chunks) qz_pending[par ^ 1] = true;
-    // beta of this chunk was loaded one chunk ahead; start the next one's load now
+    // beta of this chunk was loaded one chunk ahead (logits pass through a sigmoid)
     if (tid < 64) {
-      S.f32(sb + MS_BETA + 4 * tid) = tid < L ? beta_next : 0.f;
-      beta_next = (n + 1 < n_chunks && t0 + 64 + tid < t_end)
-                      ? bf2f(p.beta[static_cast<size_t>(t0 + 64 + tid) * H + h])
-                      : 0.f;
+      const float b = (p.pre & KDA_PRE_SIGMOID_BETA) ? 1.0f / (1.0f + __expf(-beta_next)) : beta_next;
+      S.f32(sb + MS_BETA + 4 * tid) = tid < L ? b : 0.f;
     }
     if (!wait_all(bar_qz0 + 8 * par, (n >> 1) & 1)) { aborted = true; break; }
     qz_pending[par] = false;
@@ -482,8 +501,59 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         S.f32(sb + MS_LAM + 4 * (R * TD + c0 + 1)) = s01 * s11 * s21 * s31;
       }
     }
+    // the next chunk's beta, issued while the store queue is quiet
+    if (tid < 64)
+      beta_next = (n + 1 < n_chunks && t0 + 64 + tid < t_end)
+                      ? ldg_bf16_pinned(p.beta + static_cast<size_t>(t0 + 64 + tid) * H + h)
+                      : 0.f;
     if (!wait_all(bar_kv, n & 1)) { aborted = true; break; }  // also orders the Lam table
     kv_pending = false;
+
+    if (p.pre & KDA_PRE_L2NORM_QK) {
+      // Raw q and k: scale every (token, head) row to unit L2 norm in place
+      // (fp32 norm, result rounded back to bf16).  Row sums of squares: this
+      // thread's two channels, then its half-warp (16 channel pairs), then the
+      // 4 warps of the sub-tile through a table in the other parity's A3 rows
+      // 0..63, which hold nothing during this chunk.
+      const uint32_t tab = sb + SM_A3 + (par ^ 1) * A3_BYTES;  // [64 rows][4 warps][k, q]
+      float ssk[8], ssq[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = rbase + (j & 3) + 8 * (j >> 2);
+        const uint32_t o16 = static_cast<uint32_t>(r) * 128u + sw16[j & 3];
+        const float2 kk = unpack_bf16x2(S.u32(sb + SM_KB + rg16_64 + o16));
+        const float2 qq = unpack_bf16x2(S.u32(a3 + rg16_128 + 64 * 128 + o16));
+        ssk[j] = kk.x * kk.x + kk.y * kk.y;
+        ssq[j] = qq.x * qq.x + qq.y * qq.y;
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) {
+          ssk[j] += __shfl_xor_sync(0xffffffffu, ssk[j], off);
+          ssq[j] += __shfl_xor_sync(0xffffffffu, ssq[j], off);
+        }
+        if ((lane & 15) == 0)
+          S.u64(tab + static_cast<uint32_t>(r * 4 + (warp & 3)) * 8u) =
+              make_uint2(__float_as_uint(ssk[j]), __float_as_uint(ssq[j]));
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = rbase + (j & 3) + 8 * (j >> 2);
+        float tk = 0.f, tq = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint2 e = S.u64(tab + static_cast<uint32_t>(r * 4 + w) * 8u);
+          tk += __uint_as_float(e.x);
+          tq += __uint_as_float(e.y);
+        }
+        const float ik = tk > 0.f ? rsqrtf(tk) : 0.f, iq = tq > 0.f ? rsqrtf(tq) : 0.f;
+        const uint32_t o16 = static_cast<uint32_t>(r) * 128u + sw16[j & 3];
+        const uint32_t ak = sb + SM_KB + rg16_64 + o16, aq = a3 + rg16_128 + 64 * 128 + o16;
+        const float2 kk = unpack_bf16x2(S.u32(ak)), qq = unpack_bf16x2(S.u32(aq));
+        S.u32(ak) = pack_bf16x2(kk.x * ik, kk.y * ik);
+        S.u32(aq) = pack_bf16x2(qq.x * iq, qq.y * iq);
+      }
+      // each thread now reads only its own normalised elements
+    }
 
     // ---- element phase B: scaled operands, one row-block pair at a time -----------------
     // Pass pp builds the tf32 operands of sub-tiles {2pp, 2pp+1} and runs their
@@ -538,15 +608,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               // rows 32 lb + (r - 16R) (KE) and +16 (QE), lb = R - 2pp:
               // byte offset r * 128 + 2048 R - 8192 pp, same swizzle phase as r
               const uint32_t ab = sb + SM_APB + rg32_b + o32 + 2048u * R - 8192u * pp;
-              S.u64(ab) = make_uint2(to_tf32(ke0), to_tf32(ke1));
-              S.u64(ab + 16 * 128) = make_uint2(to_tf32(qe0), to_tf32(qe1));
+              S.u64(ab) = make_uint2(tf32_rna(ke0), tf32_rna(ke1));
+              S.u64(ab + 16 * 128) = make_uint2(tf32_rna(qe0), tf32_rna(qe1));
             }
 #pragma unroll
             for (int rl = 0; rl < 2; ++rl) {
               const int rp = 2 * pp + rl;
               if (rp >= R)
                 S.u64(sb + SM_APA + rg32_a + 64 * 128 * rl + o32) =
-                    make_uint2(to_tf32(kb0 * f0[rp]), to_tf32(kb1 * f1[rp]));
+                    make_uint2(tf32_rna(kb0 * f0[rp]), tf32_rna(kb1 * f1[rp]));
             }
             if (pp == 1) {
               S.u32(a_kb) = pack_bf16x2(ke0 * x0, ke1 * x1);
@@ -570,8 +640,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (mma_pending) { aborted = true; break; }
     }
 
-    // zero A5 (its upper block stays zero; -P fills the lower block)
-    for (int x = tid; x < 1024; x += TC_THREADS) S.u128(sb + SM_A5 + 16 * x) = make_uint4(0, 0, 0, 0);
+    // zero A5 (its upper block stays zero; -P fills the lower block) and T'
+    // (rows >= 64 and the upper triangle stay zero; the T blocks fill the rest)
+    for (int x = tid; x < 1024; x += TC_THREADS) {
+      S.u128(sb + SM_A5 + 16 * x) = make_uint4(0, 0, 0, 0);
+      S.u128(sb + SM_TP + 16 * x) = make_uint4(0, 0, 0, 0);
+    }
     __syncthreads();
     {
       // Pair q4 >> 1 of the products: lanes < 64 (rows i of Khat_2pair) hold
@@ -612,8 +686,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int r = m + 1; r < 16; ++r)
           x[r] -= S.f32(sb + SM_AKK + 4 * ((o + r) * 65 + o + m)) * x[m];
       }
+      const float bj = S.f32(sb + MS_BETA + 4 * (o + jc));
 #pragma unroll
-      for (int r = 0; r < 16; ++r) S.f32(sb + SM_TF + 4 * ((o + r) * 65 + o + jc)) = x[r];
+      for (int r = 0; r < 16; ++r) {
+        S.f32(sb + SM_TF + 4 * ((o + r) * 65 + o + jc)) = x[r];
+        if (r >= jc) {  // T' = T diag(beta) in bf16 (upper triangle stays zero)
+          __nv_bfloat16 tb = __float2bfloat16_rn(x[r] * bj);
+          S.u16(sb + SM_TP + sw128_off(o + r, o + jc, REG128)) =
+              *reinterpret_cast<unsigned short *>(&tb);
+        }
+      }
     }
     __syncthreads();
     // Off-diagonal blocks, one block column J per warp (warps 0..2), top to
@@ -645,30 +727,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           dst[g * 65 + 8 * nt + 2 * t + 1] = -e[nt][1];
           dst[(g + 8) * 65 + 8 * nt + 2 * t] = -e[nt][2];
           dst[(g + 8) * 65 + 8 * nt + 2 * t + 1] = -e[nt][3];
+          // T' = T diag(beta) in bf16, two adjacent columns per store
+          const int col = 16 * J + 8 * nt + 2 * t;
+          const float b0 = S.f32(sb + MS_BETA + 4 * col), b1 = S.f32(sb + MS_BETA + 4 * (col + 1));
+          S.u32(sb + SM_TP + sw128_off(16 * Rr + g, col, REG128)) =
+              pack_bf16x2(-e[nt][0] * b0, -e[nt][1] * b1);
+          S.u32(sb + SM_TP + sw128_off(16 * Rr + g + 8, col, REG128)) =
+              pack_bf16x2(-e[nt][2] * b0, -e[nt][3] * b1);
         }
         __syncwarp();
       }
     }
-    __syncthreads();
-    // T' = T diag(beta) in bf16, K-major [128 rows x 64]; rows >= 64 and the upper triangle zero.
-    for (int x = tid; x < 128 * 8; x += TC_THREADS) {
-      const int row = x >> 3, ch = x & 7;
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-      if (row < 64) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i0 = 8 * ch + 2 * e;
-          const float t0v = (i0 <= row) ? S.f32(sb + SM_TF + 4 * (row * 65 + i0)) *
-                                              S.f32(sb + MS_BETA + 4 * i0) : 0.f;
-          const float t1v = (i0 + 1 <= row) ? S.f32(sb + SM_TF + 4 * (row * 65 + i0 + 1)) *
-                                                  S.f32(sb + MS_BETA + 4 * (i0 + 1)) : 0.f;
-          w[e] = pack_bf16x2(t0v, t1v);
-        }
-      }
-      S.u128(sb + SM_TP + row * 128 + (static_cast<uint32_t>(ch ^ (row & 7)) << 4)) =
-          make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    fence_proxy_async();
+    fence_proxy_async();  // T' was written by the T blocks above
     tc_fence_before();
     __syncthreads();
 
@@ -682,10 +752,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     mma_pending = true;
     if (!wait_mma()) { aborted = true; break; }
-    if (tid == 0 && n + 1 < n_chunks) {  // k and v of the next chunk
-      fence_proxy_async();
-      issue_kv(n + 1);
-    }
+    if (tid == kTmaThread && n + 1 < n_chunks) issue_kv(n + 1);  // next chunk's k and v
     if (n + 1 < n_chunks) kv_pending = true;
 
     // -Wk -> A3 rows 0..63;  S (fp32, TMEM) -> fp16 S for the MMA, then S *= e^{G_last}.
@@ -871,7 +938,8 @@ cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
                               const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
                               int64_t fixed_len, int H, const float *S0, kda_bf16 *o,
                               float *S_final, float *snaps, const int64_t *snap_offsets,
-                              int *status, int zero_v, int s0_identity, cudaStream_t stream) {
+                              int *status, int zero_v, int s0_identity, const int32_t *slots,
+                              unsigned pre, cudaStream_t stream) {
   CUtensorMap mq, mk, mz, mv;
   if (!make_map(&mq, q, total_tokens, H, TD) || !make_map(&mk, k, total_tokens, H, TD) ||
       !make_map(&mz, z, total_tokens, H, TD) ||
@@ -882,7 +950,7 @@ cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
                                          static_cast<int>(TC_SMEM_BYTES));
   if (err != cudaSuccess) return err;
   TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, H, S0, o, S_final, snaps, snap_offsets,
-               status, zero_v, s0_identity};
+               status, slots, zero_v, s0_identity, pre};
   const dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(n_seq));
   prefill_tc_kernel<<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(mq, mk, mz, mv, prm);
   return cudaGetLastError();

@@ -335,3 +335,74 @@ ALL_PINS = [
     pin_beta0_cumprod, pin_gla_closed_form, pin_erase_is_second_order, pin_retrieval,
     pin_decay_floor, pin_chunk_form, pin_linearity, pin_state_passing, pin_norm_bound,
 ]
+
+
+# --- input pre-ops (L2 norm of q, k rows; sigmoid of beta) -------------------------------
+
+def _pre(pre):
+    if pre is None:
+        from oracle import preops as pre
+    return pre
+
+
+def pin_preop_l2norm(orc, pre=None):
+    """Unit rows by hand (a 3-4-5 triangle, a 2x2x... cube diagonal, a signed
+    axis vector), a zero row, and for random rows: unit length, the same
+    direction, and no change under a positive rescale of the row."""
+    pre = _pre(pre)
+    x = np.array([[3.0, 4.0, 0.0, 0.0], [1.0, 1.0, 1.0, 1.0], [0.0, -2.5, 0.0, 0.0],
+                  [0.0, 0.0, 0.0, 0.0]])
+    want = np.array([[0.6, 0.8, 0.0, 0.0], [0.5, 0.5, 0.5, 0.5], [0.0, -1.0, 0.0, 0.0],
+                     [0.0, 0.0, 0.0, 0.0]])
+    _close(pre.l2_normalize_rows(x), want, 1e-15, "hand-normalised rows")
+    rng = _rng(21)
+    r = rng.standard_normal((5, 3, 16)) * rng.uniform(0.1, 30.0, (5, 3, 1))
+    u = pre.l2_normalize_rows(r)
+    _close(np.sum(u * u, axis=-1), np.ones((5, 3)), 1e-14, "unit length")
+    cos = np.sum(u * r, axis=-1) ** 2 / np.sum(r * r, axis=-1)
+    _close(cos, np.ones((5, 3)), 1e-14, "same direction (cos^2 = 1)")
+    assert np.all(np.sum(u * r, axis=-1) > 0), "direction flipped"
+    _close(pre.l2_normalize_rows(r * 7.25), u, 1e-14, "rescale invariance")
+
+
+def pin_preop_sigmoid(orc, pre=None):
+    """Logistic values fixed by logarithms: sigma(0) = 1/2, sigma(ln 3) = 3/4,
+    sigma(-ln 3) = 1/4, sigma(ln 9) = 9/10; saturation without overflow; and
+    the derivative identity sigma' = sigma (1 - sigma) by central differences."""
+    pre = _pre(pre)
+    x = np.array([0.0, math.log(3.0), -math.log(3.0), math.log(9.0), 800.0, -800.0])
+    want = np.array([0.5, 0.75, 0.25, 0.9, 1.0, 0.0])
+    _close(pre.sigmoid(x), want, 1e-15, "sigmoid at log points")
+    xs = np.linspace(-6.0, 6.0, 49)
+    h = 1e-5
+    d = (pre.sigmoid(xs + h) - pre.sigmoid(xs - h)) / (2 * h)
+    s = pre.sigmoid(xs)
+    _close(d, s * (1 - s), 1e-8, "sigmoid derivative identity")
+
+
+def pin_preop_prefill_invariance(orc, pre=None):
+    """The recurrence on raw inputs after the pre-ops equals the recurrence on
+    the unit rows and beta themselves: q, k given with arbitrary positive row
+    scales (different for q and k), beta given as its logit."""
+    pre = _pre(pre)
+    rng = _rng(22)
+    T, H, dk, dv = 70, 2, 8, 6
+    q, k, v, z, beta, A = _rand_inputs(rng, T, H, dk, dv)
+    cq = rng.uniform(0.05, 20.0, (T, H, 1))
+    ck = rng.uniform(0.05, 20.0, (T, H, 1))
+    logit = np.log(beta / (1.0 - beta))
+    q2, k2, b2 = pre.apply(q * cq, k * ck, logit, True, True)
+    ref = orc.prefill(q, k, v, z, beta, A)
+    got = orc.prefill(q2, k2, v, z, b2, A)
+    _close(got["o"], ref["o"], 1e-12, "outputs after the pre-ops")
+    _close(got["S_final"], ref["S_final"], 1e-12, "state after the pre-ops")
+    # each switch alone leaves the other input untouched
+    q3, k3, b3 = pre.apply(q * cq, k * ck, logit, False, True)
+    _close(q3, q * cq, 0.0, "q without the norm switch")
+    _close(b3, beta, 1e-13, "beta with the sigmoid switch")
+    q4, k4, b4 = pre.apply(q * cq, k * ck, logit, True, False)
+    _close(k4, k, 1e-14, "k with the norm switch")
+    _close(b4, logit, 0.0, "beta without the sigmoid switch")
+
+
+PREOP_PINS = [pin_preop_l2norm, pin_preop_sigmoid, pin_preop_prefill_invariance]

@@ -88,6 +88,51 @@ def test_state_snapshot_rejects_before_launch(L, kw, status):
     assert L.kda_state_snapshot(*a.values()) == status
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=80), 4), (dict(n=-1), 2), (dict(slots=None), 1), (dict(cu=None), 1),
+    (dict(pool=None), 1), (dict(o=ctypes.c_void_p(0x10008)), 3), (dict(n=0, total=0), 0),
+])
+def test_decode_tokens_rejects_before_launch(L, kw, status):
+    fake = ctypes.c_void_p(0x10000)
+    a = dict(q=fake, k=fake, v=fake, z=fake, beta=fake, A=fake, gmin=-5.0, cu=fake, n=4,
+             total=20, H=2, dk=64, dv=64, pre=0, pool=fake, slots=fake, commit=1, o=fake,
+             stream=None)
+    a.update(kw)
+    assert L.kda_decode_tokens(*a.values()) == status
+
+
+def _ex_args(**kw):
+    """kda_chunk_fwd_ex arguments: kda_chunk_fwd's with `pre` after chunk."""
+    args = _chunk_args(**{k: v for k, v in kw.items() if k != "pre"})
+    return args[:14] + [kw.get("pre", 0)] + args[14:]
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(pre=4), 4), (dict(pre=0x80000000), 4), (dict(pre=3, dk=96), 4),
+    (dict(pre=3, q=None), 1), (dict(pre=1, H=0), 2), (dict(pre=3, n_seq=0, total=0), 0),
+    (dict(pre=2, q=ctypes.c_void_p(0x10008)), 3),
+])
+def test_chunk_fwd_ex_rejects_before_launch(L, kw, status):
+    assert L.kda_chunk_fwd_ex(*_ex_args(**kw)) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(pre=8), 4), (dict(pre=3, dk=48), 4), (dict(pre=3, q=None), 1), (dict(pre=1, n=0), 0),
+])
+def test_decode_step_ex_rejects_before_launch(L, kw, status):
+    fake = ctypes.c_void_p(0x10000)
+    a = dict(q=fake, k=fake, v=fake, z=fake, beta=fake, A=fake, gmin=-5.0, pool=fake, slots=None,
+             n=4, H=2, dk=64, dv=64, pre=0, o=fake, stream=None)
+    a.update(kw)
+    assert L.kda_decode_step_ex(*a.values()) == status
+
+
+def test_decode_tokens_rejects_unknown_pre_flags(L):
+    fake = ctypes.c_void_p(0x10000)
+    assert L.kda_decode_tokens(fake, fake, fake, fake, fake, fake, -5.0, fake, 4, 20, 2, 64, 64,
+                               16, fake, fake, 1, fake, None) == 4
+
+
 def test_workspace_query_is_pure_host(L):
     assert L.kda_chunk_fwd_workspace_bytes(4, 4 * 8192, 16, 128, 128, 64) >= 0
 

@@ -16,6 +16,7 @@ import torch
 
 import kda_inputs
 import oracle
+from oracle import preops
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +50,7 @@ def s_err(S_gpu, S_ref):
     return float(np.linalg.norm(S_gpu - S_ref) / max(np.linalg.norm(S_ref), 1e-30))
 
 
-def run_prefill(kda, x, snapshots=True, S0=True):
+def run_prefill(kda, x, snapshots=True, S0=True, pre=0):
     n_seq = len(x["lengths"])
     total, H, dk = x["k"].shape
     dv = x["v"].shape[2]
@@ -61,15 +62,16 @@ def run_prefill(kda, x, snapshots=True, S0=True):
     o = torch.full((total, H, dv), float("nan"), dtype=torch.bfloat16, device=dev)
     kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], cu_seqlens=x["cu_seqlens"],
                   S0=x["S0"] if S0 else None, o=o, S_final=S_final, snaps=snaps,
-                  snap_offsets=offs if snapshots else None)
+                  snap_offsets=offs if snapshots else None, pre=pre)
     torch.cuda.synchronize()
     assert kda.device_status() == 0
     return o, S_final, snaps, offs
 
 
-def oracle_subset(x, seqs, heads, t_limit=None, snapshots=True):
+def oracle_subset(x, seqs, heads, t_limit=None, snapshots=True, pre=0):
     """Oracle on sequences ``seqs`` and heads ``heads`` (optionally only the
-    first t_limit tokens of each sequence).  Inputs are gathered on the host."""
+    first t_limit tokens of each sequence).  Inputs are gathered on the host;
+    ``pre`` applies the oracle's own input pre-ops to them first."""
     cu = x["cu_seqlens"].cpu().numpy().astype(np.int64)
     hs = torch.tensor(heads, device=x["k"].device)
     parts = {n: [] for n in ("q", "k", "v", "z", "beta")}
@@ -81,6 +83,9 @@ def oracle_subset(x, seqs, heads, t_limit=None, snapshots=True):
         for n in parts:
             parts[n].append(f64(x[n][a:a + L].index_select(1, hs)))
     cat = {n: np.concatenate(parts[n], axis=0) for n in parts}
+    if pre:
+        cat["q"], cat["k"], cat["beta"] = preops.apply(cat["q"], cat["k"], cat["beta"],
+                                                       bool(pre & 1), bool(pre & 2))
     S0 = None
     if x["S0"] is not None:
         S0 = f64(x["S0"][torch.tensor(seqs, device=x["k"].device)].index_select(1, hs))
@@ -108,13 +113,13 @@ def gather_gpu(x, o, S_final, snaps, offs, seqs, heads, t_limit=None):
             np.concatenate(sn) if sn else None)
 
 
-def check_all(x, kda, seqs=None, heads=None, t_limit=None):
-    o, S_final, snaps, offs = run_prefill(kda, x)
+def check_all(x, kda, seqs=None, heads=None, t_limit=None, pre=0):
+    o, S_final, snaps, offs = run_prefill(kda, x, pre=pre)
     n_seq = len(x["lengths"])
     H = x["k"].shape[1]
     seqs = list(range(n_seq)) if seqs is None else seqs
     heads = list(range(H)) if heads is None else heads
-    ref = oracle_subset(x, seqs, heads, t_limit)
+    ref = oracle_subset(x, seqs, heads, t_limit, pre=pre)
     go, gs, gsn = gather_gpu(x, o, S_final, snaps, offs, seqs, heads, t_limit)
     e_o = o_err(go, ref["o"])
     assert np.all(np.isfinite(go)), "non-finite outputs"
@@ -194,6 +199,30 @@ def test_segment_scan_long_sequences(kda, S0_std):
     assert o_err(f64(o), ref["o"]) <= O_TOL
     assert s_err(f64(S_final), ref["S_final"]) <= S_TOL
     assert s_err(f64(snaps), ref["snaps"]) <= S_TOL
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_tokens_multi_token(kda, d):
+    """Multi-token decode / speculative verify on resident states: runs of 1 to
+    70 tokens per sequence from state slots; commit=False leaves the pool
+    untouched, commit=True stores the final states; both match the oracle."""
+    lengths = [1, 2, 5, 16, 17, 40, 64, 70]
+    n, H = len(lengths), 2
+    x = kda_inputs.make_prefill(H, d, d, lengths, seed=23, device="cuda", S0_std=0.02)
+    perm = torch.tensor([5, 2, 7, 0, 3, 6, 1, 4], dtype=torch.int32, device="cuda")
+    pool = torch.zeros((8, H, d, d), device="cuda")
+    pool[perm.long()] = x["S0"]
+    before = pool.clone()
+    args = [x[nm] for nm in ("q", "k", "v", "z", "beta")] + [x["A"]]
+    o_v = kda.decode_tokens(*args, pool, perm, x["cu_seqlens"], commit=False)
+    torch.cuda.synchronize()
+    assert torch.equal(pool, before)
+    o_c = kda.decode_tokens(*args, pool, perm, x["cu_seqlens"], commit=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o_v, o_c)
+    ref = oracle_subset(x, list(range(n)), [0, 1], snapshots=False)
+    assert o_err(f64(o_c), ref["o"]) <= O_TOL
+    assert s_err(f64(pool[perm.long()]), ref["S_final"]) <= S_TOL
 
 
 def test_decode_1000_steps(kda):
@@ -343,3 +372,69 @@ def test_runs_on_a_side_stream(kda):
     s.synchronize()
     ref = oracle_subset(x, [0], [0, 1], snapshots=False)
     assert o_err(f64(o), ref["o"]) <= O_TOL
+
+
+# --- fused input pre-ops (L2 norm of q, k rows; sigmoid of beta) -------------------------
+
+@pytest.mark.parametrize("d,pre", [(128, 3), (64, 3), (128, 1), (128, 2)])
+def test_preops_prefill(kda, d, pre):
+    """Raw projections (q, k rows of norm 0.25..4 x sqrt(d), beta logits): the
+    kernels' fused pre-ops against the oracle's pre-ops followed by the
+    oracle, ragged varlen batch with S0; d = 128 runs the tensor-core kernel,
+    d = 64 the SIMT kernel."""
+    x = kda_inputs.make_raw_prefill(3, d, d, [200, 64, 1, 130], seed=41 + pre, device="cuda",
+                                    S0_std=0.02)
+    if not pre & 1:  # norm pre-op off: hand in unit rows, as the plain entry point expects
+        for nm in ("q", "k"):
+            t = x[nm].float()
+            x[nm] = (t / torch.linalg.vector_norm(t, dim=-1, keepdim=True)).to(torch.bfloat16)
+    if not pre & 2:
+        x["beta"] = torch.sigmoid(x["beta"].float()).to(torch.bfloat16)
+    check_all(x, kda, pre=pre)
+
+
+def test_preops_segment_scan(kda):
+    """The scan's three prefill passes all apply the pre-ops (2 x 16,384
+    tokens, H = 2: 4 segments of 4096 per chain)."""
+    x = kda_inputs.make_raw_prefill(2, 128, 128, [16384, 16384], seed=45, device="cuda",
+                                    S0_std=0.02)
+    assert kda.workspace_bytes(2, 2 * 16384, 2, 128, 128) > 0
+    S_final = torch.full((2, 2, 128, 128), float("nan"), device="cuda")
+    o = kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], n_seq=2, S0=x["S0"],
+                      S_final=S_final, pre=kda.PRE_L2NORM_QK | kda.PRE_SIGMOID_BETA)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    ref = oracle_subset(x, [0, 1], [0, 1], snapshots=False, pre=3)
+    assert o_err(f64(o), ref["o"]) <= O_TOL
+    assert s_err(f64(S_final), ref["S_final"]) <= S_TOL
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_preops_decode(kda, d):
+    """kda_decode_step_ex and kda_decode_tokens with the pre-ops: 20 chained
+    single-token steps, then a 2..33-token run per sequence."""
+    n, H = 6, 2
+    pool = kda_inputs.make_prefill(H, d, d, [1] * n, seed=46, device="cuda",
+                                   S0_std=0.02)["S0"].contiguous()
+    state = np.ascontiguousarray(f64(pool))
+    A = None
+    for step in range(20):
+        t = kda_inputs.make_raw_prefill(H, d, d, [1] * n, seed=1000 + step, device="cuda")
+        A = t["A"] if A is None else A
+        o = kda.decode_step(t["q"], t["k"], t["v"], t["z"], t["beta"], A, pool, pre=3)
+        qf, kf, bf = preops.apply(f64(t["q"]), f64(t["k"]), f64(t["beta"]), True, True)
+        o_ref = oracle.decode_step(qf, kf, f64(t["v"]), f64(t["z"]), bf, f64(A), state)
+        assert o_err(f64(o), o_ref) <= O_TOL
+    torch.cuda.synchronize()
+    assert s_err(f64(pool), state) <= DECODE_TOL
+    lengths = [2, 3, 9, 16, 33, 5]
+    x = kda_inputs.make_raw_prefill(H, d, d, lengths, seed=47, device="cuda")
+    x["A"] = A
+    x["S0"] = pool.clone()
+    slots = torch.arange(n, dtype=torch.int32, device="cuda")
+    o = kda.decode_tokens(x["q"], x["k"], x["v"], x["z"], x["beta"], A, pool, slots,
+                          x["cu_seqlens"], commit=True, pre=3)
+    torch.cuda.synchronize()
+    ref = oracle_subset(x, list(range(n)), [0, 1], snapshots=False, pre=3)
+    assert o_err(f64(o), ref["o"]) <= O_TOL
+    assert s_err(f64(pool), ref["S_final"]) <= S_TOL

@@ -78,3 +78,52 @@ def test_unmodified_copy_passes(tmp_path):
 def test_mutant_is_caught(tmp_path, name, old, new):
     failed = _failures(tmp_path, name, old, new)
     assert failed, f"no pin catches the planted mistake '{name}'"
+
+
+# Planted mistakes in the oracle's input pre-ops (a Python module: the variant
+# is imported from a copy and the pre-op pins run against it in-process).
+PRE_SRC = os.path.join(os.path.dirname(oracle.__file__), "preops.py")
+PRE_MUTANTS = [
+    ("norm without square root", "norm = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))",
+     "norm = np.sum(x * x, axis=-1, keepdims=True)"),
+    ("norm over the token axis", "np.sum(x * x, axis=-1, keepdims=True)",
+     "np.sum(x * x, axis=0, keepdims=True)"),
+    ("sigmoid branches swapped", "np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))",
+     "np.where(x >= 0, e / (1.0 + e), 1.0 / (1.0 + e))"),
+    ("sigmoid without abs", "e = np.exp(-np.abs(x))", "e = np.exp(-x)"),
+    ("k left raw", "q, k = l2_normalize_rows(q), l2_normalize_rows(k)",
+     "q, k = l2_normalize_rows(q), k"),
+    ("q normalised by k", "q, k = l2_normalize_rows(q), l2_normalize_rows(k)",
+     "q, k = q / np.linalg.norm(k, axis=-1, keepdims=True), l2_normalize_rows(k)"),
+]
+
+
+def _pre_failures(tmp_path, orc, old, new):
+    import importlib.util
+
+    import oracle_pins
+    text = open(PRE_SRC).read()
+    if old is not None:
+        assert text.count(old) == 1, f"mutation anchor {old!r} must occur once"
+        text = text.replace(old, new)
+    path = tmp_path / "preops_variant.py"
+    path.write_text(text)
+    spec = importlib.util.spec_from_file_location("preops_variant", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    failed = []
+    for pin in oracle_pins.PREOP_PINS:
+        try:
+            pin(orc, pre=mod)
+        except Exception:
+            failed.append(pin.__name__)
+    return failed
+
+
+def test_unmodified_preops_pass(tmp_path, orc):
+    assert _pre_failures(tmp_path, orc, None, None) == []
+
+
+@pytest.mark.parametrize("name,old,new", PRE_MUTANTS, ids=[m[0] for m in PRE_MUTANTS])
+def test_preop_mutant_is_caught(tmp_path, orc, name, old, new):
+    assert _pre_failures(tmp_path, orc, old, new), f"no pin catches '{name}'"

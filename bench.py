@@ -67,36 +67,50 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms.
+
+    Entering starts nvidia-smi and waits (up to 5 s) for its first sample, so
+    that sampling is running before the timed region starts; ``window(t0, t1)``
+    then keeps the samples taken between those host times (time.monotonic())
+    plus one interval, i.e. during the timed region."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, gpu_id):
         self.gpu_id = gpu_id
         self.proc = None
         self.lines = []
         self.thread = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_id), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            deadline = time.monotonic() + 5.0
+            while not self.lines and time.monotonic() < deadline and self.proc.poll() is None:
+                time.sleep(0.005)
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(2 * self.INTERVAL_MS / 1e3)  # the sample that closes the window
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -108,7 +122,11 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in self.lines:
+        lines = self.lines
+        if self.t0 is not None:
+            slack = self.INTERVAL_MS / 1e3
+            lines = [(t, l) for t, l in lines if self.t0 <= t <= self.t1 + slack]
+        for _, line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 7:
                 continue
@@ -253,10 +271,13 @@ def run_ours(args, rank, world, local):
     o = torch.empty((B * T, H, dv), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    ws_bytes = kda.workspace_bytes(B, B * T, H, dk, dv)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
     def step():
         kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
                       cu_seqlens=x["cu_seqlens"], o=o, S_final=S_final, snaps=snaps,
-                      snap_offsets=offs, stream=stream)
+                      snap_offsets=offs, workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -275,6 +296,7 @@ def run_ours(args, rank, world, local):
     with ClockSampler(gpu_id) as clocks:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        h0 = time.monotonic()
         t0.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
@@ -282,6 +304,7 @@ def run_ours(args, rank, world, local):
             ev[i][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
+        clocks.window(h0, time.monotonic())
     barrier(world)
     elapsed_ms = reduce_max(t0.elapsed_time(t1), world)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
@@ -300,7 +323,8 @@ def run_ours(args, rank, world, local):
                            "peak_tflops": tc_peak,
                            "frac": alg_flops / avg_launch_s / 1e12 / tc_peak}}
 
-    e2e = None if args.no_e2e else run_e2e(args, x, o, S_final, snaps, offs, stream, world, B, T)
+    e2e = None if args.no_e2e else run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world,
+                                           B, T)
     decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak, peak_src, world)
 
     cpu_baseline = None
@@ -324,7 +348,7 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, x, o, S_final, snaps, offs, stream, world, B, T):
+def run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world, B, T):
     """The same step through the public API with host buffers: pinned host
     inputs -> device -> kda_chunk_fwd -> host outputs, all inside the timed
     region."""
@@ -346,7 +370,7 @@ def run_e2e(args, x, o, S_final, snaps, offs, stream, world, B, T):
             dev_in[n].copy_(t, non_blocking=True)
         kda.chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["z"], dev_in["beta"],
                       dev_in["A"], cu_seqlens=dev_in["cu_seqlens"], o=o, S_final=S_final,
-                      snaps=snaps, snap_offsets=offs, stream=stream)
+                      snaps=snaps, snap_offsets=offs, workspace=ws, stream=stream)
         host_out["o"].copy_(o, non_blocking=True)
         host_out["S_final"].copy_(S_final, non_blocking=True)
         host_out["snaps"].copy_(snaps, non_blocking=True)
@@ -425,7 +449,7 @@ def run_decode(args, dev, stream, hbm_peak, peak_src, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--decode-steps", type=int, default=1000)

@@ -56,8 +56,9 @@ typedef uint16_t kda_bf16;                 /* raw bfloat16 bit pattern */
  *   q <- q / ||q||_2, k <- k / ||k||_2   per (token, head) row, in fp32
  *                                         (an all-zero row stays zero), and
  *   beta <- 1 / (1 + exp(-beta)),
- * right after loading them, before any other use.  The tensor-core prefill
- * rounds the normalised q, k back to bf16 (its operands are bf16). */
+ * right after loading them, before any other use.  The normalised rows are
+ * kept in fp32 until they are combined with the decay factors (rounding them
+ * to bf16 first would move the outputs by about 2.4e-2 RMS). */
 #define KDA_PRE_L2NORM_QK 1u
 #define KDA_PRE_SIGMOID_BETA 2u
 typedef struct CUstream_st *kda_stream_t;  /* same type as cudaStream_t */
@@ -80,15 +81,24 @@ const char *kda_status_string(int status);
 int kda_version(void);
 
 /*
- * Workspace bytes kda_chunk_fwd needs for these sizes (may be 0).  Pure
- * host arithmetic; returns 0 for unsupported sizes as well.  It is non-zero
- * only for equal-length batches (cu_seqlens NULL) with dk = dv = 128 whose
- * (sequence, head) chains would fill under a quarter of the GPU (n_seq * H
- * <= 38) and whose sequences are long: those run as a segment-parallel scan
- * (each segment's zero-start state N and transition M, an fp32 chain
- * S_start[g+1] = M_g S_start[g] + N_g, then a pass from the true segment
- * starts), which keeps three [n_seq * n_segs, H, 128, 128] fp32 arrays in the
- * workspace.  Calls with cu_seqlens need no workspace.
+ * Workspace bytes for the fastest kda_chunk_fwd path at these sizes (0 when
+ * that path needs none).  Pure host arithmetic; 0 for unsupported sizes.
+ *  - Equal-length batches (cu_seqlens NULL) with dk = dv = 128 whose
+ *    (sequence, head) chains would fill under a quarter of the GPU (n_seq * H
+ *    <= 38) and whose sequences are long run as a segment-parallel scan (each
+ *    segment's zero-start state N and transition M, an fp32 chain
+ *    S_start[g+1] = M_g S_start[g] + N_g, then a pass from the true segment
+ *    starts): three [n_seq * n_segs, H, 128, 128] fp32 arrays.  This path
+ *    REQUIRES its workspace (KDA_ERR_WORKSPACE otherwise).
+ *  - Other dk = dv = 128 calls run in two passes when the workspace allows:
+ *    a parallel pass prepares every (chunk, head)'s state-independent part
+ *    (73 KiB records), then one pass per (sequence, head) carries the state.
+ *    The value returned holds the records of all heads for up to
+ *    ceil(total_tokens / 64) + n_seq chunks (any split of the tokens), plus a
+ *    small table.  A smaller workspace makes the call run the heads in
+ *    groups; one too small for a single head's records, or none, makes it
+ *    run the single-pass kernel instead.  Either way the results are the same
+ *    up to rounding.
  */
 size_t kda_chunk_fwd_workspace_bytes(int n_seq, int64_t total_tokens, int H, int dk, int dv,
                                      int chunk);
@@ -113,8 +123,9 @@ size_t kda_chunk_fwd_workspace_bytes(int n_seq, int64_t total_tokens, int H, int
  *               a [rows, H, dk, dv] fp32 array.  S0 itself is not a snapshot.
  *   snap_offsets device int64 [n_seq + 1], prefix sums of floor(L_s / 64);
  *               may be NULL only when cu_seqlens is NULL (rows s * (T / 64)).
- *   workspace   device scratch of kda_chunk_fwd_workspace_bytes() bytes
- *               (NULL allowed when that is 0), 16-byte aligned; contents need
+ *   workspace   device scratch, 16-byte aligned, of workspace_bytes bytes
+ *               (see kda_chunk_fwd_workspace_bytes: required for the scan,
+ *               optional otherwise; NULL allowed with 0 bytes); contents need
  *               not be zeroed and are garbage afterwards.  Calls sharing one
  *               workspace must not overlap on the GPU.
  *   Errors: KDA_ERR_NULL, _SHAPE, _ALIGN, _UNSUPPORTED, _WORKSPACE, _CUDA.
@@ -146,15 +157,16 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
  * path because it can synchronise the device).  The pages have no
  * counterpart: this is a convenience of this library.
  *
- * Same arguments as kda_chunk_fwd without the workspace.  When the call needs
- * a workspace (kda_chunk_fwd_workspace_bytes() > 0 for an equal-length batch:
- * the segment-parallel scan) it uses a fixed scratch array of
- * KDA_NOALLOC_WORKSPACE_BYTES in device memory that the library holds on
- * every GPU that loads it; calls needing more return KDA_ERR_WORKSPACE
- * before launching anything.  The first call on a device looks up the
- * array's device address (with that device current); make it before any
- * stream capture.  All calls share the array: calls that overlap on the GPU
- * race.  Allocates nothing.
+ * Same arguments as kda_chunk_fwd without the workspace.  When the call
+ * takes the segment-parallel scan (an equal-length batch with few long
+ * chains: kda_chunk_fwd_workspace_bytes() then gives the scan's size) it
+ * uses a fixed scratch array of KDA_NOALLOC_WORKSPACE_BYTES in device memory
+ * that the library holds on every GPU that loads it; calls needing more
+ * return KDA_ERR_WORKSPACE before launching anything.  Every other call runs
+ * the single-pass kernel, which needs no scratch.  The first call on a device
+ * looks up the array's device address (with that device current); make it
+ * before any stream capture.  All calls share the array: calls that overlap
+ * on the GPU race.  Allocates nothing.
  */
 #define KDA_NOALLOC_WORKSPACE_BYTES (32u << 20)
 

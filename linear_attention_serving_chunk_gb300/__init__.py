@@ -160,9 +160,13 @@ def chunk_fwd(q, k, v, z, beta, A, gmin=GMIN, cu_seqlens=None, n_seq=None, S0=No
     if o is None:
         o = torch.empty((total, H, dv), dtype=torch.bfloat16, device=k.device)
     _check(o, "o", torch.bfloat16, (total, H, dv))
-    need = 0 if cu_seqlens is not None else workspace_bytes(n_seq, total, H, dk, dv, chunk)
+    need = workspace_bytes(n_seq, total, H, dk, dv, chunk)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=k.device)
+        if stream is not None and isinstance(stream, torch.cuda.Stream):
+            # allocated on the current stream, used on `stream`: keep the
+            # block out of the allocator until the call's kernels are done
+            workspace.record_stream(stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if pre:
         st = lib().kda_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),

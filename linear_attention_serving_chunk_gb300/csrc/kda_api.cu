@@ -35,6 +35,19 @@ cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
                               float *S_final, float *snaps, const int64_t *snap_offsets,
                               int *status, int zero_v, int s0_identity, const int32_t *slots,
                               unsigned pre, cudaStream_t stream);
+cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                              const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                              const int32_t *cu_seqlens, const int32_t *chunk_start, int n_seq,
+                              int64_t total_tokens, int64_t fixed_len, int H, int h0, int hg,
+                              int64_t max_tasks, uint8_t *rec, int *status, unsigned pre,
+                              int n_ctas, cudaStream_t stream);
+cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
+                              const int32_t *chunk_start, int n_seq, int64_t fixed_len, int H,
+                              int h0, int hg, const float *S0, kda_bf16 *o, float *S_final,
+                              float *snaps, const int64_t *snap_offsets, int *status,
+                              const int32_t *slots, cudaStream_t stream);
+cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int32_t *chunk_start,
+                               cudaStream_t stream);
 cudaError_t segment_combine_launch(const float *M, const float *N, const float *S0,
                                    float *S_start, float *S_final, int n_seq, int n_segs, int H,
                                    cudaStream_t stream);
@@ -76,6 +89,36 @@ size_t scan_workspace_bytes(int n_seq, int H, const ScanPlan &plan) {
   return 3 * static_cast<size_t>(n_seq) * plan.n_segs * H * 128 * 128 * sizeof(float);
 }
 
+// Two-pass prefill (dk = dv = 128): a chunk-preparation pass over every
+// (chunk, head) of a group of hg heads, then the state pass over that group's
+// chains.  Workspace: the varlen chunk-start table (1 KiB granules), then one
+// record per (chunk, head of the group).  The chunk count is bounded by
+// ceil(total / 64) + n_seq, which covers any split of the tokens.
+constexpr size_t kRecordBytes = 73 * 1024;  // kRecBytes of kda_split.cuh
+
+size_t split_table_bytes(int n_seq) {
+  return ((static_cast<size_t>(n_seq) + 1) * sizeof(int32_t) + 1023) / 1024 * 1024;
+}
+
+int64_t split_max_chunks(int n_seq, int64_t total_tokens) {
+  return (total_tokens + 63) / 64 + n_seq;
+}
+
+size_t split_workspace_bytes(int n_seq, int64_t total_tokens, int hg) {
+  return split_table_bytes(n_seq) +
+         static_cast<size_t>(split_max_chunks(n_seq, total_tokens)) * hg * kRecordBytes;
+}
+
+// Largest head group whose records fit in `bytes` (0: none fits).
+int split_heads(int n_seq, int64_t total_tokens, int H, size_t bytes) {
+  const size_t table = split_table_bytes(n_seq);
+  if (bytes <= table) return 0;
+  const size_t per_head =
+      static_cast<size_t>(split_max_chunks(n_seq, total_tokens)) * kRecordBytes;
+  const size_t hg = (bytes - table) / per_head;
+  return static_cast<int>(hg < static_cast<size_t>(H) ? hg : static_cast<size_t>(H));
+}
+
 int *status_word() {
   void *p = nullptr;
   return cudaGetSymbolAddress(&p, g_status) == cudaSuccess ? static_cast<int *>(p) : nullptr;
@@ -92,6 +135,15 @@ bool gmin_ok(float gmin) { return isfinite(gmin) && gmin <= 0.f && gmin >= -5.5f
 bool pre_ok(unsigned pre) { return (pre & ~(KDA_PRE_L2NORM_QK | KDA_PRE_SIGMOID_BETA)) == 0; }
 
 }  // namespace
+
+// Workspace the segment-parallel scan needs at these sizes (0: no scan).
+size_t chunk_fwd_scan_bytes(int n_seq, int64_t total_tokens, int H, int dk, int dv, int chunk) {
+  ScanPlan plan;
+  if (chunk != kChunk || H <= 0 || n_seq <= 0 || total_tokens <= 0 ||
+      !plan_scan(n_seq, total_tokens, H, dk, dv, &plan))
+    return 0;
+  return scan_workspace_bytes(n_seq, H, plan);
+}
 
 }  // namespace kda
 
@@ -117,9 +169,11 @@ int kda_version(void) { return 100; }
 
 size_t kda_chunk_fwd_workspace_bytes(int n_seq, int64_t total_tokens, int H, int dk, int dv,
                                      int chunk) {
+  if (chunk != kChunk || H <= 0 || n_seq <= 0 || total_tokens <= 0) return 0;
   ScanPlan plan;
-  if (chunk != kChunk || H <= 0 || !plan_scan(n_seq, total_tokens, H, dk, dv, &plan)) return 0;
-  return scan_workspace_bytes(n_seq, H, plan);
+  if (plan_scan(n_seq, total_tokens, H, dk, dv, &plan)) return scan_workspace_bytes(n_seq, H, plan);
+  if (!prefill_tc_supported(dk, dv, total_tokens)) return 0;
+  return split_workspace_bytes(n_seq, total_tokens, H);
 }
 
 int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *z,
@@ -189,6 +243,34 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }
   cudaError_t err;
+  const int hg = prefill_tc_supported(dk, dv, total_tokens) && workspace && aligned16(workspace)
+                     ? split_heads(n_seq, total_tokens, H, workspace_bytes)
+                     : 0;
+  if (hg > 0) {
+    // two passes per group of hg heads: chunk preparation, then the state pass
+    int *status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *chunk_start = nullptr;
+    err = cudaSuccess;
+    if (cu_seqlens) {
+      chunk_start = reinterpret_cast<int32_t *>(ws);
+      err = chunk_start_launch(cu_seqlens, n_seq, chunk_start, st);
+    }
+    uint8_t *rec = ws + split_table_bytes(n_seq);
+    const int64_t max_chunks = cu_seqlens ? split_max_chunks(n_seq, total_tokens)
+                                          : static_cast<int64_t>(n_seq) * ((fixed_len + 63) / 64);
+    for (int h0 = 0; h0 < H && err == cudaSuccess; h0 += hg) {
+      const int g = H - h0 < hg ? H - h0 : hg;
+      err = chunk_prep_launch(q, k, v, z, beta, A, gmin, cu_seqlens, chunk_start, n_seq,
+                              total_tokens, fixed_len, H, h0, g, max_chunks * g, rec, status, pre,
+                              kSMs, st);
+      if (err == cudaSuccess)
+        err = state_pass_launch(rec, cu_seqlens, chunk_start, n_seq, fixed_len, H, h0, g, S0, o,
+                                S_final, snaps, snap_offsets, status, nullptr, st);
+    }
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  }
   if (prefill_tc_supported(dk, dv, total_tokens)) {
     int *status = status_word();
     if (!status) return KDA_ERR_CUDA;

@@ -29,6 +29,8 @@
 
 namespace kda {
 
+size_t chunk_fwd_scan_bytes(int n_seq, int64_t total_tokens, int H, int dk, int dv, int chunk);
+
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_workspace[KDA_NOALLOC_WORKSPACE_BYTES];
@@ -61,9 +63,10 @@ extern "C" int kda_chunk_fwd_noalloc(const kda_bf16 *q, const kda_bf16 *k, const
                                      int64_t total_tokens, int H, int dk, int dv, int chunk,
                                      const float *S0, kda_bf16 *o, float *S_final, float *snaps,
                                      const int64_t *snap_offsets, kda_stream_t stream) {
-  // Varlen calls never take the scan and need no scratch.
+  // Only the segment-parallel scan needs scratch (varlen calls never take it);
+  // every other call runs the single-pass kernel, which needs none.
   const size_t need =
-      cu_seqlens ? 0 : kda_chunk_fwd_workspace_bytes(n_seq, total_tokens, H, dk, dv, chunk);
+      cu_seqlens ? 0 : kda::chunk_fwd_scan_bytes(n_seq, total_tokens, H, dk, dv, chunk);
   if (need > KDA_NOALLOC_WORKSPACE_BYTES) return KDA_ERR_WORKSPACE;
   void *ws = nullptr;
   if (need > 0) {

@@ -23,9 +23,12 @@
 // (factors up to e^80) and more than bf16's 8-bit mantissa (outputs are
 // heavy-tailed and P feeds them directly), so they run as kind::tf32
 // (10-bit mantissa, operands rounded to nearest).  T' K~ and T' V use bf16
-// (V arrives as bf16).  The
-// state-dependent products use fp16 operands (11-bit mantissa; |S|, |W|,
-// |Wk| stay far below 65504 for unit keys and beta in [0, 1]).
+// operands (V arrives as bf16) with T' = T diag(beta) split into bf16 hi + lo
+// tiles, two accumulating MMAs each: the diagonal of T' is beta itself, the
+// main write strength, and rounding it to bf16 alone moves the outputs by a
+// few 1e-2 RMS.  The state-dependent products use fp16 operands (11-bit
+// mantissa; |S|, |W|, |Wk| stay far below 65504 for unit keys and beta in
+// [0, 1]).
 //
 // Per chunk (one CTA per (sequence, head), 512 threads, chunks in order):
 //   TMA     q -> A3 lower half, z -> ZB, k -> KB, v -> VB (next chunk's q/z
@@ -44,16 +47,18 @@
 // KDA_ERR_TIMEOUT in the status word and the CTA stops cleanly.
 #include "kda_common.cuh"
 #include "kda_sm100.cuh"
+#include "kda_split.cuh"
+#include "kda_tc_common.cuh"
 
 namespace kda {
 
 namespace {
 
 using namespace sm100;
+using namespace tcx;
 
 constexpr int TC_THREADS = 512;
 constexpr int TD = 128;  // dk = dv handled by this kernel
-constexpr uint32_t KiB = 1024;
 
 // Shared-memory map, byte offsets from the (1024-aligned) dynamic base.
 constexpr uint32_t SM_A3 = 0;                     // 2 x 32 KiB: [-Wk ; q -> -Q~], K-major
@@ -68,7 +73,8 @@ constexpr uint32_t SM_TF = SM_AP + 64 * 65 * 4;   // fp32 [64][65] T
 constexpr uint32_t SM_TY = SM_AP + 34 * KiB;      // fp32 [3][16][17] block products
 constexpr uint32_t SM_SBF = SM_AP;                // [dk x dv] S in fp16, MN-major (after T')
 constexpr uint32_t SM_A5 = SM_AP + 48 * KiB;      // [128 x 64] K-major: [0 ; -P]
-constexpr uint32_t SM_TP = SM_AP + 64 * KiB;      // [128 x 64] K-major: [T diag(beta) ; 0]
+constexpr uint32_t SM_TP = SM_AP + 64 * KiB;      // [128 x 64] K-major: [T diag(beta) ; 0], bf16 hi
+constexpr uint32_t SM_TPL = SM_AP + 80 * KiB;     // the same, bf16 lo (T' - hi)
 constexpr uint32_t SM_WBF = SM_AP + 64 * KiB;     // [tok x dv] W in fp16 (after T' is used)
 
 constexpr uint32_t SM_MISC = 224 * KiB;
@@ -78,15 +84,14 @@ constexpr uint32_t MS_BAR_MMA = SM_MISC + 24;
 constexpr uint32_t MS_TMEM = SM_MISC + 32;
 constexpr uint32_t MS_BETA = SM_MISC + 64;        // 64 fp32
 constexpr uint32_t MS_LAM = SM_MISC + 320;        // [4][128] fp32 sub-tile decay totals
-constexpr uint32_t TC_SMEM_BYTES = MS_LAM + 4 * TD * 4;
+constexpr uint32_t MS_NRM = MS_LAM + 4 * TD * 4;  // [64][2] fp32 1/||k_r||, 1/||q_r|| (pre-op)
+constexpr uint32_t TC_SMEM_BYTES = MS_NRM + 64 * 8;
 static_assert(SM_TF + 64 * 65 * 4 <= SM_TY, "T scratch overlaps");
 static_assert(SM_TY + 3 * 16 * 17 * 4 <= SM_A5, "block scratch overlaps A5");
 static_assert(TC_SMEM_BYTES <= 232448, "shared memory budget");
 
 constexpr uint32_t A3_BYTES = 32 * KiB;
 constexpr uint32_t TILE_BYTES = 16 * KiB;   // a [64 tok x 128] bf16 tile
-constexpr uint32_t REG64 = 8 * KiB;         // one 64-column region of a 64-row tile
-constexpr uint32_t REG128 = 16 * KiB;       // one 64-column region of a 128-row tile
 // tf32 tiles: 32-column regions of 128-byte rows
 constexpr uint32_t APA_REG = 128 * 128;     // 128 rows
 constexpr uint32_t APB_REG = 64 * 128;      // 64 rows
@@ -97,6 +102,7 @@ constexpr uint32_t TM_D1 = 128;   // U -> W (rows 0..63), -O (rows 64..127)
 constexpr uint32_t TM_S = 256;    // fp32 state S (row = key channel)
 
 constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t TM_COLS_PREP = 256;  // chunk preparation: no state
 
 constexpr uint32_t kWaitPolls = 1u << 24;
 // TMA loads are issued by lane 0 of warp 4 (a warp with no output stores),
@@ -126,21 +132,11 @@ struct TcParams {
   int zero_v;       // 1: treat v as zero (U = 0) and do not read it
   int s0_identity;  // 1: start every chain from S0 = I (dk = dv) instead of S0
   unsigned pre;     // KDA_PRE_* input pre-ops (L2-normalise q, k; sigmoid of beta)
+  // chunk-preparation mode: records [chunk][head in group] of heads h0 .. h0 + hg - 1
+  uint8_t *rec;
+  const int32_t *chunk_start;  // varlen: first chunk of each sequence, [n_seq + 1]
+  int n_seq, h0, hg;
 };
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
-
-__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
-  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
-}
 
 // Round fp32 to tf32 (nearest, ties away from zero) on the integer ALU: add
 // half a unit of the 10-bit mantissa, clear the 13 low bits.  (Values here are
@@ -156,30 +152,6 @@ __device__ __forceinline__ float ldg_bf16_pinned(const kda_bf16 *ptr) {
   asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(raw) : "l"(ptr));
   return __uint_as_float(static_cast<uint32_t>(raw) << 16);
 }
-
-// Shared memory seen by the threads: plain C++ accesses (so the compiler can
-// schedule and overlap them) addressed by the same 32-bit shared-window
-// addresses the descriptors and TMA use.
-struct Smem {
-  uint8_t *base;
-  uint32_t sb;
-  __device__ __forceinline__ uint8_t *ptr(uint32_t a) const { return base + (a - sb); }
-  __device__ __forceinline__ uint32_t &u32(uint32_t a) const {
-    return *reinterpret_cast<uint32_t *>(ptr(a));
-  }
-  __device__ __forceinline__ float &f32(uint32_t a) const {
-    return *reinterpret_cast<float *>(ptr(a));
-  }
-  __device__ __forceinline__ uint2 &u64(uint32_t a) const {
-    return *reinterpret_cast<uint2 *>(ptr(a));
-  }
-  __device__ __forceinline__ uint4 &u128(uint32_t a) const {
-    return *reinterpret_cast<uint4 *>(ptr(a));
-  }
-  __device__ __forceinline__ unsigned short &u16(uint32_t a) const {
-    return *reinterpret_cast<unsigned short *>(ptr(a));
-  }
-};
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -197,6 +169,14 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // in: c1 = -eA log2(e), c2 = gmin log2(e).  z = +inf gives e^gmin, z = -inf 1.
 __device__ __forceinline__ float fast_decay2(float c1, float c2, float z) {
   return ex2_approx(c2 * rcp_approx(1.0f + ex2_approx(c1 * z)));
+}
+
+// (a, b) as bf16 pairs hi = bf16(a, b), lo = bf16((a, b) - hi): hi + lo
+// carries about 16 mantissa bits.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi, uint32_t &lo) {
+  hi = pack_bf16x2(a, b);
+  const float2 h = unpack_bf16x2(hi);
+  lo = pack_bf16x2(a - h.x, b - h.y);
 }
 
 // Warp-level D(16x8) += A(16x8) B(8x8) in tf32 with fp32 accumulation.
@@ -227,47 +207,11 @@ __device__ __forceinline__ void warp_mma16(const float *X, int ldx, const float 
   }
 }
 
-// Write 32 fp32 values (columns [32 q4, 32 q4 + 32) of `row`) as fp16 into a
-// 128-byte-swizzled tile whose 64-column regions are `region` bytes apart.
-__device__ __forceinline__ void store_row32_f16(const Smem &S, uint32_t tile, int row, int q4,
-                                                uint32_t region, const float (&v)[32],
-                                                float scale) {
-  const uint32_t base =
-      tile + static_cast<uint32_t>(q4 >> 1) * region + static_cast<uint32_t>(row) * 128u;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t pos = static_cast<uint32_t>((4 * (q4 & 1) + j) ^ (row & 7)) << 4;
-    S.u128(base + pos) = make_uint4(pack_f16x2(scale * v[8 * j + 0], scale * v[8 * j + 1]),
-                                    pack_f16x2(scale * v[8 * j + 2], scale * v[8 * j + 3]),
-                                    pack_f16x2(scale * v[8 * j + 4], scale * v[8 * j + 5]),
-                                    pack_f16x2(scale * v[8 * j + 6], scale * v[8 * j + 7]));
-  }
-}
-
-// Issue the MMAs of one product: K-steps of 16 elements (8 for tf32, the same
-// 32 bytes).  K-major operands advance 32 bytes per step inside a 128-byte
-// row and jump one region per 4 steps; MN-major operands advance 2048 bytes
-// (16 rows) per step and find their 64-element MN blocks `region` apart.
-__device__ __forceinline__ void issue_mma(uint32_t d_tmem, uint32_t a_base, bool a_mn,
-                                          uint32_t a_region, uint32_t b_base, bool b_mn,
-                                          uint32_t b_region, int ksteps, uint32_t idesc,
-                                          uint32_t accumulate, bool tf32 = false) {
-  for (int ks = 0; ks < ksteps; ++ks) {
-    const uint32_t a_addr = a_mn ? a_base + static_cast<uint32_t>(ks) * 2048u
-                                 : a_base + static_cast<uint32_t>(ks >> 2) * a_region +
-                                       static_cast<uint32_t>(ks & 3) * 32u;
-    const uint32_t b_addr = b_mn ? b_base + static_cast<uint32_t>(ks) * 2048u
-                                 : b_base + static_cast<uint32_t>(ks >> 2) * b_region +
-                                       static_cast<uint32_t>(ks & 3) * 32u;
-    const uint64_t ad = sw128_desc(a_addr, a_mn ? a_region : 16u, 1024u);
-    const uint64_t bd = sw128_desc(b_addr, b_mn ? b_region : 16u, 1024u);
-    if (tf32)
-      mma_tf32(d_tmem, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
-    else
-      mma_f16(d_tmem, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
-  }
-}
-
+// kPrep = false: one CTA per (sequence, head) chain, the whole chunk step.
+// kPrep = true (chunk preparation): persistent CTAs take (chunk, head) tasks
+// of the whole batch, run the state-independent part of the step and store
+// each chunk's record (kda_split.cuh) for the state pass.
+template <bool kPrep>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
@@ -284,22 +228,67 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     return;
   }
 
-  int64_t t_begin, t_end;
-  if (p.cu_seqlens) {
-    t_begin = p.cu_seqlens[s];
-    t_end = p.cu_seqlens[s + 1];
+  int64_t t_begin = 0, t_end = 0;
+  int n_chunks = 0;      // iterations of this CTA
+  int64_t n_tasks = 0;   // chunk preparation: (chunk, head) tasks of the batch
+  const int64_t cps = (p.fixed_len + 63) / 64;  // chunks per sequence (equal lengths)
+  if constexpr (!kPrep) {
+    if (p.cu_seqlens) {
+      t_begin = p.cu_seqlens[s];
+      t_end = p.cu_seqlens[s + 1];
+    } else {
+      t_begin = static_cast<int64_t>(s) * p.fixed_len;
+      t_end = t_begin + p.fixed_len;
+    }
+    n_chunks = static_cast<int>((t_end - t_begin + 63) / 64);
   } else {
-    t_begin = static_cast<int64_t>(s) * p.fixed_len;
-    t_end = t_begin + p.fixed_len;
+    n_tasks = (p.cu_seqlens ? static_cast<int64_t>(p.chunk_start[p.n_seq])
+                            : static_cast<int64_t>(p.n_seq) * cps) * p.hg;
+    n_chunks = n_tasks > static_cast<int64_t>(blockIdx.x)
+                   ? static_cast<int>((n_tasks - blockIdx.x + gridDim.x - 1) / gridDim.x)
+                   : 0;
   }
-  const int n_chunks = static_cast<int>((t_end - t_begin + 63) / 64);
+  // Iteration n's chunk: first token, length, head.
+  struct Task {
+    int64_t t0;
+    int L, h;
+  };
+  auto task_at = [&](int n) -> Task {
+    if constexpr (!kPrep) {
+      const int64_t t0 = t_begin + 64LL * n;
+      return {t0, static_cast<int>(min(static_cast<int64_t>(64), t_end - t0)), h};
+    } else {
+      const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
+      const int64_t c = t / p.hg;
+      int64_t sb0, se0, j;
+      if (p.cu_seqlens) {
+        int lo = 0, hi = p.n_seq;  // the sequence q with chunk_start[q] <= c < chunk_start[q + 1]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (p.chunk_start[mid] <= c) lo = mid; else hi = mid;
+        }
+        sb0 = p.cu_seqlens[lo];
+        se0 = p.cu_seqlens[lo + 1];
+        j = c - p.chunk_start[lo];
+      } else {
+        const int64_t q = c / cps;
+        sb0 = q * p.fixed_len;
+        se0 = sb0 + p.fixed_len;
+        j = c - q * cps;
+      }
+      const int64_t t0 = sb0 + 64 * j;
+      return {t0, static_cast<int>(min(static_cast<int64_t>(64), se0 - t0)),
+              p.h0 + static_cast<int>(t % p.hg)};
+    }
+  };
   int64_t snap_row = 0;
-  if (p.snaps)
+  if (!kPrep && p.snaps)
     snap_row = p.snap_offsets ? p.snap_offsets[s] : static_cast<int64_t>(s) * (p.fixed_len / 64);
   const float kLog2e = 1.4426950408889634f;
-  const float dc1 = -__expf(p.A[h]) * kLog2e, dc2 = p.gmin * kLog2e;
+  float dc1 = kPrep ? 0.f : -__expf(p.A[h]) * kLog2e;  // chunk preparation: per task
+  const float dc2 = p.gmin * kLog2e;
   const size_t state_off =
-      (static_cast<size_t>(p.slots ? p.slots[s] : s) * H + h) * TD * TD;
+      kPrep ? 0 : (static_cast<size_t>(p.slots ? p.slots[s] : s) * H + h) * TD * TD;
 
   const uint32_t bar_qz0 = sb + MS_BAR_QZ, bar_kv = sb + MS_BAR_KV, bar_mma = sb + MS_BAR_MMA;
   if (tid == 0) {
@@ -314,7 +303,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     prefetch_tensormap(&tm_v);
   }
   if (warp == 1) {
-    tmem_alloc(sb + MS_TMEM, TM_COLS);
+    tmem_alloc(sb + MS_TMEM, kPrep ? TM_COLS_PREP : TM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -329,7 +318,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
 
   // Initial state -> TMEM (row trow, columns [32 q4, 32 q4 + 32)).
-  {
+  if constexpr (!kPrep) {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
@@ -341,7 +330,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   auto issue_qz = [&](int n) {  // q -> A3[n&1] lower half, z -> ZB[n&1]
     const int par = n & 1;
-    const int t0 = static_cast<int>(t_begin + 64LL * n);
+    const Task tk = task_at(n);
+    const int t0 = static_cast<int>(tk.t0), h = tk.h;
     const uint32_t bar = bar_qz0 + 8 * par;
     mbar_expect_tx(bar, 2 * TILE_BYTES);
     const uint32_t a3 = sb + SM_A3 + par * A3_BYTES;
@@ -352,7 +342,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tma_load_3d(zb + REG64, &tm_z, 64, h, t0, bar);
   };
   auto issue_kv = [&](int n) {
-    const int t0 = static_cast<int>(t_begin + 64LL * n);
+    const Task tk = task_at(n);
+    const int t0 = static_cast<int>(tk.t0), h = tk.h;
     mbar_expect_tx(bar_kv, (p.zero_v ? 1 : 2) * TILE_BYTES);
     tma_load_3d(sb + SM_KB, &tm_k, 0, h, t0, bar_kv);
     tma_load_3d(sb + SM_KB + REG64, &tm_k, 64, h, t0, bar_kv);
@@ -363,9 +354,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   };
 
   bool qz_pending[2] = {false, false}, kv_pending = false, mma_pending = false;
-  float beta_next = (tid < 64 && t_begin + tid < t_end)
-                        ? bf2f(p.beta[static_cast<size_t>(t_begin + tid) * H + h])
-                        : 0.f;
+  float beta_next = 0.f;
+  if (tid < 64 && n_chunks > 0) {
+    const Task tk = task_at(0);
+    if (tid < tk.L) beta_next = bf2f(p.beta[static_cast<size_t>(tk.t0 + tid) * H + tk.h]);
+  }
   // A full chunk's snapshot is written from the next chunk's state read-out
   // (or after the last chunk): the row it goes to, or -1.
   int64_t snap_pending = -1;
@@ -421,15 +414,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int rbase = 16 * R + 4 * hf;
   for (int n = 0; n < n_chunks && !aborted; ++n) {
     const int par = n & 1;
-    const int64_t t0 = t_begin + 64LL * n;
-    const int L = static_cast<int>(min(static_cast<int64_t>(64), t_end - t0));
+    const Task tk = task_at(n);
+    const int64_t t0 = tk.t0;
+    const int L = tk.L;
+    if constexpr (kPrep) dc1 = -__expf(p.A[tk.h]) * kLog2e;
     const uint32_t a3 = sb + SM_A3 + par * A3_BYTES;
     const uint32_t zb = sb + SM_ZB + par * TILE_BYTES;
 
     // Prefetch the next chunk's q and z into the other parity buffers.  (The
     // threads that last wrote those buffers fenced their generic-proxy
-    // writes before the barrier that ended the previous chunk.)
-    if (tid == kTmaThread && n + 1 < n_chunks) issue_qz(n + 1);
+    // writes before the barrier that ended the previous chunk.)  Chunk
+    // preparation issues it later, once the previous record has been read.
+    if (!kPrep && tid == kTmaThread && n + 1 < n_chunks) issue_qz(n + 1);
     if (n + 1 < n_chunks) qz_pending[par ^ 1] = true;
     // beta of this chunk was loaded one chunk ahead (logits pass through a sigmoid)
     if (tid < 64) {
@@ -502,57 +498,64 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     // the next chunk's beta, issued while the store queue is quiet
-    if (tid < 64)
-      beta_next = (n + 1 < n_chunks && t0 + 64 + tid < t_end)
-                      ? ldg_bf16_pinned(p.beta + static_cast<size_t>(t0 + 64 + tid) * H + h)
-                      : 0.f;
+    if (tid < 64) {
+      beta_next = 0.f;
+      if (n + 1 < n_chunks) {
+        const Task nx = task_at(n + 1);
+        if (tid < nx.L)
+          beta_next = ldg_bf16_pinned(p.beta + static_cast<size_t>(nx.t0 + tid) * H + nx.h);
+      }
+    }
+    if constexpr (kPrep) {
+      // The previous record's bulk stores must have read A3 / ZB [par ^ 1],
+      // A5 and the U tile before they are overwritten (q, z of the next task
+      // now; the work region from phase B on).
+      if (tid == kTmaThread) {
+        bulk_wait_read0();
+        if (n + 1 < n_chunks) issue_qz(n + 1);
+      }
+    }
     if (!wait_all(bar_kv, n & 1)) { aborted = true; break; }  // also orders the Lam table
     kv_pending = false;
 
-    if (p.pre & KDA_PRE_L2NORM_QK) {
-      // Raw q and k: scale every (token, head) row to unit L2 norm in place
-      // (fp32 norm, result rounded back to bf16).  Row sums of squares: this
-      // thread's two channels, then its half-warp (16 channel pairs), then the
-      // 4 warps of the sub-tile through a table in the other parity's A3 rows
-      // 0..63, which hold nothing during this chunk.
+    const bool l2n = (p.pre & KDA_PRE_L2NORM_QK) != 0;
+    if (l2n) {
+      // Raw q and k: 1 / ||k_r||, 1 / ||q_r|| of every row (fp32) into MS_NRM;
+      // phase B multiplies them in, so the normalised rows are never rounded
+      // back to bf16 (their rounding alone moves the outputs by ~2.4e-2 RMS).
+      // Sums of squares: this thread's two channels, its half-warp (16
+      // channel pairs), then the 4 warps of the sub-tile through a table in
+      // the other parity's A3 rows 0..15, which hold nothing during this chunk.
       const uint32_t tab = sb + SM_A3 + (par ^ 1) * A3_BYTES;  // [64 rows][4 warps][k, q]
-      float ssk[8], ssq[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int r = rbase + (j & 3) + 8 * (j >> 2);
         const uint32_t o16 = static_cast<uint32_t>(r) * 128u + sw16[j & 3];
         const float2 kk = unpack_bf16x2(S.u32(sb + SM_KB + rg16_64 + o16));
         const float2 qq = unpack_bf16x2(S.u32(a3 + rg16_128 + 64 * 128 + o16));
-        ssk[j] = kk.x * kk.x + kk.y * kk.y;
-        ssq[j] = qq.x * qq.x + qq.y * qq.y;
+        float sk = kk.x * kk.x + kk.y * kk.y, sq = qq.x * qq.x + qq.y * qq.y;
 #pragma unroll
         for (int off = 1; off < 16; off <<= 1) {
-          ssk[j] += __shfl_xor_sync(0xffffffffu, ssk[j], off);
-          ssq[j] += __shfl_xor_sync(0xffffffffu, ssq[j], off);
+          sk += __shfl_xor_sync(0xffffffffu, sk, off);
+          sq += __shfl_xor_sync(0xffffffffu, sq, off);
         }
         if ((lane & 15) == 0)
           S.u64(tab + static_cast<uint32_t>(r * 4 + (warp & 3)) * 8u) =
-              make_uint2(__float_as_uint(ssk[j]), __float_as_uint(ssq[j]));
+              make_uint2(__float_as_uint(sk), __float_as_uint(sq));
       }
       __syncthreads();
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = rbase + (j & 3) + 8 * (j >> 2);
+      if (tid < 64) {
         float tk = 0.f, tq = 0.f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          const uint2 e = S.u64(tab + static_cast<uint32_t>(r * 4 + w) * 8u);
+          const uint2 e = S.u64(tab + static_cast<uint32_t>(tid * 4 + w) * 8u);
           tk += __uint_as_float(e.x);
           tq += __uint_as_float(e.y);
         }
-        const float ik = tk > 0.f ? rsqrtf(tk) : 0.f, iq = tq > 0.f ? rsqrtf(tq) : 0.f;
-        const uint32_t o16 = static_cast<uint32_t>(r) * 128u + sw16[j & 3];
-        const uint32_t ak = sb + SM_KB + rg16_64 + o16, aq = a3 + rg16_128 + 64 * 128 + o16;
-        const float2 kk = unpack_bf16x2(S.u32(ak)), qq = unpack_bf16x2(S.u32(aq));
-        S.u32(ak) = pack_bf16x2(kk.x * ik, kk.y * ik);
-        S.u32(aq) = pack_bf16x2(qq.x * iq, qq.y * iq);
+        S.u64(sb + MS_NRM + 8 * tid) = make_uint2(__float_as_uint(tk > 0.f ? rsqrtf(tk) : 0.f),
+                                                 __float_as_uint(tq > 0.f ? rsqrtf(tq) : 0.f));
       }
-      // each thread now reads only its own normalised elements
+      __syncthreads();
     }
 
     // ---- element phase B: scaled operands, one row-block pair at a time -----------------
@@ -597,6 +600,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const uint32_t a_z = zb + rg16_64 + o16;
             float2 kk = unpack_bf16x2(S.u32(a_kb));
             float2 qq = unpack_bf16x2(S.u32(a_q));
+            if (l2n) {
+              const uint2 nr = S.u64(sb + MS_NRM + 8 * r);
+              kk.x *= __uint_as_float(nr.x);
+              kk.y *= __uint_as_float(nr.x);
+              qq.x *= __uint_as_float(nr.y);
+              qq.y *= __uint_as_float(nr.y);
+            }
             if (r >= L) {
               kk = make_float2(0.f, 0.f);
               qq = make_float2(0.f, 0.f);
@@ -641,10 +651,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 
     // zero A5 (its upper block stays zero; -P fills the lower block) and T'
-    // (rows >= 64 and the upper triangle stay zero; the T blocks fill the rest)
+    // hi / lo (rows >= 64 and the upper triangle stay zero; the T blocks fill
+    // the rest)
     for (int x = tid; x < 1024; x += TC_THREADS) {
       S.u128(sb + SM_A5 + 16 * x) = make_uint4(0, 0, 0, 0);
       S.u128(sb + SM_TP + 16 * x) = make_uint4(0, 0, 0, 0);
+      S.u128(sb + SM_TPL + 16 * x) = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
     {
@@ -690,10 +702,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
         S.f32(sb + SM_TF + 4 * ((o + r) * 65 + o + jc)) = x[r];
-        if (r >= jc) {  // T' = T diag(beta) in bf16 (upper triangle stays zero)
-          __nv_bfloat16 tb = __float2bfloat16_rn(x[r] * bj);
-          S.u16(sb + SM_TP + sw128_off(o + r, o + jc, REG128)) =
-              *reinterpret_cast<unsigned short *>(&tb);
+        if (r >= jc) {  // T' = T diag(beta) as bf16 hi + lo (upper triangle stays zero)
+          const float tv = x[r] * bj;
+          const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
+          const uint32_t off = sw128_off(o + r, o + jc, REG128);
+          S.u16(sb + SM_TP + off) = *reinterpret_cast<const unsigned short *>(&hi);
+          S.u16(sb + SM_TPL + off) = *reinterpret_cast<const unsigned short *>(&lo);
         }
       }
     }
@@ -727,13 +742,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           dst[g * 65 + 8 * nt + 2 * t + 1] = -e[nt][1];
           dst[(g + 8) * 65 + 8 * nt + 2 * t] = -e[nt][2];
           dst[(g + 8) * 65 + 8 * nt + 2 * t + 1] = -e[nt][3];
-          // T' = T diag(beta) in bf16, two adjacent columns per store
+          // T' = T diag(beta) as bf16 hi + lo, two adjacent columns per store
           const int col = 16 * J + 8 * nt + 2 * t;
           const float b0 = S.f32(sb + MS_BETA + 4 * col), b1 = S.f32(sb + MS_BETA + 4 * (col + 1));
-          S.u32(sb + SM_TP + sw128_off(16 * Rr + g, col, REG128)) =
-              pack_bf16x2(-e[nt][0] * b0, -e[nt][1] * b1);
-          S.u32(sb + SM_TP + sw128_off(16 * Rr + g + 8, col, REG128)) =
-              pack_bf16x2(-e[nt][2] * b0, -e[nt][3] * b1);
+          uint32_t hi, lo;
+          split_bf16x2(-e[nt][0] * b0, -e[nt][1] * b1, hi, lo);
+          S.u32(sb + SM_TP + sw128_off(16 * Rr + g, col, REG128)) = hi;
+          S.u32(sb + SM_TPL + sw128_off(16 * Rr + g, col, REG128)) = lo;
+          split_bf16x2(-e[nt][2] * b0, -e[nt][3] * b1, hi, lo);
+          S.u32(sb + SM_TP + sw128_off(16 * Rr + g + 8, col, REG128)) = hi;
+          S.u32(sb + SM_TPL + sw128_off(16 * Rr + g + 8, col, REG128)) = lo;
         }
         __syncwarp();
       }
@@ -746,14 +764,52 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
       tc_fence_after();
       issue_mma(tmem + TM_AP, sb + SM_TP, false, REG128, sb + SM_KB, true, REG64, 4, ID_TPROD, 0);
+      issue_mma(tmem + TM_AP, sb + SM_TPL, false, REG128, sb + SM_KB, true, REG64, 4, ID_TPROD, 1);
       if (!p.zero_v)
+      {
         issue_mma(tmem + TM_D1, sb + SM_TP, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD, 0);
+        issue_mma(tmem + TM_D1, sb + SM_TPL, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD,
+                  1);
+      }
       mma_commit(bar_mma);
     }
     mma_pending = true;
     if (!wait_mma()) { aborted = true; break; }
     if (tid == kTmaThread && n + 1 < n_chunks) issue_kv(n + 1);  // next chunk's k and v
     if (n + 1 < n_chunks) kv_pending = true;
+
+    if constexpr (kPrep) {
+      // ---- the chunk's record: -Wk -> A3 rows 0..63, U -> fp16 tile, gamma; then
+      //      A3 (with -Q~), K' (ZB), -P (A5 rows 64..127) and U go out as bulk stores.
+      const int64_t task = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
+      uint8_t *rec = p.rec + static_cast<size_t>(task) * kRecBytes;
+      if (quad < 2) {
+        float v[32];
+        tmem_ld32(t_lane + TM_AP + 32 * q4, v);
+        tmem_wait_ld();
+        store_row32_f16(S, a3, trow, q4, REG128, v, -1.f);
+        tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
+        tmem_wait_ld();
+        store_row32_f16(S, sb + SM_WBF, trow, q4, REG64, v, 1.f);
+      } else if (q4 < 2) {  // warps 2, 3, 6, 7: one key channel per thread
+        const int c = (2 * q4 + quad - 2) * 32 + lane;
+        float gam = 1.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) gam *= S.f32(sb + MS_LAM + 4 * (m * TD + c));
+        reinterpret_cast<float *>(rec + kRecG)[c] = gam;
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == kTmaThread) {
+        bulk_s2g(rec + kRecA3, a3, 32 * KiB);
+        bulk_s2g(rec + kRecKP, zb, 16 * KiB);
+        bulk_s2g(rec + kRecU, sb + SM_WBF, 16 * KiB);
+        bulk_s2g(rec + kRecP, sb + SM_A5 + 8 * KiB, 8 * KiB);
+        bulk_commit();
+      }
+      continue;
+    } else {
 
     // -Wk -> A3 rows 0..63;  S (fp32, TMEM) -> fp16 S for the MMA, then S *= e^{G_last}.
     {
@@ -855,6 +911,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (L == 64) ++snap_row;
     tc_fence_before();
     __syncthreads();
+    }  // !kPrep
+  }
+  if constexpr (kPrep) {
+    if (tid == kTmaThread) bulk_wait0();  // the last record is out before the CTA ends
   }
 
   if (!aborted && (p.S_final || snap_pending >= 0)) {
@@ -890,7 +950,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TM_COLS);
+    tmem_dealloc(tmem, kPrep ? TM_COLS_PREP : TM_COLS);
   }
 }
 
@@ -945,14 +1005,37 @@ cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
       !make_map(&mz, z, total_tokens, H, TD) ||
       !make_map(&mv, zero_v ? k : v, total_tokens, H, TD))
     return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel,
+  cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(TC_SMEM_BYTES));
   if (err != cudaSuccess) return err;
   TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, H, S0, o, S_final, snaps, snap_offsets,
-               status, slots, zero_v, s0_identity, pre};
+               status, slots, zero_v, s0_identity, pre, nullptr, nullptr, n_seq, 0, H};
   const dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(n_seq));
-  prefill_tc_kernel<<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(mq, mk, mz, mv, prm);
+  prefill_tc_kernel<false><<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(mq, mk, mz, mv, prm);
+  return cudaGetLastError();
+}
+
+cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                              const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                              const int32_t *cu_seqlens, const int32_t *chunk_start, int n_seq,
+                              int64_t total_tokens, int64_t fixed_len, int H, int h0, int hg,
+                              int64_t max_tasks, uint8_t *rec, int *status, unsigned pre,
+                              int n_ctas, cudaStream_t stream) {
+  CUtensorMap mq, mk, mz, mv;
+  if (!make_map(&mq, q, total_tokens, H, TD) || !make_map(&mk, k, total_tokens, H, TD) ||
+      !make_map(&mz, z, total_tokens, H, TD) || !make_map(&mv, v, total_tokens, H, TD))
+    return cudaErrorInvalidValue;
+  cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(TC_SMEM_BYTES));
+  if (err != cudaSuccess) return err;
+  TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, H, nullptr, nullptr, nullptr, nullptr,
+               nullptr, status, nullptr, 0, 0, pre, rec, chunk_start, n_seq, h0, hg};
+  const int64_t ctas = max_tasks < n_ctas ? max_tasks : n_ctas;
+  if (ctas <= 0) return cudaSuccess;
+  prefill_tc_kernel<true><<<static_cast<unsigned>(ctas), TC_THREADS, TC_SMEM_BYTES, stream>>>(
+      mq, mk, mz, mv, prm);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,384 @@
+// Sequential state pass of the two-pass tensor-core prefill (dk = dv = 128,
+// chunk C = 64).
+//
+// The chunkwise form ("Kimi K3 Technical Report - Open Frontier
+// Intelligence", sec. 2.1) splits every chunk into a part that depends only
+// on the chunk's own inputs (the gate, A_kk, T = (I + A_kk)^{-1}, Wk, U, P
+// and the scaled Q~, K') and a part that carries the state:
+//
+//   W  = U - Wk S                       O = Q~ S + P W  (Q~ = Q e^G)
+//   S' = Diag(gamma) S + K'^T W         gamma = e^{G_last}, K' = K e^{G_last - G}
+//
+// The first part has no order between chunks and runs for every (chunk,
+// head) at once in the chunk-preparation pass, which leaves one record per
+// (chunk, head) (layout in kda_split.cuh).  This kernel is the second part:
+// one CTA per (sequence, head) chain walks its chunks in order with the fp32
+// state in TMEM; per chunk it
+//   - reads the state out of TMEM (fp16 copy for the MMA, snapshot of the
+//     previous chunk's state, scaling by gamma in place),
+//   - D1 = [-Wk ; -Q~] S_fp16        (rows 0..63: -Wk S, rows 64..127: -Q~ S)
+//   - W = U + D1[0..63] -> fp16
+//   - S += K'^T W,  D1[64..127] += -P W   (= -O)
+//   - writes o.
+// The records arrive by bulk async copies two chunks ahead (two stages), so
+// the chain only waits on its own three MMAs.  Every wait is bounded; a wait
+// that gives up records KDA_ERR_TIMEOUT and the CTA stops cleanly.
+#include "kda_common.cuh"
+#include "kda_sm100.cuh"
+#include "kda_split.cuh"
+#include "kda_tc_common.cuh"
+
+namespace kda {
+
+namespace {
+
+using namespace sm100;
+using namespace tcx;
+
+constexpr int SP_THREADS = 512;
+constexpr int TD = 128;
+
+// One stage holds one record: A3 | KP | U | A5 (rows 0..63 stay zero) | gamma.
+constexpr uint32_t ST_A3 = 0;
+constexpr uint32_t ST_KP = 32 * KiB;
+constexpr uint32_t ST_U = 48 * KiB;
+constexpr uint32_t ST_A5 = 64 * KiB;
+constexpr uint32_t ST_G = 80 * KiB;
+constexpr uint32_t ST_BYTES = 81 * KiB;
+constexpr uint32_t SM_SBF = 2 * ST_BYTES;        // [dk x dv] S in fp16, MN-major
+constexpr uint32_t SM_WBF = SM_SBF + 32 * KiB;   // [tok x dv] W in fp16, MN-major
+constexpr uint32_t SM_MISC = SM_WBF + 16 * KiB;
+constexpr uint32_t MS_BAR_FULL = SM_MISC;        // 2 mbarriers (records in)
+constexpr uint32_t MS_BAR_MMA = SM_MISC + 16;
+constexpr uint32_t MS_TMEM = SM_MISC + 32;
+constexpr uint32_t SP_SMEM_BYTES = SM_MISC + 64;
+static_assert(SP_SMEM_BYTES + 1024 <= 232448, "shared memory budget");
+
+constexpr uint32_t kRecInBytes = 32 * KiB + 16 * KiB + 16 * KiB + 8 * KiB + 512;
+
+constexpr uint32_t TM_S = 0;     // fp32 state (row = key channel)
+constexpr uint32_t TM_D1 = 128;  // -Wk S -> (rows 0..63); -O (rows 64..127)
+constexpr uint32_t TM_COLS = 256;
+
+constexpr uint32_t kWaitPolls = 1u << 24;
+constexpr int kCopyThread = 128;  // issues the record copies (warp 4: no TMEM lane 0..31 role)
+
+constexpr uint32_t ID_KMN = idesc_mma(128, 128, kFmtF16, kFmtF16, 0, 1);   // K-major x MN
+constexpr uint32_t ID_MNMN = idesc_mma(128, 128, kFmtF16, kFmtF16, 1, 1);  // MN x MN
+
+struct SpParams {
+  const uint8_t *rec;          // records [chunk][head in group]
+  const int32_t *cu_seqlens;   // or NULL: equal lengths fixed_len
+  const int32_t *chunk_start;  // first chunk of each sequence (varlen), or NULL
+  int64_t fixed_len;
+  int H, h0, hg;               // heads h0 .. h0 + hg - 1 of H
+  const float *S0;
+  kda_bf16 *o;
+  float *S_final;
+  float *snaps;
+  const int64_t *snap_offsets;
+  int *status;
+  const int32_t *slots;
+};
+
+__global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled tiles need 1024-byte alignment: round the base up
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const Smem S{smem, sb};
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hh = blockIdx.x, s = blockIdx.y;
+  const int H = p.H, h = p.h0 + hh;
+
+  int64_t t_begin, t_end, chunk0;
+  if (p.cu_seqlens) {
+    t_begin = p.cu_seqlens[s];
+    t_end = p.cu_seqlens[s + 1];
+    chunk0 = p.chunk_start[s];
+  } else {
+    t_begin = static_cast<int64_t>(s) * p.fixed_len;
+    t_end = t_begin + p.fixed_len;
+    chunk0 = static_cast<int64_t>(s) * ((p.fixed_len + 63) / 64);
+  }
+  const int n_chunks = static_cast<int>((t_end - t_begin + 63) / 64);
+  int64_t snap_row = 0;
+  if (p.snaps)
+    snap_row = p.snap_offsets ? p.snap_offsets[s] : static_cast<int64_t>(s) * (p.fixed_len / 64);
+  const size_t state_off = (static_cast<size_t>(p.slots ? p.slots[s] : s) * H + h) * TD * TD;
+
+  const uint32_t bar_full = sb + MS_BAR_FULL, bar_mma = sb + MS_BAR_MMA;
+  if (tid == 0) {
+    mbar_init(bar_full, 1);
+    mbar_init(bar_full + 8, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + MS_TMEM, TM_COLS);
+    tmem_relinquish();
+  }
+  // rows 0..63 of both stages' [0 ; -P] tiles stay zero (the copies fill rows 64..127)
+  for (int x = tid; x < 2 * 512; x += SP_THREADS)
+    S.u128(sb + (x >> 9) * ST_BYTES + ST_A5 + 16 * (x & 511)) = make_uint4(0, 0, 0, 0);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + MS_TMEM);
+
+  // TMEM read-outs: a warp reaches the 32 lanes of its quadrant; the 16 warps
+  // split the 128 columns in quarters.
+  const int quad = warp & 3, q4 = warp >> 2;
+  const int trow = quad * 32 + lane;  // TMEM lane = matrix row
+  const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+
+  {  // initial state -> TMEM (row trow, columns [32 q4, 32 q4 + 32))
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      v[j] = p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + 32 * q4 + j] : 0.f;
+    tmem_st32(t_lane + TM_S + 32 * q4, v);
+    tmem_wait_st();
+  }
+
+  auto issue = [&](int n) {  // record of chunk n -> stage n & 1
+    const uint32_t st = sb + static_cast<uint32_t>(n & 1) * ST_BYTES;
+    const uint8_t *rec =
+        p.rec + (static_cast<size_t>(chunk0 + n) * p.hg + hh) * static_cast<size_t>(kRecBytes);
+    const uint32_t bar = bar_full + 8u * static_cast<uint32_t>(n & 1);
+    mbar_expect_tx(bar, kRecInBytes);
+    bulk_g2s(st + ST_A3, rec + kRecA3, 32 * KiB, bar);
+    bulk_g2s(st + ST_KP, rec + kRecKP, 16 * KiB, bar);
+    bulk_g2s(st + ST_U, rec + kRecU, 16 * KiB, bar);
+    bulk_g2s(st + ST_A5 + 8 * KiB, rec + kRecP, 8 * KiB, bar);
+    bulk_g2s(st + ST_G, rec + kRecG, 512, bar);
+  };
+  bool full_pending[2] = {false, false}, mma_pending = false, aborted = false;
+  if (tid == kCopyThread) {
+    if (n_chunks > 0) issue(0);
+    if (n_chunks > 1) issue(1);
+  }
+  full_pending[0] = n_chunks > 0;
+  full_pending[1] = n_chunks > 1;
+  uint32_t mma_phase = 0;
+  int64_t snap_pending = -1;
+
+  auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+    const bool ok = mbar_wait_bounded(bar, parity, kWaitPolls);
+    if (__syncthreads_or(ok ? 0 : 1)) {
+      if (tid == 0) atomicOr(p.status, KDA_ERR_TIMEOUT);
+      return false;
+    }
+    return true;
+  };
+  auto wait_mma = [&]() -> bool {
+    const bool ok = wait_all(bar_mma, mma_phase);
+    if (ok) {
+      mma_phase ^= 1u;
+      mma_pending = false;
+    }
+    tc_fence_after();
+    return ok;
+  };
+
+  for (int n = 0; n < n_chunks; ++n) {
+    const int stg = n & 1;
+    const uint32_t st = sb + static_cast<uint32_t>(stg) * ST_BYTES;
+    const int64_t t0 = t_begin + 64LL * n;
+    const int L = static_cast<int>(min(static_cast<int64_t>(64), t_end - t0));
+    if (!wait_all(bar_full + 8u * stg, (n >> 1) & 1)) { aborted = true; break; }
+    full_pending[stg] = false;
+
+    // ---- state read-out: snapshot, fp16 copy for the MMA, S *= gamma -------------------
+    {
+      float v[32];
+      tmem_ld32(t_lane + TM_S + 32 * q4, v);
+      tmem_wait_ld();
+      if (snap_pending >= 0) {  // the state after the previous (full) chunk
+        float4 *dst = reinterpret_cast<float4 *>(
+            p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
+            static_cast<size_t>(trow) * TD + 32 * q4);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        snap_pending = -1;
+      }
+      store_row32_f16(S, sb + SM_SBF, trow, q4, REG128, v, 1.f);
+      const float gam = S.f32(st + ST_G + 4 * trow);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= gam;
+      tmem_st32(t_lane + TM_S + 32 * q4, v);
+      tmem_wait_st();
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- D1 = [-Wk ; -Q~] S ------------------------------------------------------------
+    if (tid == 0) {
+      tc_fence_after();
+      issue_mma(tmem + TM_D1, st + ST_A3, false, REG128, sb + SM_SBF, true, REG128, 8, ID_KMN, 0);
+      mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    if (!wait_mma()) { aborted = true; break; }
+
+    // ---- W = U - Wk S -> fp16 ----------------------------------------------------------------
+    if (quad < 2) {
+      float v[32];
+      tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
+      tmem_wait_ld();
+      add_row32_f16(S, st + ST_U, trow, q4, REG64, v);
+      store_row32_f16(S, sb + SM_WBF, trow, q4, REG64, v, 1.f);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- S += K'^T W;  D1 += [0 ; -P] W ------------------------------------------------------
+    if (tid == 0) {
+      tc_fence_after();
+      issue_mma(tmem + TM_S, st + ST_KP, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
+      issue_mma(tmem + TM_D1, st + ST_A5, false, REG128, sb + SM_WBF, true, REG64, 4, ID_KMN, 1);
+      mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    if (!wait_mma()) { aborted = true; break; }
+    // every reader of this stage is done: refill it with chunk n + 2
+    if (tid == kCopyThread && n + 2 < n_chunks) issue(n + 2);
+    if (n + 2 < n_chunks) full_pending[stg] = true;
+
+    // ---- outputs: o = -D1 rows 64..127 -------------------------------------------------------
+    if (quad >= 2) {
+      const int r = trow - 64;
+      float v[32];
+      tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
+      tmem_wait_ld();
+      if (r < L && p.o) {
+        uint4 *dst = reinterpret_cast<uint4 *>(
+            p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + 32 * q4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_uint4(pack_bf16x2(-v[8 * j + 0], -v[8 * j + 1]),
+                              pack_bf16x2(-v[8 * j + 2], -v[8 * j + 3]),
+                              pack_bf16x2(-v[8 * j + 4], -v[8 * j + 5]),
+                              pack_bf16x2(-v[8 * j + 6], -v[8 * j + 7]));
+      }
+    }
+    if (p.snaps && L == 64) snap_pending = snap_row;
+    if (L == 64) ++snap_row;
+    // the next chunk's first MMA overwrites D1 only after its state read-out
+    // barrier, which every thread reaches after its o stores above
+  }
+
+  if (!aborted && (p.S_final || snap_pending >= 0)) {
+    float v[32];
+    tmem_ld32(t_lane + TM_S + 32 * q4, v);
+    tmem_wait_ld();
+    if (p.S_final) {
+      float4 *dst = reinterpret_cast<float4 *>(p.S_final + state_off +
+                                               static_cast<size_t>(trow) * TD + 32 * q4);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+    if (snap_pending >= 0) {
+      float4 *dst = reinterpret_cast<float4 *>(
+          p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
+          static_cast<size_t>(trow) * TD + 32 * q4);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+    }
+  }
+
+  // Drain anything still in flight (bounded) before TMEM and shared memory go.
+  if (aborted && tid == 0) {
+    if (mma_pending) mbar_wait_bounded(bar_mma, mma_phase, kWaitPolls);
+  }
+  if (aborted && tid == kCopyThread) {
+    for (int b = 0; b < 2; ++b)
+      if (full_pending[b]) mbar_wait_bounded(bar_full + 8 * b, 0, kWaitPolls) ||
+                               mbar_wait_bounded(bar_full + 8 * b, 1, kWaitPolls);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
+                              const int32_t *chunk_start, int n_seq, int64_t fixed_len, int H,
+                              int h0, int hg, const float *S0, kda_bf16 *o, float *S_final,
+                              float *snaps, const int64_t *snap_offsets, int *status,
+                              const int32_t *slots, cudaStream_t stream) {
+  const uint32_t smem = SP_SMEM_BYTES + 1024;  // + alignment slack
+  cudaError_t err = cudaFuncSetAttribute(state_pass_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  SpParams prm{rec, cu_seqlens, chunk_start, fixed_len, H, h0, hg, S0, o, S_final, snaps,
+               snap_offsets, status, slots};
+  const dim3 grid(static_cast<unsigned>(hg), static_cast<unsigned>(n_seq));
+  state_pass_kernel<<<grid, SP_THREADS, smem, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+}  // namespace kda
+
+namespace kda {
+
+namespace {
+
+// chunk_start[i] = sum over sequences j < i of ceil(len_j / 64), i = 0 .. n_seq:
+// one CTA, a running prefix over blocks of 1024 sequences.
+__global__ void __launch_bounds__(1024) chunk_start_kernel(const int32_t *__restrict__ cu,
+                                                           int n_seq,
+                                                           int32_t *__restrict__ chunk_start) {
+  __shared__ int32_t warp_sum[32];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < n_seq; base += 1024) {
+    const int i = base + tid;
+    const int c = i < n_seq ? (cu[i + 1] - cu[i] + 63) / 64 : 0;
+    int x = c;  // inclusive scan inside the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_sum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sum[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, off);
+        if (lane >= off) w += y;
+      }
+      warp_sum[lane] = w;
+    }
+    __syncthreads();
+    if (i < n_seq) chunk_start[i] = carry + (warp > 0 ? warp_sum[warp - 1] : 0) + x - c;
+    __syncthreads();
+    if (tid == 0) carry += warp_sum[31];
+    __syncthreads();
+  }
+  if (tid == 0) chunk_start[n_seq] = carry;
+}
+
+}  // namespace
+
+cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int32_t *chunk_start,
+                               cudaStream_t stream) {
+  chunk_start_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, n_seq, chunk_start);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -61,6 +61,18 @@ typedef uint16_t kda_bf16;                 /* raw bfloat16 bit pattern */
  * to bf16 first would move the outputs by about 2.4e-2 RMS). */
 #define KDA_PRE_L2NORM_QK 1u
 #define KDA_PRE_SIGMOID_BETA 2u
+
+/* Split-phase calls of kda_chunk_fwd_ex (dk = dv = 128): with
+ * KDA_PASS_PREPARE the call only runs the parallel chunk-preparation pass and
+ * leaves every (chunk, head)'s record in the workspace; a later call with
+ * KDA_PASS_STATE and the same workspace, sizes and cu_seqlens runs only the
+ * state pass from those records (q, k, v, z, beta, A are not read; S0, o,
+ * S_final, snaps are).  The workspace must hold the records of all heads
+ * (kda_chunk_fwd_workspace_bytes(), else KDA_ERR_WORKSPACE); both flags at
+ * once, or other shapes, give KDA_ERR_UNSUPPORTED.  Used to time the passes
+ * separately or to run them on different streams (order them). */
+#define KDA_PASS_PREPARE 0x100u
+#define KDA_PASS_STATE 0x200u
 typedef struct CUstream_st *kda_stream_t;  /* same type as cudaStream_t */
 
 typedef enum {
@@ -139,8 +151,8 @@ int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
 
 /*
  * kda_chunk_fwd_ex - kda_chunk_fwd with input pre-ops: `pre` is a set of
- * KDA_PRE_* flags (other bits: KDA_ERR_UNSUPPORTED).  pre = 0 is exactly
- * kda_chunk_fwd.  The pre-ops run inside the prefill kernels on every pass
+ * KDA_PRE_* flags, optionally with one KDA_PASS_* flag (other bits:
+ * KDA_ERR_UNSUPPORTED).  pre = 0 is exactly kda_chunk_fwd.  The pre-ops run inside the prefill kernels on every pass
  * (the scan's segment passes included); no normalised copy of q, k or beta is
  * written anywhere.
  */

@@ -26,6 +26,10 @@ PREFILL_COMPUTE_DTYPE = "bf16"
 # Input pre-ops (KDA_PRE_* in kda.h): L2-normalise q, k rows; sigmoid of beta.
 PRE_L2NORM_QK = 1
 PRE_SIGMOID_BETA = 2
+# Split-phase calls of chunk_fwd (KDA_PASS_* in kda.h): only the chunk
+# preparation, or only the state pass from the records it left in `workspace`.
+PASS_PREPARE = 0x100
+PASS_STATE = 0x200
 
 KDA_OK = 0
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_ALIGN",

@@ -134,6 +134,8 @@ bool gmin_ok(float gmin) { return isfinite(gmin) && gmin <= 0.f && gmin >= -5.5f
 
 bool pre_ok(unsigned pre) { return (pre & ~(KDA_PRE_L2NORM_QK | KDA_PRE_SIGMOID_BETA)) == 0; }
 
+constexpr unsigned kPassFlags = KDA_PASS_PREPARE | KDA_PASS_STATE;
+
 }  // namespace
 
 // Workspace the segment-parallel scan needs at these sizes (0: no scan).
@@ -194,6 +196,8 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
                      float *S_final, float *snaps, const int64_t *snap_offsets, void *workspace,
                      size_t workspace_bytes, kda_stream_t stream) {
   if (n_seq < 0 || total_tokens < 0 || H <= 0 || H > 65535) return KDA_ERR_SHAPE;
+  const unsigned passes = pre & kPassFlags;
+  pre &= ~kPassFlags;
   if (!dim_ok(dk) || !dim_ok(dv) || chunk != kChunk || !gmin_ok(gmin) || !pre_ok(pre))
     return KDA_ERR_UNSUPPORTED;
   if (n_seq == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_SHAPE;
@@ -211,8 +215,17 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_ALIGN;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (passes) {
+    // one of the two passes on its own: all heads in one group, so the
+    // records of the whole call sit in the workspace between the calls
+    if (passes == kPassFlags || !prefill_tc_supported(dk, dv, total_tokens))
+      return KDA_ERR_UNSUPPORTED;
+    if (!workspace || !aligned16(workspace) ||
+        split_heads(n_seq, total_tokens, H, workspace_bytes) < H)
+      return KDA_ERR_WORKSPACE;
+  }
   ScanPlan plan;
-  const bool scan = !cu_seqlens && !(snaps && snap_offsets) &&
+  const bool scan = !passes && !cu_seqlens && !(snaps && snap_offsets) &&
                     prefill_tc_supported(dk, dv, total_tokens) &&
                     plan_scan(n_seq, total_tokens, H, dk, dv, &plan);
   if (scan) {
@@ -253,19 +266,21 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *chunk_start = nullptr;
     err = cudaSuccess;
+    const bool run_prep = passes != KDA_PASS_STATE, run_state = passes != KDA_PASS_PREPARE;
     if (cu_seqlens) {
       chunk_start = reinterpret_cast<int32_t *>(ws);
-      err = chunk_start_launch(cu_seqlens, n_seq, chunk_start, st);
+      if (run_prep) err = chunk_start_launch(cu_seqlens, n_seq, chunk_start, st);
     }
     uint8_t *rec = ws + split_table_bytes(n_seq);
     const int64_t max_chunks = cu_seqlens ? split_max_chunks(n_seq, total_tokens)
                                           : static_cast<int64_t>(n_seq) * ((fixed_len + 63) / 64);
     for (int h0 = 0; h0 < H && err == cudaSuccess; h0 += hg) {
       const int g = H - h0 < hg ? H - h0 : hg;
-      err = chunk_prep_launch(q, k, v, z, beta, A, gmin, cu_seqlens, chunk_start, n_seq,
-                              total_tokens, fixed_len, H, h0, g, max_chunks * g, rec, status, pre,
-                              kSMs, st);
-      if (err == cudaSuccess)
+      if (run_prep)
+        err = chunk_prep_launch(q, k, v, z, beta, A, gmin, cu_seqlens, chunk_start, n_seq,
+                                total_tokens, fixed_len, H, h0, g, max_chunks * g, rec, status,
+                                pre, kSMs, st);
+      if (err == cudaSuccess && run_state)
         err = state_pass_launch(rec, cu_seqlens, chunk_start, n_seq, fixed_len, H, h0, g, S0, o,
                                 S_final, snaps, snap_offsets, status, nullptr, st);
     }

@@ -79,9 +79,10 @@ constexpr uint32_t SM_WBF = SM_AP + 64 * KiB;     // [tok x dv] W in fp16 (after
 
 constexpr uint32_t SM_MISC = 224 * KiB;
 constexpr uint32_t MS_BAR_QZ = SM_MISC + 0;       // 2 mbarriers
-constexpr uint32_t MS_BAR_KV = SM_MISC + 16;
+constexpr uint32_t MS_BAR_K = SM_MISC + 16;
 constexpr uint32_t MS_BAR_MMA = SM_MISC + 24;
 constexpr uint32_t MS_TMEM = SM_MISC + 32;
+constexpr uint32_t MS_BAR_V = SM_MISC + 40;
 constexpr uint32_t MS_BETA = SM_MISC + 64;        // 64 fp32
 constexpr uint32_t MS_LAM = SM_MISC + 320;        // [4][128] fp32 sub-tile decay totals
 constexpr uint32_t MS_NRM = MS_LAM + 4 * TD * 4;  // [64][2] fp32 1/||k_r||, 1/||q_r|| (pre-op)
@@ -290,11 +291,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const size_t state_off =
       kPrep ? 0 : (static_cast<size_t>(p.slots ? p.slots[s] : s) * H + h) * TD * TD;
 
-  const uint32_t bar_qz0 = sb + MS_BAR_QZ, bar_kv = sb + MS_BAR_KV, bar_mma = sb + MS_BAR_MMA;
+  const uint32_t bar_qz0 = sb + MS_BAR_QZ, bar_k = sb + MS_BAR_K, bar_v = sb + MS_BAR_V,
+                 bar_mma = sb + MS_BAR_MMA;
   if (tid == 0) {
     mbar_init(bar_qz0, 1);
     mbar_init(bar_qz0 + 8, 1);
-    mbar_init(bar_kv, 1);
+    mbar_init(bar_k, 1);
+    mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
     fence_mbar_init();
     prefetch_tensormap(&tm_q);
@@ -341,19 +344,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tma_load_3d(zb, &tm_z, 0, h, t0, bar);
     tma_load_3d(zb + REG64, &tm_z, 64, h, t0, bar);
   };
-  auto issue_kv = [&](int n) {
+  // k is refilled as soon as the operand build has read it (K~ goes to A3),
+  // v once T'V is done; each has its own barrier.
+  auto issue_k = [&](int n) {
     const Task tk = task_at(n);
     const int t0 = static_cast<int>(tk.t0), h = tk.h;
-    mbar_expect_tx(bar_kv, (p.zero_v ? 1 : 2) * TILE_BYTES);
-    tma_load_3d(sb + SM_KB, &tm_k, 0, h, t0, bar_kv);
-    tma_load_3d(sb + SM_KB + REG64, &tm_k, 64, h, t0, bar_kv);
-    if (!p.zero_v) {
-      tma_load_3d(sb + SM_VB, &tm_v, 0, h, t0, bar_kv);
-      tma_load_3d(sb + SM_VB + REG64, &tm_v, 64, h, t0, bar_kv);
-    }
+    mbar_expect_tx(bar_k, TILE_BYTES);
+    tma_load_3d(sb + SM_KB, &tm_k, 0, h, t0, bar_k);
+    tma_load_3d(sb + SM_KB + REG64, &tm_k, 64, h, t0, bar_k);
+  };
+  auto issue_v = [&](int n) {
+    const Task tk = task_at(n);
+    const int t0 = static_cast<int>(tk.t0), h = tk.h;
+    mbar_expect_tx(bar_v, TILE_BYTES);
+    tma_load_3d(sb + SM_VB, &tm_v, 0, h, t0, bar_v);
+    tma_load_3d(sb + SM_VB + REG64, &tm_v, 64, h, t0, bar_v);
   };
 
-  bool qz_pending[2] = {false, false}, kv_pending = false, mma_pending = false;
+  bool qz_pending[2] = {false, false}, k_pending = false, v_pending = false, mma_pending = false;
   float beta_next = 0.f;
   if (tid < 64 && n_chunks > 0) {
     const Task tk = task_at(0);
@@ -387,9 +395,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   if (tid == kTmaThread && n_chunks > 0) {
     issue_qz(0);
-    issue_kv(0);
+    issue_k(0);
+    if (!p.zero_v) issue_v(0);
   }
-  qz_pending[0] = kv_pending = (n_chunks > 0);
+  qz_pending[0] = k_pending = (n_chunks > 0);
+  v_pending = n_chunks > 0 && !p.zero_v;
 
   // Element-phase mapping: channel pair cp (channels c0, c0 + 1), sub-tile R,
   // and half hf of the sub-tile's rows.  Thread rows, in order, are
@@ -515,8 +525,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (n + 1 < n_chunks) issue_qz(n + 1);
       }
     }
-    if (!wait_all(bar_kv, n & 1)) { aborted = true; break; }  // also orders the Lam table
-    kv_pending = false;
+    if (!wait_all(bar_k, n & 1)) { aborted = true; break; }  // also orders the Lam table
+    k_pending = false;
 
     const bool l2n = (p.pre & KDA_PRE_L2NORM_QK) != 0;
     if (l2n) {
@@ -629,7 +639,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     make_uint2(tf32_rna(kb0 * f0[rp]), tf32_rna(kb1 * f1[rp]));
             }
             if (pp == 1) {
-              S.u32(a_kb) = pack_bf16x2(ke0 * x0, ke1 * x1);
+              // K~ into A3 rows 0..63 (free until -Wk), so k can be refilled now
+              S.u32(a3 + rg16_128 + o16) = pack_bf16x2(ke0 * x0, ke1 * x1);
               S.u32(a_q) = pack_f16x2(-qe0 * x0, -qe1 * x1);
               S.u32(a_z) = pack_f16x2(kb0 * y0, kb1 * y1);
             }
@@ -643,6 +654,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           issue_mma(tmem + TM_AP + 64 * pp, sb + SM_APA, false, APA_REG, sb + SM_APB, false,
                     APB_REG, 16, ID_AP, 0, true);
           mma_commit(bar_mma);
+        }
+        if (pp == 1) {  // every read of k is done: the next chunk's k
+          if (tid == kTmaThread && n + 1 < n_chunks) issue_k(n + 1);
+          if (n + 1 < n_chunks) k_pending = true;
         }
         mma_pending = true;
         if (!wait_mma()) break;
@@ -758,13 +773,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     fence_proxy_async();  // T' was written by the T blocks above
     tc_fence_before();
-    __syncthreads();
+    {
+      // v of this chunk (loaded a chunk ahead) must be in before T'V
+      const bool v_ok = p.zero_v || mbar_wait_bounded(bar_v, n & 1, kWaitPolls);
+      if (__syncthreads_or(v_ok ? 0 : 1)) {
+        if (tid == 0) atomicOr(p.status, KDA_ERR_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      v_pending = false;
+    }
 
     // ---- Wk = T' K~ -> TM_AP,  U = T' V -> D1 ---------------------------------------------
     if (tid == 0) {
       tc_fence_after();
-      issue_mma(tmem + TM_AP, sb + SM_TP, false, REG128, sb + SM_KB, true, REG64, 4, ID_TPROD, 0);
-      issue_mma(tmem + TM_AP, sb + SM_TPL, false, REG128, sb + SM_KB, true, REG64, 4, ID_TPROD, 1);
+      issue_mma(tmem + TM_AP, sb + SM_TP, false, REG128, a3, true, REG128, 4, ID_TPROD, 0);
+      issue_mma(tmem + TM_AP, sb + SM_TPL, false, REG128, a3, true, REG128, 4, ID_TPROD, 1);
       if (!p.zero_v)
       {
         issue_mma(tmem + TM_D1, sb + SM_TP, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD, 0);
@@ -775,8 +799,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     mma_pending = true;
     if (!wait_mma()) { aborted = true; break; }
-    if (tid == kTmaThread && n + 1 < n_chunks) issue_kv(n + 1);  // next chunk's k and v
-    if (n + 1 < n_chunks) kv_pending = true;
+    if (!p.zero_v) {  // the next chunk's v
+      if (tid == kTmaThread && n + 1 < n_chunks) issue_v(n + 1);
+      if (n + 1 < n_chunks) v_pending = true;
+    }
 
     if constexpr (kPrep) {
       // ---- the chunk's record: -Wk -> A3 rows 0..63, U -> fp16 tile, gamma; then
@@ -944,7 +970,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int b = 0; b < 2; ++b)
       if (qz_pending[b]) mbar_wait_bounded(bar_qz0 + 8 * b, 0, kWaitPolls) ||
                              mbar_wait_bounded(bar_qz0 + 8 * b, 1, kWaitPolls);
-    if (kv_pending) mbar_wait_bounded(bar_kv, 0, kWaitPolls) || mbar_wait_bounded(bar_kv, 1, kWaitPolls);
+    if (k_pending) mbar_wait_bounded(bar_k, 0, kWaitPolls) || mbar_wait_bounded(bar_k, 1, kWaitPolls);
+    if (v_pending) mbar_wait_bounded(bar_v, 0, kWaitPolls) || mbar_wait_bounded(bar_v, 1, kWaitPolls);
   }
   tc_fence_before();
   __syncthreads();

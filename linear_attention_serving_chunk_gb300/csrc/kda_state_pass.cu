@@ -38,21 +38,26 @@ using namespace tcx;
 constexpr int SP_THREADS = 512;
 constexpr int TD = 128;
 
-// One stage holds one record: A3 | KP | U | A5 (rows 0..63 stay zero) | gamma.
+// One stage holds one record: A3 | KP | U | P | gamma.  The M5 operand
+// [X ; -P] (128 x 64, K-major) starts 8 KiB before P, so its rows 0..63 X are
+// the second region of U: they only feed D1 rows 0..63, which nothing reads
+// after M5 (the next chunk's first MMA overwrites them).
 constexpr uint32_t ST_A3 = 0;
 constexpr uint32_t ST_KP = 32 * KiB;
 constexpr uint32_t ST_U = 48 * KiB;
-constexpr uint32_t ST_A5 = 64 * KiB;
-constexpr uint32_t ST_G = 80 * KiB;
-constexpr uint32_t ST_BYTES = 81 * KiB;
+constexpr uint32_t ST_P = 64 * KiB;
+constexpr uint32_t ST_A5 = ST_P - 8 * KiB;
+constexpr uint32_t ST_G = 72 * KiB;
+constexpr uint32_t ST_BYTES = 73 * KiB;
 constexpr uint32_t SM_SBF = 2 * ST_BYTES;        // [dk x dv] S in fp16, MN-major
-constexpr uint32_t SM_WBF = SM_SBF + 32 * KiB;   // [tok x dv] W in fp16, MN-major
-constexpr uint32_t SM_MISC = SM_WBF + 16 * KiB;
+constexpr uint32_t SM_WBF = SM_SBF + 32 * KiB;   // [tok x dv] W in fp16, MN-major; o staging
+constexpr uint32_t SM_SNAP = SM_WBF + 16 * KiB;  // 8 x 4 KiB snapshot staging tiles
+constexpr uint32_t SM_MISC = SM_SNAP + 32 * KiB;
 constexpr uint32_t MS_BAR_FULL = SM_MISC;        // 2 mbarriers (records in)
 constexpr uint32_t MS_BAR_MMA = SM_MISC + 16;
 constexpr uint32_t MS_TMEM = SM_MISC + 32;
 constexpr uint32_t SP_SMEM_BYTES = SM_MISC + 64;
-static_assert(SP_SMEM_BYTES + 1024 <= 232448, "shared memory budget");
+static_assert(SP_SMEM_BYTES <= 232448, "shared memory budget");
 
 constexpr uint32_t kRecInBytes = 32 * KiB + 16 * KiB + 16 * KiB + 8 * KiB + 512;
 
@@ -82,12 +87,14 @@ struct SpParams {
 };
 
 __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParams p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // the swizzled tiles need 1024-byte alignment: round the base up
-  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
   const Smem S{smem, sb};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if ((sb & 1023u) != 0) {  // the swizzled layouts need 1024-byte alignment
+    if (tid == 0) atomicOr(p.status, KDA_ERR_UNSUPPORTED);
+    return;
+  }
   const int hh = blockIdx.x, s = blockIdx.y;
   const int H = p.H, h = p.h0 + hh;
 
@@ -118,9 +125,6 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
     tmem_alloc(sb + MS_TMEM, TM_COLS);
     tmem_relinquish();
   }
-  // rows 0..63 of both stages' [0 ; -P] tiles stay zero (the copies fill rows 64..127)
-  for (int x = tid; x < 2 * 512; x += SP_THREADS)
-    S.u128(sb + (x >> 9) * ST_BYTES + ST_A5 + 16 * (x & 511)) = make_uint4(0, 0, 0, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
     bulk_g2s(st + ST_A3, rec + kRecA3, 32 * KiB, bar);
     bulk_g2s(st + ST_KP, rec + kRecKP, 16 * KiB, bar);
     bulk_g2s(st + ST_U, rec + kRecU, 16 * KiB, bar);
-    bulk_g2s(st + ST_A5 + 8 * KiB, rec + kRecP, 8 * KiB, bar);
+    bulk_g2s(st + ST_P, rec + kRecP, 8 * KiB, bar);
     bulk_g2s(st + ST_G, rec + kRecG, 512, bar);
   };
   bool full_pending[2] = {false, false}, mma_pending = false, aborted = false;
@@ -186,21 +190,44 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
     const uint32_t st = sb + static_cast<uint32_t>(stg) * ST_BYTES;
     const int64_t t0 = t_begin + 64LL * n;
     const int L = static_cast<int>(min(static_cast<int64_t>(64), t_end - t0));
-    if (!wait_all(bar_full + 8u * stg, (n >> 1) & 1)) { aborted = true; break; }
-    full_pending[stg] = false;
+    // Each thread waits for the record on its own (no CTA barrier here, so the
+    // previous chunk's o stores overlap this read-out); a wait that gives up
+    // is agreed on at the barrier before the first MMA.
+    const bool rec_ok = mbar_wait_bounded(bar_full + 8u * stg, (n >> 1) & 1, kWaitPolls);
 
     // ---- state read-out: snapshot, fp16 copy for the MMA, S *= gamma -------------------
     {
       float v[32];
       tmem_ld32(t_lane + TM_S + 32 * q4, v);
       tmem_wait_ld();
-      if (snap_pending >= 0) {  // the state after the previous (full) chunk
-        float4 *dst = reinterpret_cast<float4 *>(
-            p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
-            static_cast<size_t>(trow) * TD + 32 * q4);
+      if (snap_pending >= 0) {
+        // The state after the previous (full) chunk.  Each warp stages its
+        // 32 x 32 fp32 tile (float4 slots swizzled by row) and stores it so
+        // that every instruction writes four whole 128-byte rows; eight
+        // staging tiles, so the warps go in two rounds.
+        float *base = p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
+                      static_cast<size_t>(quad * 32) * TD + 32 * q4;
+        const uint32_t tile = sb + SM_SNAP + static_cast<uint32_t>(warp & 7) * 4096u;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        for (int rd = 0; rd < 2; ++rd) {
+          if ((warp >> 3) == rd) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              S.u128(tile + lane * 128u + (static_cast<uint32_t>(j ^ (lane & 7)) << 4)) =
+                  make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                             __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + (lane >> 3), c = lane & 7;
+              const uint4 w = S.u128(tile + r * 128u + (static_cast<uint32_t>(c ^ (r & 7)) << 4));
+              __stcs(reinterpret_cast<float4 *>(base + static_cast<size_t>(r) * TD) + c,
+                     make_float4(__uint_as_float(w.x), __uint_as_float(w.y),
+                                 __uint_as_float(w.z), __uint_as_float(w.w)));
+            }
+          }
+          __syncthreads();  // round 0's tiles are read before round 1 reuses them
+        }
         snap_pending = -1;
       }
       store_row32_f16(S, sb + SM_SBF, trow, q4, REG128, v, 1.f);
@@ -212,7 +239,12 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
     }
     fence_proxy_async();
     tc_fence_before();
-    __syncthreads();
+    if (__syncthreads_or(rec_ok ? 0 : 1)) {
+      if (tid == 0) atomicOr(p.status, KDA_ERR_TIMEOUT);
+      aborted = true;
+      break;
+    }
+    full_pending[stg] = false;
 
     // ---- D1 = [-Wk ; -Q~] S ------------------------------------------------------------
     if (tid == 0) {
@@ -249,20 +281,31 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
     if (n + 2 < n_chunks) full_pending[stg] = true;
 
     // ---- outputs: o = -D1 rows 64..127 -------------------------------------------------------
+    // Each of the 8 warps holds 32 rows x 32 columns (64 bytes of bf16 per
+    // row); it stages them in its 2 KiB slice of the W tile (free once the
+    // MMAs above are done) and stores 8 rows x 64 bytes per instruction.
     if (quad >= 2) {
-      const int r = trow - 64;
       float v[32];
       tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
       tmem_wait_ld();
-      if (r < L && p.o) {
-        uint4 *dst = reinterpret_cast<uint4 *>(
-            p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + 32 * q4);
+      const uint32_t tile = sb + SM_WBF + static_cast<uint32_t>((quad - 2) * 4 + q4) * 2048u;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          dst[j] = make_uint4(pack_bf16x2(-v[8 * j + 0], -v[8 * j + 1]),
-                              pack_bf16x2(-v[8 * j + 2], -v[8 * j + 3]),
-                              pack_bf16x2(-v[8 * j + 4], -v[8 * j + 5]),
-                              pack_bf16x2(-v[8 * j + 6], -v[8 * j + 7]));
+      for (int j = 0; j < 4; ++j)
+        S.u128(tile + lane * 64u + (static_cast<uint32_t>(j ^ (lane & 3)) << 4)) =
+            make_uint4(pack_bf16x2(-v[8 * j + 0], -v[8 * j + 1]),
+                       pack_bf16x2(-v[8 * j + 2], -v[8 * j + 3]),
+                       pack_bf16x2(-v[8 * j + 4], -v[8 * j + 5]),
+                       pack_bf16x2(-v[8 * j + 6], -v[8 * j + 7]));
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rl = 8 * i + (lane >> 2), c = lane & 3;  // row in the warp's 32, 16-byte piece
+        const int r = (quad - 2) * 32 + rl;
+        if (r < L) {
+          const uint4 w = S.u128(tile + rl * 64u + (static_cast<uint32_t>(c ^ (rl & 3)) << 4));
+          reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(t0 + r) * H + h) * TD +
+                                    32 * q4)[c] = w;
+        }
       }
     }
     if (p.snaps && L == 64) snap_pending = snap_row;
@@ -316,7 +359,7 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               int h0, int hg, const float *S0, kda_bf16 *o, float *S_final,
                               float *snaps, const int64_t *snap_offsets, int *status,
                               const int32_t *slots, cudaStream_t stream) {
-  const uint32_t smem = SP_SMEM_BYTES + 1024;  // + alignment slack
+  const uint32_t smem = SP_SMEM_BYTES;
   cudaError_t err = cudaFuncSetAttribute(state_pass_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

@@ -104,10 +104,14 @@ def test_decode_tokens_rejects_before_launch(L, kw, status):
 def _ex_args(**kw):
     """kda_chunk_fwd_ex arguments: kda_chunk_fwd's with `pre` after chunk."""
     args = _chunk_args(**{k: v for k, v in kw.items() if k != "pre"})
+    if "ws_bytes" in kw:  # a (fake, never touched) workspace pointer of that size
+        args[19] = ctypes.c_void_p(0x40000)
     return args[:14] + [kw.get("pre", 0)] + args[14:]
 
 
 @pytest.mark.parametrize("kw,status", [
+    (dict(pre=0x300, dk=128, dv=128), 4), (dict(pre=0x100), 4),
+    (dict(pre=0x100, dk=128, dv=128), 5), (dict(pre=0x200, dk=128, dv=128, ws_bytes=4096), 5),
     (dict(pre=4), 4), (dict(pre=0x80000000), 4), (dict(pre=3, dk=96), 4),
     (dict(pre=3, q=None), 1), (dict(pre=1, H=0), 2), (dict(pre=3, n_seq=0, total=0), 0),
     (dict(pre=2, q=ctypes.c_void_p(0x10008)), 3),

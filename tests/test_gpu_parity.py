@@ -438,3 +438,34 @@ def test_preops_decode(kda, d):
     ref = oracle_subset(x, list(range(n)), [0, 1], snapshots=False, pre=3)
     assert o_err(f64(o), ref["o"]) <= O_TOL
     assert s_err(f64(pool), ref["S_final"]) <= S_TOL
+
+
+def test_split_phase_calls_match_one_call(kda):
+    """chunk_fwd with PASS_PREPARE then PASS_STATE (the bench's step) gives
+    exactly the one-call result, and a state pass can be repeated from the
+    same records; both match the oracle."""
+    x = kda_inputs.make_prefill(4, 128, 128, [300, 64, 129, 1000], seed=51, device="cuda",
+                                S0_std=0.02)
+    n = len(x["lengths"])
+    total = x["k"].shape[0]
+    ws = torch.empty(kda.workspace_bytes(n, total, 4, 128, 128), dtype=torch.uint8,
+                     device="cuda")
+    offs = kda.snapshot_offsets(x["lengths"])
+    args = [x[nm] for nm in ("q", "k", "v", "z", "beta", "A")]
+    outs = []
+    for passes in ((0,), (kda.PASS_PREPARE, kda.PASS_STATE, kda.PASS_STATE)):
+        S_final = torch.full((n, 4, 128, 128), float("nan"), device="cuda")
+        snaps = torch.full((int(offs[-1]), 4, 128, 128), float("nan"), device="cuda")
+        o = torch.full((total, 4, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        for ps in passes:
+            kda.chunk_fwd(*args, cu_seqlens=x["cu_seqlens"], S0=x["S0"], o=o, S_final=S_final,
+                          snaps=snaps, snap_offsets=offs, workspace=ws, pre=ps)
+        torch.cuda.synchronize()
+        assert kda.device_status() == 0
+        outs.append((o, S_final, snaps))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    ref = oracle_subset(x, list(range(n)), [0, 1, 2, 3])
+    assert o_err(f64(outs[1][0]), ref["o"]) <= O_TOL
+    assert s_err(f64(outs[1][1]), ref["S_final"]) <= S_TOL
+    assert s_err(f64(outs[1][2]), ref["snaps"]) <= S_TOL

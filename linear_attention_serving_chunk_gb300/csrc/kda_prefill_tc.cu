@@ -70,7 +70,7 @@ constexpr uint32_t SM_APA = SM_AP;                // tf32 [Khat_2p ; Khat_2p+1] 
 constexpr uint32_t SM_APB = SM_AP + 64 * KiB;     // tf32 [KE_2p; QE_2p; KE_2p+1; QE_2p+1] 64 x 128
 constexpr uint32_t SM_AKK = SM_AP;                // fp32 [64][65] A_kk (after the AP MMAs)
 constexpr uint32_t SM_TF = SM_AP + 64 * 65 * 4;   // fp32 [64][65] T
-constexpr uint32_t SM_TY = SM_AP + 34 * KiB;      // fp32 [3][16][17] block products
+constexpr uint32_t SM_TY = SM_AP + 34 * KiB;      // fp32 [4][16][17] block products
 constexpr uint32_t SM_SBF = SM_AP;                // [dk x dv] S in fp16, MN-major (after T')
 constexpr uint32_t SM_A5 = SM_AP + 48 * KiB;      // [128 x 64] K-major: [0 ; -P]
 constexpr uint32_t SM_TP = SM_AP + 64 * KiB;      // [128 x 64] K-major: [T diag(beta) ; 0], bf16 hi
@@ -86,9 +86,10 @@ constexpr uint32_t MS_BAR_V = SM_MISC + 40;
 constexpr uint32_t MS_BETA = SM_MISC + 64;        // 64 fp32
 constexpr uint32_t MS_LAM = SM_MISC + 320;        // [4][128] fp32 sub-tile decay totals
 constexpr uint32_t MS_NRM = MS_LAM + 4 * TD * 4;  // [64][2] fp32 1/||k_r||, 1/||q_r|| (pre-op)
-constexpr uint32_t TC_SMEM_BYTES = MS_NRM + 64 * 8;
+constexpr uint32_t MS_TASK = MS_NRM + 64 * 8;     // chunk preparation: 3 x 32-byte task slots
+constexpr uint32_t TC_SMEM_BYTES = MS_TASK + 3 * 32;
 static_assert(SM_TF + 64 * 65 * 4 <= SM_TY, "T scratch overlaps");
-static_assert(SM_TY + 3 * 16 * 17 * 4 <= SM_A5, "block scratch overlaps A5");
+static_assert(SM_TY + 4 * 16 * 17 * 4 <= SM_A5, "block scratch overlaps A5");
 static_assert(TC_SMEM_BYTES <= 232448, "shared memory budget");
 
 constexpr uint32_t A3_BYTES = 32 * KiB;
@@ -282,6 +283,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               p.h0 + static_cast<int>(t % p.hg)};
     }
   };
+  // Chunk preparation resolves its tasks ahead of use: task n sits in slot
+  // n % 3, written during iteration n - 2 by an idle thread (a varlen task
+  // takes a binary search over chunk_start and two cu_seqlens loads, a chain
+  // of dependent global loads that would stall whoever needs the task).
+  // A slot also carries the head's decay constant -e^{A_h} log2(e).
+  auto put_task = [&](int n) {
+    const Task tk = task_at(n);
+    const uint32_t slot = sb + MS_TASK + 32u * static_cast<uint32_t>(n % 3);
+    S.u128(slot) = make_uint4(static_cast<uint32_t>(tk.t0), static_cast<uint32_t>(tk.t0 >> 32),
+                              static_cast<uint32_t>(tk.L), static_cast<uint32_t>(tk.h));
+    S.f32(slot + 16) = -__expf(p.A[tk.h]) * 1.4426950408889634f;
+  };
+  auto task_of = [&](int n) -> Task {
+    if constexpr (kPrep) {
+      const uint4 w = S.u128(sb + MS_TASK + 32u * static_cast<uint32_t>(n % 3));
+      return {static_cast<int64_t>((static_cast<uint64_t>(w.y) << 32) | w.x),
+              static_cast<int>(w.z), static_cast<int>(w.w)};
+    } else {
+      return task_at(n);
+    }
+  };
   int64_t snap_row = 0;
   if (!kPrep && p.snaps)
     snap_row = p.snap_offsets ? p.snap_offsets[s] : static_cast<int64_t>(s) * (p.fixed_len / 64);
@@ -309,6 +331,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tmem_alloc(sb + MS_TMEM, kPrep ? TM_COLS_PREP : TM_COLS);
     tmem_relinquish();
   }
+  if constexpr (kPrep) {
+    if (tid == 64) {
+      if (n_chunks > 0) put_task(0);
+      if (n_chunks > 1) put_task(1);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -333,7 +361,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   auto issue_qz = [&](int n) {  // q -> A3[n&1] lower half, z -> ZB[n&1]
     const int par = n & 1;
-    const Task tk = task_at(n);
+    const Task tk = task_of(n);
     const int t0 = static_cast<int>(tk.t0), h = tk.h;
     const uint32_t bar = bar_qz0 + 8 * par;
     mbar_expect_tx(bar, 2 * TILE_BYTES);
@@ -347,14 +375,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // k is refilled as soon as the operand build has read it (K~ goes to A3),
   // v once T'V is done; each has its own barrier.
   auto issue_k = [&](int n) {
-    const Task tk = task_at(n);
+    const Task tk = task_of(n);
     const int t0 = static_cast<int>(tk.t0), h = tk.h;
     mbar_expect_tx(bar_k, TILE_BYTES);
     tma_load_3d(sb + SM_KB, &tm_k, 0, h, t0, bar_k);
     tma_load_3d(sb + SM_KB + REG64, &tm_k, 64, h, t0, bar_k);
   };
   auto issue_v = [&](int n) {
-    const Task tk = task_at(n);
+    const Task tk = task_of(n);
     const int t0 = static_cast<int>(tk.t0), h = tk.h;
     mbar_expect_tx(bar_v, TILE_BYTES);
     tma_load_3d(sb + SM_VB, &tm_v, 0, h, t0, bar_v);
@@ -364,7 +392,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   bool qz_pending[2] = {false, false}, k_pending = false, v_pending = false, mma_pending = false;
   float beta_next = 0.f;
   if (tid < 64 && n_chunks > 0) {
-    const Task tk = task_at(0);
+    const Task tk = task_of(0);
     if (tid < tk.L) beta_next = bf2f(p.beta[static_cast<size_t>(tk.t0 + tid) * H + tk.h]);
   }
   // A full chunk's snapshot is written from the next chunk's state read-out
@@ -424,10 +452,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int rbase = 16 * R + 4 * hf;
   for (int n = 0; n < n_chunks && !aborted; ++n) {
     const int par = n & 1;
-    const Task tk = task_at(n);
+    const Task tk = task_of(n);
     const int64_t t0 = tk.t0;
     const int L = tk.L;
-    if constexpr (kPrep) dc1 = -__expf(p.A[tk.h]) * kLog2e;
+    if constexpr (kPrep) dc1 = S.f32(sb + MS_TASK + 32u * static_cast<uint32_t>(n % 3) + 16);
     const uint32_t a3 = sb + SM_A3 + par * A3_BYTES;
     const uint32_t zb = sb + SM_ZB + par * TILE_BYTES;
 
@@ -511,7 +539,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid < 64) {
       beta_next = 0.f;
       if (n + 1 < n_chunks) {
-        const Task nx = task_at(n + 1);
+        const Task nx = task_of(n + 1);
         if (tid < nx.L)
           beta_next = ldg_bf16_pinned(p.beta + static_cast<size_t>(nx.t0 + tid) * H + nx.h);
       }
@@ -639,7 +667,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     make_uint2(tf32_rna(kb0 * f0[rp]), tf32_rna(kb1 * f1[rp]));
             }
             if (pp == 1) {
-              // K~ into A3 rows 0..63 (free until -Wk), so k can be refilled now
+              // K~ into A3 rows 0..63 (free until -Wk), so k can be refilled now;
+              // -Q~ over q, K' over z
               S.u32(a3 + rg16_128 + o16) = pack_bf16x2(ke0 * x0, ke1 * x1);
               S.u32(a_q) = pack_f16x2(-qe0 * x0, -qe1 * x1);
               S.u32(a_z) = pack_f16x2(kb0 * y0, kb1 * y1);
@@ -728,47 +757,72 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     __syncthreads();
-    // Off-diagonal blocks, one block column J per warp (warps 0..2), top to
-    // bottom: T[R][J] = -T[R][R] sum_{M=J}^{R-1} A[R][M] T[M][J].  Every
-    // operand a warp needs is a diagonal block or one it wrote itself.
-    if (warp < 3) {
-      const int J = warp, g = lane >> 2, t = lane & 3;
+    if constexpr (kPrep) {  // warp 15 is idle during the off-diagonal blocks
+      if (tid == 480 && n + 2 < n_chunks) put_task(n + 2);
+    }
+    // Off-diagonal blocks by the 2 x 2 block inverse: with Ta, Tb the inverses
+    // of the top-left and bottom-right 32 x 32 blocks, the bottom-left block
+    // is -Tb A_ba Ta.  Level 1: T10 = -T11 A10 T00 and T32 = -T33 A32 T22;
+    // level 2: X = A_ba Ta; level 3: T_RJ = -sum_{M=2}^{R} T_RM X_MJ.
+    // Chains of 2 + 2 + 2 16 x 16 products, four warps at most.
+    {
+      const int g = lane >> 2, t = lane & 3;
       float *akk = reinterpret_cast<float *>(S.ptr(sb + SM_AKK));
       float *tf = reinterpret_cast<float *>(S.ptr(sb + SM_TF));
-      float *ty = reinterpret_cast<float *>(S.ptr(sb + SM_TY)) + J * 16 * 17;
-      for (int Rr = J + 1; Rr < 4; ++Rr) {
-        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (int M = J; M < Rr; ++M)
-          warp_mma16(akk + (16 * Rr) * 65 + 16 * M, 65, tf + (16 * M) * 65 + 16 * J, 65, c, lane);
+      float *xs = reinterpret_cast<float *>(S.ptr(sb + SM_TY));  // 4 blocks of [16][17]
+      // c (two 16x8 fragments) -> fp32 [16][ld] block, negated or not
+      auto put16 = [&](float *dst, int ld, const float (&c)[2][4], float sgn) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          ty[g * 17 + 8 * nt + 2 * t] = c[nt][0];
-          ty[g * 17 + 8 * nt + 2 * t + 1] = c[nt][1];
-          ty[(g + 8) * 17 + 8 * nt + 2 * t] = c[nt][2];
-          ty[(g + 8) * 17 + 8 * nt + 2 * t + 1] = c[nt][3];
+          dst[g * ld + 8 * nt + 2 * t] = sgn * c[nt][0];
+          dst[g * ld + 8 * nt + 2 * t + 1] = sgn * c[nt][1];
+          dst[(g + 8) * ld + 8 * nt + 2 * t] = sgn * c[nt][2];
+          dst[(g + 8) * ld + 8 * nt + 2 * t + 1] = sgn * c[nt][3];
         }
-        __syncwarp();
-        float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mma16(tf + (16 * Rr) * 65 + 16 * Rr, 65, ty, 17, e, lane);
-        float *dst = tf + (16 * Rr) * 65 + 16 * J;
+      };
+      // block (R, J) of T = -e: fp32 T, and T' = T diag(beta) as bf16 hi + lo
+      auto put_t = [&](int R, int J, const float (&e)[2][4]) {
+        put16(tf + (16 * R) * 65 + 16 * J, 65, e, -1.f);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          dst[g * 65 + 8 * nt + 2 * t] = -e[nt][0];
-          dst[g * 65 + 8 * nt + 2 * t + 1] = -e[nt][1];
-          dst[(g + 8) * 65 + 8 * nt + 2 * t] = -e[nt][2];
-          dst[(g + 8) * 65 + 8 * nt + 2 * t + 1] = -e[nt][3];
-          // T' = T diag(beta) as bf16 hi + lo, two adjacent columns per store
           const int col = 16 * J + 8 * nt + 2 * t;
           const float b0 = S.f32(sb + MS_BETA + 4 * col), b1 = S.f32(sb + MS_BETA + 4 * (col + 1));
           uint32_t hi, lo;
           split_bf16x2(-e[nt][0] * b0, -e[nt][1] * b1, hi, lo);
-          S.u32(sb + SM_TP + sw128_off(16 * Rr + g, col, REG128)) = hi;
-          S.u32(sb + SM_TPL + sw128_off(16 * Rr + g, col, REG128)) = lo;
+          S.u32(sb + SM_TP + sw128_off(16 * R + g, col, REG128)) = hi;
+          S.u32(sb + SM_TPL + sw128_off(16 * R + g, col, REG128)) = lo;
           split_bf16x2(-e[nt][2] * b0, -e[nt][3] * b1, hi, lo);
-          S.u32(sb + SM_TP + sw128_off(16 * Rr + g + 8, col, REG128)) = hi;
-          S.u32(sb + SM_TPL + sw128_off(16 * Rr + g + 8, col, REG128)) = lo;
+          S.u32(sb + SM_TP + sw128_off(16 * R + g + 8, col, REG128)) = hi;
+          S.u32(sb + SM_TPL + sw128_off(16 * R + g + 8, col, REG128)) = lo;
         }
+      };
+      if (warp < 2) {  // level 1
+        const int R = 2 * warp + 1, J = R - 1;
+        float *y = xs + warp * 16 * 17;
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mma16(akk + (16 * R) * 65 + 16 * J, 65, tf + (16 * J) * 65 + 16 * J, 65, c, lane);
+        put16(y, 17, c, 1.f);
         __syncwarp();
+        float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_mma16(tf + (16 * R) * 65 + 16 * R, 65, y, 17, e, lane);
+        put_t(R, J, e);
+      }
+      __syncthreads();
+      if (warp < 4) {  // level 2: X_RJ = sum_{M=J}^{1} A_RM T_MJ, R = 2, 3, J = 0, 1
+        const int R = 2 + (warp >> 1), J = warp & 1;
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int M = J; M < 2; ++M)
+          warp_mma16(akk + (16 * R) * 65 + 16 * M, 65, tf + (16 * M) * 65 + 16 * J, 65, c, lane);
+        put16(xs + warp * 16 * 17, 17, c, 1.f);
+      }
+      __syncthreads();
+      if (warp < 4) {  // level 3: T_RJ = -sum_{M=2}^{R} T_RM X_MJ
+        const int R = 2 + (warp >> 1), J = warp & 1;
+        float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int M = 2; M <= R; ++M)
+          warp_mma16(tf + (16 * R) * 65 + 16 * M, 65, xs + ((M - 2) * 2 + J) * 16 * 17, 17, e,
+                     lane);
+        put_t(R, J, e);
       }
     }
     fence_proxy_async();  // T' was written by the T blocks above

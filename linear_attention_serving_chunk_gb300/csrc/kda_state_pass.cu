@@ -37,21 +37,23 @@ using namespace tcx;
 
 constexpr int SP_THREADS = 512;
 constexpr int TD = 128;
+constexpr int NC = 64;  // value columns of the state per CTA (two CTAs per chain)
 
-// One stage holds one record: A3 | KP | U | P | gamma.  The M5 operand
-// [X ; -P] (128 x 64, K-major) starts 8 KiB before P, so its rows 0..63 X are
-// the second region of U: they only feed D1 rows 0..63, which nothing reads
-// after M5 (the next chunk's first MMA overwrites them).
+// One stage holds one record, with only this CTA's half of U:
+// A3 | KP | U half | P | gamma.  The M5 operand [X ; -P] (128 x 64, K-major)
+// starts 8 KiB before P, so its rows 0..63 X are the U half: they only feed
+// D1 rows 0..63, which nothing reads after M5 (the next chunk's first MMA
+// overwrites them).
 constexpr uint32_t ST_A3 = 0;
 constexpr uint32_t ST_KP = 32 * KiB;
 constexpr uint32_t ST_U = 48 * KiB;
-constexpr uint32_t ST_P = 64 * KiB;
+constexpr uint32_t ST_P = 56 * KiB;
 constexpr uint32_t ST_A5 = ST_P - 8 * KiB;
-constexpr uint32_t ST_G = 72 * KiB;
-constexpr uint32_t ST_BYTES = 73 * KiB;
-constexpr uint32_t SM_SBF = 2 * ST_BYTES;        // [dk x dv] S in fp16, MN-major
-constexpr uint32_t SM_WBF = SM_SBF + 32 * KiB;   // [tok x dv] W in fp16, MN-major; o staging
-constexpr uint32_t SM_SNAP = SM_WBF + 16 * KiB;  // 8 x 4 KiB snapshot staging tiles
+constexpr uint32_t ST_G = 64 * KiB;
+constexpr uint32_t ST_BYTES = 65 * KiB;
+constexpr uint32_t SM_SBF = 2 * ST_BYTES;        // [dk x NC] S in fp16, MN-major
+constexpr uint32_t SM_WBF = SM_SBF + 16 * KiB;   // [tok x NC] W in fp16, MN-major; o staging
+constexpr uint32_t SM_SNAP = SM_WBF + 8 * KiB;   // 16 x 2 KiB snapshot staging tiles
 constexpr uint32_t SM_MISC = SM_SNAP + 32 * KiB;
 constexpr uint32_t MS_BAR_FULL = SM_MISC;        // 2 mbarriers (records in)
 constexpr uint32_t MS_BAR_MMA = SM_MISC + 16;
@@ -59,17 +61,17 @@ constexpr uint32_t MS_TMEM = SM_MISC + 32;
 constexpr uint32_t SP_SMEM_BYTES = SM_MISC + 64;
 static_assert(SP_SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr uint32_t kRecInBytes = 32 * KiB + 16 * KiB + 16 * KiB + 8 * KiB + 512;
+constexpr uint32_t kRecInBytes = 32 * KiB + 16 * KiB + 8 * KiB + 8 * KiB + 512;
 
-constexpr uint32_t TM_S = 0;     // fp32 state (row = key channel)
-constexpr uint32_t TM_D1 = 128;  // -Wk S -> (rows 0..63); -O (rows 64..127)
-constexpr uint32_t TM_COLS = 256;
+constexpr uint32_t TM_S = 0;    // fp32 state columns (row = key channel)
+constexpr uint32_t TM_D1 = NC;  // -Wk S (rows 0..63); -O (rows 64..127)
+constexpr uint32_t TM_COLS = 128;
 
 constexpr uint32_t kWaitPolls = 1u << 24;
-constexpr int kCopyThread = 128;  // issues the record copies (warp 4: no TMEM lane 0..31 role)
+constexpr int kCopyThread = 128;  // issues the record copies
 
-constexpr uint32_t ID_KMN = idesc_mma(128, 128, kFmtF16, kFmtF16, 0, 1);   // K-major x MN
-constexpr uint32_t ID_MNMN = idesc_mma(128, 128, kFmtF16, kFmtF16, 1, 1);  // MN x MN
+constexpr uint32_t ID_KMN = idesc_mma(128, NC, kFmtF16, kFmtF16, 0, 1);   // K-major x MN
+constexpr uint32_t ID_MNMN = idesc_mma(128, NC, kFmtF16, kFmtF16, 1, 1);  // MN x MN
 
 struct SpParams {
   const uint8_t *rec;          // records [chunk][head in group]
@@ -86,6 +88,8 @@ struct SpParams {
   const int32_t *slots;
 };
 
+// One CTA per (sequence, head, half of the value columns): the columns of the
+// state never mix, so each half runs on its own with the same records.
 __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
@@ -95,8 +99,9 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
     if (tid == 0) atomicOr(p.status, KDA_ERR_UNSUPPORTED);
     return;
   }
-  const int hh = blockIdx.x, s = blockIdx.y;
+  const int hh = blockIdx.x >> 1, half = blockIdx.x & 1, s = blockIdx.y;
   const int H = p.H, h = p.h0 + hh;
+  const int col0 = NC * half;
 
   int64_t t_begin, t_end, chunk0;
   if (p.cu_seqlens) {
@@ -131,17 +136,18 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + MS_TMEM);
 
   // TMEM read-outs: a warp reaches the 32 lanes of its quadrant; the 16 warps
-  // split the 128 columns in quarters.
+  // split the CTA's 64 columns in quarters of 16.
   const int quad = warp & 3, q4 = warp >> 2;
   const int trow = quad * 32 + lane;  // TMEM lane = matrix row
   const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  const int cq = col0 + 16 * q4;      // first state column of this thread
 
-  {  // initial state -> TMEM (row trow, columns [32 q4, 32 q4 + 32))
-    float v[32];
+  {  // initial state -> TMEM
+    float v[16];
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      v[j] = p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + 32 * q4 + j] : 0.f;
-    tmem_st32(t_lane + TM_S + 32 * q4, v);
+    for (int j = 0; j < 16; ++j)
+      v[j] = p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + cq + j] : 0.f;
+    tmem_st16(t_lane + TM_S + 16 * q4, v);
     tmem_wait_st();
   }
 
@@ -153,7 +159,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
     mbar_expect_tx(bar, kRecInBytes);
     bulk_g2s(st + ST_A3, rec + kRecA3, 32 * KiB, bar);
     bulk_g2s(st + ST_KP, rec + kRecKP, 16 * KiB, bar);
-    bulk_g2s(st + ST_U, rec + kRecU, 16 * KiB, bar);
+    bulk_g2s(st + ST_U, rec + kRecU + half * 8 * KiB, 8 * KiB, bar);
     bulk_g2s(st + ST_P, rec + kRecP, 8 * KiB, bar);
     bulk_g2s(st + ST_G, rec + kRecG, 512, bar);
   };
@@ -167,22 +173,17 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
   uint32_t mma_phase = 0;
   int64_t snap_pending = -1;
 
-  auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-    const bool ok = mbar_wait_bounded(bar, parity, kWaitPolls);
+  auto wait_mma = [&]() -> bool {
+    const bool ok = mbar_wait_bounded(bar_mma, mma_phase, kWaitPolls);
     if (__syncthreads_or(ok ? 0 : 1)) {
       if (tid == 0) atomicOr(p.status, KDA_ERR_TIMEOUT);
+      tc_fence_after();
       return false;
     }
-    return true;
-  };
-  auto wait_mma = [&]() -> bool {
-    const bool ok = wait_all(bar_mma, mma_phase);
-    if (ok) {
-      mma_phase ^= 1u;
-      mma_pending = false;
-    }
+    mma_phase ^= 1u;
+    mma_pending = false;
     tc_fence_after();
-    return ok;
+    return true;
   };
 
   for (int n = 0; n < n_chunks; ++n) {
@@ -197,44 +198,37 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
 
     // ---- state read-out: snapshot, fp16 copy for the MMA, S *= gamma -------------------
     {
-      float v[32];
-      tmem_ld32(t_lane + TM_S + 32 * q4, v);
+      float v[16];
+      tmem_ld16(t_lane + TM_S + 16 * q4, v);
       tmem_wait_ld();
       if (snap_pending >= 0) {
-        // The state after the previous (full) chunk.  Each warp stages its
-        // 32 x 32 fp32 tile (float4 slots swizzled by row) and stores it so
-        // that every instruction writes four whole 128-byte rows; eight
-        // staging tiles, so the warps go in two rounds.
+        // The state after the previous (full) chunk: each warp stages its
+        // 32 x 16 fp32 tile (16-byte pieces rotated by row) and stores it
+        // as 8 rows x 64 bytes per instruction.
+        const uint32_t tile = sb + SM_SNAP + static_cast<uint32_t>(warp) * 2048u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          S.u128(tile + lane * 64u + (static_cast<uint32_t>(j ^ (lane & 3)) << 4)) =
+              make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                         __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+        __syncwarp();
         float *base = p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
-                      static_cast<size_t>(quad * 32) * TD + 32 * q4;
-        const uint32_t tile = sb + SM_SNAP + static_cast<uint32_t>(warp & 7) * 4096u;
+                      static_cast<size_t>(quad * 32) * TD + cq;
 #pragma unroll
-        for (int rd = 0; rd < 2; ++rd) {
-          if ((warp >> 3) == rd) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              S.u128(tile + lane * 128u + (static_cast<uint32_t>(j ^ (lane & 7)) << 4)) =
-                  make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
-                             __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int r = 4 * i + (lane >> 3), c = lane & 7;
-              const uint4 w = S.u128(tile + r * 128u + (static_cast<uint32_t>(c ^ (r & 7)) << 4));
-              __stcs(reinterpret_cast<float4 *>(base + static_cast<size_t>(r) * TD) + c,
-                     make_float4(__uint_as_float(w.x), __uint_as_float(w.y),
-                                 __uint_as_float(w.z), __uint_as_float(w.w)));
-            }
-          }
-          __syncthreads();  // round 0's tiles are read before round 1 reuses them
+        for (int i = 0; i < 4; ++i) {
+          const int r = 8 * i + (lane >> 2), c = lane & 3;
+          const uint4 w = S.u128(tile + r * 64u + (static_cast<uint32_t>(c ^ (r & 3)) << 4));
+          __stcs(reinterpret_cast<float4 *>(base + static_cast<size_t>(r) * TD) + c,
+                 make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                             __uint_as_float(w.w)));
         }
         snap_pending = -1;
       }
-      store_row32_f16(S, sb + SM_SBF, trow, q4, REG128, v, 1.f);
+      store_row16_f16(S, sb + SM_SBF, trow, q4, v, 1.f);
       const float gam = S.f32(st + ST_G + 4 * trow);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= gam;
-      tmem_st32(t_lane + TM_S + 32 * q4, v);
+      for (int j = 0; j < 16; ++j) v[j] *= gam;
+      tmem_st16(t_lane + TM_S + 16 * q4, v);
       tmem_wait_st();
     }
     fence_proxy_async();
@@ -257,17 +251,17 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
 
     // ---- W = U - Wk S -> fp16 ----------------------------------------------------------------
     if (quad < 2) {
-      float v[32];
-      tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
+      float v[16];
+      tmem_ld16(t_lane + TM_D1 + 16 * q4, v);
       tmem_wait_ld();
-      add_row32_f16(S, st + ST_U, trow, q4, REG64, v);
-      store_row32_f16(S, sb + SM_WBF, trow, q4, REG64, v, 1.f);
+      add_row16_f16(S, st + ST_U, trow, q4, v);
+      store_row16_f16(S, sb + SM_WBF, trow, q4, v, 1.f);
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
 
-    // ---- S += K'^T W;  D1 += [0 ; -P] W ------------------------------------------------------
+    // ---- S += K'^T W;  D1 += [X ; -P] W -------------------------------------------------------
     if (tid == 0) {
       tc_fence_after();
       issue_mma(tmem + TM_S, st + ST_KP, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
@@ -281,30 +275,29 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
     if (n + 2 < n_chunks) full_pending[stg] = true;
 
     // ---- outputs: o = -D1 rows 64..127 -------------------------------------------------------
-    // Each of the 8 warps holds 32 rows x 32 columns (64 bytes of bf16 per
-    // row); it stages them in its 2 KiB slice of the W tile (free once the
-    // MMAs above are done) and stores 8 rows x 64 bytes per instruction.
+    // Each of the 8 warps holds 32 rows x 16 columns (32 bytes of bf16 per
+    // row); it stages them in its 1 KiB slice of the W tile (free once the
+    // MMAs above are done) and stores 16 rows x 32 bytes per instruction.
     if (quad >= 2) {
-      float v[32];
-      tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
+      float v[16];
+      tmem_ld16(t_lane + TM_D1 + 16 * q4, v);
       tmem_wait_ld();
-      const uint32_t tile = sb + SM_WBF + static_cast<uint32_t>((quad - 2) * 4 + q4) * 2048u;
+      const uint32_t tile = sb + SM_WBF + static_cast<uint32_t>((quad - 2) * 4 + q4) * 1024u;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        S.u128(tile + lane * 64u + (static_cast<uint32_t>(j ^ (lane & 3)) << 4)) =
+      for (int j = 0; j < 2; ++j)
+        S.u128(tile + lane * 32u + (static_cast<uint32_t>(j ^ (lane & 1)) << 4)) =
             make_uint4(pack_bf16x2(-v[8 * j + 0], -v[8 * j + 1]),
                        pack_bf16x2(-v[8 * j + 2], -v[8 * j + 3]),
                        pack_bf16x2(-v[8 * j + 4], -v[8 * j + 5]),
                        pack_bf16x2(-v[8 * j + 6], -v[8 * j + 7]));
       __syncwarp();
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int rl = 8 * i + (lane >> 2), c = lane & 3;  // row in the warp's 32, 16-byte piece
+      for (int i = 0; i < 2; ++i) {
+        const int rl = 16 * i + (lane >> 1), c = lane & 1;  // row in the warp's 32, 16-byte piece
         const int r = (quad - 2) * 32 + rl;
         if (r < L) {
-          const uint4 w = S.u128(tile + rl * 64u + (static_cast<uint32_t>(c ^ (rl & 3)) << 4));
-          reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(t0 + r) * H + h) * TD +
-                                    32 * q4)[c] = w;
+          const uint4 w = S.u128(tile + rl * 32u + (static_cast<uint32_t>(c ^ (rl & 1)) << 4));
+          reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + cq)[c] = w;
         }
       }
     }
@@ -315,22 +308,22 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
   }
 
   if (!aborted && (p.S_final || snap_pending >= 0)) {
-    float v[32];
-    tmem_ld32(t_lane + TM_S + 32 * q4, v);
+    float v[16];
+    tmem_ld16(t_lane + TM_S + 16 * q4, v);
     tmem_wait_ld();
     if (p.S_final) {
       float4 *dst = reinterpret_cast<float4 *>(p.S_final + state_off +
-                                               static_cast<size_t>(trow) * TD + 32 * q4);
+                                               static_cast<size_t>(trow) * TD + cq);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 4; ++j)
         dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
     if (snap_pending >= 0) {
       float4 *dst = reinterpret_cast<float4 *>(
           p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
-          static_cast<size_t>(trow) * TD + 32 * q4);
+          static_cast<size_t>(trow) * TD + cq);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 4; ++j)
         __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
     }
   }
@@ -366,7 +359,7 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
   if (err != cudaSuccess) return err;
   SpParams prm{rec, cu_seqlens, chunk_start, fixed_len, H, h0, hg, S0, o, S_final, snaps,
                snap_offsets, status, slots};
-  const dim3 grid(static_cast<unsigned>(hg), static_cast<unsigned>(n_seq));
+  const dim3 grid(static_cast<unsigned>(2 * hg), static_cast<unsigned>(n_seq));
   state_pass_kernel<<<grid, SP_THREADS, smem, stream>>>(prm);
   return cudaGetLastError();
 }

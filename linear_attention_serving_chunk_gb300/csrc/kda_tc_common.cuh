@@ -74,6 +74,40 @@ __device__ __forceinline__ void store_row32_f16(const Smem &S, uint32_t tile, in
   }
 }
 
+// Write 16 fp32 values (columns [16 c4, 16 c4 + 16) of `row`, c4 = 0..3) as
+// fp16 into a 64-column, 128-byte-swizzled tile.
+__device__ __forceinline__ void store_row16_f16(const Smem &S, uint32_t tile, int row, int c4,
+                                                const float (&v)[16], float scale) {
+  const uint32_t base = tile + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t pos = static_cast<uint32_t>((2 * c4 + j) ^ (row & 7)) << 4;
+    S.u128(base + pos) = make_uint4(pack_f16x2(scale * v[8 * j + 0], scale * v[8 * j + 1]),
+                                    pack_f16x2(scale * v[8 * j + 2], scale * v[8 * j + 3]),
+                                    pack_f16x2(scale * v[8 * j + 4], scale * v[8 * j + 5]),
+                                    pack_f16x2(scale * v[8 * j + 6], scale * v[8 * j + 7]));
+  }
+}
+
+// Add the 16 fp16 values at columns [16 c4, 16 c4 + 16) of `row` of a
+// 64-column, 128-byte-swizzled tile to v.
+__device__ __forceinline__ void add_row16_f16(const Smem &S, uint32_t tile, int row, int c4,
+                                              float (&v)[16]) {
+  const uint32_t base = tile + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t pos = static_cast<uint32_t>((2 * c4 + j) ^ (row & 7)) << 4;
+    const uint4 w = S.u128(base + pos);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ws[e]));
+      v[8 * j + 2 * e] += f.x;
+      v[8 * j + 2 * e + 1] += f.y;
+    }
+  }
+}
+
 // Add the 32 fp16 values at columns [32 q4, 32 q4 + 32) of `row` of a
 // 128-byte-swizzled tile (regions `region` bytes apart) to v.
 __device__ __forceinline__ void add_row32_f16(const Smem &S, uint32_t tile, int row, int q4,

@@ -694,13 +694,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (mma_pending) { aborted = true; break; }
     }
 
-    // zero A5 (its upper block stays zero; -P fills the lower block) and T'
-    // hi / lo (rows >= 64 and the upper triangle stay zero; the T blocks fill
-    // the rest)
-    for (int x = tid; x < 1024; x += TC_THREADS) {
-      S.u128(sb + SM_A5 + 16 * x) = make_uint4(0, 0, 0, 0);
+    // Zero what the read-out and the T blocks do not write: the upper
+    // triangle of -P (rows 64..127 of A5) and of T' hi / lo.  Rows 0..63 of
+    // A5 only feed D1 rows that are never read after M5, and rows 64..127 of
+    // T' only the D1 / Wk rows 64..127, which the chunk preparation never
+    // reads; the single pass needs them zero (U's rows 64..127 start -O).
+    for (int x = tid; x < 512; x += TC_THREADS) {
+      S.u128(sb + SM_A5 + 8 * KiB + 16 * x) = make_uint4(0, 0, 0, 0);
       S.u128(sb + SM_TP + 16 * x) = make_uint4(0, 0, 0, 0);
       S.u128(sb + SM_TPL + 16 * x) = make_uint4(0, 0, 0, 0);
+      if constexpr (!kPrep) {
+        S.u128(sb + SM_TP + 8 * KiB + 16 * x) = make_uint4(0, 0, 0, 0);
+        S.u128(sb + SM_TPL + 8 * KiB + 16 * x) = make_uint4(0, 0, 0, 0);
+      }
     }
     __syncthreads();
     {

@@ -73,6 +73,8 @@ PROFILED_TRAFFIC = {
     "state_pass_kernel": (304.270848e6 + 288.862976e6, 4096, "d378b5f7008b1b9f",
                           ("kda_state_pass.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
                            "kda_split.cuh", "kda_common.cuh")),
+    "kda_decode_step": (1.090611e9 + 1.017646e9, 16384, "d7fab05fc3519b6c",
+                        ("kda_decode.cu", "kda_common.cuh")),
 }
 
 
@@ -394,6 +396,7 @@ def run_ours(args, rank, world, local):
     e2e = None if args.no_e2e else run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world,
                                            B, T)
     decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak, peak_src, world)
+    long_ctx = None if args.no_long else run_long(args, dev, stream, hbm_peak, peak_src, world)
 
     cpu_baseline = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -412,54 +415,108 @@ def run_ours(args, rank, world, local):
                 "scaling": "weak", "vs_baseline": None, "dtype": kda_dtype(),
                 "data": "synthetic", "config": workload_config(w),
                 "clocks": clocks.summary(), "roofline": roofline, "cpu_baseline": cpu_baseline,
-                "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "decode": decode}
+                "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "decode": decode,
+                "long_context": long_ctx}
         print(json.dumps(line), flush=True)
 
 
 def run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world, B, T):
-    """The same step through the public API with host buffers: pinned host
-    inputs -> device -> kda_chunk_fwd -> host outputs, all inside the timed
-    region."""
+    """The same step through the public API with host buffers: every step copies
+    its inputs from pinned host memory to the device, runs kda_chunk_fwd and
+    copies o, the final states and the snapshots back to pinned host memory,
+    all inside the timed region.  Steps are pipelined over two buffer slots on
+    three streams (inputs in, compute, outputs out), as a serving loop would
+    run them: step i's outputs go back while step i+1's inputs come in."""
     import torch
 
     import linear_attention_serving_chunk_gb300 as kda
     dev = o.device
-    host_in = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "z", "beta", "A",
-                                                     "cu_seqlens")}
+    names_in = ("q", "k", "v", "z", "beta", "A", "cu_seqlens")
+    host_in = {n: x[n].cpu().pin_memory() for n in names_in}
     host_out = {"o": torch.empty_like(o, device="cpu").pin_memory(),
                 "S_final": torch.empty_like(S_final, device="cpu").pin_memory(),
                 "snaps": torch.empty_like(snaps, device="cpu").pin_memory()}
-    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+    slots = [{"in": {n: torch.empty_like(t, device=dev) for n, t in host_in.items()},
+              "out": {"o": o if i == 0 else torch.empty_like(o),
+                      "S_final": S_final if i == 0 else torch.empty_like(S_final),
+                      "snaps": snaps if i == 0 else torch.empty_like(snaps)}}
+             for i in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    # Copies can be split over NCS streams per direction (big tensors in
+    # slices along their first dimension); on GB300 four streams per direction
+    # measured no faster than one (the host link is the limit, ~275 GB/s for
+    # both directions together), so one each.
+    NCS = 1
 
-    def e2e_step():
-        for n, t in host_in.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        kda.chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["z"], dev_in["beta"],
-                      dev_in["A"], cu_seqlens=dev_in["cu_seqlens"], o=o, S_final=S_final,
-                      snaps=snaps, snap_offsets=offs, workspace=ws, stream=stream)
-        host_out["o"].copy_(o, non_blocking=True)
-        host_out["S_final"].copy_(S_final, non_blocking=True)
-        host_out["snaps"].copy_(snaps, non_blocking=True)
+    def pieces(src, dst):
+        out = []
+        for n, t in src.items():
+            k = NCS if t.shape[0] >= NCS and t.numel() * t.element_size() > (64 << 20) else 1
+            step = (t.shape[0] + k - 1) // k
+            for a0 in range(0, t.shape[0], step):
+                out.append((t[a0:a0 + step], dst[n][a0:a0 + step]))
+        return out
 
-    e2e_step()
+    s_comp = torch.cuda.Stream(dev)
+    s_in = [torch.cuda.Stream(dev) for _ in range(NCS)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(NCS)]
+    ev = {"in": [[torch.cuda.Event() for _ in range(NCS)] for _ in range(2)],
+          "out": [[torch.cuda.Event() for _ in range(NCS)] for _ in range(2)],
+          "comp": [torch.cuda.Event() for _ in range(2)]}
+    copies_in = [pieces(host_in, slots[sl]["in"]) for sl in range(2)]
+    copies_out = [pieces(slots[sl]["out"], host_out) for sl in range(2)]
+    used = [False, False]
+
+    def e2e_step(i):
+        sl = i & 1
+        d = slots[sl]
+        for j, st in enumerate(s_in):
+            if used[sl]:  # this slot's previous compute has read its inputs
+                st.wait_event(ev["comp"][sl])
+            with torch.cuda.stream(st):
+                for src, dst in copies_in[sl][j::NCS]:
+                    dst.copy_(src, non_blocking=True)
+            ev["in"][sl][j].record(st)
+            s_comp.wait_event(ev["in"][sl][j])
+        if used[sl]:  # and its previous outputs have left
+            for j in range(NCS):
+                s_comp.wait_event(ev["out"][sl][j])
+        kda.chunk_fwd(d["in"]["q"], d["in"]["k"], d["in"]["v"], d["in"]["z"], d["in"]["beta"],
+                      d["in"]["A"], cu_seqlens=d["in"]["cu_seqlens"], o=d["out"]["o"],
+                      S_final=d["out"]["S_final"], snaps=d["out"]["snaps"], snap_offsets=offs,
+                      workspace=ws, stream=s_comp)
+        ev["comp"][sl].record(s_comp)
+        for j, st in enumerate(s_out):
+            st.wait_event(ev["comp"][sl])
+            with torch.cuda.stream(st):
+                for src, dst in copies_out[sl][j::NCS]:
+                    dst.copy_(src, non_blocking=True)
+            ev["out"][sl][j].record(st)
+        used[sl] = True
+
+    for i in range(2):  # warm-up: both slots once
+        e2e_step(i)
     torch.cuda.synchronize()
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(2, min(args.steps, 10))
     barrier(world)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(stream)
+    a.record(s_comp)
+    for st in s_in:
+        st.wait_event(a)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    for j in range(NCS):  # the end waits for every stream's last copy
+        s_comp.wait_event(ev["out"][(e2e_steps - 1) & 1][j])
+    b.record(s_comp)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(a.elapsed_time(b), world)
     e2e = {"value": B * T * e2e_steps * world / (e2e_ms / 1e3), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    del host_in, host_out, dev_in
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "pipelined": f"2 buffer slots; copies in and out each on {NCS} streams, compute on 1"}
+    del host_in, host_out, slots, copies_in, copies_out
     return e2e
-
 
 
 def kda_dtype():
@@ -510,8 +567,54 @@ def run_decode(args, dev, stream, hbm_peak, peak_src, world):
                         f"{n_steps} chained steps with fresh inputs",
             "gpu_launches": n_steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None,
+                         "frac": achieved / hbm_peak,
+                         "traffic": profiled_traffic("kda_decode_step", Bd * H),
                          "kernel": "kda_decode_step", "peak_source": peak_src}}
+
+
+def run_long(args, dev, stream, hbm_peak, peak_src, world):
+    """The long-context prefill: one sequence of 1,048,576 tokens, H = 16,
+    dk = dv = 128, final state and chunk snapshots (the path the library picks
+    for it: the segment-parallel scan)."""
+    import torch
+
+    import kda_inputs
+    import linear_attention_serving_chunk_gb300 as kda
+    w = kda_inputs.WORKLOADS["long"]
+    B, H, T, dk, dv = w["B"], w["H"], w["T"], w["dk"], w["dv"]
+    x = kda_inputs.make_workload_prefill("long", device=dev)
+    snaps = torch.empty((B * (T // 64), H, dk, dv), dtype=torch.float32, device=dev)
+    S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    o = torch.empty((B * T, H, dv), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(kda.workspace_bytes(B, B * T, H, dk, dv), 1), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], n_seq=B, o=o,
+                      S_final=S_final, snaps=snaps, workspace=ws, stream=stream)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = args.long_steps
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(a.elapsed_time(b), world) / n
+    nbytes = prefill_bytes(B * T * H, B * H, dk, dv)
+    del x, snaps, o, ws
+    return {"value": B * T * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": n,
+            "workload": f"kda prefill B={B} H={H} T={T} dk={dk} dv={dv} chunk=64, final state + "
+                        "chunk snapshots",
+            "path": {"what": "whole step against the algorithmic bytes of inputs and outputs",
+                     "achieved": nbytes / (ms / 1e3) / 1e9,
+                     "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, "unit": "GB/s",
+                     "peak": hbm_peak, "peak_source": peak_src}}
 
 
 def main(argv=None):
@@ -522,6 +625,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-long", action="store_true", help="skip the 1M-token prefill line")
+    ap.add_argument("--long-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=2048,
                     help="tokens per sequence in the oracle's bounded sample")

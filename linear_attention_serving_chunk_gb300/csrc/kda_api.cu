@@ -42,10 +42,11 @@ cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
                               int64_t max_tasks, uint8_t *rec, int *status, unsigned pre,
                               int n_ctas, cudaStream_t stream);
 cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
-                              const int32_t *chunk_start, int n_seq, int64_t fixed_len, int H,
-                              int h0, int hg, const float *S0, kda_bf16 *o, float *S_final,
-                              float *snaps, const int64_t *snap_offsets, int *status,
-                              const int32_t *slots, cudaStream_t stream);
+                              const int32_t *chunk_start, int n_seq, int64_t fixed_len,
+                              int64_t total_tokens, int H, int h0, int hg, const float *S0,
+                              kda_bf16 *o, float *S_final, float *snaps,
+                              const int64_t *snap_offsets, int *status, const int32_t *slots,
+                              cudaStream_t stream);
 cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int32_t *chunk_start,
                                cudaStream_t stream);
 cudaError_t segment_combine_launch(const float *M, const float *N, const float *S0,
@@ -281,8 +282,8 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
                                 total_tokens, fixed_len, H, h0, g, max_chunks * g, rec, status,
                                 pre, kSMs, st);
       if (err == cudaSuccess && run_state)
-        err = state_pass_launch(rec, cu_seqlens, chunk_start, n_seq, fixed_len, H, h0, g, S0, o,
-                                S_final, snaps, snap_offsets, status, nullptr, st);
+        err = state_pass_launch(rec, cu_seqlens, chunk_start, n_seq, fixed_len, total_tokens, H,
+                                h0, g, S0, o, S_final, snaps, snap_offsets, status, nullptr, st);
     }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }

@@ -23,6 +23,8 @@
 // The records arrive by bulk async copies two chunks ahead (two stages), so
 // the chain only waits on its own three MMAs.  Every wait is bounded; a wait
 // that gives up records KDA_ERR_TIMEOUT and the CTA stops cleanly.
+#include <string.h>
+
 #include "kda_common.cuh"
 #include "kda_sm100.cuh"
 #include "kda_split.cuh"
@@ -53,7 +55,7 @@ constexpr uint32_t ST_G = 64 * KiB;
 constexpr uint32_t ST_BYTES = 65 * KiB;
 constexpr uint32_t SM_SBF = 2 * ST_BYTES;        // [dk x NC] S in fp16, MN-major
 constexpr uint32_t SM_WBF = SM_SBF + 16 * KiB;   // [tok x NC] W in fp16, MN-major; o staging
-constexpr uint32_t SM_SNAP = SM_WBF + 8 * KiB;   // 16 x 2 KiB snapshot staging tiles
+constexpr uint32_t SM_SNAP = SM_WBF + 8 * KiB;   // snapshot staging: 2 boxes [128 rows][32 fp32], 128-byte swizzle
 constexpr uint32_t SM_MISC = SM_SNAP + 32 * KiB;
 constexpr uint32_t MS_BAR_FULL = SM_MISC;        // 2 mbarriers (records in)
 constexpr uint32_t MS_BAR_MMA = SM_MISC + 16;
@@ -90,7 +92,8 @@ struct SpParams {
 
 // One CTA per (sequence, head, half of the value columns): the columns of the
 // state never mix, so each half runs on its own with the same records.
-__global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParams p) {
+__global__ void __launch_bounds__(SP_THREADS, 1)
+state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
   const Smem S{smem, sb};
@@ -196,45 +199,27 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
     // is agreed on at the barrier before the first MMA.
     const bool rec_ok = mbar_wait_bounded(bar_full + 8u * stg, (n >> 1) & 1, kWaitPolls);
 
-    // ---- state read-out: snapshot, fp16 copy for the MMA, S *= gamma -------------------
+    // ---- state read-out: fp16 copy for the MMA, S *= gamma in place ----------------------
+    // The unscaled values stay in registers for the snapshot, which is
+    // written while the first MMA runs; the TMEM store is waited for only
+    // before the barrier ahead of S += K'^T W.
+    float sv[16];
+    tmem_ld16(t_lane + TM_S + 16 * q4, sv);
+    tmem_wait_ld();
     {
-      float v[16];
-      tmem_ld16(t_lane + TM_S + 16 * q4, v);
-      tmem_wait_ld();
-      if (snap_pending >= 0) {
-        // The state after the previous (full) chunk: each warp stages its
-        // 32 x 16 fp32 tile (16-byte pieces rotated by row) and stores it
-        // as 8 rows x 64 bytes per instruction.
-        const uint32_t tile = sb + SM_SNAP + static_cast<uint32_t>(warp) * 2048u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          S.u128(tile + lane * 64u + (static_cast<uint32_t>(j ^ (lane & 3)) << 4)) =
-              make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
-                         __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
-        __syncwarp();
-        float *base = p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
-                      static_cast<size_t>(quad * 32) * TD + cq;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 8 * i + (lane >> 2), c = lane & 3;
-          const uint4 w = S.u128(tile + r * 64u + (static_cast<uint32_t>(c ^ (r & 3)) << 4));
-          __stcs(reinterpret_cast<float4 *>(base + static_cast<size_t>(r) * TD) + c,
-                 make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                             __uint_as_float(w.w)));
-        }
-        snap_pending = -1;
-      }
-      store_row16_f16(S, sb + SM_SBF, trow, q4, v, 1.f);
+      store_row16_f16(S, sb + SM_SBF, trow, q4, sv, 1.f);
       const float gam = S.f32(st + ST_G + 4 * trow);
+      float v[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] *= gam;
+      for (int j = 0; j < 16; ++j) v[j] = sv[j] * gam;
       tmem_st16(t_lane + TM_S + 16 * q4, v);
-      tmem_wait_st();
     }
+    if (tid == kCopyThread) bulk_wait_read0();  // the last snapshot's stores have read the tile
     fence_proxy_async();
     tc_fence_before();
     if (__syncthreads_or(rec_ok ? 0 : 1)) {
       if (tid == 0) atomicOr(p.status, KDA_ERR_TIMEOUT);
+      tmem_wait_st();
       aborted = true;
       break;
     }
@@ -247,7 +232,30 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
       mma_commit(bar_mma);
     }
     mma_pending = true;
-    if (!wait_mma()) { aborted = true; break; }
+    if (snap_pending >= 0) {
+      // The state after the previous (full) chunk, while the MMA runs: staged
+      // as two [128 rows][32 fp32] boxes in the 128-byte-swizzled layout (so a
+      // warp's 16-byte writes to 32 consecutive rows hit every bank once per
+      // 8 rows) and stored by TMA after the next barrier.
+      const uint32_t box = sb + SM_SNAP + static_cast<uint32_t>(q4 >> 1) * 16384u +
+                           static_cast<uint32_t>(trow) * 128u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        S.u128(box + (static_cast<uint32_t>(((q4 & 1) * 4 + j) ^ (trow & 7)) << 4)) =
+            make_uint4(__float_as_uint(sv[4 * j]), __float_as_uint(sv[4 * j + 1]),
+                       __float_as_uint(sv[4 * j + 2]), __float_as_uint(sv[4 * j + 3]));
+      fence_proxy_async();
+    }
+    if (!wait_mma()) { tmem_wait_st(); aborted = true; break; }
+    if (snap_pending >= 0) {
+      if (tid == kCopyThread) {
+        const int y = static_cast<int>((snap_pending * H + h) * TD);
+        tma_store_2d(&tm_snap, col0, y, sb + SM_SNAP);
+        tma_store_2d(&tm_snap, col0 + 32, y, sb + SM_SNAP + 16384u);
+        bulk_commit();
+      }
+      snap_pending = -1;
+    }
 
     // ---- W = U - Wk S -> fp16 ----------------------------------------------------------------
     if (quad < 2) {
@@ -257,6 +265,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
       add_row16_f16(S, st + ST_U, trow, q4, v);
       store_row16_f16(S, sb + SM_WBF, trow, q4, v, 1.f);
     }
+    tmem_wait_st();  // the gamma-scaled state is in TMEM before S += K'^T W
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -328,6 +337,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
     }
   }
 
+  if (tid == kCopyThread) bulk_wait0();  // snapshot stores complete before the CTA ends
   // Drain anything still in flight (bounded) before TMEM and shared memory go.
   if (aborted && tid == 0) {
     if (mma_pending) mbar_wait_bounded(bar_mma, mma_phase, kWaitPolls);
@@ -347,11 +357,44 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(const SpParam
 
 }  // namespace
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
 cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
-                              const int32_t *chunk_start, int n_seq, int64_t fixed_len, int H,
-                              int h0, int hg, const float *S0, kda_bf16 *o, float *S_final,
-                              float *snaps, const int64_t *snap_offsets, int *status,
-                              const int32_t *slots, cudaStream_t stream) {
+                              const int32_t *chunk_start, int n_seq, int64_t fixed_len,
+                              int64_t total_tokens, int H, int h0, int hg, const float *S0,
+                              kda_bf16 *o, float *S_final, float *snaps,
+                              const int64_t *snap_offsets, int *status, const int32_t *slots,
+                              cudaStream_t stream) {
+  // Snapshots as a 2-D fp32 array [rows * H * dk][dv]; rows <= total_tokens / 64
+  // (each snapshot follows a full chunk), which bounds the map's extent.
+  CUtensorMap tm_snap;
+  memset(&tm_snap, 0, sizeof(tm_snap));
+  if (snaps) {
+    static EncodeTiledFn encode = nullptr;
+    if (!encode) {
+      void *ptr = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess)
+        return cudaErrorInvalidValue;
+      encode = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    const uint64_t rows = static_cast<uint64_t>(total_tokens / 64) * H * TD;
+    // TMA row coordinates are 32-bit signed
+    if (rows == 0 || rows > 0x7fffffffull) return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(TD), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(TD) * 4};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tm_snap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, snaps, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   const uint32_t smem = SP_SMEM_BYTES;
   cudaError_t err = cudaFuncSetAttribute(state_pass_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -360,7 +403,7 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
   SpParams prm{rec, cu_seqlens, chunk_start, fixed_len, H, h0, hg, S0, o, S_final, snaps,
                snap_offsets, status, slots};
   const dim3 grid(static_cast<unsigned>(2 * hg), static_cast<unsigned>(n_seq));
-  state_pass_kernel<<<grid, SP_THREADS, smem, stream>>>(prm);
+  state_pass_kernel<<<grid, SP_THREADS, smem, stream>>>(tm_snap, prm);
   return cudaGetLastError();
 }
 

@@ -68,11 +68,11 @@ constexpr uint32_t SM_VB = 112 * KiB;             // 16 KiB: v             [tok 
 constexpr uint32_t SM_AP = 128 * KiB;             // 96 KiB work region
 constexpr uint32_t SM_APA = SM_AP;                // tf32 [Khat_2p ; Khat_2p+1]   128 x 128
 constexpr uint32_t SM_APB = SM_AP + 64 * KiB;     // tf32 [KE_2p; QE_2p; KE_2p+1; QE_2p+1] 64 x 128
-constexpr uint32_t SM_AKK = SM_AP;                // fp32 [64][65] A_kk (after the AP MMAs)
-constexpr uint32_t SM_TF = SM_AP + 64 * 65 * 4;   // fp32 [64][65] T
+constexpr uint32_t SM_AKK = SM_AP;                // fp32 [64][68] A_kk transposed: [i][r] (after the AP MMAs)
+constexpr uint32_t SM_TF = SM_AP + 64 * 68 * 4;   // fp32 [64][65] T
 constexpr uint32_t SM_TY = SM_AP + 34 * KiB;      // fp32 [4][16][17] block products
 constexpr uint32_t SM_SBF = SM_AP;                // [dk x dv] S in fp16, MN-major (after T')
-constexpr uint32_t SM_A5 = SM_AP + 48 * KiB;      // [128 x 64] K-major: [0 ; -P]
+constexpr uint32_t SM_A5 = SM_AP + 48 * KiB;      // [128 x 64] MN-major: [X ; -P] (X unused)
 constexpr uint32_t SM_TP = SM_AP + 64 * KiB;      // [128 x 64] K-major: [T diag(beta) ; 0], bf16 hi
 constexpr uint32_t SM_TPL = SM_AP + 80 * KiB;     // the same, bf16 lo (T' - hi)
 constexpr uint32_t SM_WBF = SM_AP + 64 * KiB;     // [tok x dv] W in fp16 (after T' is used)
@@ -192,16 +192,18 @@ __device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], const uint32_t (
 }
 
 // One warp: C[16x16] (two 16x8 fragments) += X[16x16] Y[16x16] with X and Y
-// fp32 in shared memory (row strides ldx, ldy floats).
+// fp32 in shared memory (row strides ldx, ldy floats); with XT, X is given
+// transposed (X[g][k] at X[k * ldx + g]).
+template <bool XT = false>
 __device__ __forceinline__ void warp_mma16(const float *X, int ldx, const float *Y, int ldy,
                                            float (&c)[2][4], int lane) {
   const int g = lane >> 2, t = lane & 3;
+  auto xa = [&](int row, int col) { return XT ? X[col * ldx + row] : X[row * ldx + col]; };
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     const int k0 = 8 * ks;
-    const uint32_t a[4] = {tf32_rna(X[g * ldx + k0 + t]), tf32_rna(X[(g + 8) * ldx + k0 + t]),
-                           tf32_rna(X[g * ldx + k0 + t + 4]),
-                           tf32_rna(X[(g + 8) * ldx + k0 + t + 4])};
+    const uint32_t a[4] = {tf32_rna(xa(g, k0 + t)), tf32_rna(xa(g + 8, k0 + t)),
+                           tf32_rna(xa(g, k0 + t + 4)), tf32_rna(xa(g + 8, k0 + t + 4))};
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
       mma_m16n8k8_tf32(c[nt], a, tf32_rna(Y[(k0 + t) * ldy + 8 * nt + g]),
@@ -720,15 +722,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const int i = trow & 63;
       const int Rb = 2 * pair + (quad >= 2 ? 1 : 0);  // sub-tile of the rows r
       if (i < 16 * Rb + 16) {
+        if (sub == 0) {
+          // A_kk[r][i] = beta_r D[i][r] into row i of the transposed tile (the
+          // entries with i >= r are never read)
+          const uint32_t row = sb + SM_AKK + 4u * static_cast<uint32_t>(i * 68 + 16 * Rb);
 #pragma unroll
-        for (int nn = 0; nn < 16; ++nn) {
-          const int r = 16 * Rb + nn;
-          if (sub == 0) {
-            if (i < r) S.f32(sb + SM_AKK + 4 * (r * 65 + i)) = S.f32(sb + MS_BETA + 4 * r) * v[nn];
-          } else if (i <= r) {
-            __half hv = __float2half_rn(-v[nn]);  // -P[r][i] in fp16
-            S.u16(sb + SM_A5 + sw128_off(64 + r, i, REG128)) = *reinterpret_cast<unsigned short *>(&hv);
+          for (int j = 0; j < 4; ++j) {
+            const float4 b = *reinterpret_cast<const float4 *>(
+                S.ptr(sb + MS_BETA + 4 * (16 * Rb + 4 * j)));
+            S.u128(row + 16 * j) = make_uint4(
+                __float_as_uint(b.x * v[4 * j]), __float_as_uint(b.y * v[4 * j + 1]),
+                __float_as_uint(b.z * v[4 * j + 2]), __float_as_uint(b.w * v[4 * j + 3]));
           }
+        } else {
+          // -P[r][i] (zero above the diagonal) into K-row i of the MN-major
+          // [X ; -P] tile: the r's of -P are the second 64-element MN block
+          float pv[16];
+#pragma unroll
+          for (int nn = 0; nn < 16; ++nn) pv[nn] = (i <= 16 * Rb + nn) ? -v[nn] : 0.f;
+          const uint32_t row = sb + SM_A5 + REG64 + static_cast<uint32_t>(i) * 128u;
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            S.u128(row + (static_cast<uint32_t>((2 * Rb + c) ^ (i & 7)) << 4)) =
+                make_uint4(pack_f16x2(pv[8 * c], pv[8 * c + 1]),
+                           pack_f16x2(pv[8 * c + 2], pv[8 * c + 3]),
+                           pack_f16x2(pv[8 * c + 4], pv[8 * c + 5]),
+                           pack_f16x2(pv[8 * c + 6], pv[8 * c + 7]));
         }
       }
     }
@@ -746,7 +765,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int m = 0; m < 15; ++m) {
 #pragma unroll
         for (int r = m + 1; r < 16; ++r)
-          x[r] -= S.f32(sb + SM_AKK + 4 * ((o + r) * 65 + o + m)) * x[m];
+          x[r] -= S.f32(sb + SM_AKK + 4 * ((o + m) * 68 + o + r)) * x[m];
       }
       const float bj = S.f32(sb + MS_BETA + 4 * (o + jc));
 #pragma unroll
@@ -806,7 +825,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int R = 2 * warp + 1, J = R - 1;
         float *y = xs + warp * 16 * 17;
         float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mma16(akk + (16 * R) * 65 + 16 * J, 65, tf + (16 * J) * 65 + 16 * J, 65, c, lane);
+        warp_mma16<true>(akk + (16 * J) * 68 + 16 * R, 68, tf + (16 * J) * 65 + 16 * J, 65, c,
+                         lane);
         put16(y, 17, c, 1.f);
         __syncwarp();
         float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -818,7 +838,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int R = 2 + (warp >> 1), J = warp & 1;
         float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         for (int M = J; M < 2; ++M)
-          warp_mma16(akk + (16 * R) * 65 + 16 * M, 65, tf + (16 * M) * 65 + 16 * J, 65, c, lane);
+          warp_mma16<true>(akk + (16 * M) * 68 + 16 * R, 68, tf + (16 * M) * 65 + 16 * J, 65, c,
+                           lane);
         put16(xs + warp * 16 * 17, 17, c, 1.f);
       }
       __syncthreads();
@@ -970,7 +991,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
       tc_fence_after();
       issue_mma(tmem + TM_S, zb, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
-      issue_mma(tmem + TM_D1, sb + SM_A5, false, REG128, sb + SM_WBF, true, REG64, 4, ID_KMN, 1);
+      issue_mma(tmem + TM_D1, sb + SM_A5, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
       mma_commit(bar_mma);
     }
     mma_pending = true;

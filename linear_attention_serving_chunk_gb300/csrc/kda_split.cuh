@@ -9,7 +9,8 @@
 //   A3   [-Wk ; -Q~]   128 rows x 128 K, fp16, K-major (two 64-column regions)
 //   KP   K' = K e^{G_last - G}  [64 tok x 128 dk], fp16, MN-major
 //   U    U = T diag(beta) V     [64 tok x 128 dv], fp16, MN-major
-//   P    rows 64..127 of [0 ; -P] (128 x 64, K-major): -P, fp16
+//   P    -P (64 r x 64 i, zero for i > r), fp16, MN-major: K-row i holds the
+//        64 r's, i.e. the second MN block of the 128 x 64 operand [X ; -P]
 //   G    gamma = e^{G_last}, 128 fp32 (one per key channel)
 //
 // Rows of a ragged last chunk beyond its length are zero in every tile.

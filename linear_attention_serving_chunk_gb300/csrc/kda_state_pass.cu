@@ -42,10 +42,10 @@ constexpr int TD = 128;
 constexpr int NC = 64;  // value columns of the state per CTA (two CTAs per chain)
 
 // One stage holds one record, with only this CTA's half of U:
-// A3 | KP | U half | P | gamma.  The M5 operand [X ; -P] (128 x 64, K-major)
-// starts 8 KiB before P, so its rows 0..63 X are the U half: they only feed
-// D1 rows 0..63, which nothing reads after M5 (the next chunk's first MMA
-// overwrites them).
+// A3 | KP | U half | P | gamma.  The M5 operand [X ; -P] (128 x 64, MN-major:
+// two 64-row blocks 8 KiB apart) starts 8 KiB before P, so its first block X
+// is the U half: it only feeds D1 rows 0..63, which nothing reads after M5
+// (the next chunk's first MMA overwrites them).
 constexpr uint32_t ST_A3 = 0;
 constexpr uint32_t ST_KP = 32 * KiB;
 constexpr uint32_t ST_U = 48 * KiB;
@@ -274,7 +274,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     if (tid == 0) {
       tc_fence_after();
       issue_mma(tmem + TM_S, st + ST_KP, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
-      issue_mma(tmem + TM_D1, st + ST_A5, false, REG128, sb + SM_WBF, true, REG64, 4, ID_KMN, 1);
+      issue_mma(tmem + TM_D1, st + ST_A5, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
       mma_commit(bar_mma);
     }
     mma_pending = true;

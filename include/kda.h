@@ -100,8 +100,11 @@ int kda_version(void);
  *    <= 38) and whose sequences are long run as a segment-parallel scan (each
  *    segment's zero-start state N and transition M, an fp32 chain
  *    S_start[g+1] = M_g S_start[g] + N_g, then a pass from the true segment
- *    starts): three [n_seq * n_segs, H, 128, 128] fp32 arrays.  This path
- *    REQUIRES its workspace (KDA_ERR_WORKSPACE otherwise).
+ *    starts).  The scan needs three [n_seq * n_segs, H, 128, 128] fp32 arrays
+ *    and REQUIRES them (KDA_ERR_WORKSPACE otherwise); the value returned adds
+ *    the two-pass records of every (chunk, head) (73 KiB each), with which
+ *    the scan runs on the two-pass kernels (chunk preparation once, three
+ *    state passes); with the arrays alone it runs on the single-pass kernel.
  *  - Other dk = dv = 128 calls run in two passes when the workspace allows:
  *    a parallel pass prepares every (chunk, head)'s state-independent part
  *    (73 KiB records), then one pass per (sequence, head) carries the state.

@@ -46,7 +46,7 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               int64_t total_tokens, int H, int h0, int hg, const float *S0,
                               kda_bf16 *o, float *S_final, float *snaps,
                               const int64_t *snap_offsets, int *status, const int32_t *slots,
-                              cudaStream_t stream);
+                              int zero_u, int s0_identity, cudaStream_t stream);
 cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int32_t *chunk_start,
                                cudaStream_t stream);
 cudaError_t segment_combine_launch(const float *M, const float *N, const float *S0,
@@ -88,6 +88,12 @@ bool plan_scan(int n_seq, int64_t total_tokens, int H, int dk, int dv, ScanPlan 
 size_t scan_workspace_bytes(int n_seq, int H, const ScanPlan &plan) {
   // M, N and the segment start states: three [n_seq * n_segs, H, 128, 128] fp32 arrays
   return 3 * static_cast<size_t>(n_seq) * plan.n_segs * H * 128 * 128 * sizeof(float);
+}
+
+// The scan on the two-pass kernels: the three arrays, then one record per
+// (chunk, head) of the whole batch.
+size_t scan_records_bytes(int n_seq, int64_t total_tokens, int H) {
+  return static_cast<size_t>((total_tokens / n_seq + 63) / 64) * n_seq * H * (73 * 1024);
 }
 
 // Two-pass prefill (dk = dv = 128): a chunk-preparation pass over every
@@ -174,7 +180,8 @@ size_t kda_chunk_fwd_workspace_bytes(int n_seq, int64_t total_tokens, int H, int
                                      int chunk) {
   if (chunk != kChunk || H <= 0 || n_seq <= 0 || total_tokens <= 0) return 0;
   ScanPlan plan;
-  if (plan_scan(n_seq, total_tokens, H, dk, dv, &plan)) return scan_workspace_bytes(n_seq, H, plan);
+  if (plan_scan(n_seq, total_tokens, H, dk, dv, &plan))
+    return scan_workspace_bytes(n_seq, H, plan) + scan_records_bytes(n_seq, total_tokens, H);
   if (!prefill_tc_supported(dk, dv, total_tokens)) return 0;
   return split_workspace_bytes(n_seq, total_tokens, H);
 }
@@ -238,6 +245,30 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
     const int n2 = n_seq * plan.n_segs;
     const size_t arr = static_cast<size_t>(n2) * H * 128 * 128;
     float *Mb = static_cast<float *>(workspace), *Nb = Mb + arr, *Ss = Nb + arr;
+    if (workspace_bytes >= need + scan_records_bytes(n_seq, total_tokens, H)) {
+      // On the two-pass kernels: every chunk's record once, then the state
+      // pass over the segments three times (N from zero, M from the identity
+      // with v = 0, the outputs from the true segment starts).  The records
+      // are laid out by global chunk, which is also what the segment view
+      // (n2 sequences of seg_len tokens) addresses.
+      uint8_t *rec = static_cast<uint8_t *>(workspace) + need;
+      const int64_t cps = (fixed_len + 63) / 64;
+      cudaError_t err = chunk_prep_launch(q, k, v, z, beta, A, gmin, nullptr, nullptr, n_seq,
+                                          total_tokens, fixed_len, H, 0, H, n_seq * cps * H, rec,
+                                          status, pre, kSMs, st);
+      if (err == cudaSuccess)
+        err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, 0, H,
+                                nullptr, nullptr, Nb, nullptr, nullptr, status, nullptr, 0, 0, st);
+      if (err == cudaSuccess)
+        err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, 0, H,
+                                nullptr, nullptr, Mb, nullptr, nullptr, status, nullptr, 1, 1, st);
+      if (err == cudaSuccess)
+        err = segment_combine_launch(Mb, Nb, S0, Ss, S_final, n_seq, plan.n_segs, H, st);
+      if (err == cudaSuccess)
+        err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, 0, H, Ss,
+                                o, nullptr, snaps, nullptr, status, nullptr, 0, 0, st);
+      return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
     // 1. every segment from a zero state (N) and its transition from S0 = I with v = 0 (M)
     cudaError_t err = prefill_tc_launch(q, k, v, z, beta, A, gmin, nullptr, n2, total_tokens,
                                         plan.seg_len, H, nullptr, nullptr, Nb, nullptr, nullptr,
@@ -283,7 +314,8 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
                                 pre, kSMs, st);
       if (err == cudaSuccess && run_state)
         err = state_pass_launch(rec, cu_seqlens, chunk_start, n_seq, fixed_len, total_tokens, H,
-                                h0, g, S0, o, S_final, snaps, snap_offsets, status, nullptr, st);
+                                h0, g, S0, o, S_final, snaps, snap_offsets, status, nullptr, 0, 0,
+                                st);
     }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }

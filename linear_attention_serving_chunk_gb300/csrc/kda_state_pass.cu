@@ -88,6 +88,8 @@ struct SpParams {
   const int64_t *snap_offsets;
   int *status;
   const int32_t *slots;
+  int zero_u;       // 1: v taken as zero (W = -Wk S; U is not loaded)
+  int s0_identity;  // 1: every chain starts from S0 = I (dk = dv)
 };
 
 // One CTA per (sequence, head, half of the value columns): the columns of the
@@ -149,7 +151,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     float v[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      v[j] = p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + cq + j] : 0.f;
+      v[j] = p.s0_identity ? (trow == cq + j ? 1.f : 0.f)
+             : p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + cq + j] : 0.f;
     tmem_st16(t_lane + TM_S + 16 * q4, v);
     tmem_wait_st();
   }
@@ -159,10 +162,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     const uint8_t *rec =
         p.rec + (static_cast<size_t>(chunk0 + n) * p.hg + hh) * static_cast<size_t>(kRecBytes);
     const uint32_t bar = bar_full + 8u * static_cast<uint32_t>(n & 1);
-    mbar_expect_tx(bar, kRecInBytes);
+    mbar_expect_tx(bar, p.zero_u ? kRecInBytes - 8 * KiB : kRecInBytes);
     bulk_g2s(st + ST_A3, rec + kRecA3, 32 * KiB, bar);
     bulk_g2s(st + ST_KP, rec + kRecKP, 16 * KiB, bar);
-    bulk_g2s(st + ST_U, rec + kRecU + half * 8 * KiB, 8 * KiB, bar);
+    if (!p.zero_u) bulk_g2s(st + ST_U, rec + kRecU + half * 8 * KiB, 8 * KiB, bar);
     bulk_g2s(st + ST_P, rec + kRecP, 8 * KiB, bar);
     bulk_g2s(st + ST_G, rec + kRecG, 512, bar);
   };
@@ -262,7 +265,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
       float v[16];
       tmem_ld16(t_lane + TM_D1 + 16 * q4, v);
       tmem_wait_ld();
-      add_row16_f16(S, st + ST_U, trow, q4, v);
+      if (!p.zero_u) add_row16_f16(S, st + ST_U, trow, q4, v);
       store_row16_f16(S, sb + SM_WBF, trow, q4, v, 1.f);
     }
     tmem_wait_st();  // the gamma-scaled state is in TMEM before S += K'^T W
@@ -304,7 +307,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
       for (int i = 0; i < 2; ++i) {
         const int rl = 16 * i + (lane >> 1), c = lane & 1;  // row in the warp's 32, 16-byte piece
         const int r = (quad - 2) * 32 + rl;
-        if (r < L) {
+        if (r < L && p.o) {
           const uint4 w = S.u128(tile + rl * 32u + (static_cast<uint32_t>(c ^ (rl & 1)) << 4));
           reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + cq)[c] = w;
         }
@@ -367,7 +370,7 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               int64_t total_tokens, int H, int h0, int hg, const float *S0,
                               kda_bf16 *o, float *S_final, float *snaps,
                               const int64_t *snap_offsets, int *status, const int32_t *slots,
-                              cudaStream_t stream) {
+                              int zero_u, int s0_identity, cudaStream_t stream) {
   // Snapshots as a 2-D fp32 array [rows * H * dk][dv]; rows <= total_tokens / 64
   // (each snapshot follows a full chunk), which bounds the map's extent.
   CUtensorMap tm_snap;
@@ -400,8 +403,9 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  SpParams prm{rec, cu_seqlens, chunk_start, fixed_len, H, h0, hg, S0, o, S_final, snaps,
-               snap_offsets, status, slots};
+  SpParams prm{rec,   cu_seqlens,   chunk_start, fixed_len, H,      h0,     hg,
+               S0,    o,            S_final,     snaps,     snap_offsets, status, slots,
+               zero_u, s0_identity};
   const dim3 grid(static_cast<unsigned>(2 * hg), static_cast<unsigned>(n_seq));
   state_pass_kernel<<<grid, SP_THREADS, smem, stream>>>(tm_snap, prm);
   return cudaGetLastError();

@@ -67,10 +67,10 @@ def state_bytes(token_heads, chunk_heads, full_chunk_heads, seq_heads, dk, dv):
 # recorded with the capture (else the kernel has changed since: null).
 _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
 PROFILED_TRAFFIC = {
-    "prefill_tc_kernel<prep>": (269.1712e6 + 252.712704e6, 4096, "1d5693bc3dc287eb",
+    "prefill_tc_kernel<prep>": (269.040384e6 + 252.304896e6, 4096, "ab08995c28e76432",
                                 ("kda_prefill_tc.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
                                  "kda_split.cuh", "kda_common.cuh")),
-    "state_pass_kernel": (304.270848e6 + 288.862976e6, 4096, "d378b5f7008b1b9f",
+    "state_pass_kernel": (304.222464e6 + 289.514240e6, 4096, "cf3b40ff4101b4cd",
                           ("kda_state_pass.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
                            "kda_split.cuh", "kda_common.cuh")),
     "kda_decode_step": (1.090611e9 + 1.017646e9, 16384, "d7fab05fc3519b6c",

@@ -696,13 +696,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (mma_pending) { aborted = true; break; }
     }
 
-    // Zero what the read-out and the T blocks do not write: the upper
-    // triangle of -P (rows 64..127 of A5) and of T' hi / lo.  Rows 0..63 of
-    // A5 only feed D1 rows that are never read after M5, and rows 64..127 of
-    // T' only the D1 / Wk rows 64..127, which the chunk preparation never
-    // reads; the single pass needs them zero (U's rows 64..127 start -O).
+    // Zero what the T blocks do not write: the upper triangle of T' hi / lo
+    // (rows 64..127 of T' only feed the D1 / Wk rows 64..127, which the chunk
+    // preparation never reads; the single pass needs them zero, as U's rows
+    // 64..127 start -O).  The read-out below writes all of -P itself, zeros
+    // included, and the first block X of [X ; -P] only feeds D1 rows that
+    // are never read after M5; so no barrier is needed before it.
     for (int x = tid; x < 512; x += TC_THREADS) {
-      S.u128(sb + SM_A5 + 8 * KiB + 16 * x) = make_uint4(0, 0, 0, 0);
       S.u128(sb + SM_TP + 16 * x) = make_uint4(0, 0, 0, 0);
       S.u128(sb + SM_TPL + 16 * x) = make_uint4(0, 0, 0, 0);
       if constexpr (!kPrep) {
@@ -710,7 +710,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         S.u128(sb + SM_TPL + 8 * KiB + 16 * x) = make_uint4(0, 0, 0, 0);
       }
     }
-    __syncthreads();
     {
       // Pair q4 >> 1 of the products: lanes < 64 (rows i of Khat_2pair) hold
       // columns [0, 32), lanes >= 64 (Khat_2pair+1) columns [32, 64); the
@@ -721,8 +720,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tmem_wait_ld();
       const int i = trow & 63;
       const int Rb = 2 * pair + (quad >= 2 ? 1 : 0);  // sub-tile of the rows r
-      if (i < 16 * Rb + 16) {
-        if (sub == 0) {
+      if (sub == 0 && i < 16 * Rb + 16) {
+        {
           // A_kk[r][i] = beta_r D[i][r] into row i of the transposed tile (the
           // entries with i >= r are never read)
           const uint32_t row = sb + SM_AKK + 4u * static_cast<uint32_t>(i * 68 + 16 * Rb);
@@ -734,9 +733,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 __float_as_uint(b.x * v[4 * j]), __float_as_uint(b.y * v[4 * j + 1]),
                 __float_as_uint(b.z * v[4 * j + 2]), __float_as_uint(b.w * v[4 * j + 3]));
           }
-        } else {
+        }
+      } else if (sub == 1) {
+        {
           // -P[r][i] (zero above the diagonal) into K-row i of the MN-major
-          // [X ; -P] tile: the r's of -P are the second 64-element MN block
+          // [X ; -P] tile: the r's of -P are the second 64-element MN block;
+          // every (i, 16 r's) is written by exactly one thread
           float pv[16];
 #pragma unroll
           for (int nn = 0; nn < 16; ++nn) pv[nn] = (i <= 16 * Rb + nn) ? -v[nn] : 0.f;

@@ -469,3 +469,43 @@ def test_split_phase_calls_match_one_call(kda):
     assert o_err(f64(outs[1][0]), ref["o"]) <= O_TOL
     assert s_err(f64(outs[1][1]), ref["S_final"]) <= S_TOL
     assert s_err(f64(outs[1][2]), ref["snaps"]) <= S_TOL
+
+
+def test_single_pass_kernel_ragged_batch(kda):
+    """With a workspace too small for any records the prefill runs the
+    single-pass tensor-core kernel: ragged varlen batch with S0, every output,
+    final state and snapshot against the oracle."""
+    lengths = [0, 1, 63, 64, 65, 127, 128, 200, 331]
+    x = kda_inputs.make_prefill(3, 128, 128, lengths, seed=52, device="cuda", S0_std=0.02)
+    total = x["k"].shape[0]
+    n = len(lengths)
+    offs = kda.snapshot_offsets(lengths)
+    S_final = torch.full((n, 3, 128, 128), float("nan"), device="cuda")
+    snaps = torch.full((int(offs[-1]), 3, 128, 128), float("nan"), device="cuda")
+    o = torch.full((total, 3, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tiny = torch.empty(16, dtype=torch.uint8, device="cuda")
+    kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], cu_seqlens=x["cu_seqlens"],
+                  S0=x["S0"], o=o, S_final=S_final, snaps=snaps, snap_offsets=offs,
+                  workspace=tiny)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    ref = oracle_subset(x, list(range(n)), [0, 1, 2])
+    assert np.all(np.isfinite(f64(o)))
+    assert o_err(f64(o), ref["o"]) <= O_TOL
+    assert s_err(f64(S_final), ref["S_final"]) <= S_TOL
+    assert s_err(f64(snaps), ref["snaps"]) <= S_TOL
+    assert torch.equal(S_final[0], x["S0"][0])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_all_empty_batch(kda, d):
+    """A batch of empty sequences: nothing to write in o, every final state is
+    its initial state."""
+    x = kda_inputs.make_prefill(2, d, d, [0, 0, 0], seed=53, device="cuda", S0_std=0.02)
+    S_final = torch.full((3, 2, d, d), float("nan"), device="cuda")
+    o = kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                      cu_seqlens=x["cu_seqlens"], S0=x["S0"], S_final=S_final)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    assert o.shape[0] == 0
+    assert torch.equal(S_final, x["S0"])

@@ -360,11 +360,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
 
 }  // namespace
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               const int32_t *chunk_start, int n_seq, int64_t fixed_len,
                               int64_t total_tokens, int H, int h0, int hg, const float *S0,
@@ -376,16 +371,8 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
   CUtensorMap tm_snap;
   memset(&tm_snap, 0, sizeof(tm_snap));
   if (snaps) {
-    static EncodeTiledFn encode = nullptr;
-    if (!encode) {
-      void *ptr = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) !=
-              cudaSuccess ||
-          q != cudaDriverEntryPointSuccess)
-        return cudaErrorInvalidValue;
-      encode = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
+    const EncodeTiledFn encode = tensor_map_encoder();
+    if (!encode) return cudaErrorInvalidValue;
     const uint64_t rows = static_cast<uint64_t>(total_tokens / 64) * H * TD;
     // TMA row coordinates are 32-bit signed
     if (rows == 0 || rows > 0x7fffffffull) return cudaErrorInvalidValue;

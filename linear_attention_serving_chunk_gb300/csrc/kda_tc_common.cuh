@@ -6,6 +6,8 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "kda_sm100.cuh"
@@ -150,6 +152,26 @@ __device__ __forceinline__ void issue_mma(uint32_t d_tmem, uint32_t a_base, bool
     else
       mma_f16(d_tmem, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
   }
+}
+
+// Host: the driver's cuTensorMapEncodeTiled, looked up once per process
+// (nullptr if the driver does not provide it).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn tensor_map_encoder() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return nullptr;
+  }();
+  return fn;
 }
 
 }  // namespace tcx

@@ -509,3 +509,29 @@ def test_all_empty_batch(kda, d):
     assert kda.device_status() == 0
     assert o.shape[0] == 0
     assert torch.equal(S_final, x["S0"])
+
+
+@pytest.mark.parametrize("heads_per_group", [1, 3])
+def test_two_pass_in_head_groups(kda, heads_per_group):
+    """A workspace holding the records of only some heads makes the two-pass
+    prefill run the heads in groups (here 4 heads as 4 x 1 or 3 + 1): same
+    results as the oracle, ragged varlen batch with S0 and snapshots."""
+    H = 4
+    lengths = [300, 130, 64, 1]
+    x = kda_inputs.make_prefill(H, 128, 128, lengths, seed=54, device="cuda", S0_std=0.02)
+    n, total = len(lengths), x["k"].shape[0]
+    table = ((n + 1) * 4 + 1023) // 1024 * 1024
+    per_head = ((total + 63) // 64 + n) * 73 * 1024
+    assert kda.workspace_bytes(n, total, H, 128, 128) == table + H * per_head
+    ws = torch.empty(table + heads_per_group * per_head, dtype=torch.uint8, device="cuda")
+    offs = kda.snapshot_offsets(lengths)
+    S_final = torch.full((n, H, 128, 128), float("nan"), device="cuda")
+    snaps = torch.full((int(offs[-1]), H, 128, 128), float("nan"), device="cuda")
+    o = kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], cu_seqlens=x["cu_seqlens"],
+                      S0=x["S0"], S_final=S_final, snaps=snaps, snap_offsets=offs, workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    ref = oracle_subset(x, list(range(n)), list(range(H)))
+    assert o_err(f64(o), ref["o"]) <= O_TOL
+    assert s_err(f64(S_final), ref["S_final"]) <= S_TOL
+    assert s_err(f64(snaps), ref["snaps"]) <= S_TOL

@@ -67,10 +67,10 @@ def state_bytes(token_heads, chunk_heads, full_chunk_heads, seq_heads, dk, dv):
 # recorded with the capture (else the kernel has changed since: null).
 _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
 PROFILED_TRAFFIC = {
-    "prefill_tc_kernel<prep>": (269.040384e6 + 252.304896e6, 4096, "ab08995c28e76432",
+    "prefill_tc_kernel<prep>": (269.080576e6 + 252.442880e6, 4096, "5587e425d951719d",
                                 ("kda_prefill_tc.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
                                  "kda_split.cuh", "kda_common.cuh")),
-    "state_pass_kernel": (304.222464e6 + 289.514240e6, 4096, "cf3b40ff4101b4cd",
+    "state_pass_kernel": (304.283904e6 + 289.827584e6, 4096, "15549457af2fe8fb",
                           ("kda_state_pass.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
                            "kda_split.cuh", "kda_common.cuh")),
     "kda_decode_step": (1.090611e9 + 1.017646e9, 16384, "d7fab05fc3519b6c",
@@ -422,11 +422,13 @@ def run_ours(args, rank, world, local):
 
 def run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world, B, T):
     """The same step through the public API with host buffers: every step copies
-    its inputs from pinned host memory to the device, runs kda_chunk_fwd and
-    copies o, the final states and the snapshots back to pinned host memory,
-    all inside the timed region.  Steps are pipelined over two buffer slots on
-    three streams (inputs in, compute, outputs out), as a serving loop would
-    run them: step i's outputs go back while step i+1's inputs come in."""
+    its inputs from pinned host memory to the device, runs kda_chunk_fwd
+    (snapshots included) and copies its result, o and the final states, back
+    to pinned host memory, all inside the timed region.  The chunk snapshots
+    stay in device memory: they are the prefix cache, which kda_state_snapshot
+    restores from there.  Steps are pipelined over two buffer slots on three
+    streams (inputs in, compute, outputs out), as a serving loop would run
+    them: step i's outputs go back while step i+1's inputs come in."""
     import torch
 
     import linear_attention_serving_chunk_gb300 as kda
@@ -434,8 +436,7 @@ def run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world, B, T):
     names_in = ("q", "k", "v", "z", "beta", "A", "cu_seqlens")
     host_in = {n: x[n].cpu().pin_memory() for n in names_in}
     host_out = {"o": torch.empty_like(o, device="cpu").pin_memory(),
-                "S_final": torch.empty_like(S_final, device="cpu").pin_memory(),
-                "snaps": torch.empty_like(snaps, device="cpu").pin_memory()}
+                "S_final": torch.empty_like(S_final, device="cpu").pin_memory()}
     slots = [{"in": {n: torch.empty_like(t, device=dev) for n, t in host_in.items()},
               "out": {"o": o if i == 0 else torch.empty_like(o),
                       "S_final": S_final if i == 0 else torch.empty_like(S_final),
@@ -465,7 +466,7 @@ def run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world, B, T):
           "out": [[torch.cuda.Event() for _ in range(NCS)] for _ in range(2)],
           "comp": [torch.cuda.Event() for _ in range(2)]}
     copies_in = [pieces(host_in, slots[sl]["in"]) for sl in range(2)]
-    copies_out = [pieces(slots[sl]["out"], host_out) for sl in range(2)]
+    copies_out = [pieces({n: slots[sl]["out"][n] for n in host_out}, host_out) for sl in range(2)]
     used = [False, False]
 
     def e2e_step(i):
@@ -514,6 +515,8 @@ def run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world, B, T):
     e2e_ms = reduce_max(a.elapsed_time(b), world)
     e2e = {"value": B * T * e2e_steps * world / (e2e_ms / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "d2h": "o and final states; the chunk snapshots are computed every step and stay in "
+                  "device memory (the prefix cache)",
            "pipelined": f"2 buffer slots; copies in and out each on {NCS} streams, compute on 1"}
     del host_in, host_out, slots, copies_in, copies_out
     return e2e

@@ -73,8 +73,14 @@ constexpr uint32_t SM_TF = SM_AP + 64 * 68 * 4;   // fp32 [64][65] T
 constexpr uint32_t SM_TY = SM_AP + 34 * KiB;      // fp32 [4][16][17] block products
 constexpr uint32_t SM_SBF = SM_AP;                // [dk x dv] S in fp16, MN-major (after T')
 constexpr uint32_t SM_A5 = SM_AP + 48 * KiB;      // [128 x 64] MN-major: [X ; -P] (X unused)
-constexpr uint32_t SM_TP = SM_AP + 64 * KiB;      // [128 x 64] K-major: [T diag(beta) ; 0], bf16 hi
-constexpr uint32_t SM_TPL = SM_AP + 80 * KiB;     // the same, bf16 lo (T' - hi)
+// T' = T diag(beta) as bf16 hi + lo, two [128 x 64] K-major tiles.  The
+// single pass: TP = [hi ; 0], TPL = [lo ; 0] (rows 64..127 of D1 carry -O).
+// Chunk preparation stacks the halves in M instead: TP = [hi ; lo] and
+// TPL = [lo ; hi], so one MMA gives both halves of T'K~ (and of T'V) and the
+// read-out adds them across the lane quadrants.
+constexpr uint32_t SM_TP = SM_AP + 64 * KiB;
+constexpr uint32_t SM_TPL = SM_AP + 80 * KiB;
+constexpr uint32_t SM_XCH = SM_AP;                // chunk preparation: [2][16 KiB] bf16 exchange of the lo halves
 constexpr uint32_t SM_WBF = SM_AP + 64 * KiB;     // [tok x dv] W in fp16 (after T' is used)
 
 constexpr uint32_t SM_MISC = 224 * KiB;
@@ -110,6 +116,12 @@ constexpr uint32_t kWaitPolls = 1u << 24;
 // TMA loads are issued by lane 0 of warp 4 (a warp with no output stores),
 // the MMAs by thread 0.
 constexpr int kTmaThread = 128;
+// Chunk preparation: lane 0 of warps 4..7 each store one part of the record
+// (and later wait for its own bulk group); warps 12..15 build nothing in the
+// first operand pass, so one of them issues the next task's q / z loads and
+// another resolves the task after that.
+constexpr int kQzThread = 416;
+constexpr int kTaskThread = 480;
 
 // Instruction descriptors (fp32 accumulation).
 constexpr uint32_t ID_AP = idesc_mma(128, 64, kFmtTF32, kFmtTF32, 0, 0);      // A_kk / P
@@ -147,12 +159,13 @@ __device__ __forceinline__ uint32_t tf32_rna(float x) {
   return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
 }
 
-// bf16 global load kept where it is written (a prefetch the compiler must not
-// sink to its use).
-__device__ __forceinline__ float ldg_bf16_pinned(const kda_bf16 *ptr) {
+// Raw bf16 global load kept where it is written (a prefetch the compiler must
+// not sink to its use); the caller widens the bits where it uses them, so the
+// load's latency is not waited for here.
+__device__ __forceinline__ unsigned short ldg_u16_pinned(const kda_bf16 *ptr) {
   unsigned short raw;
   asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(raw) : "l"(ptr));
-  return __uint_as_float(static_cast<uint32_t>(raw) << 16);
+  return raw;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -391,12 +404,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tma_load_3d(sb + SM_VB + REG64, &tm_v, 64, h, t0, bar_v);
   };
 
-  bool qz_pending[2] = {false, false}, k_pending = false, v_pending = false, mma_pending = false;
-  float beta_next = 0.f;
+  // bit b: a q / z load into parity b is in flight (a bit mask, not an array
+  // indexed by the parity, which would live in local memory)
+  uint32_t qz_pending = 0;
+  bool k_pending = false, v_pending = false, mma_pending = false;
+  unsigned short beta_raw = 0;  // bf16 bits of this thread's beta, one chunk ahead
   if (tid < 64 && n_chunks > 0) {
     const Task tk = task_of(0);
-    if (tid < tk.L) beta_next = bf2f(p.beta[static_cast<size_t>(tk.t0 + tid) * H + tk.h]);
+    if (tid < tk.L) beta_raw = p.beta[static_cast<size_t>(tk.t0 + tid) * H + tk.h];
   }
+  const bool rec_thread = kPrep && lane == 0 && warp >= 4 && warp < 8;
   // A full chunk's snapshot is written from the next chunk's state read-out
   // (or after the last chunk): the row it goes to, or -1.
   int64_t snap_pending = -1;
@@ -428,7 +445,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     issue_k(0);
     if (!p.zero_v) issue_v(0);
   }
-  qz_pending[0] = k_pending = (n_chunks > 0);
+  qz_pending = n_chunks > 0 ? 1u : 0u;
+  k_pending = (n_chunks > 0);
   v_pending = n_chunks > 0 && !p.zero_v;
 
   // Element-phase mapping: channel pair cp (channels c0, c0 + 1), sub-tile R,
@@ -466,14 +484,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // writes before the barrier that ended the previous chunk.)  Chunk
     // preparation issues it later, once the previous record has been read.
     if (!kPrep && tid == kTmaThread && n + 1 < n_chunks) issue_qz(n + 1);
-    if (n + 1 < n_chunks) qz_pending[par ^ 1] = true;
+    if (n + 1 < n_chunks) qz_pending |= 1u << (par ^ 1);
     // beta of this chunk was loaded one chunk ahead (logits pass through a sigmoid)
     if (tid < 64) {
-      const float b = (p.pre & KDA_PRE_SIGMOID_BETA) ? 1.0f / (1.0f + __expf(-beta_next)) : beta_next;
+      const float bn = __uint_as_float(static_cast<uint32_t>(beta_raw) << 16);
+      const float b = (p.pre & KDA_PRE_SIGMOID_BETA) ? 1.0f / (1.0f + __expf(-bn)) : bn;
       S.f32(sb + MS_BETA + 4 * tid) = tid < L ? b : 0.f;
     }
     if (!wait_all(bar_qz0 + 8 * par, (n >> 1) & 1)) { aborted = true; break; }
-    qz_pending[par] = false;
+    qz_pending &= ~(1u << par);
 
     // ---- element phase A: decay factors and their running products ---------------------
     float ef0[8], ef1[8], eb0[8], eb1[8];
@@ -539,22 +558,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     // the next chunk's beta, issued while the store queue is quiet
     if (tid < 64) {
-      beta_next = 0.f;
+      beta_raw = 0;
       if (n + 1 < n_chunks) {
         const Task nx = task_of(n + 1);
         if (tid < nx.L)
-          beta_next = ldg_bf16_pinned(p.beta + static_cast<size_t>(nx.t0 + tid) * H + nx.h);
+          beta_raw = ldg_u16_pinned(p.beta + static_cast<size_t>(nx.t0 + tid) * H + nx.h);
       }
     }
-    if constexpr (kPrep) {
-      // The previous record's bulk stores must have read A3 / ZB [par ^ 1],
-      // A5 and the U tile before they are overwritten (q, z of the next task
-      // now; the work region from phase B on).
-      if (tid == kTmaThread) {
-        bulk_wait_read0();
-        if (n + 1 < n_chunks) issue_qz(n + 1);
-      }
-    }
+    // Chunk preparation: the previous record's bulk stores must have read
+    // A3 / ZB [par ^ 1], A5 and the U tile before they are overwritten (the
+    // next task's q, z and the work region, both after the barrier below).
+    if (rec_thread) bulk_wait_read0();
     if (!wait_all(bar_k, n & 1)) { aborted = true; break; }  // also orders the Lam table
     k_pending = false;
 
@@ -616,19 +630,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (m < R) { x0 *= l0[m]; x1 *= l1[m]; }
         if (m > R) { y0 *= l0[m]; y1 *= l1[m]; }
       }
-      // column factors of Khat_{R'} for R' >= R (this thread's rows are sub-tile R)
-      float f0[4], f1[4];
-#pragma unroll
-      for (int rp = 0; rp < 4; ++rp) {
-        float a = 1.f, b = 1.f;
+      // column factors of Khat_{R'} for R' >= R (this thread's rows are sub-tile
+      // R), as scalars: an array indexed by the pass would live in local memory
+      auto colf = [&](int rp, const float (&l)[4]) {
+        float a = 1.f;
 #pragma unroll
         for (int m = 0; m < 4; ++m)
-          if (m > R && m < rp) { a *= l0[m]; b *= l1[m]; }
-        f0[rp] = (rp == R) ? rcp_approx(l0[R]) : a;
-        f1[rp] = (rp == R) ? rcp_approx(l1[R]) : b;
-      }
+          if (m > R && m < rp) a *= l[m];
+        const float lr = R == 0 ? l[0] : R == 1 ? l[1] : R == 2 ? l[2] : l[3];
+        return (rp == R) ? rcp_approx(lr) : a;
+      };
+      const float f0_0 = colf(0, l0), f0_1 = colf(1, l0), f0_2 = colf(2, l0), f0_3 = colf(3, l0);
+      const float f1_0 = colf(0, l1), f1_1 = colf(1, l1), f1_2 = colf(2, l1), f1_3 = colf(3, l1);
       for (int pp = 0; pp < 2; ++pp) {
+        if constexpr (kPrep) {
+          if (pp == 0 && tid == kQzThread && n + 1 < n_chunks) issue_qz(n + 1);
+          if (pp == 0 && tid == kTaskThread && n + 2 < n_chunks) put_task(n + 2);
+        }
         if (2 * pp + 1 >= R) {
+          // column factors of the two Khat blocks of this pass
+          const float fa0 = pp ? f0_2 : f0_0, fa1 = pp ? f1_2 : f1_0;
+          const float fb0 = pp ? f0_3 : f0_1, fb1 = pp ? f1_3 : f1_1;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int r = rbase + (j & 3) + 8 * (j >> 2);
@@ -661,13 +683,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               S.u64(ab) = make_uint2(tf32_rna(ke0), tf32_rna(ke1));
               S.u64(ab + 16 * 128) = make_uint2(tf32_rna(qe0), tf32_rna(qe1));
             }
-#pragma unroll
-            for (int rl = 0; rl < 2; ++rl) {
-              const int rp = 2 * pp + rl;
-              if (rp >= R)
-                S.u64(sb + SM_APA + rg32_a + 64 * 128 * rl + o32) =
-                    make_uint2(tf32_rna(kb0 * f0[rp]), tf32_rna(kb1 * f1[rp]));
-            }
+            if (2 * pp >= R)
+              S.u64(sb + SM_APA + rg32_a + o32) = make_uint2(tf32_rna(kb0 * fa0), tf32_rna(kb1 * fa1));
+            S.u64(sb + SM_APA + rg32_a + 64 * 128 + o32) =
+                make_uint2(tf32_rna(kb0 * fb0), tf32_rna(kb1 * fb1));
             if (pp == 1) {
               // K~ into A3 rows 0..63 (free until -Wk), so k can be refilled now;
               // -Q~ over q, K' over z
@@ -696,19 +715,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (mma_pending) { aborted = true; break; }
     }
 
-    // Zero what the T blocks do not write: the upper triangle of T' hi / lo
-    // (rows 64..127 of T' only feed the D1 / Wk rows 64..127, which the chunk
-    // preparation never reads; the single pass needs them zero, as U's rows
+    // Zero what the T blocks do not write: the upper triangles of the T' hi /
+    // lo tiles (in the single pass also their rows 64..127, as U's rows
     // 64..127 start -O).  The read-out below writes all of -P itself, zeros
     // included, and the first block X of [X ; -P] only feeds D1 rows that
     // are never read after M5; so no barrier is needed before it.
-    for (int x = tid; x < 512; x += TC_THREADS) {
+    for (int x = tid; x < 1024; x += TC_THREADS) {
       S.u128(sb + SM_TP + 16 * x) = make_uint4(0, 0, 0, 0);
       S.u128(sb + SM_TPL + 16 * x) = make_uint4(0, 0, 0, 0);
-      if constexpr (!kPrep) {
-        S.u128(sb + SM_TP + 8 * KiB + 16 * x) = make_uint4(0, 0, 0, 0);
-        S.u128(sb + SM_TPL + 8 * KiB + 16 * x) = make_uint4(0, 0, 0, 0);
-      }
     }
     {
       // Pair q4 >> 1 of the products: lanes < 64 (rows i of Khat_2pair) hold
@@ -756,37 +770,62 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncthreads();
 
     // ---- T = (I + A_kk)^{-1}: diagonal 16x16 blocks, then off-diagonal by distance ------
-    if (tid < 64) {
-      // column jc of the inverse of diagonal block Rd, by column updates: once
-      // x[m] is final, subtract A[r][m] x[m] from every later row r.
-      const int Rd = tid >> 4, jc = tid & 15, o = 16 * Rd;
-      float x[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) x[r] = (r == jc) ? 1.f : 0.f;
+    // T' hi / lo at byte offset `off` of the [128 x 64] tiles (row r < 64, see SM_TP).
+    auto put_tp16 = [&](uint32_t off, unsigned short hi, unsigned short lo) {
+      S.u16(sb + SM_TP + off) = hi;
+      S.u16(sb + SM_TPL + off) = lo;
+      if constexpr (kPrep) {
+        S.u16(sb + SM_TP + 8 * KiB + off) = lo;
+        S.u16(sb + SM_TPL + 8 * KiB + off) = hi;
+      }
+    };
+    auto put_tp32 = [&](uint32_t off, uint32_t hi, uint32_t lo) {
+      S.u32(sb + SM_TP + off) = hi;
+      S.u32(sb + SM_TPL + off) = lo;
+      if constexpr (kPrep) {
+        S.u32(sb + SM_TP + 8 * KiB + off) = lo;
+        S.u32(sb + SM_TPL + 8 * KiB + off) = hi;
+      }
+    };
+    {
+      // Column jc of the inverse of diagonal block Rd by column updates (once
+      // x[m] is final, subtract A[r][m] x[m] from every later row r): eight
+      // lanes per column, each holding rows rq and rq + 8; x[m] is passed
+      // along by shuffle.  Every CTA thread takes part (64 columns x 8 lanes).
+      const int Rd = warp >> 2, jc = 4 * (warp & 3) + (lane >> 3), rq = lane & 7, o = 16 * Rd;
+      float a0[7], a1[15];  // A[rq][m] (m < rq), A[rq + 8][m] (m < rq + 8), zero elsewhere
 #pragma unroll
       for (int m = 0; m < 15; ++m) {
+        const float e1 = S.f32(sb + SM_AKK + 4 * ((o + m) * 68 + o + rq + 8));
+        a1[m] = (m < rq + 8) ? e1 : 0.f;
+        if (m < 7) {
+          const float e0 = S.f32(sb + SM_AKK + 4 * ((o + m) * 68 + o + rq));
+          a0[m] = (m < rq) ? e0 : 0.f;
+        }
+      }
+      float x0 = (rq == jc) ? 1.f : 0.f, x1 = (rq + 8 == jc) ? 1.f : 0.f;
 #pragma unroll
-        for (int r = m + 1; r < 16; ++r)
-          x[r] -= S.f32(sb + SM_AKK + 4 * ((o + m) * 68 + o + r)) * x[m];
+      for (int m = 0; m < 15; ++m) {
+        const float xm = __shfl_sync(0xffffffffu, m < 8 ? x0 : x1, m & 7, 8);
+        if (m < 7) x0 -= a0[m] * xm;
+        x1 -= a1[m] * xm;
       }
       const float bj = S.f32(sb + MS_BETA + 4 * (o + jc));
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        S.f32(sb + SM_TF + 4 * ((o + r) * 65 + o + jc)) = x[r];
-        if (r >= jc) {  // T' = T diag(beta) as bf16 hi + lo (upper triangle stays zero)
-          const float tv = x[r] * bj;
+      for (int hr = 0; hr < 2; ++hr) {
+        const int r = rq + 8 * hr;
+        const float xr = hr ? x1 : x0;
+        S.f32(sb + SM_TF + 4 * ((o + r) * 65 + o + jc)) = xr;
+        if (r >= jc) {  // T' = T diag(beta) as bf16 hi + lo (the upper triangle stays zero)
+          const float tv = xr * bj;
           const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
           const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
-          const uint32_t off = sw128_off(o + r, o + jc, REG128);
-          S.u16(sb + SM_TP + off) = *reinterpret_cast<const unsigned short *>(&hi);
-          S.u16(sb + SM_TPL + off) = *reinterpret_cast<const unsigned short *>(&lo);
+          put_tp16(sw128_off(o + r, o + jc, REG128), *reinterpret_cast<const unsigned short *>(&hi),
+                   *reinterpret_cast<const unsigned short *>(&lo));
         }
       }
     }
     __syncthreads();
-    if constexpr (kPrep) {  // warp 15 is idle during the off-diagonal blocks
-      if (tid == 480 && n + 2 < n_chunks) put_task(n + 2);
-    }
     // Off-diagonal blocks by the 2 x 2 block inverse: with Ta, Tb the inverses
     // of the top-left and bottom-right 32 x 32 blocks, the bottom-left block
     // is -Tb A_ba Ta.  Level 1: T10 = -T11 A10 T00 and T32 = -T33 A32 T22;
@@ -816,11 +855,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const float b0 = S.f32(sb + MS_BETA + 4 * col), b1 = S.f32(sb + MS_BETA + 4 * (col + 1));
           uint32_t hi, lo;
           split_bf16x2(-e[nt][0] * b0, -e[nt][1] * b1, hi, lo);
-          S.u32(sb + SM_TP + sw128_off(16 * R + g, col, REG128)) = hi;
-          S.u32(sb + SM_TPL + sw128_off(16 * R + g, col, REG128)) = lo;
+          put_tp32(sw128_off(16 * R + g, col, REG128), hi, lo);
           split_bf16x2(-e[nt][2] * b0, -e[nt][3] * b1, hi, lo);
-          S.u32(sb + SM_TP + sw128_off(16 * R + g + 8, col, REG128)) = hi;
-          S.u32(sb + SM_TPL + sw128_off(16 * R + g + 8, col, REG128)) = lo;
+          put_tp32(sw128_off(16 * R + g + 8, col, REG128), hi, lo);
         }
       };
       if (warp < 2) {  // level 1
@@ -870,13 +907,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // ---- Wk = T' K~ -> TM_AP,  U = T' V -> D1 ---------------------------------------------
     if (tid == 0) {
       tc_fence_after();
-      issue_mma(tmem + TM_AP, sb + SM_TP, false, REG128, a3, true, REG128, 4, ID_TPROD, 0);
-      issue_mma(tmem + TM_AP, sb + SM_TPL, false, REG128, a3, true, REG128, 4, ID_TPROD, 1);
-      if (!p.zero_v)
-      {
-        issue_mma(tmem + TM_D1, sb + SM_TP, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD, 0);
+      if constexpr (kPrep) {
+        // [hi ; lo] K~ and [lo ; hi] V: the halves land in different lane quadrants
+        issue_mma(tmem + TM_AP, sb + SM_TP, false, REG128, a3, true, REG128, 4, ID_TPROD, 0);
         issue_mma(tmem + TM_D1, sb + SM_TPL, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD,
-                  1);
+                  0);
+      } else {
+        issue_mma(tmem + TM_AP, sb + SM_TP, false, REG128, a3, true, REG128, 4, ID_TPROD, 0);
+        issue_mma(tmem + TM_AP, sb + SM_TPL, false, REG128, a3, true, REG128, 4, ID_TPROD, 1);
+        if (!p.zero_v) {
+          issue_mma(tmem + TM_D1, sb + SM_TP, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD,
+                    0);
+          issue_mma(tmem + TM_D1, sb + SM_TPL, false, REG128, sb + SM_VB, true, REG64, 4,
+                    ID_TPROD, 1);
+        }
       }
       mma_commit(bar_mma);
     }
@@ -892,29 +936,57 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       //      A3 (with -Q~), K' (ZB), -P (A5 rows 64..127) and U go out as bulk stores.
       const int64_t task = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
       uint8_t *rec = p.rec + static_cast<size_t>(task) * kRecBytes;
-      if (quad < 2) {
-        float v[32];
-        tmem_ld32(t_lane + TM_AP + 32 * q4, v);
+      {
+        // Lanes 0..63 hold the hi half of T'K~ and the lo half of T'V, lanes
+        // 64..127 the other two.  Each quadrant pair passes its lo half (small:
+        // bf16 keeps it to ~2^-17 of the sum) through the exchange tile
+        // [16 column chunks][64 rows][8 bf16] and finishes one product:
+        // lanes 0..63 -Wk, lanes 64..127 U.
+        const int r = trow & 63;
+        const bool top = quad < 2;
+        float v[32], x[32];
+        tmem_ld32(t_lane + (top ? TM_D1 : TM_AP) + 32 * q4, x);
+        tmem_ld32(t_lane + (top ? TM_AP : TM_D1) + 32 * q4, v);
         tmem_wait_ld();
-        store_row32_f16(S, a3, trow, q4, REG128, v, -1.f);
-        tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
-        tmem_wait_ld();
-        store_row32_f16(S, sb + SM_WBF, trow, q4, REG64, v, 1.f);
-      } else if (q4 < 2) {  // warps 2, 3, 6, 7: one key channel per thread
-        const int c = (2 * q4 + quad - 2) * 32 + lane;
-        float gam = 1.f;
+        const uint32_t xo = sb + SM_XCH + (top ? 16 * KiB : 0);  // lo of Wk at 0, of U at 16 KiB
 #pragma unroll
-        for (int m = 0; m < 4; ++m) gam *= S.f32(sb + MS_LAM + 4 * (m * TD + c));
-        reinterpret_cast<float *>(rec + kRecG)[c] = gam;
+        for (int j = 0; j < 4; ++j)
+          S.u128(xo + static_cast<uint32_t>(((4 * q4 + j) * 64 + r) * 16)) =
+              make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]), pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
+                         pack_bf16x2(x[8 * j + 4], x[8 * j + 5]), pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+        if (!top && q4 < 2) {  // warps 2, 3, 6, 7: gamma, one key channel per thread
+          const int c = (2 * q4 + quad - 2) * 32 + lane;
+          float gam = 1.f;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) gam *= S.f32(sb + MS_LAM + 4 * (m * TD + c));
+          reinterpret_cast<float *>(rec + kRecG)[c] = gam;
+        }
+        __syncthreads();
+        const uint32_t xi = sb + SM_XCH + (top ? 0 : 16 * KiB);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 w = S.u128(xi + static_cast<uint32_t>(((4 * q4 + j) * 64 + r) * 16));
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(ws[e]);
+            v[8 * j + 2 * e] += f.x;
+            v[8 * j + 2 * e + 1] += f.y;
+          }
+        }
+        if (top)
+          store_row32_f16(S, a3, r, q4, REG128, v, -1.f);
+        else
+          store_row32_f16(S, sb + SM_WBF, r, q4, REG64, v, 1.f);
       }
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
-      if (tid == kTmaThread) {
-        bulk_s2g(rec + kRecA3, a3, 32 * KiB);
-        bulk_s2g(rec + kRecKP, zb, 16 * KiB);
-        bulk_s2g(rec + kRecU, sb + SM_WBF, 16 * KiB);
-        bulk_s2g(rec + kRecP, sb + SM_A5 + 8 * KiB, 8 * KiB);
+      if (rec_thread) {  // one bulk store per thread, issued side by side
+        if (warp == 4) bulk_s2g(rec + kRecA3, a3, 32 * KiB);
+        if (warp == 5) bulk_s2g(rec + kRecKP, zb, 16 * KiB);
+        if (warp == 6) bulk_s2g(rec + kRecU, sb + SM_WBF, 16 * KiB);
+        if (warp == 7) bulk_s2g(rec + kRecP, sb + SM_A5 + 8 * KiB, 8 * KiB);
         bulk_commit();
       }
       continue;
@@ -1023,7 +1095,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }  // !kPrep
   }
   if constexpr (kPrep) {
-    if (tid == kTmaThread) bulk_wait0();  // the last record is out before the CTA ends
+    if (rec_thread) bulk_wait0();  // the last record is out before the CTA ends
   }
 
   if (!aborted && (p.S_final || snap_pending >= 0)) {
@@ -1051,7 +1123,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (aborted && tid == 0) {
     if (mma_pending) mbar_wait_bounded(bar_mma, mma_phase, kWaitPolls);
     for (int b = 0; b < 2; ++b)
-      if (qz_pending[b]) mbar_wait_bounded(bar_qz0 + 8 * b, 0, kWaitPolls) ||
+      if ((qz_pending >> b) & 1u) mbar_wait_bounded(bar_qz0 + 8 * b, 0, kWaitPolls) ||
                              mbar_wait_bounded(bar_qz0 + 8 * b, 1, kWaitPolls);
     if (k_pending) mbar_wait_bounded(bar_k, 0, kWaitPolls) || mbar_wait_bounded(bar_k, 1, kWaitPolls);
     if (v_pending) mbar_wait_bounded(bar_v, 0, kWaitPolls) || mbar_wait_bounded(bar_v, 1, kWaitPolls);

@@ -169,13 +169,15 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     bulk_g2s(st + ST_P, rec + kRecP, 8 * KiB, bar);
     bulk_g2s(st + ST_G, rec + kRecG, 512, bar);
   };
-  bool full_pending[2] = {false, false}, mma_pending = false, aborted = false;
+  // bit b: stage b's record copy is in flight (a mask: an array indexed by
+  // the stage would live in local memory)
+  uint32_t full_pending = 0;
+  bool mma_pending = false, aborted = false;
   if (tid == kCopyThread) {
     if (n_chunks > 0) issue(0);
     if (n_chunks > 1) issue(1);
   }
-  full_pending[0] = n_chunks > 0;
-  full_pending[1] = n_chunks > 1;
+  full_pending = (n_chunks > 0 ? 1u : 0u) | (n_chunks > 1 ? 2u : 0u);
   uint32_t mma_phase = 0;
   int64_t snap_pending = -1;
 
@@ -226,7 +228,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
       aborted = true;
       break;
     }
-    full_pending[stg] = false;
+    full_pending &= ~(1u << stg);
 
     // ---- D1 = [-Wk ; -Q~] S ------------------------------------------------------------
     if (tid == 0) {
@@ -284,7 +286,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     if (!wait_mma()) { aborted = true; break; }
     // every reader of this stage is done: refill it with chunk n + 2
     if (tid == kCopyThread && n + 2 < n_chunks) issue(n + 2);
-    if (n + 2 < n_chunks) full_pending[stg] = true;
+    if (n + 2 < n_chunks) full_pending |= 1u << stg;
 
     // ---- outputs: o = -D1 rows 64..127 -------------------------------------------------------
     // Each of the 8 warps holds 32 rows x 16 columns (32 bytes of bf16 per
@@ -347,7 +349,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
   }
   if (aborted && tid == kCopyThread) {
     for (int b = 0; b < 2; ++b)
-      if (full_pending[b]) mbar_wait_bounded(bar_full + 8 * b, 0, kWaitPolls) ||
+      if ((full_pending >> b) & 1u) mbar_wait_bounded(bar_full + 8 * b, 0, kWaitPolls) ||
                                mbar_wait_bounded(bar_full + 8 * b, 1, kWaitPolls);
   }
   tc_fence_before();

@@ -642,6 +642,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       };
       const float f0_0 = colf(0, l0), f0_1 = colf(1, l0), f0_2 = colf(2, l0), f0_3 = colf(3, l0);
       const float f1_0 = colf(0, l1), f1_1 = colf(1, l1), f1_2 = colf(2, l1), f1_3 = colf(3, l1);
+#pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
         if constexpr (kPrep) {
           if (pp == 0 && tid == kQzThread && n + 1 < n_chunks) issue_qz(n + 1);
@@ -907,19 +908,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // ---- Wk = T' K~ -> TM_AP,  U = T' V -> D1 ---------------------------------------------
     if (tid == 0) {
       tc_fence_after();
+      // T'K~ and T'V interleaved K-step by K-step (independent accumulators)
       if constexpr (kPrep) {
         // [hi ; lo] K~ and [lo ; hi] V: the halves land in different lane quadrants
-        issue_mma(tmem + TM_AP, sb + SM_TP, false, REG128, a3, true, REG128, 4, ID_TPROD, 0);
-        issue_mma(tmem + TM_D1, sb + SM_TPL, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD,
-                  0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          issue_mma_step(tmem + TM_AP, sb + SM_TP, false, REG128, a3, true, REG128, ks, ID_TPROD,
+                         ks > 0 ? 1u : 0u);
+          issue_mma_step(tmem + TM_D1, sb + SM_TPL, false, REG128, sb + SM_VB, true, REG64, ks,
+                         ID_TPROD, ks > 0 ? 1u : 0u);
+        }
       } else {
-        issue_mma(tmem + TM_AP, sb + SM_TP, false, REG128, a3, true, REG128, 4, ID_TPROD, 0);
-        issue_mma(tmem + TM_AP, sb + SM_TPL, false, REG128, a3, true, REG128, 4, ID_TPROD, 1);
-        if (!p.zero_v) {
-          issue_mma(tmem + TM_D1, sb + SM_TP, false, REG128, sb + SM_VB, true, REG64, 4, ID_TPROD,
-                    0);
-          issue_mma(tmem + TM_D1, sb + SM_TPL, false, REG128, sb + SM_VB, true, REG64, 4,
-                    ID_TPROD, 1);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // T' hi, then T' lo
+          const uint32_t tp = h ? sb + SM_TPL : sb + SM_TP;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t acc = (h > 0 || ks > 0) ? 1u : 0u;
+            issue_mma_step(tmem + TM_AP, tp, false, REG128, a3, true, REG128, ks, ID_TPROD, acc);
+            if (!p.zero_v)
+              issue_mma_step(tmem + TM_D1, tp, false, REG128, sb + SM_VB, true, REG64, ks,
+                             ID_TPROD, acc);
+          }
         }
       }
       mma_commit(bar_mma);
@@ -1064,8 +1074,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // ---- S += K'^T W;  D1 += [0; -P] W -------------------------------------------------------
     if (tid == 0) {
       tc_fence_after();
-      issue_mma(tmem + TM_S, zb, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
-      issue_mma(tmem + TM_D1, sb + SM_A5, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {  // the two products interleaved
+        issue_mma_step(tmem + TM_S, zb, true, REG64, sb + SM_WBF, true, REG64, ks, ID_MNMN, 1);
+        issue_mma_step(tmem + TM_D1, sb + SM_A5, true, REG64, sb + SM_WBF, true, REG64, ks,
+                       ID_MNMN, 1);
+      }
       mma_commit(bar_mma);
     }
     mma_pending = true;

@@ -278,8 +278,13 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     // ---- S += K'^T W;  D1 += [X ; -P] W -------------------------------------------------------
     if (tid == 0) {
       tc_fence_after();
-      issue_mma(tmem + TM_S, st + ST_KP, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
-      issue_mma(tmem + TM_D1, st + ST_A5, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {  // the two products interleaved
+        issue_mma_step(tmem + TM_S, st + ST_KP, true, REG64, sb + SM_WBF, true, REG64, ks,
+                       ID_MNMN, 1);
+        issue_mma_step(tmem + TM_D1, st + ST_A5, true, REG64, sb + SM_WBF, true, REG64, ks,
+                       ID_MNMN, 1);
+      }
       mma_commit(bar_mma);
     }
     mma_pending = true;

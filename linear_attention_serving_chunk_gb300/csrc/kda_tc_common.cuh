@@ -130,28 +130,41 @@ __device__ __forceinline__ void add_row32_f16(const Smem &S, uint32_t tile, int 
   }
 }
 
-// Issue the MMAs of one product: K-steps of 16 elements (8 for tf32, the same
-// 32 bytes).  K-major operands advance 32 bytes per step inside a 128-byte
-// row and jump one region per 4 steps; MN-major operands advance 2048 bytes
-// (16 rows) per step and find their 64-element MN blocks `region` apart.
+// One K-step of a product: K-steps of 16 elements (8 for tf32, the same 32
+// bytes).  K-major operands advance 32 bytes per step inside a 128-byte row
+// and jump one region per 4 steps; MN-major operands advance 2048 bytes (16
+// rows) per step and find their 64-element MN blocks `region` apart.
+// A single thread issues the MMAs, and each waits for its descriptors: so the
+// descriptor of the operand base is built once (the same for every step of a
+// product) and the step's offset is added to its 14-bit address field, which
+// cannot carry for shared-memory addresses below 256 KiB.
+__device__ __forceinline__ void issue_mma_step(uint32_t d_tmem, uint32_t a_base, bool a_mn,
+                                               uint32_t a_region, uint32_t b_base, bool b_mn,
+                                               uint32_t b_region, int ks, uint32_t idesc,
+                                               uint32_t accumulate, bool tf32 = false) {
+  const uint32_t a_off = a_mn ? static_cast<uint32_t>(ks) * 2048u
+                              : static_cast<uint32_t>(ks >> 2) * a_region +
+                                    static_cast<uint32_t>(ks & 3) * 32u;
+  const uint32_t b_off = b_mn ? static_cast<uint32_t>(ks) * 2048u
+                              : static_cast<uint32_t>(ks >> 2) * b_region +
+                                    static_cast<uint32_t>(ks & 3) * 32u;
+  const uint64_t ad = sw128_desc(a_base, a_mn ? a_region : 16u, 1024u) + (a_off >> 4);
+  const uint64_t bd = sw128_desc(b_base, b_mn ? b_region : 16u, 1024u) + (b_off >> 4);
+  if (tf32)
+    mma_tf32(d_tmem, ad, bd, idesc, accumulate);
+  else
+    mma_f16(d_tmem, ad, bd, idesc, accumulate);
+}
+
+// Issue the MMAs of one product, K-step by K-step into one accumulator.
 __device__ __forceinline__ void issue_mma(uint32_t d_tmem, uint32_t a_base, bool a_mn,
                                           uint32_t a_region, uint32_t b_base, bool b_mn,
                                           uint32_t b_region, int ksteps, uint32_t idesc,
                                           uint32_t accumulate, bool tf32 = false) {
-  for (int ks = 0; ks < ksteps; ++ks) {
-    const uint32_t a_addr = a_mn ? a_base + static_cast<uint32_t>(ks) * 2048u
-                                 : a_base + static_cast<uint32_t>(ks >> 2) * a_region +
-                                       static_cast<uint32_t>(ks & 3) * 32u;
-    const uint32_t b_addr = b_mn ? b_base + static_cast<uint32_t>(ks) * 2048u
-                                 : b_base + static_cast<uint32_t>(ks >> 2) * b_region +
-                                       static_cast<uint32_t>(ks & 3) * 32u;
-    const uint64_t ad = sw128_desc(a_addr, a_mn ? a_region : 16u, 1024u);
-    const uint64_t bd = sw128_desc(b_addr, b_mn ? b_region : 16u, 1024u);
-    if (tf32)
-      mma_tf32(d_tmem, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
-    else
-      mma_f16(d_tmem, ad, bd, idesc, (ks > 0 || accumulate) ? 1u : 0u);
-  }
+#pragma unroll
+  for (int ks = 0; ks < ksteps; ++ks)
+    issue_mma_step(d_tmem, a_base, a_mn, a_region, b_base, b_mn, b_region, ks, idesc,
+                   (ks > 0 || accumulate) ? 1u : 0u, tf32);
 }
 
 // Host: the driver's cuTensorMapEncodeTiled, looked up once per process

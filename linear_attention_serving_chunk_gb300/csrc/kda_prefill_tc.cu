@@ -70,7 +70,7 @@ constexpr uint32_t SM_APA = SM_AP;                // tf32 [Khat_2p ; Khat_2p+1] 
 constexpr uint32_t SM_APB = SM_AP + 64 * KiB;     // tf32 [KE_2p; QE_2p; KE_2p+1; QE_2p+1] 64 x 128
 constexpr uint32_t SM_AKK = SM_AP;                // fp32 [64][68] A_kk transposed: [i][r] (after the AP MMAs)
 constexpr uint32_t SM_TF = SM_AP + 64 * 68 * 4;   // fp32 [64][65] T
-constexpr uint32_t SM_TY = SM_AP + 34 * KiB;      // fp32 [4][16][17] block products
+constexpr uint32_t SM_TY = SM_AP + 34 * KiB;      // fp32 [10][16][17] block products
 constexpr uint32_t SM_SBF = SM_AP;                // [dk x dv] S in fp16, MN-major (after T')
 constexpr uint32_t SM_A5 = SM_AP + 48 * KiB;      // [128 x 64] MN-major: [X ; -P] (X unused)
 // T' = T diag(beta) as bf16 hi + lo, two [128 x 64] K-major tiles.  The
@@ -95,7 +95,7 @@ constexpr uint32_t MS_NRM = MS_LAM + 4 * TD * 4;  // [64][2] fp32 1/||k_r||, 1/|
 constexpr uint32_t MS_TASK = MS_NRM + 64 * 8;     // chunk preparation: 3 x 32-byte task slots
 constexpr uint32_t TC_SMEM_BYTES = MS_TASK + 3 * 32;
 static_assert(SM_TF + 64 * 65 * 4 <= SM_TY, "T scratch overlaps");
-static_assert(SM_TY + 4 * 16 * 17 * 4 <= SM_A5, "block scratch overlaps A5");
+static_assert(SM_TY + 10 * 16 * 17 * 4 <= SM_A5, "block scratch overlaps A5");
 static_assert(TC_SMEM_BYTES <= 232448, "shared memory budget");
 
 constexpr uint32_t A3_BYTES = 32 * KiB;
@@ -206,12 +206,13 @@ __device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], const uint32_t (
 
 // One warp: C[16x16] (two 16x8 fragments) += X[16x16] Y[16x16] with X and Y
 // fp32 in shared memory (row strides ldx, ldy floats); with XT, X is given
-// transposed (X[g][k] at X[k * ldx + g]).
-template <bool XT = false>
+// transposed (X[g][k] at X[k * ldx + g]), with YT likewise Y.
+template <bool XT = false, bool YT = false>
 __device__ __forceinline__ void warp_mma16(const float *X, int ldx, const float *Y, int ldy,
                                            float (&c)[2][4], int lane) {
   const int g = lane >> 2, t = lane & 3;
   auto xa = [&](int row, int col) { return XT ? X[col * ldx + row] : X[row * ldx + col]; };
+  auto yb = [&](int row, int col) { return YT ? Y[col * ldy + row] : Y[row * ldy + col]; };
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     const int k0 = 8 * ks;
@@ -219,8 +220,8 @@ __device__ __forceinline__ void warp_mma16(const float *X, int ldx, const float 
                            tf32_rna(xa(g, k0 + t + 4)), tf32_rna(xa(g + 8, k0 + t + 4))};
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
-      mma_m16n8k8_tf32(c[nt], a, tf32_rna(Y[(k0 + t) * ldy + 8 * nt + g]),
-                       tf32_rna(Y[(k0 + t + 4) * ldy + 8 * nt + g]));
+      mma_m16n8k8_tf32(c[nt], a, tf32_rna(yb(k0 + t, 8 * nt + g)),
+                       tf32_rna(yb(k0 + t + 4, 8 * nt + g)));
   }
 }
 
@@ -827,69 +828,97 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     __syncthreads();
-    // Off-diagonal blocks by the 2 x 2 block inverse: with Ta, Tb the inverses
-    // of the top-left and bottom-right 32 x 32 blocks, the bottom-left block
-    // is -Tb A_ba Ta.  Level 1: T10 = -T11 A10 T00 and T32 = -T33 A32 T22;
-    // level 2: X = A_ba Ta; level 3: T_RJ = -sum_{M=2}^{R} T_RM X_MJ.
-    // Chains of 2 + 2 + 2 16 x 16 products, four warps at most.
+    // Off-diagonal blocks.  With D = blockdiag(T_RR) (the diagonal inverses
+    // above) and E = D A_off (E_RJ = T_RR A_RJ, strictly block-lower, E^4 = 0):
+    //   I + A_kk = D^-1 (I + E),  T = (I - E + E^2 - E^3) D,
+    // so with N = I - E + E^2 - E^3, block by block
+    //   N_10 = -E_10, N_21 = -E_21, N_32 = -E_32,
+    //   N_20 = E_21 E_10 - E_20,  N_31 = E_32 E_21 - E_31,
+    //   N_30 = E_31 E_10 - E_30 - E_32 N_20,      and  T_RJ = N_RJ T_JJ.
+    // Four levels of single 16 x 16 products on up to six warps.  Only the
+    // diagonal T blocks are read again, so the off-diagonal ones go straight
+    // to T' (bf16 hi + lo).
     {
       const int g = lane >> 2, t = lane & 3;
-      float *akk = reinterpret_cast<float *>(S.ptr(sb + SM_AKK));
-      float *tf = reinterpret_cast<float *>(S.ptr(sb + SM_TF));
-      float *xs = reinterpret_cast<float *>(S.ptr(sb + SM_TY));  // 4 blocks of [16][17]
-      // c (two 16x8 fragments) -> fp32 [16][ld] block, negated or not
-      auto put16 = [&](float *dst, int ld, const float (&c)[2][4], float sgn) {
+      const float *akk = reinterpret_cast<const float *>(S.ptr(sb + SM_AKK));
+      const float *tf = reinterpret_cast<const float *>(S.ptr(sb + SM_TF));
+      float *xs = reinterpret_cast<float *>(S.ptr(sb + SM_TY));  // 10 blocks of [16][17]
+      // block slots: E_10, E_20, E_21, E_30, E_31, E_32, N_20, N_31, E_31 E_10, N_30
+      auto blk = [&](int i) { return xs + i * 16 * 17; };
+      auto tdiag = [&](int R) { return tf + R * (16 * 65 + 16); };  // T_RR
+      // c (two 16x8 fragments) -> fp32 [16][17] block, minus the block `sub` if given
+      auto put16 = [&](float *dst, const float (&c)[2][4], const float *sub) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          dst[g * ld + 8 * nt + 2 * t] = sgn * c[nt][0];
-          dst[g * ld + 8 * nt + 2 * t + 1] = sgn * c[nt][1];
-          dst[(g + 8) * ld + 8 * nt + 2 * t] = sgn * c[nt][2];
-          dst[(g + 8) * ld + 8 * nt + 2 * t + 1] = sgn * c[nt][3];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int o = (g + 8 * h) * 17 + 8 * nt + 2 * t;
+            dst[o] = c[nt][2 * h] - (sub ? sub[o] : 0.f);
+            dst[o + 1] = c[nt][2 * h + 1] - (sub ? sub[o + 1] : 0.f);
+          }
         }
       };
-      // block (R, J) of T = -e: fp32 T, and T' = T diag(beta) as bf16 hi + lo
-      auto put_t = [&](int R, int J, const float (&e)[2][4]) {
-        put16(tf + (16 * R) * 65 + 16 * J, 65, e, -1.f);
+      // T_RJ = sgn c as T' = T diag(beta) in bf16 hi + lo
+      auto put_t = [&](int R, int J, const float (&c)[2][4], float sgn) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const int col = 16 * J + 8 * nt + 2 * t;
-          const float b0 = S.f32(sb + MS_BETA + 4 * col), b1 = S.f32(sb + MS_BETA + 4 * (col + 1));
+          const float b0 = sgn * S.f32(sb + MS_BETA + 4 * col);
+          const float b1 = sgn * S.f32(sb + MS_BETA + 4 * (col + 1));
           uint32_t hi, lo;
-          split_bf16x2(-e[nt][0] * b0, -e[nt][1] * b1, hi, lo);
+          split_bf16x2(c[nt][0] * b0, c[nt][1] * b1, hi, lo);
           put_tp32(sw128_off(16 * R + g, col, REG128), hi, lo);
-          split_bf16x2(-e[nt][2] * b0, -e[nt][3] * b1, hi, lo);
+          split_bf16x2(c[nt][2] * b0, c[nt][3] * b1, hi, lo);
           put_tp32(sw128_off(16 * R + g + 8, col, REG128), hi, lo);
         }
       };
-      if (warp < 2) {  // level 1
-        const int R = 2 * warp + 1, J = R - 1;
-        float *y = xs + warp * 16 * 17;
-        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mma16<true>(akk + (16 * J) * 68 + 16 * R, 68, tf + (16 * J) * 65 + 16 * J, 65, c,
-                         lane);
-        put16(y, 17, c, 1.f);
-        __syncwarp();
-        float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_mma16(tf + (16 * R) * 65 + 16 * R, 65, y, 17, e, lane);
-        put_t(R, J, e);
+      float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      if (warp < 6) {  // level 1: E_RJ = T_RR A_RJ (A_kk is stored transposed)
+        const int R = warp == 0 ? 1 : warp < 3 ? 2 : 3;
+        const int J = warp == 0 ? 0 : warp < 3 ? warp - 1 : warp - 3;
+        warp_mma16<false, true>(tdiag(R), 65, akk + (16 * J) * 68 + 16 * R, 68, c, lane);
+        put16(blk(warp), c, nullptr);
       }
       __syncthreads();
-      if (warp < 4) {  // level 2: X_RJ = sum_{M=J}^{1} A_RM T_MJ, R = 2, 3, J = 0, 1
-        const int R = 2 + (warp >> 1), J = warp & 1;
-        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (int M = J; M < 2; ++M)
-          warp_mma16<true>(akk + (16 * M) * 68 + 16 * R, 68, tf + (16 * M) * 65 + 16 * J, 65, c,
-                           lane);
-        put16(xs + warp * 16 * 17, 17, c, 1.f);
+      if (warp < 6) {  // level 2
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[e >> 1][e & 1] = c[e >> 1][2 + (e & 1)] = 0.f;
+        switch (warp) {
+          case 0: warp_mma16(blk(0), 17, tdiag(0), 65, c, lane); put_t(1, 0, c, -1.f); break;
+          case 1: warp_mma16(blk(2), 17, tdiag(1), 65, c, lane); put_t(2, 1, c, -1.f); break;
+          case 2: warp_mma16(blk(5), 17, tdiag(2), 65, c, lane); put_t(3, 2, c, -1.f); break;
+          case 3: warp_mma16(blk(2), 17, blk(0), 17, c, lane); put16(blk(6), c, blk(1)); break;
+          case 4: warp_mma16(blk(5), 17, blk(2), 17, c, lane); put16(blk(7), c, blk(4)); break;
+          default: warp_mma16(blk(4), 17, blk(0), 17, c, lane); put16(blk(8), c, nullptr); break;
+        }
       }
       __syncthreads();
-      if (warp < 4) {  // level 3: T_RJ = -sum_{M=2}^{R} T_RM X_MJ
-        const int R = 2 + (warp >> 1), J = warp & 1;
-        float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (int M = 2; M <= R; ++M)
-          warp_mma16(tf + (16 * R) * 65 + 16 * M, 65, xs + ((M - 2) * 2 + J) * 16 * 17, 17, e,
-                     lane);
-        put_t(R, J, e);
+      if (warp < 3) {  // level 3
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[e >> 1][e & 1] = c[e >> 1][2 + (e & 1)] = 0.f;
+        switch (warp) {
+          case 0: warp_mma16(blk(6), 17, tdiag(0), 65, c, lane); put_t(2, 0, c, 1.f); break;
+          case 1: warp_mma16(blk(7), 17, tdiag(1), 65, c, lane); put_t(3, 1, c, 1.f); break;
+          default:
+            // N_30 = (E_31 E_10 - E_30) - E_32 N_20: the product enters with a minus sign
+            warp_mma16(blk(5), 17, blk(6), 17, c, lane);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int o = (g + 8 * h) * 17 + 8 * nt + 2 * t;
+                blk(9)[o] = (blk(8)[o] - blk(3)[o]) - c[nt][2 * h];
+                blk(9)[o + 1] = (blk(8)[o + 1] - blk(3)[o + 1]) - c[nt][2 * h + 1];
+              }
+            break;
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {  // level 4: T_30 = N_30 T_00
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[e >> 1][e & 1] = c[e >> 1][2 + (e & 1)] = 0.f;
+        warp_mma16(blk(9), 17, tdiag(0), 65, c, lane);
+        put_t(3, 0, c, 1.f);
       }
     }
     fence_proxy_async();  // T' was written by the T blocks above

@@ -275,15 +275,19 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     tc_fence_before();
     __syncthreads();
 
-    // ---- S += K'^T W;  D1 += [X ; -P] W -------------------------------------------------------
+    // ---- S += K'^T W;  D1 += [X ; -P] W (only when o is wanted) ---------------------------------
     if (tid == 0) {
       tc_fence_after();
+      if (p.o) {
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {  // the two products interleaved
-        issue_mma_step(tmem + TM_S, st + ST_KP, true, REG64, sb + SM_WBF, true, REG64, ks,
-                       ID_MNMN, 1);
-        issue_mma_step(tmem + TM_D1, st + ST_A5, true, REG64, sb + SM_WBF, true, REG64, ks,
-                       ID_MNMN, 1);
+        for (int ks = 0; ks < 4; ++ks) {  // the two products interleaved
+          issue_mma_step(tmem + TM_S, st + ST_KP, true, REG64, sb + SM_WBF, true, REG64, ks,
+                         ID_MNMN, 1);
+          issue_mma_step(tmem + TM_D1, st + ST_A5, true, REG64, sb + SM_WBF, true, REG64, ks,
+                         ID_MNMN, 1);
+        }
+      } else {  // the segment scan's passes for N and M
+        issue_mma(tmem + TM_S, st + ST_KP, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
       }
       mma_commit(bar_mma);
     }
@@ -297,7 +301,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     // Each of the 8 warps holds 32 rows x 16 columns (32 bytes of bf16 per
     // row); it stages them in its 1 KiB slice of the W tile (free once the
     // MMAs above are done) and stores 16 rows x 32 bytes per instruction.
-    if (quad >= 2) {
+    if (quad >= 2 && p.o) {
       float v[16];
       tmem_ld16(t_lane + TM_D1 + 16 * q4, v);
       tmem_wait_ld();
@@ -314,7 +318,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
       for (int i = 0; i < 2; ++i) {
         const int rl = 16 * i + (lane >> 1), c = lane & 1;  // row in the warp's 32, 16-byte piece
         const int r = (quad - 2) * 32 + rl;
-        if (r < L && p.o) {
+        if (r < L) {
           const uint4 w = S.u128(tile + rl * 32u + (static_cast<uint32_t>(c ^ (rl & 1)) << 4));
           reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + cq)[c] = w;
         }

@@ -67,10 +67,10 @@ def state_bytes(token_heads, chunk_heads, full_chunk_heads, seq_heads, dk, dv):
 # recorded with the capture (else the kernel has changed since: null).
 _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
 PROFILED_TRAFFIC = {
-    "prefill_tc_kernel<prep>": (269.076224e6 + 250.675200e6, 4096, "3f23154dba096547",
+    "prefill_tc_kernel<prep>": (269.051136e6 + 250.364672e6, 4096, "302d4d3c920be85e",
                                 ("kda_prefill_tc.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
                                  "kda_split.cuh", "kda_common.cuh")),
-    "state_pass_kernel": (304.157952e6 + 289.087744e6, 4096, "2eeae5eaf22d63e9",
+    "state_pass_kernel": (304.151296e6 + 289.067008e6, 4096, "a492962f1c96c2cf",
                           ("kda_state_pass.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
                            "kda_split.cuh", "kda_common.cuh")),
     "kda_decode_step": (1.090611e9 + 1.017646e9, 16384, "d7fab05fc3519b6c",

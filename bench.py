@@ -67,7 +67,7 @@ def state_bytes(token_heads, chunk_heads, full_chunk_heads, seq_heads, dk, dv):
 # recorded with the capture (else the kernel has changed since: null).
 _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
 PROFILED_TRAFFIC = {
-    "prefill_tc_kernel<prep>": (269.051136e6 + 250.364672e6, 4096, "302d4d3c920be85e",
+    "prefill_tc_kernel<prep>": (269.051136e6 + 250.364672e6, 4096, "733acfdaf611aa8b",
                                 ("kda_prefill_tc.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
                                  "kda_split.cuh", "kda_common.cuh")),
     "state_pass_kernel": (304.151296e6 + 289.067008e6, 4096, "a492962f1c96c2cf",

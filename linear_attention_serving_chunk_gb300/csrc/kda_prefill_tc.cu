@@ -35,9 +35,10 @@
 //           double-buffered, k/v refilled as soon as their MMAs finish)
 //   SIMT    gate exp(g), per-sub-tile running products, then every scaled
 //           operand in place: k -> K e^G, q -> -(Q e^G), z -> K e^{G_last-G}
-//   MMA     A_kk and P (2 x M128 N64 K128, tf32), T on the CUDA cores (blocked
-//           16x16 forward substitution, fp32), Wk = T' K~ and U = T' V
-//           (M128 N128 K64; U lands in the output accumulator D1)
+//   MMA     A_kk and P (2 x M128 N64 K128, tf32); T on the CUDA cores (the
+//           16x16 diagonal blocks by column updates in fp32, the others as
+//           (I - E + E^2 - E^3) D with warp-level tf32 products); Wk = T' K~
+//           and U = T' V (M128 N128 K64; U lands in the output accumulator D1)
 //   serial  D1 += [-Wk; -Q~] S_fp16  (W in rows 0..63, -Q~S in rows 64..127)
 //           S_tm = e^{G_last} S_tm + K'^T W   (fp32 state kept in TMEM)
 //           D1 += [0; -P] W                   (-O in rows 64..127)
@@ -113,8 +114,8 @@ constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t TM_COLS_PREP = 256;  // chunk preparation: no state
 
 constexpr uint32_t kWaitPolls = 1u << 24;
-// TMA loads are issued by lane 0 of warp 4 (a warp with no output stores),
-// the MMAs by thread 0.
+// TMA loads are issued by lane 0 of warp 4 (a warp with no output stores;
+// in chunk preparation only those of k and v), the MMAs by thread 0.
 constexpr int kTmaThread = 128;
 // Chunk preparation: lane 0 of warps 4..7 each store one part of the record
 // (and later wait for its own bulk group); warps 12..15 build nothing in the

@@ -573,6 +573,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (rec_thread) bulk_wait_read0();
     if (!wait_all(bar_k, n & 1)) { aborted = true; break; }  // also orders the Lam table
     k_pending = false;
+    if (L < 64) {
+      // A partial chunk: rows L..63 of k and q hold other tokens (or the TMA
+      // fill); zero them once, so that the operand passes need no per-row test.
+      // A row is 2 x 128 bytes in each tile (two 64-channel regions).
+      for (int x = tid; x < (64 - L) * 32; x += TC_THREADS) {
+        const int r = L + (x >> 5), c = x & 31;
+        const uint32_t reg = static_cast<uint32_t>((c >> 3) & 1), ch = static_cast<uint32_t>(c & 7);
+        const uint32_t addr =
+            c < 16 ? sb + SM_KB + reg * REG64 + static_cast<uint32_t>(r) * 128u + ch * 16u
+                   : a3 + reg * REG128 + static_cast<uint32_t>(64 + r) * 128u + ch * 16u;
+        S.u128(addr) = make_uint4(0, 0, 0, 0);
+      }
+      __syncthreads();
+    }
 
     const bool l2n = (p.pre & KDA_PRE_L2NORM_QK) != 0;
     if (l2n) {
@@ -671,10 +685,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               kk.y *= __uint_as_float(nr.x);
               qq.x *= __uint_as_float(nr.y);
               qq.y *= __uint_as_float(nr.y);
-            }
-            if (r >= L) {
-              kk = make_float2(0.f, 0.f);
-              qq = make_float2(0.f, 0.f);
             }
             const float ke0 = kk.x * ef0[j], ke1 = kk.y * ef1[j];
             const float qe0 = qq.x * ef0[j], qe1 = qq.y * ef1[j];

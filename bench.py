@@ -67,10 +67,10 @@ def state_bytes(token_heads, chunk_heads, full_chunk_heads, seq_heads, dk, dv):
 # recorded with the capture (else the kernel has changed since: null).
 _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
 PROFILED_TRAFFIC = {
-    "prefill_tc_kernel<prep>": (269.051136e6 + 250.364672e6, 4096, "733acfdaf611aa8b",
+    "prefill_tc_kernel<prep>": (269.252352e6 + 250.642944e6, 4096, "4e96eed0f04c6a83",
                                 ("kda_prefill_tc.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
                                  "kda_split.cuh", "kda_common.cuh")),
-    "state_pass_kernel": (304.151296e6 + 289.067008e6, 4096, "a492962f1c96c2cf",
+    "state_pass_kernel": (304.155136e6 + 289.254656e6, 4096, "a492962f1c96c2cf",
                           ("kda_state_pass.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
                            "kda_split.cuh", "kda_common.cuh")),
     "kda_decode_step": (1.090611e9 + 1.017646e9, 16384, "d7fab05fc3519b6c",

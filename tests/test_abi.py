@@ -141,6 +141,31 @@ def test_workspace_query_is_pure_host(L):
     assert L.kda_chunk_fwd_workspace_bytes(4, 4 * 8192, 16, 128, 128, 64) >= 0
 
 
+REC = 73 * 1024  # one (chunk, head) record of the two-pass prefill
+
+
+@pytest.mark.parametrize("n_seq,total,H,dk,dv,chunk,expect", [
+    # the bench workload: two passes, records of every head for ceil(T/64) + n_seq
+    # chunks after a 1 KiB chunk-start table
+    (4, 4 * 8192, 16, 128, 128, 64, 1024 + (512 + 4) * 16 * REC),
+    # one 2^20-token sequence, 16 heads: the segment scan (64 segments of 16,384
+    # tokens: three [64, 16, 128, 128] fp32 arrays) plus every chunk's record
+    (1, 1 << 20, 16, 128, 128, 64, 3 * 64 * 16 * 128 * 128 * 4 + (1 << 14) * 16 * REC),
+    # too short for four segments of at least 4096 tokens: two passes
+    (1, 8192, 4, 128, 128, 64, 1024 + (128 + 1) * 4 * REC),
+    # other head sizes run on the CUDA cores without a workspace
+    (1, 256, 2, 64, 64, 64, 0),
+    # only chunk = 64 exists
+    (4, 4 * 8192, 16, 128, 128, 32, 0),
+])
+def test_workspace_bytes_formula(L, n_seq, total, H, dk, dv, chunk, expect):
+    """The sizes include/kda.h documents for kda_chunk_fwd_workspace_bytes."""
+    L.kda_chunk_fwd_workspace_bytes.restype = ctypes.c_size_t
+    L.kda_chunk_fwd_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    assert L.kda_chunk_fwd_workspace_bytes(n_seq, total, H, dk, dv, chunk) == expect
+
+
 def test_python_binding_fails_loudly_without_cuda_tensors(L):
     import torch
     x = torch.zeros(64, 1, 64, dtype=torch.bfloat16)

@@ -1,10 +1,13 @@
 """KDA prefill / decode benchmark on GB300.
 
-One step = one kda_chunk_fwd over the prefill workload B=4, H=16, T=8192,
-dk=dv=128, chunk=64, with the final state and every chunk-boundary snapshot
-written (inputs larger than L2).  The decode step (512 x 32 resident states,
-dk=dv=128, 1000 chained steps) is measured in the same run and reported as
-its own object.  Prints ONE JSON line on rank 0.
+One step = one kda_chunk_fwd over the packed varlen prefill workload (64
+sequences of U[512, 32768] tokens, seeded; H = 32, dk = dv = 128, chunk 64,
+initial states given; final states and every chunk-boundary snapshot written;
+inputs far larger than L2), the largest single-GPU configuration.  The same
+run reports, as their own objects, the B=4 H=16 T=8192 prefill, the
+1,048,576-token prefill, the decode step (512 x 32 resident states, 1000
+chained steps) and the latency of the tiny B=1 H=2 T=256 dk=dv=64 prefill.
+Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -30,7 +33,7 @@ if ROOT not in sys.path:
 
 METRIC = "KDA prefill tokens/s and decode steps/s on 1 GB300; % of TC / HBM roofline"
 UNIT = "tokens/s"
-WORKLOAD = "mid"
+WORKLOAD = "varlen"
 
 # Algorithmic traffic and work per token-head at chunk 64 (bf16 in/out, fp32 states):
 #   q, k, z (dk each), v, o (dv each) in bf16 plus beta: 2 (3 dk + 2 dv) + 2 bytes;
@@ -38,10 +41,17 @@ WORKLOAD = "mid"
 #   flops: 6 dk dv + 64 (3 dk + 2 dv) + 64^2 / 3 (causal halves once, masked tiles not counted).
 
 
-def prefill_bytes(token_heads, seq_heads, dk, dv, snapshots=True, s0=False, s_final=True):
+def prefill_bytes(token_heads, seq_heads, dk, dv, snapshots=True, s0=False, s_final=True,
+                  full_chunk_heads=None):
+    """Bytes the prefill must move: inputs, outputs, snapshots, S0 / S_final.
+    Snapshots follow every full chunk (token_heads / 64 of them for lengths
+    that are multiples of 64; pass full_chunk_heads otherwise)."""
     b = token_heads * (2 * (3 * dk + 2 * dv) + 2)
     if snapshots:
-        b += token_heads * 4 * dk * dv // 64
+        if full_chunk_heads is None:
+            b += token_heads * 4 * dk * dv // 64
+        else:
+            b += full_chunk_heads * 4 * dk * dv
     b += seq_heads * 4 * dk * dv * (int(s0) + int(s_final))
     return b
 
@@ -49,33 +59,27 @@ def prefill_bytes(token_heads, seq_heads, dk, dv, snapshots=True, s0=False, s_fi
 REC_BYTES = 74240  # bytes of one (chunk, head) record the two passes exchange
 
 
-def prep_bytes(token_heads, chunk_heads, dk, dv):
-    """Chunk preparation: reads q, k, z, v, beta; writes one record per chunk-head."""
-    return token_heads * (2 * (3 * dk + dv) + 2) + chunk_heads * REC_BYTES
+def prep_bytes(token_heads, dk, dv):
+    """Chunk preparation, algorithmic: it reads q, k, z, v and beta.  (It also
+    writes one record per (chunk, head): traffic the two-pass design adds,
+    reported apart as traffic_overhead.)"""
+    return token_heads * (2 * (3 * dk + dv) + 2)
 
 
-def state_bytes(token_heads, chunk_heads, full_chunk_heads, seq_heads, dk, dv):
-    """State pass: reads the records; writes o, the snapshots and the final states."""
-    return (chunk_heads * REC_BYTES + token_heads * 2 * dv + full_chunk_heads * 4 * dk * dv +
-            seq_heads * 4 * dk * dv)
+def state_bytes(token_heads, full_chunk_heads, seq_heads, dk, dv, s0=False):
+    """State pass, algorithmic: it writes o, the snapshots and the final states
+    (and reads S0 when given).  (It also reads the records.)"""
+    return (token_heads * 2 * dv + full_chunk_heads * 4 * dk * dv +
+            seq_heads * 4 * dk * dv * (1 + int(s0)))
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch from
-# the ncu captures summarised under profiles/, taken on 4096 (chunk, head)
-# tasks (B=4 H=16 T=4096) and scaled here by the tasks of the timed launch.
-# They are reported only while the kernel's sources hash to the sha256 prefix
-# recorded with the capture (else the kernel has changed since: null).
+# the ncu captures summarised under profiles/, per (chunk, head) task of the
+# captured launch, scaled here by the tasks of the timed launch.  They are
+# reported only while the kernel's sources hash to the sha256 prefix recorded
+# with the capture (else the kernel has changed since: null).
 _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
-PROFILED_TRAFFIC = {
-    "prefill_tc_kernel<prep>": (269.252352e6 + 250.642944e6, 4096, "4e96eed0f04c6a83",
-                                ("kda_prefill_tc.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
-                                 "kda_split.cuh", "kda_common.cuh")),
-    "state_pass_kernel": (304.155136e6 + 289.254656e6, 4096, "a492962f1c96c2cf",
-                          ("kda_state_pass.cu", "kda_tc_common.cuh", "kda_sm100.cuh",
-                           "kda_split.cuh", "kda_common.cuh")),
-    "kda_decode_step": (1.090611e9 + 1.017646e9, 16384, "d7fab05fc3519b6c",
-                        ("kda_decode.cu", "kda_common.cuh")),
-}
+PROFILED_TRAFFIC = {}
 
 
 def profiled_traffic(kernel, tasks):
@@ -222,12 +226,58 @@ def init_pg(world):
             dist.init_process_group("gloo")
 
 
+# --- workloads ---------------------------------------------------------------------------------
+
+_OVERRIDE = {}  # --seq-len / --n-seq of the headline workload (profiling runs)
+
+
+def workload_params(name):
+    import kda_inputs
+    w = dict(kda_inputs.WORKLOADS[name])
+    if name == WORKLOAD:
+        if _OVERRIDE.get("seq_len") and w["kind"] == "prefill":
+            w["T"] = _OVERRIDE["seq_len"]
+        if _OVERRIDE.get("n_seq"):
+            w["n_seq" if w["kind"] == "varlen" else "B"] = _OVERRIDE["n_seq"]
+    return w
+
+
+def workload_lengths(name):
+    import kda_inputs
+    w = workload_params(name)
+    if w["kind"] == "varlen":
+        return kda_inputs.varlen_lengths(w["n_seq"], w["len_lo"], w["len_hi"], w["seed"])
+    return [w["T"]] * w["B"]
+
+
+def make_workload(name, device):
+    import kda_inputs
+    w = workload_params(name)
+    return kda_inputs.make_prefill(w["H"], w["dk"], w["dv"], workload_lengths(name), w["seed"],
+                                   device, S0_std=w.get("S0_std"))
+
+
+def workload_config(name):
+    w = workload_params(name)
+    L = workload_lengths(name)
+    total = sum(L)
+    if w["kind"] == "varlen":
+        desc = (f"kda varlen prefill: {w['n_seq']} packed sequences, lengths "
+                f"U[{w['len_lo']}, {w['len_hi']}] (seed {w['seed']}, {total} tokens), "
+                f"H={w['H']} dk={w['dk']} dv={w['dv']} chunk={w['chunk']}, cu_seqlens, "
+                f"S0 ~ N(0, {w['S0_std']}^2), final states + chunk snapshots")
+    else:
+        desc = (f"kda prefill B={w['B']} H={w['H']} T={w['T']} dk={w['dk']} dv={w['dv']} "
+                f"chunk={w['chunk']}, final state + chunk snapshots")
+    return {"workload": desc, "global_batch": len(L), "seq_len": max(L), "tokens": total,
+            "heads": w["H"], "l2": "inputs larger than L2 (129 MB) by far, no flush"}
+
+
 # --- reference arm: the fp64 oracle on the host cores --------------------------------------
 
 def oracle_sample(x, n_tokens):
     """Host fp64 copies of the first n_tokens of every sequence, all heads."""
     import numpy as np
-    import torch
     import kda_inputs
     cu = x["cu_seqlens"].cpu().numpy()
     parts = {n: [] for n in ("q", "k", "v", "z", "beta")}
@@ -239,8 +289,8 @@ def oracle_sample(x, n_tokens):
             parts[n].append(kda_inputs.to_f64(x[n][a:a + L]))
     cat = {n: np.concatenate(parts[n]) for n in parts}
     cat["A"] = kda_inputs.to_f64(x["A"])
+    cat["S0"] = None if x.get("S0") is None else kda_inputs.to_f64(x["S0"])
     cat["cu"] = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
-    del torch
     return cat, int(sum(lens))
 
 
@@ -250,50 +300,159 @@ def time_oracle(cat, steps):
     for _ in range(steps):
         t = time.perf_counter()
         oracle.prefill(cat["q"], cat["k"], cat["v"], cat["z"], cat["beta"], cat["A"],
-                       cu_seqlens=cat["cu"], snapshots=True)
+                       cu_seqlens=cat["cu"], S0=cat["S0"], snapshots=True)
         dts.append(time.perf_counter() - t)
     return dts
 
 
+def sample_desc(name, n_tok_seq, n_tok):
+    w = workload_params(name)
+    n_seq = len(workload_lengths(name))
+    return (f"first {n_tok_seq} tokens of each of the {n_seq} sequences, all {w['H']} heads "
+            f"({n_tok * w['H']} token-heads per step), S0 and snapshots as the workload")
+
+
 def run_reference(args, rank, world):
+    """The oracle on the host cores: each step runs it over the first
+    --ref-tokens tokens of every sequence of the workload (all heads), drawn
+    with the workload's recipe and seed; only that sample is generated, the
+    whole workload would not fit the host's time budget."""
     import kda_inputs
     import oracle
     if rank != 0:
         return
-    w = kda_inputs.WORKLOADS[WORKLOAD]
-    x = kda_inputs.make_workload_prefill(WORKLOAD, device="cpu")
+    w = workload_params(WORKLOAD)
+    lens = [min(args.ref_tokens, L) for L in workload_lengths(WORKLOAD)]
+    x = kda_inputs.make_prefill(w["H"], w["dk"], w["dv"], lens, w["seed"], "cpu",
+                                S0_std=w.get("S0_std"))
     cat, n_tok = oracle_sample(x, args.ref_tokens)
-    H = w["H"]
     time_oracle(cat, args.warmup)
     dts = time_oracle(cat, args.steps)
     total = sum(dts)
     value = n_tok * args.steps / total  # tokens (all H heads) per second
     cores = oracle.num_threads()
-    sample = (f"first {args.ref_tokens} tokens of each of the {w['B']} sequences, all {H} heads "
-              f"({n_tok * H} token-heads per step), snapshots on")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": workload_config(w),
+            "data": "synthetic", "config": workload_config(WORKLOAD),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample_desc(WORKLOAD, args.ref_tokens, n_tok)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w):
-    return {"workload": f"kda prefill B={w['B']} H={w['H']} T={w['T']} dk={w['dk']} "
-                        f"dv={w['dv']} chunk={w['chunk']}, final state + chunk snapshots",
-            "global_batch": w["B"], "seq_len": w["T"], "heads": w["H"],
-            "l2": "inputs larger than L2 (~1.2 GB of HBM traffic per step), no flush"}
-
-
 # --- our arm ------------------------------------------------------------------------------------
 
+def prefill_buffers(kda, x, dev, with_ws=True):
+    import torch
+    total, H, dk = x["k"].shape
+    dv = x["v"].shape[2]
+    n_seq = len(x["lengths"])
+    offs = kda.snapshot_offsets(x["lengths"], device=dev)
+    b = {"offs": offs,
+         "snaps": torch.empty((int(offs[-1]), H, dk, dv), dtype=torch.float32, device=dev),
+         "S_final": torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev),
+         "o": torch.empty((total, H, dv), dtype=torch.bfloat16, device=dev)}
+    if with_ws:
+        b["ws"] = torch.empty(max(kda.workspace_bytes(n_seq, total, H, dk, dv), 1),
+                              dtype=torch.uint8, device=dev)
+    return b
+
+
+def time_two_pass(kda, x, b, stream, steps, warmup, world, clock_gpu=None):
+    """Time `steps` prefill steps, each the two passes as split-phase calls
+    (chunk preparation, then the state pass) with CUDA events around each on
+    the launching stream; returns the per-pass mean times, the step time and
+    the clock summary when a GPU id is given."""
+    import torch
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                      cu_seqlens=x["cu_seqlens"], S0=x.get("S0"), o=b["o"],
+                      S_final=b["S_final"], snaps=b["snaps"], snap_offsets=b["offs"],
+                      workspace=b["ws"], pre=kda.PASS_PREPARE, stream=stream)
+        if e is not None:
+            e[1].record(stream)
+        kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                      cu_seqlens=x["cu_seqlens"], S0=x.get("S0"), o=b["o"],
+                      S_final=b["S_final"], snaps=b["snaps"], snap_offsets=b["offs"],
+                      workspace=b["ws"], pre=kda.PASS_STATE, stream=stream)
+        if e is not None:
+            e[2].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if kda.device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(clock_gpu) if clock_gpu is not None else None
+    if clocks is not None:
+        clocks.__enter__()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    h0 = time.monotonic()
+    t0.record(stream)
+    for i in range(steps):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.window(h0, time.monotonic())
+        clocks.__exit__(None, None, None)
+    barrier(world)
+    if kda.device_status() != 0:
+        raise RuntimeError("device status word set during the timed steps")
+    return {"elapsed_ms": reduce_max(t0.elapsed_time(t1), world),
+            "prep_s": statistics.mean(a.elapsed_time(bb) for a, bb, _ in ev) / 1e3,
+            "state_s": statistics.mean(bb.elapsed_time(c) for _, bb, c in ev) / 1e3,
+            "step_s": statistics.mean(a.elapsed_time(c) for a, _, c in ev) / 1e3,
+            "clocks": clocks.summary() if clocks is not None else None}
+
+
+def prefill_roofline(name, t, hbm_peak, tc_peak, peak_src, s0):
+    """Roofline of the dominant kernel of one prefill step (algorithmic bytes)
+    and of the whole step."""
+    w = workload_params(name)
+    L = workload_lengths(name)
+    H, dk, dv = w["H"], w["dk"], w["dv"]
+    token_heads = sum(L) * H
+    chunk_heads = sum((l + 63) // 64 for l in L) * H
+    full_heads = sum(l // 64 for l in L) * H
+    seq_heads = len(L) * H
+    kernels = {
+        "prefill_tc_kernel<prep>": (t["prep_s"], prep_bytes(token_heads, dk, dv)),
+        "state_pass_kernel": (t["state_s"], state_bytes(token_heads, full_heads, seq_heads, dk,
+                                                        dv, s0=s0)),
+    }
+    dom = max(kernels, key=lambda k: kernels[k][0])
+    dom_s, dom_bytes = kernels[dom]
+    achieved = dom_bytes / dom_s / 1e9
+    alg = prefill_bytes(token_heads, seq_heads, dk, dv, s0=s0, full_chunk_heads=full_heads)
+    flops = prefill_flops(token_heads, dk, dv)
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "traffic": profiled_traffic(dom, chunk_heads),
+            "kernel": dom, "bytes_per_launch": dom_bytes, "launch_ms": 1e3 * dom_s,
+            "peak_source": peak_src + " (HBM copy bandwidth)",
+            "passes_ms": {k: 1e3 * v[0] for k, v in kernels.items()},
+            "traffic_overhead": {
+                "what": "the two-pass records: written by the chunk preparation, read by the "
+                        "state pass (not algorithmic bytes)",
+                "bytes_per_step": 2 * chunk_heads * REC_BYTES},
+            "path": {"what": "whole prefill step (both passes) against the algorithmic bytes "
+                             "of its inputs and outputs",
+                     "bytes": alg, "achieved": alg / t["step_s"] / 1e9,
+                     "frac": alg / t["step_s"] / 1e9 / hbm_peak},
+            "tensor": {"achieved_tflops": flops / t["step_s"] / 1e12, "peak_tflops": tc_peak,
+                       "frac": flops / t["step_s"] / 1e12 / tc_peak}}
+
+
 def run_ours(args, rank, world, local):
-    import numpy as np
     import torch
 
     import kda_inputs
@@ -304,123 +463,82 @@ def run_ours(args, rank, world, local):
     kda.build()
     kda.lib()
     hbm_peak, tc_peak, tc_sus, peak_src = load_peaks()
-    w = dict(kda_inputs.WORKLOADS[WORKLOAD])
-    if args.seq_len:
-        w["T"] = args.seq_len
-    B, H, T, dk, dv = w["B"], w["H"], w["T"], w["dk"], w["dv"]
-    x = kda_inputs.make_workload_prefill(WORKLOAD, device=dev, T=T)
-    offs = kda.snapshot_offsets(x["lengths"], device=dev)
-    snaps = torch.empty((int(offs[-1]), H, dk, dv), dtype=torch.float32, device=dev)
-    S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
-    o = torch.empty((B * T, H, dv), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    ws_bytes = kda.workspace_bytes(B, B * T, H, dk, dv)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-
-    # One step = the two passes of the prefill, as two split-phase calls so
-    # that each pass is timed on its own: chunk preparation (the chunk-start
-    # table + the preparation kernel), then the state pass.
-    def step(e=None):
-        if e is not None:
-            e[0].record(stream)
-        kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
-                      cu_seqlens=x["cu_seqlens"], o=o, S_final=S_final, snaps=snaps,
-                      snap_offsets=offs, workspace=ws, pre=kda.PASS_PREPARE, stream=stream)
-        if e is not None:
-            e[1].record(stream)
-        kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
-                      cu_seqlens=x["cu_seqlens"], o=o, S_final=S_final, snaps=snaps,
-                      snap_offsets=offs, workspace=ws, pre=kda.PASS_STATE, stream=stream)
-        if e is not None:
-            e[2].record(stream)
-    launches_per_step = 3  # chunk-start table, chunk preparation, state pass
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if kda.device_status() != 0:
-        raise RuntimeError("device status word set during warm-up")
-
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid).replace("GPU-", "")
     except Exception:
         gpu_id = local
-    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
-          for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(gpu_id) as clocks:
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        h0 = time.monotonic()
-        t0.record(stream)
-        for i in range(args.steps):
-            step(ev[i])
-        t1.record(stream)
-        torch.cuda.synchronize()
-        clocks.window(h0, time.monotonic())
-    barrier(world)
-    elapsed_ms = reduce_max(t0.elapsed_time(t1), world)
-    prep_s = statistics.mean(a.elapsed_time(b) for a, b, _ in ev) / 1e3
-    state_s = statistics.mean(b.elapsed_time(c) for _, b, c in ev) / 1e3
-    step_s = statistics.mean(a.elapsed_time(c) for a, _, c in ev) / 1e3
 
-    token_heads = B * T * H
-    chunk_heads = B * ((T + 63) // 64) * H
-    value = B * T * args.steps * world / (elapsed_ms / 1e3)
-    alg_bytes = prefill_bytes(token_heads, B * H, dk, dv)
-    alg_flops = prefill_flops(token_heads, dk, dv)
-    kernels = {
-        "prefill_tc_kernel<prep>": (prep_s, prep_bytes(token_heads, chunk_heads, dk, dv)),
-        "state_pass_kernel": (state_s, state_bytes(token_heads, chunk_heads,
-                                                    B * (T // 64) * H, B * H, dk, dv)),
-    }
-    dom = max(kernels, key=lambda k: kernels[k][0])
-    dom_s, dom_bytes = kernels[dom]
-    achieved = dom_bytes / dom_s / 1e9
-    traffic = args.traffic if args.traffic is not None else profiled_traffic(dom, chunk_heads)
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": traffic, "kernel": dom,
-                "bytes_per_launch": dom_bytes, "launch_ms": 1e3 * dom_s,
-                "peak_source": peak_src,
-                "passes_ms": {k: 1e3 * t for k, (t, _) in kernels.items()},
-                "path": {"what": "whole prefill step (both passes), algorithmic bytes of the "
-                                 "inputs and outputs only",
-                         "achieved": alg_bytes / step_s / 1e9,
-                         "frac": alg_bytes / step_s / 1e9 / hbm_peak},
-                "tensor": {"achieved_tflops": alg_flops / step_s / 1e12,
-                           "peak_tflops": tc_peak,
-                           "frac": alg_flops / step_s / 1e12 / tc_peak}}
-
-    e2e = None if args.no_e2e else run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world,
-                                           B, T)
-    decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak, peak_src, world)
-    long_ctx = None if args.no_long else run_long(args, dev, stream, hbm_peak, peak_src, world)
+    # the headline: the packed varlen prefill
+    x = make_workload(WORKLOAD, dev)
+    b = prefill_buffers(kda, x, dev)
+    t = time_two_pass(kda, x, b, stream, args.steps, args.warmup, world, clock_gpu=gpu_id)
+    n_tok = x["k"].shape[0]
+    value = n_tok * args.steps * world / (t["elapsed_ms"] / 1e3)
+    roofline = prefill_roofline(WORKLOAD, t, hbm_peak, tc_peak, peak_src,
+                                s0=x.get("S0") is not None)
 
     cpu_baseline = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
-        cat, n_tok = oracle_sample(x, args.ref_tokens)
+        cat, n_s = oracle_sample(x, args.cpu_tokens)
         dts = time_oracle(cat, 1)
-        cpu_baseline = {"value": n_tok / dts[0], "unit": UNIT, "cores": oracle.num_threads(),
-                        "kind": "oracle",
-                        "sample": f"first {args.ref_tokens} tokens of each of the {B} sequences,"
-                                  f" all {H} heads ({n_tok * H} token-heads), snapshots on"}
+        cpu_baseline = {"value": n_s / dts[0], "unit": UNIT, "cores": oracle.num_threads(),
+                        "kind": "oracle", "sample": sample_desc(WORKLOAD, args.cpu_tokens, n_s)}
+    e2e = None if args.no_e2e else run_e2e(args, x, b, stream, world)
+    del x, b
+    torch.cuda.empty_cache()
+
+    mid = None if args.no_mid else run_mid(args, dev, stream, hbm_peak, tc_peak, peak_src, world)
+    long_ctx = None if args.no_long else run_long(args, dev, stream, hbm_peak, peak_src, world)
+    decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak, peak_src, world)
+    tiny = None if args.no_tiny else run_tiny(args, dev, stream, world)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+                "ms_per_step": t["elapsed_ms"] / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": kda_dtype(),
-                "data": "synthetic", "config": workload_config(w),
-                "clocks": clocks.summary(), "roofline": roofline, "cpu_baseline": cpu_baseline,
-                "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "decode": decode,
-                "long_context": long_ctx}
+                "data": "synthetic", "config": workload_config(WORKLOAD),
+                "clocks": t["clocks"], "roofline": roofline, "cpu_baseline": cpu_baseline,
+                "e2e": e2e, "gpu_launches": 3 * args.steps,
+                "mid": mid, "long_context": long_ctx, "decode": decode, "tiny": tiny}
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world, B, T):
+def host_mem_available():
+    """Bytes of host memory this process may still use (MemAvailable, capped
+    by a cgroup limit when there is one)."""
+    avail = None
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    for path in ("/sys/fs/cgroup/memory.max", "/sys/fs/cgroup/memory/memory.limit_in_bytes"):
+        try:
+            with open(path) as f:
+                lim = f.read().strip()
+            if lim.isdigit():
+                used = 0
+                for upath in ("/sys/fs/cgroup/memory.current",
+                              "/sys/fs/cgroup/memory/memory.usage_in_bytes"):
+                    try:
+                        with open(upath) as g:
+                            used = int(g.read().strip())
+                        break
+                    except OSError:
+                        continue
+                room = int(lim) - used
+                avail = room if avail is None else min(avail, room)
+        except OSError:
+            continue
+    return avail
+
+
+def run_e2e(args, x, b, stream, world):
     """The same step through the public API with host buffers: every step copies
     its inputs from pinned host memory to the device, runs kda_chunk_fwd
     (snapshots included) and copies its result, o and the final states, back
@@ -428,72 +546,53 @@ def run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world, B, T):
     stay in device memory: they are the prefix cache, which kda_state_snapshot
     restores from there.  Steps are pipelined over two buffer slots on three
     streams (inputs in, compute, outputs out), as a serving loop would run
-    them: step i's outputs go back while step i+1's inputs come in."""
+    them: step i's outputs go back while step i+1's inputs come in.  The
+    compute of the steps is serialised on one stream, so the snapshot array
+    and the workspace are shared by the slots."""
     import torch
 
     import linear_attention_serving_chunk_gb300 as kda
-    dev = o.device
-    names_in = ("q", "k", "v", "z", "beta", "A", "cu_seqlens")
+    dev = b["o"].device
+    names_in = ("q", "k", "v", "z", "beta", "A", "cu_seqlens", "S0")
+    h2d = sum(x[n].numel() * x[n].element_size() for n in names_in)
+    d2h = sum(b[n].numel() * b[n].element_size() for n in ("o", "S_final"))
+    avail = host_mem_available()
+    if avail is not None and 2 * (h2d + d2h) > avail:
+        return {"value": None, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "skipped": f"needs {(h2d + d2h) / 1e9:.1f} GB of pinned host memory, "
+                           f"{avail / 1e9:.1f} GB available"}
     host_in = {n: x[n].cpu().pin_memory() for n in names_in}
-    host_out = {"o": torch.empty_like(o, device="cpu").pin_memory(),
-                "S_final": torch.empty_like(S_final, device="cpu").pin_memory()}
-    slots = [{"in": {n: torch.empty_like(t, device=dev) for n, t in host_in.items()},
-              "out": {"o": o if i == 0 else torch.empty_like(o),
-                      "S_final": S_final if i == 0 else torch.empty_like(S_final),
-                      "snaps": snaps if i == 0 else torch.empty_like(snaps)}}
-             for i in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    # Copies can be split over NCS streams per direction (big tensors in
-    # slices along their first dimension); on GB300 four streams per direction
-    # measured no faster than one (the host link is the limit, ~275 GB/s for
-    # both directions together), so one each.
-    NCS = 1
-
-    def pieces(src, dst):
-        out = []
-        for n, t in src.items():
-            k = NCS if t.shape[0] >= NCS and t.numel() * t.element_size() > (64 << 20) else 1
-            step = (t.shape[0] + k - 1) // k
-            for a0 in range(0, t.shape[0], step):
-                out.append((t[a0:a0 + step], dst[n][a0:a0 + step]))
-        return out
-
-    s_comp = torch.cuda.Stream(dev)
-    s_in = [torch.cuda.Stream(dev) for _ in range(NCS)]
-    s_out = [torch.cuda.Stream(dev) for _ in range(NCS)]
-    ev = {"in": [[torch.cuda.Event() for _ in range(NCS)] for _ in range(2)],
-          "out": [[torch.cuda.Event() for _ in range(NCS)] for _ in range(2)],
-          "comp": [torch.cuda.Event() for _ in range(2)]}
-    copies_in = [pieces(host_in, slots[sl]["in"]) for sl in range(2)]
-    copies_out = [pieces({n: slots[sl]["out"][n] for n in host_out}, host_out) for sl in range(2)]
+    host_out = {n: torch.empty_like(b[n], device="cpu").pin_memory() for n in ("o", "S_final")}
+    slots = [{"in": {n: x[n] for n in names_in}, "out": {"o": b["o"], "S_final": b["S_final"]}},
+             {"in": {n: torch.empty_like(x[n]) for n in names_in},
+              "out": {"o": torch.empty_like(b["o"]), "S_final": torch.empty_like(b["S_final"])}}]
+    s_comp, s_in, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "out", "comp")}
     used = [False, False]
 
     def e2e_step(i):
         sl = i & 1
         d = slots[sl]
-        for j, st in enumerate(s_in):
-            if used[sl]:  # this slot's previous compute has read its inputs
-                st.wait_event(ev["comp"][sl])
-            with torch.cuda.stream(st):
-                for src, dst in copies_in[sl][j::NCS]:
-                    dst.copy_(src, non_blocking=True)
-            ev["in"][sl][j].record(st)
-            s_comp.wait_event(ev["in"][sl][j])
+        if used[sl]:  # this slot's previous compute has read its inputs
+            s_in.wait_event(ev["comp"][sl])
+        with torch.cuda.stream(s_in):
+            for n in names_in:
+                d["in"][n].copy_(host_in[n], non_blocking=True)
+        ev["in"][sl].record(s_in)
+        s_comp.wait_event(ev["in"][sl])
         if used[sl]:  # and its previous outputs have left
-            for j in range(NCS):
-                s_comp.wait_event(ev["out"][sl][j])
+            s_comp.wait_event(ev["out"][sl])
         kda.chunk_fwd(d["in"]["q"], d["in"]["k"], d["in"]["v"], d["in"]["z"], d["in"]["beta"],
-                      d["in"]["A"], cu_seqlens=d["in"]["cu_seqlens"], o=d["out"]["o"],
-                      S_final=d["out"]["S_final"], snaps=d["out"]["snaps"], snap_offsets=offs,
-                      workspace=ws, stream=s_comp)
+                      d["in"]["A"], cu_seqlens=d["in"]["cu_seqlens"], S0=d["in"]["S0"],
+                      o=d["out"]["o"], S_final=d["out"]["S_final"], snaps=b["snaps"],
+                      snap_offsets=b["offs"], workspace=b["ws"], stream=s_comp)
         ev["comp"][sl].record(s_comp)
-        for j, st in enumerate(s_out):
-            st.wait_event(ev["comp"][sl])
-            with torch.cuda.stream(st):
-                for src, dst in copies_out[sl][j::NCS]:
-                    dst.copy_(src, non_blocking=True)
-            ev["out"][sl][j].record(st)
+        s_out.wait_event(ev["comp"][sl])
+        with torch.cuda.stream(s_out):
+            for n in ("o", "S_final"):
+                host_out[n].copy_(d["out"][n], non_blocking=True)
+        ev["out"][sl].record(s_out)
         used[sl] = True
 
     for i in range(2):  # warm-up: both slots once
@@ -502,29 +601,49 @@ def run_e2e(args, x, o, S_final, snaps, offs, ws, stream, world, B, T):
     e2e_steps = max(2, min(args.steps, 10))
     barrier(world)
     a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
+    bb = torch.cuda.Event(enable_timing=True)
     a.record(s_comp)
-    for st in s_in:
-        st.wait_event(a)
+    s_in.wait_event(a)
     for i in range(e2e_steps):
         e2e_step(i)
-    for j in range(NCS):  # the end waits for every stream's last copy
-        s_comp.wait_event(ev["out"][(e2e_steps - 1) & 1][j])
-    b.record(s_comp)
+    s_comp.wait_event(ev["out"][(e2e_steps - 1) & 1])  # the end waits for the last copy out
+    bb.record(s_comp)
     torch.cuda.synchronize()
-    e2e_ms = reduce_max(a.elapsed_time(b), world)
-    e2e = {"value": B * T * e2e_steps * world / (e2e_ms / 1e3), "unit": UNIT,
+    e2e_ms = reduce_max(a.elapsed_time(bb), world)
+    n_tok = x["k"].shape[0]
+    out = {"value": n_tok * e2e_steps * world / (e2e_ms / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "ms_per_step": e2e_ms / e2e_steps,
            "d2h": "o and final states; the chunk snapshots are computed every step and stay in "
                   "device memory (the prefix cache)",
-           "pipelined": f"2 buffer slots; copies in and out each on {NCS} streams, compute on 1"}
-    del host_in, host_out, slots, copies_in, copies_out
-    return e2e
+           "pipelined": "2 buffer slots; copies in and out on their own streams, compute on 1"}
+    del host_in, host_out, slots
+    return out
 
 
 def kda_dtype():
     import linear_attention_serving_chunk_gb300 as kda
     return getattr(kda, "PREFILL_COMPUTE_DTYPE", "f32")
+
+
+def run_mid(args, dev, stream, hbm_peak, tc_peak, peak_src, world):
+    """The B=4 H=16 T=8192 prefill (final states and snapshots), the two passes
+    timed as in the headline."""
+    import torch
+
+    import kda_inputs
+    import linear_attention_serving_chunk_gb300 as kda
+    x = make_workload("mid", dev)
+    b = prefill_buffers(kda, x, dev)
+    steps = max(args.steps, 50)
+    t = time_two_pass(kda, x, b, stream, steps, args.warmup, world)
+    n_tok = x["k"].shape[0]
+    del x, b
+    torch.cuda.empty_cache()
+    return {"value": n_tok * steps * world / (t["elapsed_ms"] / 1e3), "unit": UNIT,
+            "ms_per_step": t["elapsed_ms"] / steps, "steps": steps,
+            "workload": workload_config("mid")["workload"],
+            "roofline": prefill_roofline("mid", t, hbm_peak, tc_peak, peak_src, s0=False)}
 
 
 def run_decode(args, dev, stream, hbm_peak, peak_src, world):
@@ -611,6 +730,7 @@ def run_long(args, dev, stream, hbm_peak, peak_src, world):
     ms = reduce_max(a.elapsed_time(b), world) / n
     nbytes = prefill_bytes(B * T * H, B * H, dk, dv)
     del x, snaps, o, ws
+    torch.cuda.empty_cache()
     return {"value": B * T * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": n,
             "workload": f"kda prefill B={B} H={H} T={T} dk={dk} dv={dv} chunk=64, final state + "
                         "chunk snapshots",
@@ -620,26 +740,75 @@ def run_long(args, dev, stream, hbm_peak, peak_src, world):
                      "peak": hbm_peak, "peak_source": peak_src}}
 
 
+def run_tiny(args, dev, stream, world):
+    """Latency of the tiny prefill (B=1, H=2, T=256, dk=dv=64, final state and
+    snapshots): launch-bound, so reported as microseconds per call, back to
+    back (no flush: its inputs fit in L2)."""
+    import torch
+
+    import kda_inputs
+    import linear_attention_serving_chunk_gb300 as kda
+    x = kda_inputs.make_workload_prefill("tiny", device=dev)
+    b = prefill_buffers(kda, x, dev)
+
+    def call():
+        kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                      cu_seqlens=x["cu_seqlens"], o=b["o"], S_final=b["S_final"],
+                      snaps=b["snaps"], snap_offsets=b["offs"], workspace=b["ws"],
+                      stream=stream)
+
+    for _ in range(10):
+        call()
+    torch.cuda.synchronize()
+    reps = args.tiny_reps
+    a = torch.cuda.Event(enable_timing=True)
+    bb = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        call()
+    bb.record(stream)
+    torch.cuda.synchronize()
+    us = reduce_max(a.elapsed_time(bb), world) * 1e3 / reps
+    return {"latency_us": us, "unit": "us per call", "reps": reps,
+            "workload": workload_config("tiny")["workload"],
+            "gpu_launches_per_call": 3,
+            "note": "launch-bound: three kernels (chunk-start table, chunk preparation, state "
+                    "pass) per call, back to back on one stream"}
+
+
 def main(argv=None):
+    global WORKLOAD
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-mid", action="store_true", help="skip the B=4 T=8192 prefill line")
     ap.add_argument("--no-long", action="store_true", help="skip the 1M-token prefill line")
+    ap.add_argument("--no-tiny", action="store_true", help="skip the tiny-prefill latency line")
     ap.add_argument("--long-steps", type=int, default=3)
+    ap.add_argument("--tiny-reps", type=int, default=1000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-tokens", type=int, default=2048,
-                    help="tokens per sequence in the oracle's bounded sample")
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu DRAM bytes per prefill launch, when measured for this kernel")
-    ap.add_argument("--seq-len", type=int, default=None,
-                    help="override T of the prefill workload (small cases for profiling)")
+    ap.add_argument("--cpu-tokens", type=int, default=2048,
+                    help="tokens per sequence in the cpu_baseline sample (one timed run)")
+    ap.add_argument("--ref-tokens", type=int, default=128,
+                    help="tokens per sequence in each step of the reference arm")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=("varlen", "mid", "long", "tiny"), default=WORKLOAD,
+                    help="prefill workload of the headline (default: the varlen batch)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override the sequence length (equal-length workloads; small cases "
+                         "for profiling)")
+    ap.add_argument("--n-seq", type=int, default=None,
+                    help="override the number of sequences (small cases for profiling)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    WORKLOAD = args.workload
+    _OVERRIDE.update(seq_len=args.seq_len, n_seq=args.n_seq)
+    if WORKLOAD == "mid":
+        args.no_mid = True
     rank, world, local = dist_setup(args.gpus)
     init_pg(world)
     if args.impl == "reference":

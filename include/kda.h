@@ -27,6 +27,18 @@
  *  - Arguments the host can check are checked before anything is launched;
  *    a rejected call returns a non-zero kda_status and enqueues nothing.
  *    A launch failure returns KDA_ERR_CUDA.  Nothing aborts, traps or throws.
+ *  - Values only the GPU sees (cu_seqlens, snap_offsets, slot and row
+ *    indices) are checked by the kernels before they are used: a malformed
+ *    entry is skipped (no memory outside the caller's arrays is touched) and
+ *    KDA_ERR_SHAPE is recorded in the device status word (kda_device_status);
+ *    the outputs of the skipped sequence or row are then undefined.
+ *  - Value range: the tensor-core prefill (dk = dv = 128) carries the state
+ *    and the chunk terms U = T diag(beta) V and W = U - Wk S through fp16
+ *    operands (fp32 accumulation).  Entries whose magnitude would exceed the
+ *    fp16 maximum 65504 are detected and recorded as KDA_ERR_RANGE in the
+ *    device status word (the outputs are then undefined, never silently
+ *    inf).  With unit q, k rows and beta in (0, 1), |v| <= 1024 and
+ *    |S0| <= 1024 stay well inside that range.
  *  - Supported sizes: dk, dv in {64, 128}; chunk = 64; -5.5 <= gmin <= 0.
  *    The chunkwise prefill rescales 16-token sub-tiles by factors up to
  *    exp(-16 * gmin); the bound keeps them inside the bf16/fp32 range
@@ -73,6 +85,15 @@ typedef uint16_t kda_bf16;                 /* raw bfloat16 bit pattern */
  * separately or to run them on different streams (order them). */
 #define KDA_PASS_PREPARE 0x100u
 #define KDA_PASS_STATE 0x200u
+
+/* Test hook of kda_chunk_fwd_ex (dk = dv = 128, no workspace): the kernel
+ * first waits, with a small poll limit, on an mbarrier that nothing arrives
+ * on, before it issues any copy or MMA; the wait gives up, KDA_ERR_TIMEOUT
+ * is recorded in the device status word and every CTA returns cleanly
+ * without writing outputs.  It exercises the bounded-wait error path of the
+ * tensor-core kernels; never set it otherwise. */
+#define KDA_TEST_STALL 0x10000u
+
 typedef struct CUstream_st *kda_stream_t;  /* same type as cudaStream_t */
 
 typedef enum {
@@ -83,7 +104,8 @@ typedef enum {
   KDA_ERR_UNSUPPORTED = 4, /* dk/dv/chunk/gmin outside the supported set */
   KDA_ERR_WORKSPACE = 5,   /* workspace missing or too small */
   KDA_ERR_CUDA = 6,        /* a CUDA launch or runtime call failed */
-  KDA_ERR_TIMEOUT = 7      /* a bounded in-kernel wait gave up (device status) */
+  KDA_ERR_TIMEOUT = 7,     /* a bounded in-kernel wait gave up (device status) */
+  KDA_ERR_RANGE = 8        /* an fp16 tensor-core operand overflowed (device status) */
 } kda_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -95,7 +117,9 @@ int kda_version(void);
 /*
  * Workspace bytes for the fastest kda_chunk_fwd path at these sizes (0 when
  * that path needs none).  Pure host arithmetic; 0 for unsupported sizes.
- *  - Equal-length batches (cu_seqlens NULL) with dk = dv = 128 whose
+ * The sizes assume cu_seqlens and snap_offsets are NULL when the call gives
+ * them as NULL; a call with snap_offsets never takes the scan below.
+ *  - Equal-length batches (cu_seqlens and snap_offsets NULL) with dk = dv = 128 whose
  *    (sequence, head) chains would fill under a quarter of the GPU (n_seq * H
  *    <= 38) and whose sequences are long run as a segment-parallel scan (each
  *    segment's zero-start state N and transition M, an fp32 chain
@@ -198,21 +222,24 @@ int kda_chunk_fwd_noalloc(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *
  * Frontier Model Gets Built, Read from the Kimi K3 Report", Technical
  * Details).  Row b of q, k, v, z, beta ([n, H, ...]) is applied to state slot
  * slots[b] of state_pool [n_slots, H, dk, dv]; slots is a device int32 [n]
- * array, or NULL for slot b.  Slots must be distinct (two rows writing one
- * slot race).  o [n, H, dv] bf16 receives S_t^T q_t (the updated state).
+ * array, or NULL for slot b (then n <= n_slots).  Slots must be distinct (two
+ * rows writing one slot race); a slot outside [0, n_slots) is skipped on the
+ * device (its row of o is not written) and recorded as KDA_ERR_SHAPE in the
+ * device status word.  o [n, H, dv] bf16 receives S_t^T q_t (the updated
+ * state).
  *   Errors: KDA_ERR_NULL, _SHAPE, _ALIGN, _UNSUPPORTED, _CUDA.
  */
 int kda_decode_step(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                     const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
-                    float *state_pool, const int32_t *slots, int n, int H, int dk, int dv,
-                    kda_bf16 *o, kda_stream_t stream);
+                    float *state_pool, int n_slots, const int32_t *slots, int n, int H, int dk,
+                    int dv, kda_bf16 *o, kda_stream_t stream);
 
 /* kda_decode_step_ex - kda_decode_step with KDA_PRE_* input pre-ops (pre = 0
  * is exactly kda_decode_step). */
 int kda_decode_step_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                        const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
-                       float *state_pool, const int32_t *slots, int n, int H, int dk, int dv,
-                       unsigned pre, kda_bf16 *o, kda_stream_t stream);
+                       float *state_pool, int n_slots, const int32_t *slots, int n, int H,
+                       int dk, int dv, unsigned pre, kda_bf16 *o, kda_stream_t stream);
 
 /*
  * kda_decode_tokens - several tokens per sequence on resident states: the
@@ -224,35 +251,45 @@ int kda_decode_step_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
  * [n_slots, H, dk, dv].  o receives every token's output.  With commit != 0
  * the state after the last token is written back to the slot (in place);
  * with commit == 0 the pool is left unchanged (verify without accepting).
- * Slots must be distinct.  cu_seqlens (int32 [n + 1]) and slots (int32 [n])
- * are device arrays.  pre: KDA_PRE_* input pre-ops (0 = none).
+ * Slots must be distinct; a slot outside [0, n_slots) is skipped on the
+ * device and recorded as KDA_ERR_SHAPE.  cu_seqlens (int32 [n + 1]) and
+ * slots (int32 [n]) are device arrays.  pre: KDA_PRE_* input pre-ops (0 =
+ * none).
  *   Errors: KDA_ERR_NULL, _SHAPE, _ALIGN, _UNSUPPORTED, _CUDA.
  */
 int kda_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                       const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
                       const int32_t *cu_seqlens, int n, int64_t total_tokens, int H, int dk,
-                      int dv, unsigned pre, float *state_pool, const int32_t *slots, int commit,
+                      int dv, unsigned pre, float *state_pool, int n_slots,
+                      const int32_t *slots, int commit,
                       kda_bf16 *o, kda_stream_t stream);
 
 /*
  * kda_state_snapshot - restore chunk-boundary states for prefix caching
  * ("state-aware prefix caching", report page, Key claims / Infrastructure):
  * for b in [0, n) copy the H x dk x dv fp32 block at row src_idx[b] of snaps
- * ([rows, H, dk, dv], as written by kda_chunk_fwd) to slot dst_slots[b] of
+ * ([n_rows, H, dk, dv], as written by kda_chunk_fwd) to slot dst_slots[b] of
  * state_pool ([n_slots, H, dk, dv]).  src_idx: device int64 [n]; dst_slots:
- * device int32 [n]; destinations must be distinct.  After it, the slot is a
- * valid S0 for kda_chunk_fwd on the suffix or a state for kda_decode_step.
+ * device int32 [n]; destinations must be distinct.  A pair with src_idx[b]
+ * outside [0, n_rows) or dst_slots[b] outside [0, n_slots) is skipped on the
+ * device and recorded as KDA_ERR_SHAPE.  After it, the slot is a valid S0
+ * for kda_chunk_fwd on the suffix or a state for kda_decode_step.
  *   Errors: KDA_ERR_NULL, _SHAPE, _ALIGN, _UNSUPPORTED, _CUDA.
  */
-int kda_state_snapshot(const float *snaps, const int64_t *src_idx, float *state_pool,
-                       const int32_t *dst_slots, int n, int H, int dk, int dv,
-                       kda_stream_t stream);
+int kda_state_snapshot(const float *snaps, int64_t n_rows, const int64_t *src_idx,
+                       float *state_pool, int n_slots, const int32_t *dst_slots, int n, int H,
+                       int dk, int dv, kda_stream_t stream);
 
 /*
  * kda_device_status - read (and with reset != 0, clear) the library's
- * device-side status word on the current device.  Kernels with bounded waits
- * record KDA_ERR_TIMEOUT there instead of hanging.  This call synchronises
- * the device.  Returns KDA_OK, KDA_ERR_TIMEOUT or KDA_ERR_CUDA.
+ * device-side status word on the current device.  Kernels record there what
+ * only the GPU can see: KDA_ERR_TIMEOUT (a bounded wait gave up instead of
+ * hanging), KDA_ERR_SHAPE (a malformed cu_seqlens / snap_offsets entry or an
+ * out-of-range slot or row index, skipped), KDA_ERR_RANGE (an fp16 operand
+ * overflowed).  The word is one per device and sticky: every call on the
+ * device ORs into it until it is reset, so calls running on different
+ * streams are not told apart.  This call synchronises the device.  Returns
+ * KDA_OK, the recorded code(s) OR-ed together, or KDA_ERR_CUDA.
  */
 int kda_device_status(int reset);
 

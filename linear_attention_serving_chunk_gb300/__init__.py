@@ -19,8 +19,8 @@ from .build import LIB_PATH, build  # noqa: F401  (re-exported)
 
 GMIN = -5.0   # "Kimi K3 Technical Report - Open Frontier Intelligence", sec. 2.1.1
 CHUNK = 64
-# Arithmetic of the dk = dv = 128 prefill: bf16 in/out with tf32 / bf16 / fp16
-# tensor-core operands, fp32 accumulation and fp32 state.
+# Arithmetic of the prefill: bf16 in/out with tf32 / bf16 / fp16 tensor-core
+# operands, fp32 accumulation and fp32 state.
 PREFILL_COMPUTE_DTYPE = "bf16"
 
 # Input pre-ops (KDA_PRE_* in kda.h): L2-normalise q, k rows; sigmoid of beta.
@@ -30,11 +30,17 @@ PRE_SIGMOID_BETA = 2
 # preparation, or only the state pass from the records it left in `workspace`.
 PASS_PREPARE = 0x100
 PASS_STATE = 0x200
+# Test hook (KDA_TEST_STALL in kda.h): the kernel gives up on a wait nothing
+# arms and records KDA_ERR_TIMEOUT in the device status word.
+TEST_STALL = 0x10000
 
 KDA_OK = 0
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_ALIGN",
                 4: "KDA_ERR_UNSUPPORTED", 5: "KDA_ERR_WORKSPACE", 6: "KDA_ERR_CUDA",
-                7: "KDA_ERR_TIMEOUT"}
+                7: "KDA_ERR_TIMEOUT", 8: "KDA_ERR_RANGE"}
+KDA_ERR_SHAPE = 2
+KDA_ERR_TIMEOUT = 7
+KDA_ERR_RANGE = 8
 
 EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_bytes",
             "kda_chunk_fwd", "kda_decode_step", "kda_state_snapshot", "kda_device_status",
@@ -78,14 +84,14 @@ def lib():
         L.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, F, P, I, I64, I, I, I, I, P, P, P,
                                             P, P, P]
         L.kda_decode_tokens.restype = I
-        L.kda_decode_tokens.argtypes = [P, P, P, P, P, P, F, P, I, I64, I, I, I, U, P, P, I, P,
-                                        P]
+        L.kda_decode_tokens.argtypes = [P, P, P, P, P, P, F, P, I, I64, I, I, I, U, P, I, P, I,
+                                        P, P]
         L.kda_decode_step.restype = I
-        L.kda_decode_step.argtypes = [P, P, P, P, P, P, F, P, P, I, I, I, I, P, P]
+        L.kda_decode_step.argtypes = [P, P, P, P, P, P, F, P, I, P, I, I, I, I, P, P]
         L.kda_decode_step_ex.restype = I
-        L.kda_decode_step_ex.argtypes = [P, P, P, P, P, P, F, P, P, I, I, I, I, U, P, P]
+        L.kda_decode_step_ex.argtypes = [P, P, P, P, P, P, F, P, I, P, I, I, I, I, U, P, P]
         L.kda_state_snapshot.restype = I
-        L.kda_state_snapshot.argtypes = [P, P, P, P, I, I, I, I, P]
+        L.kda_state_snapshot.argtypes = [P, I64, P, P, I, P, I, I, I, I, P]
         L.kda_device_status.restype = I
         L.kda_device_status.argtypes = [I]
         _lib = L
@@ -213,15 +219,17 @@ def decode_step(q, k, v, z, beta, A, state_pool, slots=None, gmin=GMIN, o=None, 
     if o is None:
         o = torch.empty((n, H, dv), dtype=torch.bfloat16, device=k.device)
     _check(o, "o", torch.bfloat16, (n, H, dv))
+    n_slots = int(state_pool.shape[0])
     if pre:
         st = lib().kda_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
-                                      float(gmin), _ptr(state_pool), _ptr(slots), int(n), int(H),
-                                      int(dk), int(dv), int(pre), _ptr(o), _stream(stream))
+                                      float(gmin), _ptr(state_pool), n_slots, _ptr(slots), int(n),
+                                      int(H), int(dk), int(dv), int(pre), _ptr(o),
+                                      _stream(stream))
         _raise_on("kda_decode_step_ex", st)
         return o
     st = lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
-                               float(gmin), _ptr(state_pool), _ptr(slots), int(n), int(H),
-                               int(dk), int(dv), _ptr(o), _stream(stream))
+                               float(gmin), _ptr(state_pool), n_slots, _ptr(slots), int(n),
+                               int(H), int(dk), int(dv), _ptr(o), _stream(stream))
     _raise_on("kda_decode_step", st)
     return o
 
@@ -250,8 +258,9 @@ def decode_tokens(q, k, v, z, beta, A, state_pool, slots, cu_seqlens, commit=Tru
     _check(o, "o", torch.bfloat16, (total, H, dv))
     st = lib().kda_decode_tokens(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
                                  float(gmin), _ptr(cu_seqlens), int(n), int(total), int(H),
-                                 int(dk), int(dv), int(pre), _ptr(state_pool), _ptr(slots),
-                                 1 if commit else 0, _ptr(o), _stream(stream))
+                                 int(dk), int(dv), int(pre), _ptr(state_pool),
+                                 int(state_pool.shape[0]), _ptr(slots), 1 if commit else 0,
+                                 _ptr(o), _stream(stream))
     _raise_on("kda_decode_tokens", st)
     return o
 
@@ -267,9 +276,9 @@ def state_snapshot(snaps, src_idx, state_pool, dst_slots, stream=None):
     _, H, dk, dv = state_pool.shape
     if tuple(snaps.shape[1:]) != (H, dk, dv):
         raise ValueError("snaps and state_pool disagree on (H, dk, dv)")
-    st = lib().kda_state_snapshot(_ptr(snaps), _ptr(src_idx), _ptr(state_pool),
-                                  _ptr(dst_slots), int(n), int(H), int(dk), int(dv),
-                                  _stream(stream))
+    st = lib().kda_state_snapshot(_ptr(snaps), int(snaps.shape[0]), _ptr(src_idx),
+                                  _ptr(state_pool), int(state_pool.shape[0]), _ptr(dst_slots),
+                                  int(n), int(H), int(dk), int(dv), _stream(stream))
     _raise_on("kda_state_snapshot", st)
 
 

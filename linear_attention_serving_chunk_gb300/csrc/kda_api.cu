@@ -8,47 +8,43 @@
 
 namespace kda {
 
-// Device status word.  Kernels with bounded waits get its address as an
-// argument and record KDA_ERR_TIMEOUT there instead of hanging.
+// Device status word.  Kernels get its address as an argument and OR into it
+// what only the GPU can see: KDA_ERR_TIMEOUT (a bounded wait gave up instead
+// of hanging), KDA_ERR_SHAPE (a malformed device-side index, skipped),
+// KDA_ERR_RANGE (an fp16 operand overflowed).
 __device__ int g_status = 0;
 
 cudaError_t decode_step_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                                const kda_bf16 *z, const kda_bf16 *beta, const float *A,
-                               float gmin, float *pool, const int32_t *slots, int n, int H,
-                               int dk, int dv, kda_bf16 *o, unsigned pre, cudaStream_t stream);
-cudaError_t snapshot_restore_launch(const float *snaps, const int64_t *src_idx, float *pool,
-                                    const int32_t *dst_slots, int n, int H, int dk, int dv,
-                                    cudaStream_t stream);
-cudaError_t prefill_simt_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
-                                const kda_bf16 *z, const kda_bf16 *beta, const float *A,
-                                float gmin, const int32_t *cu_seqlens, int n_seq,
-                                int64_t fixed_len, int H, int dk, int dv, const float *S0,
-                                kda_bf16 *o, float *S_final, float *snaps,
-                                const int64_t *snap_offsets, const int32_t *slots,
-                                unsigned pre, cudaStream_t stream);
-
+                               float gmin, float *pool, const int32_t *slots, int n_slots,
+                               int n, int H, int dk, int dv, kda_bf16 *o, unsigned pre,
+                               int *status, cudaStream_t stream);
+cudaError_t snapshot_restore_launch(const float *snaps, int64_t n_rows, const int64_t *src_idx,
+                                    float *pool, int n_slots, const int32_t *dst_slots, int n,
+                                    int H, int dk, int dv, int *status, cudaStream_t stream);
 bool prefill_tc_supported(int dk, int dv, int64_t total_tokens);
 cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                               const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
                               const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
-                              int64_t fixed_len, int H, const float *S0, kda_bf16 *o,
-                              float *S_final, float *snaps, const int64_t *snap_offsets,
-                              int *status, int zero_v, int s0_identity, const int32_t *slots,
-                              unsigned pre, cudaStream_t stream);
+                              int64_t fixed_len, int H, int dk, int dv, const float *S0,
+                              kda_bf16 *o, float *S_final, float *snaps,
+                              const int64_t *snap_offsets, int *status, int zero_v,
+                              int s0_identity, const int32_t *slots, int n_slots, unsigned pre,
+                              int test_stall, cudaStream_t stream);
 cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                               const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
                               const int32_t *cu_seqlens, const int32_t *chunk_start, int n_seq,
-                              int64_t total_tokens, int64_t fixed_len, int H, int h0, int hg,
-                              int64_t max_tasks, uint8_t *rec, int *status, unsigned pre,
-                              int n_ctas, cudaStream_t stream);
+                              int64_t total_tokens, int64_t fixed_len, int H, int dk, int dv,
+                              int h0, int hg, int64_t max_tasks, uint8_t *rec, int *status,
+                              unsigned pre, int n_ctas, cudaStream_t stream);
 cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               const int32_t *chunk_start, int n_seq, int64_t fixed_len,
-                              int64_t total_tokens, int H, int h0, int hg, const float *S0,
-                              kda_bf16 *o, float *S_final, float *snaps,
+                              int64_t total_tokens, int H, int dk, int dv, int h0, int hg,
+                              const float *S0, kda_bf16 *o, float *S_final, float *snaps,
                               const int64_t *snap_offsets, int *status, const int32_t *slots,
-                              int zero_u, int s0_identity, cudaStream_t stream);
-cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int32_t *chunk_start,
-                               cudaStream_t stream);
+                              int n_slots, int zero_u, int s0_identity, cudaStream_t stream);
+cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
+                               int32_t *chunk_start, int *status, cudaStream_t stream);
 cudaError_t segment_combine_launch(const float *M, const float *N, const float *S0,
                                    float *S_start, float *S_final, int n_seq, int n_segs, int H,
                                    cudaStream_t stream);
@@ -68,6 +64,7 @@ struct ScanPlan {
 };
 
 bool plan_scan(int n_seq, int64_t total_tokens, int H, int dk, int dv, ScanPlan *plan) {
+  // segment_combine_kernel chains 128 x 128 states
   if (dk != 128 || dv != 128 || n_seq <= 0 || total_tokens <= 0) return false;
   if (total_tokens % n_seq != 0) return false;
   const int64_t T = total_tokens / n_seq;
@@ -96,7 +93,7 @@ size_t scan_records_bytes(int n_seq, int64_t total_tokens, int H) {
   return static_cast<size_t>((total_tokens / n_seq + 63) / 64) * n_seq * H * (73 * 1024);
 }
 
-// Two-pass prefill (dk = dv = 128): a chunk-preparation pass over every
+// Two-pass prefill: a chunk-preparation pass over every
 // (chunk, head) of a group of hg heads, then the state pass over that group's
 // chains.  Workspace: the varlen chunk-start table (1 KiB granules), then one
 // record per (chunk, head of the group).  The chunk count is bounded by
@@ -145,13 +142,20 @@ constexpr unsigned kPassFlags = KDA_PASS_PREPARE | KDA_PASS_STATE;
 
 }  // namespace
 
-// Workspace the segment-parallel scan needs at these sizes (0: no scan).
-size_t chunk_fwd_scan_bytes(int n_seq, int64_t total_tokens, int H, int dk, int dv, int chunk) {
+// The one rule for whether a kda_chunk_fwd call takes the segment-parallel
+// scan (shared with kda_chunk_fwd_noalloc): equal-length sequences given
+// without cu_seqlens and without snap_offsets, no split-phase flag, and a
+// plan that pays (few long chains).
+bool chunk_fwd_takes_scan(unsigned pre, const int32_t *cu_seqlens, const int64_t *snap_offsets,
+                          int n_seq, int64_t total_tokens, int H, int dk, int dv, int chunk,
+                          size_t *scan_bytes) {
   ScanPlan plan;
-  if (chunk != kChunk || H <= 0 || n_seq <= 0 || total_tokens <= 0 ||
+  if ((pre & (kPassFlags | KDA_TEST_STALL)) || cu_seqlens || snap_offsets || chunk != kChunk ||
+      H <= 0 || n_seq <= 0 || total_tokens <= 0 || !prefill_tc_supported(dk, dv, total_tokens) ||
       !plan_scan(n_seq, total_tokens, H, dk, dv, &plan))
-    return 0;
-  return scan_workspace_bytes(n_seq, H, plan);
+    return false;
+  if (scan_bytes) *scan_bytes = scan_workspace_bytes(n_seq, H, plan);
+  return true;
 }
 
 }  // namespace kda
@@ -164,17 +168,18 @@ const char *kda_status_string(int status) {
   switch (status) {
     case KDA_OK: return "ok";
     case KDA_ERR_NULL: return "null pointer";
-    case KDA_ERR_SHAPE: return "inconsistent sizes";
+    case KDA_ERR_SHAPE: return "inconsistent sizes or a malformed device-side index";
     case KDA_ERR_ALIGN: return "pointer not 16-byte aligned";
     case KDA_ERR_UNSUPPORTED: return "unsupported dk/dv/chunk/gmin";
     case KDA_ERR_WORKSPACE: return "workspace missing or too small";
     case KDA_ERR_CUDA: return "CUDA error";
     case KDA_ERR_TIMEOUT: return "bounded device wait timed out";
+    case KDA_ERR_RANGE: return "value beyond the fp16 range of a tensor-core operand";
     default: return "unknown status";
   }
 }
 
-int kda_version(void) { return 100; }
+int kda_version(void) { return 200; }
 
 size_t kda_chunk_fwd_workspace_bytes(int n_seq, int64_t total_tokens, int H, int dk, int dv,
                                      int chunk) {
@@ -205,8 +210,9 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
                      size_t workspace_bytes, kda_stream_t stream) {
   if (n_seq < 0 || total_tokens < 0 || H <= 0 || H > 65535) return KDA_ERR_SHAPE;
   const unsigned passes = pre & kPassFlags;
-  pre &= ~kPassFlags;
-  if (!dim_ok(dk) || !dim_ok(dv) || chunk != kChunk || !gmin_ok(gmin) || !pre_ok(pre))
+  const bool stall = (pre & KDA_TEST_STALL) != 0;
+  const unsigned ops = pre & ~(kPassFlags | KDA_TEST_STALL);
+  if (!dim_ok(dk) || !dim_ok(dv) || chunk != kChunk || !gmin_ok(gmin) || !pre_ok(ops))
     return KDA_ERR_UNSUPPORTED;
   if (n_seq == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_SHAPE;
   if (n_seq > 65535) return KDA_ERR_SHAPE;
@@ -222,26 +228,46 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
   const void *ptrs[] = {q, k, v, z, beta, A, S0, o, S_final, snaps, snap_offsets, cu_seqlens};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_ALIGN;
-  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (total_tokens > 0 && !prefill_tc_supported(dk, dv, total_tokens)) return KDA_ERR_SHAPE;
+  if (stall && (passes || total_tokens == 0)) return KDA_ERR_UNSUPPORTED;
   if (passes) {
     // one of the two passes on its own: all heads in one group, so the
     // records of the whole call sit in the workspace between the calls
-    if (passes == kPassFlags || !prefill_tc_supported(dk, dv, total_tokens))
-      return KDA_ERR_UNSUPPORTED;
+    if (passes == kPassFlags || total_tokens == 0) return KDA_ERR_UNSUPPORTED;
     if (!workspace || !aligned16(workspace) ||
         split_heads(n_seq, total_tokens, H, workspace_bytes) < H)
       return KDA_ERR_WORKSPACE;
   }
-  ScanPlan plan;
-  const bool scan = !passes && !cu_seqlens && !(snaps && snap_offsets) &&
-                    prefill_tc_supported(dk, dv, total_tokens) &&
-                    plan_scan(n_seq, total_tokens, H, dk, dv, &plan);
+  size_t need = 0;
+  const bool scan = chunk_fwd_takes_scan(pre, cu_seqlens, snap_offsets, n_seq, total_tokens, H,
+                                         dk, dv, chunk, &need);
   if (scan) {
-    const size_t need = scan_workspace_bytes(n_seq, H, plan);
     if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KDA_ERR_ALIGN;
-    int *status = status_word();
-    if (!status) return KDA_ERR_CUDA;
+  }
+  // every host-side check is done: from here on the call launches work
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int *status = status_word();
+  if (!status) return KDA_ERR_CUDA;
+  if (stall) {  // test hook: the single-pass kernel gives up on an unarmed wait
+    const cudaError_t err = prefill_tc_launch(
+        q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, total_tokens, fixed_len, H, dk, dv, S0, o,
+        S_final, snaps, snap_offsets, status, 0, 0, nullptr, n_seq, ops, 1, st);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  }
+  if (total_tokens == 0) {
+    // nothing to run but the final states: S_final = S0 (or zero)
+    if (S_final) {
+      const size_t bytes = static_cast<size_t>(n_seq) * H * dk * dv * sizeof(float);
+      const cudaError_t err = S0 ? cudaMemcpyAsync(S_final, S0, bytes, cudaMemcpyDeviceToDevice, st)
+                                 : cudaMemsetAsync(S_final, 0, bytes, st);
+      return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+  }
+  if (scan) {
+    ScanPlan plan;
+    plan_scan(n_seq, total_tokens, H, dk, dv, &plan);
     const int n2 = n_seq * plan.n_segs;
     const size_t arr = static_cast<size_t>(n2) * H * 128 * 128;
     float *Mb = static_cast<float *>(workspace), *Nb = Mb + arr, *Ss = Nb + arr;
@@ -254,54 +280,56 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
       uint8_t *rec = static_cast<uint8_t *>(workspace) + need;
       const int64_t cps = (fixed_len + 63) / 64;
       cudaError_t err = chunk_prep_launch(q, k, v, z, beta, A, gmin, nullptr, nullptr, n_seq,
-                                          total_tokens, fixed_len, H, 0, H, n_seq * cps * H, rec,
-                                          status, pre, kSMs, st);
+                                          total_tokens, fixed_len, H, dk, dv, 0, H,
+                                          n_seq * cps * H, rec, status, ops, kSMs, st);
       if (err == cudaSuccess)
-        err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, 0, H,
-                                nullptr, nullptr, Nb, nullptr, nullptr, status, nullptr, 0, 0, st);
+        err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, dk, dv,
+                                0, H, nullptr, nullptr, Nb, nullptr, nullptr, status, nullptr, 0,
+                                0, 0, st);
       if (err == cudaSuccess)
-        err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, 0, H,
-                                nullptr, nullptr, Mb, nullptr, nullptr, status, nullptr, 1, 1, st);
+        err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, dk, dv,
+                                0, H, nullptr, nullptr, Mb, nullptr, nullptr, status, nullptr, 0,
+                                1, 1, st);
       if (err == cudaSuccess)
         err = segment_combine_launch(Mb, Nb, S0, Ss, S_final, n_seq, plan.n_segs, H, st);
       if (err == cudaSuccess)
-        err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, 0, H, Ss,
-                                o, nullptr, snaps, nullptr, status, nullptr, 0, 0, st);
+        err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, dk, dv,
+                                0, H, Ss, o, nullptr, snaps, nullptr, status, nullptr, 0, 0, 0,
+                                st);
       return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     }
     // 1. every segment from a zero state (N) and its transition from S0 = I with v = 0 (M)
     cudaError_t err = prefill_tc_launch(q, k, v, z, beta, A, gmin, nullptr, n2, total_tokens,
-                                        plan.seg_len, H, nullptr, nullptr, Nb, nullptr, nullptr,
-                                        status, 0, 0, nullptr, pre, st);
+                                        plan.seg_len, H, dk, dv, nullptr, nullptr, Nb, nullptr,
+                                        nullptr, status, 0, 0, nullptr, 0, ops, 0, st);
     if (err == cudaSuccess)
       err = prefill_tc_launch(q, k, v, z, beta, A, gmin, nullptr, n2, total_tokens, plan.seg_len,
-                              H, nullptr, nullptr, Mb, nullptr, nullptr, status, 1, 1, nullptr,
-                              pre, st);
+                              H, dk, dv, nullptr, nullptr, Mb, nullptr, nullptr, status, 1, 1,
+                              nullptr, 0, ops, 0, st);
     // 2. chain the segments: start states and the final state
     if (err == cudaSuccess)
       err = segment_combine_launch(Mb, Nb, S0, Ss, S_final, n_seq, plan.n_segs, H, st);
     // 3. outputs and snapshots from the true start state of every segment
     if (err == cudaSuccess)
       err = prefill_tc_launch(q, k, v, z, beta, A, gmin, nullptr, n2, total_tokens, plan.seg_len,
-                              H, Ss, o, nullptr, snaps, nullptr, status, 0, 0, nullptr, pre,
-                              st);
+                              H, dk, dv, Ss, o, nullptr, snaps, nullptr, status, 0, 0, nullptr,
+                              0, ops, 0, st);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }
   cudaError_t err;
-  const int hg = prefill_tc_supported(dk, dv, total_tokens) && workspace && aligned16(workspace)
+  const int hg = workspace && aligned16(workspace)
                      ? split_heads(n_seq, total_tokens, H, workspace_bytes)
                      : 0;
   if (hg > 0) {
     // two passes per group of hg heads: chunk preparation, then the state pass
-    int *status = status_word();
-    if (!status) return KDA_ERR_CUDA;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *chunk_start = nullptr;
     err = cudaSuccess;
     const bool run_prep = passes != KDA_PASS_STATE, run_state = passes != KDA_PASS_PREPARE;
     if (cu_seqlens) {
       chunk_start = reinterpret_cast<int32_t *>(ws);
-      if (run_prep) err = chunk_start_launch(cu_seqlens, n_seq, chunk_start, st);
+      if (run_prep) err = chunk_start_launch(cu_seqlens, n_seq, total_tokens, chunk_start, status,
+                                             st);
     }
     uint8_t *rec = ws + split_table_bytes(n_seq);
     const int64_t max_chunks = cu_seqlens ? split_max_chunks(n_seq, total_tokens)
@@ -310,50 +338,46 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
       const int g = H - h0 < hg ? H - h0 : hg;
       if (run_prep)
         err = chunk_prep_launch(q, k, v, z, beta, A, gmin, cu_seqlens, chunk_start, n_seq,
-                                total_tokens, fixed_len, H, h0, g, max_chunks * g, rec, status,
-                                pre, kSMs, st);
+                                total_tokens, fixed_len, H, dk, dv, h0, g, max_chunks * g, rec,
+                                status, ops, kSMs, st);
       if (err == cudaSuccess && run_state)
         err = state_pass_launch(rec, cu_seqlens, chunk_start, n_seq, fixed_len, total_tokens, H,
-                                h0, g, S0, o, S_final, snaps, snap_offsets, status, nullptr, 0, 0,
-                                st);
+                                dk, dv, h0, g, S0, o, S_final, snaps, snap_offsets, status,
+                                nullptr, 0, 0, 0, st);
     }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }
-  if (prefill_tc_supported(dk, dv, total_tokens)) {
-    int *status = status_word();
-    if (!status) return KDA_ERR_CUDA;
-    err = prefill_tc_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, total_tokens, fixed_len,
-                            H, S0, o, S_final, snaps, snap_offsets, status, 0, 0, nullptr, pre,
-                            st);
-  } else {
-    err = prefill_simt_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, fixed_len, H, dk, dv,
-                              S0, o, S_final, snaps, snap_offsets, nullptr, pre, st);
-  }
+  err = prefill_tc_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, total_tokens, fixed_len, H,
+                          dk, dv, S0, o, S_final, snaps, snap_offsets, status, 0, 0, nullptr,
+                          n_seq, ops, 0, st);
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_decode_step(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *z,
                     const kda_bf16 *beta, const float *A, float gmin, float *state_pool,
-                    const int32_t *slots, int n, int H, int dk, int dv, kda_bf16 *o,
+                    int n_slots, const int32_t *slots, int n, int H, int dk, int dv, kda_bf16 *o,
                     kda_stream_t stream) {
-  return kda_decode_step_ex(q, k, v, z, beta, A, gmin, state_pool, slots, n, H, dk, dv, 0u, o,
-                            stream);
+  return kda_decode_step_ex(q, k, v, z, beta, A, gmin, state_pool, n_slots, slots, n, H, dk, dv,
+                            0u, o, stream);
 }
 
 int kda_decode_step_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                        const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
-                       float *state_pool, const int32_t *slots, int n, int H, int dk, int dv,
-                       unsigned pre, kda_bf16 *o, kda_stream_t stream) {
-  if (n < 0 || H <= 0) return KDA_ERR_SHAPE;
+                       float *state_pool, int n_slots, const int32_t *slots, int n, int H,
+                       int dk, int dv, unsigned pre, kda_bf16 *o, kda_stream_t stream) {
+  if (n < 0 || H <= 0 || n_slots < 0) return KDA_ERR_SHAPE;
   if (!dim_ok(dk) || !dim_ok(dv) || !gmin_ok(gmin) || !pre_ok(pre)) return KDA_ERR_UNSUPPORTED;
   if (n == 0) return KDA_OK;
   if (static_cast<int64_t>(n) * H > 0x7fffffffLL) return KDA_ERR_SHAPE;
+  if (!slots && n > n_slots) return KDA_ERR_SHAPE;
   if (!q || !k || !v || !z || !beta || !A || !state_pool || !o) return KDA_ERR_NULL;
   const void *ptrs[] = {q, k, v, z, beta, A, state_pool, slots, o};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_ALIGN;
-  const cudaError_t err = decode_step_launch(q, k, v, z, beta, A, gmin, state_pool, slots, n, H,
-                                             dk, dv, o, pre,
+  int *status = status_word();
+  if (!status) return KDA_ERR_CUDA;
+  const cudaError_t err = decode_step_launch(q, k, v, z, beta, A, gmin, state_pool, slots,
+                                             n_slots, n, H, dk, dv, o, pre, status,
                                              reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -361,9 +385,10 @@ int kda_decode_step_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
 int kda_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                       const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
                       const int32_t *cu_seqlens, int n, int64_t total_tokens, int H, int dk,
-                      int dv, unsigned pre, float *state_pool, const int32_t *slots, int commit,
-                      kda_bf16 *o, kda_stream_t stream) {
-  if (n < 0 || total_tokens < 0 || H <= 0 || H > 65535 || n > 65535) return KDA_ERR_SHAPE;
+                      int dv, unsigned pre, float *state_pool, int n_slots, const int32_t *slots,
+                      int commit, kda_bf16 *o, kda_stream_t stream) {
+  if (n < 0 || total_tokens < 0 || H <= 0 || H > 65535 || n > 65535 || n_slots < 0)
+    return KDA_ERR_SHAPE;
   if (!dim_ok(dk) || !dim_ok(dv) || !gmin_ok(gmin) || !pre_ok(pre)) return KDA_ERR_UNSUPPORTED;
   if (n == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_SHAPE;
   if (!A || !state_pool || !slots || !cu_seqlens) return KDA_ERR_NULL;
@@ -371,34 +396,34 @@ int kda_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
   const void *ptrs[] = {q, k, v, z, beta, A, state_pool, slots, cu_seqlens, o};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+  if (total_tokens == 0) return KDA_OK;  // no token: every state stays as it is
+  if (!prefill_tc_supported(dk, dv, total_tokens)) return KDA_ERR_SHAPE;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   float *S_final = commit ? state_pool : nullptr;
-  cudaError_t err;
-  if (prefill_tc_supported(dk, dv, total_tokens)) {
-    int *status = status_word();
-    if (!status) return KDA_ERR_CUDA;
-    err = prefill_tc_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n, total_tokens, 0, H,
-                            state_pool, o, S_final, nullptr, nullptr, status, 0, 0, slots, pre,
-                            st);
-  } else {
-    err = prefill_simt_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n, 0, H, dk, dv, state_pool,
-                              o, S_final, nullptr, nullptr, slots, pre, st);
-  }
+  int *status = status_word();
+  if (!status) return KDA_ERR_CUDA;
+  const cudaError_t err =
+      prefill_tc_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n, total_tokens, 0, H, dk, dv,
+                        state_pool, o, S_final, nullptr, nullptr, status, 0, 0, slots, n_slots,
+                        pre, 0, st);
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-int kda_state_snapshot(const float *snaps, const int64_t *src_idx, float *state_pool,
-                       const int32_t *dst_slots, int n, int H, int dk, int dv,
-                       kda_stream_t stream) {
-  if (n < 0 || H <= 0 || H > 65535) return KDA_ERR_SHAPE;
+int kda_state_snapshot(const float *snaps, int64_t n_rows, const int64_t *src_idx,
+                       float *state_pool, int n_slots, const int32_t *dst_slots, int n, int H,
+                       int dk, int dv, kda_stream_t stream) {
+  if (n < 0 || H <= 0 || H > 65535 || n_rows < 0 || n_slots < 0) return KDA_ERR_SHAPE;
   if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
   if (n == 0) return KDA_OK;
   if (!snaps || !src_idx || !state_pool || !dst_slots) return KDA_ERR_NULL;
   const void *ptrs[] = {snaps, src_idx, state_pool, dst_slots};
   for (const void *p : ptrs)
     if (!aligned16(p)) return KDA_ERR_ALIGN;
-  const cudaError_t err = snapshot_restore_launch(snaps, src_idx, state_pool, dst_slots, n, H, dk,
-                                                  dv, reinterpret_cast<cudaStream_t>(stream));
+  int *status = status_word();
+  if (!status) return KDA_ERR_CUDA;
+  const cudaError_t err =
+      snapshot_restore_launch(snaps, n_rows, src_idx, state_pool, n_slots, dst_slots, n, H, dk,
+                              dv, status, reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -26,7 +26,8 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
                    const kda_bf16 *__restrict__ v, const kda_bf16 *__restrict__ z,
                    const kda_bf16 *__restrict__ beta, const float *__restrict__ A,
                    float gmin, float *__restrict__ pool, const int32_t *__restrict__ slots,
-                   int H, kda_bf16 *__restrict__ o, unsigned pre) {
+                   int n_slots, int H, kda_bf16 *__restrict__ o, unsigned pre,
+                   int *__restrict__ status) {
   constexpr int TPR = DV / 4;                // threads across one row (4 columns each)
   constexpr int RG = kDecodeThreads / TPR;   // row groups
   constexpr int RPT = DK / RG;               // rows per thread
@@ -42,6 +43,10 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
   const int tid = threadIdx.x;
   const int cg = tid % TPR, rg = tid / TPR;
   const int slot = slots ? slots[b] : b;
+  if (slot < 0 || slot >= n_slots) {  // a bad slot index: the row is skipped
+    if (tid == 0) atomicOr(status, KDA_ERR_SHAPE);
+    return;
+  }
   float *S = pool + (static_cast<size_t>(slot) * H + h) * (DK * DV);
 
   // Issue the whole state read first; the gate below overlaps its latency.
@@ -133,11 +138,11 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
 template <int DK, int DV>
 cudaError_t launch_decode(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                           const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
-                          float *pool, const int32_t *slots, int n, int H, kda_bf16 *o,
-                          unsigned pre, cudaStream_t stream) {
+                          float *pool, const int32_t *slots, int n_slots, int n, int H,
+                          kda_bf16 *o, unsigned pre, int *status, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(n) * H;
   decode_step_kernel<DK, DV><<<static_cast<unsigned>(rows), kDecodeThreads, 0, stream>>>(
-      q, k, v, z, beta, A, gmin, pool, slots, H, o, pre);
+      q, k, v, z, beta, A, gmin, pool, slots, n_slots, H, o, pre, status);
   return cudaGetLastError();
 }
 
@@ -145,17 +150,21 @@ cudaError_t launch_decode(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *
 
 cudaError_t decode_step_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                                const kda_bf16 *z, const kda_bf16 *beta, const float *A,
-                               float gmin, float *pool, const int32_t *slots, int n, int H,
-                               int dk, int dv, kda_bf16 *o, unsigned pre,
-                               cudaStream_t stream) {
+                               float gmin, float *pool, const int32_t *slots, int n_slots,
+                               int n, int H, int dk, int dv, kda_bf16 *o, unsigned pre,
+                               int *status, cudaStream_t stream) {
   if (dk == 128 && dv == 128)
-    return launch_decode<128, 128>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, pre, stream);
+    return launch_decode<128, 128>(q, k, v, z, beta, A, gmin, pool, slots, n_slots, n, H, o,
+                                    pre, status, stream);
   if (dk == 64 && dv == 64)
-    return launch_decode<64, 64>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, pre, stream);
+    return launch_decode<64, 64>(q, k, v, z, beta, A, gmin, pool, slots, n_slots, n, H, o,
+                                    pre, status, stream);
   if (dk == 128 && dv == 64)
-    return launch_decode<128, 64>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, pre, stream);
+    return launch_decode<128, 64>(q, k, v, z, beta, A, gmin, pool, slots, n_slots, n, H, o,
+                                    pre, status, stream);
   if (dk == 64 && dv == 128)
-    return launch_decode<64, 128>(q, k, v, z, beta, A, gmin, pool, slots, n, H, o, pre, stream);
+    return launch_decode<64, 128>(q, k, v, z, beta, A, gmin, pool, slots, n_slots, n, H, o,
+                                    pre, status, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -29,7 +29,9 @@
 
 namespace kda {
 
-size_t chunk_fwd_scan_bytes(int n_seq, int64_t total_tokens, int H, int dk, int dv, int chunk);
+bool chunk_fwd_takes_scan(unsigned pre, const int32_t *cu_seqlens, const int64_t *snap_offsets,
+                          int n_seq, int64_t total_tokens, int H, int dk, int dv, int chunk,
+                          size_t *scan_bytes);
 
 namespace {
 
@@ -63,10 +65,13 @@ extern "C" int kda_chunk_fwd_noalloc(const kda_bf16 *q, const kda_bf16 *k, const
                                      int64_t total_tokens, int H, int dk, int dv, int chunk,
                                      const float *S0, kda_bf16 *o, float *S_final, float *snaps,
                                      const int64_t *snap_offsets, kda_stream_t stream) {
-  // Only the segment-parallel scan needs scratch (varlen calls never take it);
-  // every other call runs the single-pass kernel, which needs none.
-  const size_t need =
-      cu_seqlens ? 0 : kda::chunk_fwd_scan_bytes(n_seq, total_tokens, H, dk, dv, chunk);
+  // Only the segment-parallel scan needs scratch, and whether a call takes it
+  // is decided by the same rule kda_chunk_fwd applies; every other call gets
+  // no workspace and so runs the single-pass kernel, which needs none.
+  size_t need = 0;
+  if (!kda::chunk_fwd_takes_scan(0u, cu_seqlens, snap_offsets, n_seq, total_tokens, H, dk, dv,
+                                 chunk, &need))
+    need = 0;
   if (need > KDA_NOALLOC_WORKSPACE_BYTES) return KDA_ERR_WORKSPACE;
   void *ws = nullptr;
   if (need > 0) {

@@ -1,5 +1,12 @@
 // Chunkwise-parallel KDA prefill on the sm_103a tensor cores (tcgen05 + TMEM,
-// operands staged by TMA), dk = dv = 128, chunk C = 64.
+// operands staged by TMA), dk, dv in {64, 128}, chunk C = 64.
+//
+// The kernels are laid out for 128 key and 128 value channels.  A head of 64
+// channels runs through the same tiles: its tensor maps have 64 channels, so
+// the TMA box over channels 64..127 lies wholly out of bounds and arrives as
+// zeros.  Zero key / query channels add nothing to any product, and zero
+// value columns keep their state columns and outputs at zero; the state is
+// read and written only inside [dk, dv].
 //
 // Algebra ("Kimi K3 Technical Report - Open Frontier Intelligence", sec. 2.1
 // chunkwise-parallel form, sec. 2.1.1 / Fig. 3 bounded decay): for one chunk
@@ -136,6 +143,7 @@ struct TcParams {
   float gmin;
   const int32_t *cu_seqlens;
   int64_t fixed_len;
+  int64_t total;  // tokens of the batch (bounds every cu_seqlens entry)
   int H;
   const float *S0;
   kda_bf16 *o;
@@ -144,6 +152,9 @@ struct TcParams {
   const int64_t *snap_offsets;
   int *status;
   const int32_t *slots;  // S0 / S_final row of sequence s: slots[s] (state pool), or s
+  int n_slots;           // rows of the state pool (slots are checked against it)
+  int dk, dv;            // 64 or 128 each (the tiles always hold 128)
+  int test_stall;        // KDA_TEST_STALL: give up on an unarmed wait first
   int zero_v;       // 1: treat v as zero (U = 0) and do not read it
   int s0_identity;  // 1: start every chain from S0 = I (dk = dv) instead of S0
   unsigned pre;     // KDA_PRE_* input pre-ops (L2-normalise q, k; sigmoid of beta)
@@ -251,10 +262,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   int n_chunks = 0;      // iterations of this CTA
   int64_t n_tasks = 0;   // chunk preparation: (chunk, head) tasks of the batch
   const int64_t cps = (p.fixed_len + 63) / 64;  // chunks per sequence (equal lengths)
+  bool shape_bad = false;  // a device-side index was malformed (KDA_ERR_SHAPE)
+  int slot = s;
   if constexpr (!kPrep) {
+    if (p.slots) {
+      slot = p.slots[s];
+      if (slot < 0 || slot >= p.n_slots) {  // nothing of this sequence is touched
+        if (tid == 0) atomicOr(p.status, KDA_ERR_SHAPE);
+        return;
+      }
+    }
     if (p.cu_seqlens) {
-      t_begin = p.cu_seqlens[s];
-      t_end = p.cu_seqlens[s + 1];
+      if (!seq_range(p.cu_seqlens, s, p.total, t_begin, t_end)) shape_bad = true;
     } else {
       t_begin = static_cast<int64_t>(s) * p.fixed_len;
       t_end = t_begin + p.fixed_len;
@@ -322,13 +341,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   };
   int64_t snap_row = 0;
-  if (!kPrep && p.snaps)
-    snap_row = p.snap_offsets ? p.snap_offsets[s] : static_cast<int64_t>(s) * (p.fixed_len / 64);
+  bool want_snaps = !kPrep && p.snaps != nullptr;
+  if (want_snaps) {
+    snap_row = p.snap_offsets ? snap_first_row(p.snap_offsets, s, p.n_seq, t_end - t_begin)
+                              : static_cast<int64_t>(s) * (p.fixed_len / 64);
+    if (snap_row < 0) {
+      want_snaps = false;
+      shape_bad = true;
+    }
+  }
   const float kLog2e = 1.4426950408889634f;
   float dc1 = kPrep ? 0.f : -__expf(p.A[h]) * kLog2e;  // chunk preparation: per task
   const float dc2 = p.gmin * kLog2e;
-  const size_t state_off =
-      kPrep ? 0 : (static_cast<size_t>(p.slots ? p.slots[s] : s) * H + h) * TD * TD;
+  const int DK = p.dk, DV = p.dv;
+  const size_t state_off = kPrep ? 0 : (static_cast<size_t>(slot) * H + h) * DK * DV;
 
   const uint32_t bar_qz0 = sb + MS_BAR_QZ, bar_k = sb + MS_BAR_K, bar_v = sb + MS_BAR_V,
                  bar_mma = sb + MS_BAR_MMA;
@@ -365,13 +391,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int trow = quad * 32 + lane;  // TMEM lane = matrix row
   const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
 
-  // Initial state -> TMEM (row trow, columns [32 q4, 32 q4 + 32)).
+  // Test hook: a wait that nothing arms gives up before anything is issued.
+  bool aborted = false;
+  if (p.test_stall) {
+    const bool ok = mbar_wait_bounded(bar_mma, 0, 1u << 10);
+    if (__syncthreads_or(ok ? 0 : 1)) {
+      if (tid == 0) atomicOr(p.status, KDA_ERR_TIMEOUT);
+      aborted = true;
+      n_chunks = 0;
+    }
+  }
+
+  // Initial state -> TMEM (row trow, columns [32 q4, 32 q4 + 32)); rows and
+  // columns beyond dk, dv are zero.
+  const bool row_in = trow < DK, cols_in = 32 * q4 < DV;
   if constexpr (!kPrep) {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       v[j] = p.s0_identity ? (trow == 32 * q4 + j ? 1.f : 0.f)
-             : p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + 32 * q4 + j] : 0.f;
+             : (p.S0 && row_in && cols_in)
+                 ? p.S0[state_off + static_cast<size_t>(trow) * DV + 32 * q4 + j]
+                 : 0.f;
     tmem_st32(t_lane + TM_S + 32 * q4, v);
     tmem_wait_st();
   }
@@ -420,7 +461,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // (or after the last chunk): the row it goes to, or -1.
   int64_t snap_pending = -1;
   uint32_t mma_phase = 0;
-  bool aborted = false;
+  float range_max = 0.f;  // largest magnitude sent through an fp16 operand
 
   // Wait helper: every thread polls; the CTA agrees on the outcome.
   auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -1024,6 +1065,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             v[8 * j + 2 * e + 1] += f.y;
           }
         }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) range_max = fmaxf(range_max, fabsf(v[j]));
         if (top)
           store_row32_f16(S, a3, r, q4, REG128, v, -1.f);
         else
@@ -1058,26 +1101,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // region, then stores it so that every instruction writes four whole
         // 128-byte rows.  Warps 0..7 use [0, 32 KiB) (not yet the fp16 S),
         // warps 8..15 [64 KiB, 96 KiB) (T' is consumed, W not yet written).
-        const uint32_t tile = sb + SM_AP + (warp < 8 ? warp : warp + 8) * 4096u;
+        // A warp whose tile lies beyond dk or dv has nothing to store.
+        if (row_in && cols_in) {
+          const uint32_t tile = sb + SM_AP + (warp < 8 ? warp : warp + 8) * 4096u;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          S.u128(tile + lane * 128u + (static_cast<uint32_t>(j ^ (lane & 7)) << 4)) =
-              make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
-                         __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
-        __syncwarp();
-        float *base = p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
-                      static_cast<size_t>(quad * 32) * TD + 32 * q4;
+          for (int j = 0; j < 8; ++j)
+            S.u128(tile + lane * 128u + (static_cast<uint32_t>(j ^ (lane & 7)) << 4)) =
+                make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                           __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+          __syncwarp();
+          float *base = p.snaps + (static_cast<size_t>(snap_pending) * H + h) * DK * DV +
+                        static_cast<size_t>(quad * 32) * DV + 32 * q4;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = 4 * i + (lane >> 3), c = lane & 7;
-          const uint4 w = S.u128(tile + r * 128u + (static_cast<uint32_t>(c ^ (r & 7)) << 4));
-          __stcs(reinterpret_cast<float4 *>(base + static_cast<size_t>(r) * TD) + c,
-                 make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                             __uint_as_float(w.w)));
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3), c = lane & 7;
+            const uint4 w = S.u128(tile + r * 128u + (static_cast<uint32_t>(c ^ (r & 7)) << 4));
+            __stcs(reinterpret_cast<float4 *>(base + static_cast<size_t>(r) * DV) + c,
+                   make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                               __uint_as_float(w.w)));
+          }
         }
         snap_pending = -1;
         __syncthreads();  // staging tiles are read before the fp16 S overwrites them
       }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) range_max = fmaxf(range_max, fabsf(v[j]));
       store_row32_f16(S, sb + SM_SBF, trow, q4, REG128, v, 1.f);
       float gam = 1.f;
 #pragma unroll
@@ -1105,6 +1153,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float v[32];
       tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
       tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) range_max = fmaxf(range_max, fabsf(v[j]));
       store_row32_f16(S, sb + SM_WBF, trow, q4, REG64, v, 1.f);
     }
     fence_proxy_async();
@@ -1131,9 +1181,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float v[32];
       tmem_ld32(t_lane + TM_D1 + 32 * q4, v);
       tmem_wait_ld();
-      if (r < L && p.o) {
+      if (r < L && p.o && cols_in) {
         uint4 *dst = reinterpret_cast<uint4 *>(
-            p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + 32 * q4);
+            p.o + (static_cast<size_t>(t0 + r) * H + h) * DV + 32 * q4);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           dst[j] = make_uint4(pack_bf16x2(-v[8 * j + 0], -v[8 * j + 1]),
@@ -1142,7 +1192,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                               pack_bf16x2(-v[8 * j + 6], -v[8 * j + 7]));
       }
     }
-    if (p.snaps && L == 64) snap_pending = snap_row;
+    if (want_snaps && L == 64) snap_pending = snap_row;
     if (L == 64) ++snap_row;
     tc_fence_before();
     __syncthreads();
@@ -1156,17 +1206,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float v[32];
     tmem_ld32(t_lane + TM_S + 32 * q4, v);
     tmem_wait_ld();
-    if (p.S_final) {
+    if (p.S_final && row_in && cols_in) {
       float4 *dst = reinterpret_cast<float4 *>(p.S_final + state_off +
-                                               static_cast<size_t>(trow) * TD + 32 * q4);
+                                               static_cast<size_t>(trow) * DV + 32 * q4);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
-    if (snap_pending >= 0) {
+    if (snap_pending >= 0 && row_in && cols_in) {
       float4 *dst = reinterpret_cast<float4 *>(
-          p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
-          static_cast<size_t>(trow) * TD + 32 * q4);
+          p.snaps + (static_cast<size_t>(snap_pending) * H + h) * DK * DV +
+          static_cast<size_t>(trow) * DV + 32 * q4);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
@@ -1183,14 +1233,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (v_pending) mbar_wait_bounded(bar_v, 0, kWaitPolls) || mbar_wait_bounded(bar_v, 1, kWaitPolls);
   }
   tc_fence_before();
-  __syncthreads();
+  if (__syncthreads_or(range_max > 65504.f ? 1 : 0) && tid == 0)
+    atomicOr(p.status, KDA_ERR_RANGE);
+  if (shape_bad && tid == 0) atomicOr(p.status, KDA_ERR_SHAPE);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kPrep ? TM_COLS_PREP : TM_COLS);
   }
 }
 
-// 3-D map over a [total, H, d] bf16 tensor: box = 64 channels x 1 head x 64 tokens.
+// 3-D map over a [total, H, d] bf16 tensor: box = 64 channels x 1 head x 64
+// tokens.  With d = 64 the box at channel 64 lies outside the tensor and
+// TMA fills it with zeros.
 bool make_map(CUtensorMap *m, const void *base, int64_t total, int H, int d) {
   EncodeTiledFn fn = tensor_map_encoder();
   if (!fn) return false;
@@ -1208,27 +1262,30 @@ bool make_map(CUtensorMap *m, const void *base, int64_t total, int H, int d) {
 }  // namespace
 
 bool prefill_tc_supported(int dk, int dv, int64_t total_tokens) {
-  return dk == TD && dv == TD && total_tokens > 0 && total_tokens < (1LL << 31);
+  return (dk == 64 || dk == TD) && (dv == 64 || dv == TD) && total_tokens > 0 &&
+         total_tokens < (1LL << 31);
 }
 
 cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                               const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
                               const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
-                              int64_t fixed_len, int H, const float *S0, kda_bf16 *o,
-                              float *S_final, float *snaps, const int64_t *snap_offsets,
-                              int *status, int zero_v, int s0_identity, const int32_t *slots,
-                              unsigned pre, cudaStream_t stream) {
+                              int64_t fixed_len, int H, int dk, int dv, const float *S0,
+                              kda_bf16 *o, float *S_final, float *snaps,
+                              const int64_t *snap_offsets, int *status, int zero_v,
+                              int s0_identity, const int32_t *slots, int n_slots, unsigned pre,
+                              int test_stall, cudaStream_t stream) {
   CUtensorMap mq, mk, mz, mv;
-  if (!make_map(&mq, q, total_tokens, H, TD) || !make_map(&mk, k, total_tokens, H, TD) ||
-      !make_map(&mz, z, total_tokens, H, TD) ||
-      !make_map(&mv, zero_v ? k : v, total_tokens, H, TD))
+  if (!make_map(&mq, q, total_tokens, H, dk) || !make_map(&mk, k, total_tokens, H, dk) ||
+      !make_map(&mz, z, total_tokens, H, dk) ||
+      !make_map(&mv, zero_v ? k : v, total_tokens, H, zero_v ? dk : dv))
     return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(TC_SMEM_BYTES));
   if (err != cudaSuccess) return err;
-  TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, H, S0, o, S_final, snaps, snap_offsets,
-               status, slots, zero_v, s0_identity, pre, nullptr, nullptr, n_seq, 0, H};
+  TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, total_tokens, H, S0, o, S_final, snaps,
+               snap_offsets, status, slots, n_slots, dk, dv, test_stall, zero_v, s0_identity,
+               pre, nullptr, nullptr, n_seq, 0, H};
   const dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(n_seq));
   prefill_tc_kernel<false><<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(mq, mk, mz, mv, prm);
   return cudaGetLastError();
@@ -1237,19 +1294,20 @@ cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
 cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                               const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
                               const int32_t *cu_seqlens, const int32_t *chunk_start, int n_seq,
-                              int64_t total_tokens, int64_t fixed_len, int H, int h0, int hg,
-                              int64_t max_tasks, uint8_t *rec, int *status, unsigned pre,
-                              int n_ctas, cudaStream_t stream) {
+                              int64_t total_tokens, int64_t fixed_len, int H, int dk, int dv,
+                              int h0, int hg, int64_t max_tasks, uint8_t *rec, int *status,
+                              unsigned pre, int n_ctas, cudaStream_t stream) {
   CUtensorMap mq, mk, mz, mv;
-  if (!make_map(&mq, q, total_tokens, H, TD) || !make_map(&mk, k, total_tokens, H, TD) ||
-      !make_map(&mz, z, total_tokens, H, TD) || !make_map(&mv, v, total_tokens, H, TD))
+  if (!make_map(&mq, q, total_tokens, H, dk) || !make_map(&mk, k, total_tokens, H, dk) ||
+      !make_map(&mz, z, total_tokens, H, dk) || !make_map(&mv, v, total_tokens, H, dv))
     return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(TC_SMEM_BYTES));
   if (err != cudaSuccess) return err;
-  TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, H, nullptr, nullptr, nullptr, nullptr,
-               nullptr, status, nullptr, 0, 0, pre, rec, chunk_start, n_seq, h0, hg};
+  TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, total_tokens, H, nullptr, nullptr,
+               nullptr, nullptr, nullptr, status, nullptr, 0, dk, dv, 0, 0, 0, pre, rec,
+               chunk_start, n_seq, h0, hg};
   const int64_t ctas = max_tasks < n_ctas ? max_tasks : n_ctas;
   if (ctas <= 0) return cudaSuccess;
   prefill_tc_kernel<true><<<static_cast<unsigned>(ctas), TC_THREADS, TC_SMEM_BYTES, stream>>>(

@@ -72,6 +72,17 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int 
                : "memory");
 }
 
+// Tiled 3-D TMA store shared -> global (bulk async-group of the issuing
+// thread); the same coordinate rules as the 2-D store.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z,
+                                             uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -1,5 +1,5 @@
-// Sequential state pass of the two-pass tensor-core prefill (dk = dv = 128,
-// chunk C = 64).
+// Sequential state pass of the two-pass tensor-core prefill (dk, dv in
+// {64, 128}, chunk C = 64).
 //
 // The chunkwise form ("Kimi K3 Technical Report - Open Frontier
 // Intelligence", sec. 2.1) splits every chunk into a part that depends only
@@ -23,6 +23,9 @@
 // The records arrive by bulk async copies two chunks ahead (two stages), so
 // the chain only waits on its own three MMAs.  Every wait is bounded; a wait
 // that gives up records KDA_ERR_TIMEOUT and the CTA stops cleanly.
+//
+// Heads of 64 key channels carry zero state rows 64..127 (their records hold
+// zero key channels); heads of 64 value channels run one CTA per chain.
 #include <string.h>
 
 #include "kda_common.cuh"
@@ -80,7 +83,10 @@ struct SpParams {
   const int32_t *cu_seqlens;   // or NULL: equal lengths fixed_len
   const int32_t *chunk_start;  // first chunk of each sequence (varlen), or NULL
   int64_t fixed_len;
+  int64_t total;               // tokens of the batch
+  int n_seq;
   int H, h0, hg;               // heads h0 .. h0 + hg - 1 of H
+  int dk, dv;                  // 64 or 128 each
   const float *S0;
   kda_bf16 *o;
   float *S_final;
@@ -88,6 +94,7 @@ struct SpParams {
   const int64_t *snap_offsets;
   int *status;
   const int32_t *slots;
+  int n_slots;
   int zero_u;       // 1: v taken as zero (W = -Wk S; U is not loaded)
   int s0_identity;  // 1: every chain starts from S0 = I (dk = dv)
 };
@@ -104,15 +111,31 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     if (tid == 0) atomicOr(p.status, KDA_ERR_UNSUPPORTED);
     return;
   }
-  const int hh = blockIdx.x >> 1, half = blockIdx.x & 1, s = blockIdx.y;
+  const int halves = p.dv / NC;  // CTAs per chain
+  const int hh = blockIdx.x / halves, half = blockIdx.x - hh * halves, s = blockIdx.y;
   const int H = p.H, h = p.h0 + hh;
+  const int DK = p.dk, DV = p.dv;
   const int col0 = NC * half;
 
+  bool shape_bad = false;
+  int slot = s;
+  if (p.slots) {
+    slot = p.slots[s];
+    if (slot < 0 || slot >= p.n_slots) {  // nothing of this sequence is touched
+      if (tid == 0) atomicOr(p.status, KDA_ERR_SHAPE);
+      return;
+    }
+  }
   int64_t t_begin, t_end, chunk0;
   if (p.cu_seqlens) {
-    t_begin = p.cu_seqlens[s];
-    t_end = p.cu_seqlens[s + 1];
+    if (!seq_range(p.cu_seqlens, s, p.total, t_begin, t_end)) shape_bad = true;
     chunk0 = p.chunk_start[s];
+    // a table that does not cover this sequence's chunks (chunk_start_kernel
+    // zeroes it when cu_seqlens is malformed): read no record
+    if (chunk0 < 0 || chunk0 + (t_end - t_begin + 63) / 64 > p.chunk_start[p.n_seq]) {
+      t_end = t_begin;
+      shape_bad = true;
+    }
   } else {
     t_begin = static_cast<int64_t>(s) * p.fixed_len;
     t_end = t_begin + p.fixed_len;
@@ -120,9 +143,16 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
   }
   const int n_chunks = static_cast<int>((t_end - t_begin + 63) / 64);
   int64_t snap_row = 0;
-  if (p.snaps)
-    snap_row = p.snap_offsets ? p.snap_offsets[s] : static_cast<int64_t>(s) * (p.fixed_len / 64);
-  const size_t state_off = (static_cast<size_t>(p.slots ? p.slots[s] : s) * H + h) * TD * TD;
+  bool want_snaps = p.snaps != nullptr;
+  if (want_snaps) {
+    snap_row = p.snap_offsets ? snap_first_row(p.snap_offsets, s, p.n_seq, t_end - t_begin)
+                              : static_cast<int64_t>(s) * (p.fixed_len / 64);
+    if (snap_row < 0) {
+      want_snaps = false;
+      shape_bad = true;
+    }
+  }
+  const size_t state_off = (static_cast<size_t>(slot) * H + h) * DK * DV;
 
   const uint32_t bar_full = sb + MS_BAR_FULL, bar_mma = sb + MS_BAR_MMA;
   if (tid == 0) {
@@ -147,12 +177,14 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
   const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   const int cq = col0 + 16 * q4;      // first state column of this thread
 
-  {  // initial state -> TMEM
+  const bool row_in = trow < DK;
+  {  // initial state -> TMEM (rows beyond dk are zero)
     float v[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       v[j] = p.s0_identity ? (trow == cq + j ? 1.f : 0.f)
-             : p.S0 ? p.S0[state_off + static_cast<size_t>(trow) * TD + cq + j] : 0.f;
+             : (p.S0 && row_in) ? p.S0[state_off + static_cast<size_t>(trow) * DV + cq + j]
+                                : 0.f;
     tmem_st16(t_lane + TM_S + 16 * q4, v);
     tmem_wait_st();
   }
@@ -180,6 +212,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
   full_pending = (n_chunks > 0 ? 1u : 0u) | (n_chunks > 1 ? 2u : 0u);
   uint32_t mma_phase = 0;
   int64_t snap_pending = -1;
+  float range_max = 0.f;  // largest magnitude sent through an fp16 operand
 
   auto wait_mma = [&]() -> bool {
     const bool ok = mbar_wait_bounded(bar_mma, mma_phase, kWaitPolls);
@@ -212,6 +245,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     tmem_ld16(t_lane + TM_S + 16 * q4, sv);
     tmem_wait_ld();
     {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) range_max = fmaxf(range_max, fabsf(sv[j]));
       store_row16_f16(S, sb + SM_SBF, trow, q4, sv, 1.f);
       const float gam = S.f32(st + ST_G + 4 * trow);
       float v[16];
@@ -254,9 +289,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     if (!wait_mma()) { tmem_wait_st(); aborted = true; break; }
     if (snap_pending >= 0) {
       if (tid == kCopyThread) {
-        const int y = static_cast<int>((snap_pending * H + h) * TD);
-        tma_store_2d(&tm_snap, col0, y, sb + SM_SNAP);
-        tma_store_2d(&tm_snap, col0 + 32, y, sb + SM_SNAP + 16384u);
+        // box = 32 columns x dk rows of state (snapshot row, head) y
+        const int y = static_cast<int>(snap_pending * H + h);
+        tma_store_3d(&tm_snap, col0, 0, y, sb + SM_SNAP);
+        tma_store_3d(&tm_snap, col0 + 32, 0, y, sb + SM_SNAP + 16384u);
         bulk_commit();
       }
       snap_pending = -1;
@@ -268,6 +304,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
       tmem_ld16(t_lane + TM_D1 + 16 * q4, v);
       tmem_wait_ld();
       if (!p.zero_u) add_row16_f16(S, st + ST_U, trow, q4, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) range_max = fmaxf(range_max, fabsf(v[j]));
       store_row16_f16(S, sb + SM_WBF, trow, q4, v, 1.f);
     }
     tmem_wait_st();  // the gamma-scaled state is in TMEM before S += K'^T W
@@ -320,11 +358,11 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
         const int r = (quad - 2) * 32 + rl;
         if (r < L) {
           const uint4 w = S.u128(tile + rl * 32u + (static_cast<uint32_t>(c ^ (rl & 1)) << 4));
-          reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(t0 + r) * H + h) * TD + cq)[c] = w;
+          reinterpret_cast<uint4 *>(p.o + (static_cast<size_t>(t0 + r) * H + h) * DV + cq)[c] = w;
         }
       }
     }
-    if (p.snaps && L == 64) snap_pending = snap_row;
+    if (want_snaps && L == 64) snap_pending = snap_row;
     if (L == 64) ++snap_row;
     // the next chunk's first MMA overwrites D1 only after its state read-out
     // barrier, which every thread reaches after its o stores above
@@ -334,17 +372,17 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     float v[16];
     tmem_ld16(t_lane + TM_S + 16 * q4, v);
     tmem_wait_ld();
-    if (p.S_final) {
+    if (p.S_final && row_in) {
       float4 *dst = reinterpret_cast<float4 *>(p.S_final + state_off +
-                                               static_cast<size_t>(trow) * TD + cq);
+                                               static_cast<size_t>(trow) * DV + cq);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
-    if (snap_pending >= 0) {
+    if (snap_pending >= 0 && row_in) {
       float4 *dst = reinterpret_cast<float4 *>(
-          p.snaps + (static_cast<size_t>(snap_pending) * H + h) * TD * TD +
-          static_cast<size_t>(trow) * TD + cq);
+          p.snaps + (static_cast<size_t>(snap_pending) * H + h) * DK * DV +
+          static_cast<size_t>(trow) * DV + cq);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         __stcs(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
@@ -362,7 +400,9 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
                                mbar_wait_bounded(bar_full + 8 * b, 1, kWaitPolls);
   }
   tc_fence_before();
-  __syncthreads();
+  if (__syncthreads_or(range_max > 65504.f ? 1 : 0) && tid == 0)
+    atomicOr(p.status, KDA_ERR_RANGE);
+  if (shape_bad && tid == 0) atomicOr(p.status, KDA_ERR_SHAPE);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);
@@ -373,25 +413,29 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
 
 cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               const int32_t *chunk_start, int n_seq, int64_t fixed_len,
-                              int64_t total_tokens, int H, int h0, int hg, const float *S0,
-                              kda_bf16 *o, float *S_final, float *snaps,
+                              int64_t total_tokens, int H, int dk, int dv, int h0, int hg,
+                              const float *S0, kda_bf16 *o, float *S_final, float *snaps,
                               const int64_t *snap_offsets, int *status, const int32_t *slots,
-                              int zero_u, int s0_identity, cudaStream_t stream) {
-  // Snapshots as a 2-D fp32 array [rows * H * dk][dv]; rows <= total_tokens / 64
-  // (each snapshot follows a full chunk), which bounds the map's extent.
+                              int n_slots, int zero_u, int s0_identity, cudaStream_t stream) {
+  // Snapshots as a 3-D fp32 array [rows * H][dk][dv]; rows <= total_tokens / 64
+  // (each snapshot follows a full chunk), which bounds the map's extent.  A
+  // box is 32 value columns x dk key rows of one (row, head) state, so a
+  // 64-row state never reaches the next one.
   CUtensorMap tm_snap;
   memset(&tm_snap, 0, sizeof(tm_snap));
   if (snaps) {
     const EncodeTiledFn encode = tensor_map_encoder();
     if (!encode) return cudaErrorInvalidValue;
-    const uint64_t rows = static_cast<uint64_t>(total_tokens / 64) * H * TD;
-    // TMA row coordinates are 32-bit signed
-    if (rows == 0 || rows > 0x7fffffffull) return cudaErrorInvalidValue;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(TD), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(TD) * 4};
-    const cuuint32_t box[2] = {32, 128};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&tm_snap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, snaps, dims, strides, box, estr,
+    const uint64_t states = static_cast<uint64_t>(total_tokens / 64) * H;
+    // TMA coordinates are 32-bit signed
+    if (states == 0 || states > 0x7fffffffull) return cudaErrorInvalidValue;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(dv), static_cast<cuuint64_t>(dk),
+                                static_cast<cuuint64_t>(states)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(dv) * 4,
+                                   static_cast<cuuint64_t>(dk) * dv * 4};
+    const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(dk), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tm_snap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, snaps, dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -401,10 +445,10 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  SpParams prm{rec,   cu_seqlens,   chunk_start, fixed_len, H,      h0,     hg,
-               S0,    o,            S_final,     snaps,     snap_offsets, status, slots,
-               zero_u, s0_identity};
-  const dim3 grid(static_cast<unsigned>(2 * hg), static_cast<unsigned>(n_seq));
+  SpParams prm{rec,     cu_seqlens, chunk_start, fixed_len, total_tokens, n_seq, H,
+               h0,      hg,         dk,          dv,        S0,           o,     S_final,
+               snaps,   snap_offsets, status,    slots,     n_slots,      zero_u, s0_identity};
+  const dim3 grid(static_cast<unsigned>((dv / NC) * hg), static_cast<unsigned>(n_seq));
   state_pass_kernel<<<grid, SP_THREADS, smem, stream>>>(tm_snap, prm);
   return cudaGetLastError();
 }
@@ -416,18 +460,29 @@ namespace kda {
 namespace {
 
 // chunk_start[i] = sum over sequences j < i of ceil(len_j / 64), i = 0 .. n_seq:
-// one CTA, a running prefix over blocks of 1024 sequences.
+// one CTA, a running prefix over blocks of 1024 sequences.  cu_seqlens is
+// checked on the way (cu[0] = 0, non-decreasing, cu[n_seq] = total): if any
+// entry is malformed the whole table is set to zero (no chunk-preparation
+// task, no record read by the state pass) and KDA_ERR_SHAPE is recorded.
 __global__ void __launch_bounds__(1024) chunk_start_kernel(const int32_t *__restrict__ cu,
-                                                           int n_seq,
-                                                           int32_t *__restrict__ chunk_start) {
+                                                           int n_seq, int64_t total,
+                                                           int32_t *__restrict__ chunk_start,
+                                                           int *status) {
   __shared__ int32_t warp_sum[32];
   __shared__ int32_t carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) carry = 0;
+  int bad = 0;
+  if (tid == 0 && (cu[0] != 0 || static_cast<int64_t>(cu[n_seq]) != total)) bad = 1;
   __syncthreads();
   for (int base = 0; base < n_seq; base += 1024) {
     const int i = base + tid;
-    const int c = i < n_seq ? (cu[i + 1] - cu[i] + 63) / 64 : 0;
+    int c = 0;
+    if (i < n_seq) {
+      const int32_t a = cu[i], b = cu[i + 1];
+      if (a < 0 || b < a || static_cast<int64_t>(b) > total) bad = 1;
+      else c = (b - a + 63) / 64;
+    }
     int x = c;  // inclusive scan inside the warp
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -452,13 +507,18 @@ __global__ void __launch_bounds__(1024) chunk_start_kernel(const int32_t *__rest
     __syncthreads();
   }
   if (tid == 0) chunk_start[n_seq] = carry;
+  if (__syncthreads_or(bad)) {
+    for (int i = tid; i <= n_seq; i += 1024) chunk_start[i] = 0;
+    if (tid == 0) atomicOr(status, KDA_ERR_SHAPE);
+  }
 }
 
 }  // namespace
 
-cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int32_t *chunk_start,
-                               cudaStream_t stream) {
-  chunk_start_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, n_seq, chunk_start);
+cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
+                               int32_t *chunk_start, int *status, cudaStream_t stream) {
+  chunk_start_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, n_seq, total_tokens, chunk_start,
+                                             status);
   return cudaGetLastError();
 }
 

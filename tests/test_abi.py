@@ -39,8 +39,9 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_status_strings_and_version(L):
     assert L.kda_version() >= 100
-    for s in range(8):
+    for s in range(9):
         assert L.kda_status_string(s)
+    assert L.kda_status_string(8) != b"unknown status"
     assert L.kda_status_string(99) == b"unknown status"
 
 
@@ -68,22 +69,26 @@ def test_chunk_fwd_rejects_before_launch(L, kw, status):
 @pytest.mark.parametrize("kw,status", [
     (dict(dk=48), 4), (dict(gmin=-7.0), 4), (dict(n=-1), 2), (dict(H=0), 2), (dict(q=None), 1),
     (dict(pool=None), 1), (dict(o=ctypes.c_void_p(0x10004)), 3), (dict(n=0), 0),
+    # rows without a slot array need that many slots; a negative pool size is malformed
+    (dict(n_slots=3), 2), (dict(n_slots=-1), 2),
 ])
 def test_decode_step_rejects_before_launch(L, kw, status):
     fake = ctypes.c_void_p(0x10000)
-    a = dict(q=fake, k=fake, v=fake, z=fake, beta=fake, A=fake, gmin=-5.0, pool=fake, slots=None,
-             n=4, H=2, dk=64, dv=64, o=fake, stream=None)
+    a = dict(q=fake, k=fake, v=fake, z=fake, beta=fake, A=fake, gmin=-5.0, pool=fake, n_slots=4,
+             slots=None, n=4, H=2, dk=64, dv=64, o=fake, stream=None)
     a.update(kw)
     assert L.kda_decode_step(*a.values()) == status
 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(dk=32), 4), (dict(n=-2), 2), (dict(snaps=None), 1), (dict(dst=None), 1),
-    (dict(src=ctypes.c_void_p(0x10002)), 3), (dict(n=0), 0),
+    (dict(src=ctypes.c_void_p(0x10002)), 3), (dict(n=0), 0), (dict(n_rows=-1), 2),
+    (dict(n_slots=-3), 2),
 ])
 def test_state_snapshot_rejects_before_launch(L, kw, status):
     fake = ctypes.c_void_p(0x10000)
-    a = dict(snaps=fake, src=fake, pool=fake, dst=fake, n=2, H=2, dk=64, dv=64, stream=None)
+    a = dict(snaps=fake, n_rows=8, src=fake, pool=fake, n_slots=4, dst=fake, n=2, H=2, dk=64,
+             dv=64, stream=None)
     a.update(kw)
     assert L.kda_state_snapshot(*a.values()) == status
 
@@ -91,12 +96,13 @@ def test_state_snapshot_rejects_before_launch(L, kw, status):
 @pytest.mark.parametrize("kw,status", [
     (dict(dk=80), 4), (dict(n=-1), 2), (dict(slots=None), 1), (dict(cu=None), 1),
     (dict(pool=None), 1), (dict(o=ctypes.c_void_p(0x10008)), 3), (dict(n=0, total=0), 0),
+    (dict(n_slots=-1), 2), (dict(total=0), 0),
 ])
 def test_decode_tokens_rejects_before_launch(L, kw, status):
     fake = ctypes.c_void_p(0x10000)
     a = dict(q=fake, k=fake, v=fake, z=fake, beta=fake, A=fake, gmin=-5.0, cu=fake, n=4,
-             total=20, H=2, dk=64, dv=64, pre=0, pool=fake, slots=fake, commit=1, o=fake,
-             stream=None)
+             total=20, H=2, dk=64, dv=64, pre=0, pool=fake, n_slots=4, slots=fake, commit=1,
+             o=fake, stream=None)
     a.update(kw)
     assert L.kda_decode_tokens(*a.values()) == status
 
@@ -110,7 +116,9 @@ def _ex_args(**kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(pre=0x300, dk=128, dv=128), 4), (dict(pre=0x100), 4),
+    (dict(pre=0x300, dk=128, dv=128), 4), (dict(pre=0x100), 5),
+    # the stall test hook does not combine with a split-phase flag
+    (dict(pre=0x10100, dk=128, dv=128), 4), (dict(pre=0x10000, total=0, n_seq=1), 4),
     (dict(pre=0x100, dk=128, dv=128), 5), (dict(pre=0x200, dk=128, dv=128, ws_bytes=4096), 5),
     (dict(pre=4), 4), (dict(pre=0x80000000), 4), (dict(pre=3, dk=96), 4),
     (dict(pre=3, q=None), 1), (dict(pre=1, H=0), 2), (dict(pre=3, n_seq=0, total=0), 0),
@@ -125,8 +133,8 @@ def test_chunk_fwd_ex_rejects_before_launch(L, kw, status):
 ])
 def test_decode_step_ex_rejects_before_launch(L, kw, status):
     fake = ctypes.c_void_p(0x10000)
-    a = dict(q=fake, k=fake, v=fake, z=fake, beta=fake, A=fake, gmin=-5.0, pool=fake, slots=None,
-             n=4, H=2, dk=64, dv=64, pre=0, o=fake, stream=None)
+    a = dict(q=fake, k=fake, v=fake, z=fake, beta=fake, A=fake, gmin=-5.0, pool=fake, n_slots=4,
+             slots=None, n=4, H=2, dk=64, dv=64, pre=0, o=fake, stream=None)
     a.update(kw)
     assert L.kda_decode_step_ex(*a.values()) == status
 
@@ -134,7 +142,7 @@ def test_decode_step_ex_rejects_before_launch(L, kw, status):
 def test_decode_tokens_rejects_unknown_pre_flags(L):
     fake = ctypes.c_void_p(0x10000)
     assert L.kda_decode_tokens(fake, fake, fake, fake, fake, fake, -5.0, fake, 4, 20, 2, 64, 64,
-                               16, fake, fake, 1, fake, None) == 4
+                               16, fake, 4, fake, 1, fake, None) == 4
 
 
 def test_workspace_query_is_pure_host(L):
@@ -153,8 +161,9 @@ REC = 73 * 1024  # one (chunk, head) record of the two-pass prefill
     (1, 1 << 20, 16, 128, 128, 64, 3 * 64 * 16 * 128 * 128 * 4 + (1 << 14) * 16 * REC),
     # too short for four segments of at least 4096 tokens: two passes
     (1, 8192, 4, 128, 128, 64, 1024 + (128 + 1) * 4 * REC),
-    # other head sizes run on the CUDA cores without a workspace
-    (1, 256, 2, 64, 64, 64, 0),
+    # 64-channel heads run the same two passes (records keep the 128-channel tiles)
+    (1, 256, 2, 64, 64, 64, 1024 + (4 + 1) * 2 * REC),
+    (3, 300, 2, 128, 64, 64, 1024 + (5 + 3) * 2 * REC),
     # only chunk = 64 exists
     (4, 4 * 8192, 16, 128, 128, 32, 0),
 ])
@@ -172,3 +181,18 @@ def test_python_binding_fails_loudly_without_cuda_tensors(L):
     with pytest.raises(ValueError):
         kda.chunk_fwd(x, x, x, x, torch.zeros(64, 1, dtype=torch.bfloat16),
                       torch.zeros(1, dtype=torch.float32))
+
+
+def test_noalloc_scratch_decision_matches_chunk_fwd(L):
+    """kda_chunk_fwd_noalloc needs its fixed scratch only where kda_chunk_fwd
+    would take the segment scan.  One 2^20-token sequence with 16 heads and
+    snapshots: without snap_offsets the scan needs 192 MiB (refused with
+    KDA_ERR_WORKSPACE before anything is touched); with snap_offsets the call
+    runs the single-pass kernel, so it passes the scratch check and stops at
+    the next host check here (a misaligned o: KDA_ERR_ALIGN), launching
+    nothing."""
+    fake = ctypes.c_void_p(0x10000)
+    bad_o = ctypes.c_void_p(0x10008)
+    common = [fake] * 6 + [-5.0, None, 1, 1 << 20, 16, 128, 128, 64, None]
+    assert L.kda_chunk_fwd_noalloc(*common, fake, None, fake, None, None) == 5
+    assert L.kda_chunk_fwd_noalloc(*common, bad_o, None, fake, fake, None) == 3

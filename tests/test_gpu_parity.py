@@ -155,29 +155,39 @@ def test_varlen_64_sequences(kda):
 
 
 def test_long_context(kda):
-    """T = 1,048,576, H = 16: heads 0 and 1 are checked over the first 65,536
-    tokens (outputs and 1024 snapshots) and over the whole length (outputs
-    and final state), the oracle running segment by segment on its own state."""
+    """T = 1,048,576, H = 16, called as the benchmark calls it (one sequence,
+    no cu_seqlens, no snap_offsets): the library takes the segment-parallel
+    scan on the two-pass kernels.  Heads 0 and 1 are checked over the whole
+    length - every output, every chunk snapshot and the final state - against
+    the oracle run segment by segment on its own carried state."""
     x = kda_inputs.make_workload_prefill("long", device="cuda")
-    o, S_final, snaps, offs, _ = check_all(x, kda, seqs=[0], heads=[0, 1], t_limit=65536)
+    T, H = x["k"].shape[0], x["k"].shape[1]
+    need = kda.workspace_bytes(1, T, H, 128, 128)
+    assert need > (T // 64) * H * 73 * 1024  # the scan arrays plus every record
+    S_final = torch.full((1, H, 128, 128), float("nan"), device="cuda")
+    snaps = torch.full((T // 64, H, 128, 128), float("nan"), device="cuda")
+    o = kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], n_seq=1,
+                      S_final=S_final, snaps=snaps)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
     heads = [0, 1]
     hs = torch.tensor(heads, device="cuda")
-    T = x["k"].shape[0]
     seg = 1 << 17
     S = None
-    worst = 0.0
+    worst_o, worst_sn = 0.0, 0.0
     for a in range(0, T, seg):
         sl = slice(a, a + seg)
         ref = oracle.prefill(*(f64(x[n][sl].index_select(1, hs)) for n in ("q", "k", "v", "z",
                                                                             "beta")),
-                             f64(x["A"])[heads], S0=S)
+                             f64(x["A"])[heads], S0=S, snapshots=True)
         S = ref["S_final"]
-        worst = max(worst, o_err(f64(o[sl].index_select(1, hs)), ref["o"]))
-    assert worst <= O_TOL, f"output error {worst:.3e}"
+        worst_o = max(worst_o, o_err(f64(o[sl].index_select(1, hs)), ref["o"]))
+        g_sn = f64(snaps[a // 64:(a + seg) // 64].index_select(1, hs))
+        worst_sn = max(worst_sn, s_err(g_sn, ref["snaps"]))
+    assert worst_o <= O_TOL, f"output error {worst_o:.3e}"
+    assert worst_sn <= S_TOL, f"snapshot error {worst_sn:.3e}"
     e_s = s_err(f64(S_final[0].index_select(0, hs)), S[0])
     assert e_s <= S_TOL, f"final state error {e_s:.3e}"
-    last = f64(snaps[int(offs[1]) - 1].index_select(0, hs))
-    assert s_err(last, S[0]) <= S_TOL, "last snapshot is not the final state"
 
 
 @pytest.mark.parametrize("S0_std", [None, 0.02])
@@ -380,8 +390,8 @@ def test_runs_on_a_side_stream(kda):
 def test_preops_prefill(kda, d, pre):
     """Raw projections (q, k rows of norm 0.25..4 x sqrt(d), beta logits): the
     kernels' fused pre-ops against the oracle's pre-ops followed by the
-    oracle, ragged varlen batch with S0; d = 128 runs the tensor-core kernel,
-    d = 64 the SIMT kernel."""
+    oracle, ragged varlen batch with S0 (both head sizes on the tensor-core
+    kernels)."""
     x = kda_inputs.make_raw_prefill(3, d, d, [200, 64, 1, 130], seed=41 + pre, device="cuda",
                                     S0_std=0.02)
     if not pre & 1:  # norm pre-op off: hand in unit rows, as the plain entry point expects
@@ -535,3 +545,116 @@ def test_two_pass_in_head_groups(kda, heads_per_group):
     assert o_err(f64(o), ref["o"]) <= O_TOL
     assert s_err(f64(S_final), ref["S_final"]) <= S_TOL
     assert s_err(f64(snaps), ref["snaps"]) <= S_TOL
+
+
+# --- errors only the GPU can see -----------------------------------------------------------
+
+def test_stalled_wait_times_out_and_the_next_call_is_clean(kda):
+    """The KDA_TEST_STALL hook makes the tensor-core kernel wait on an mbarrier
+    that nothing arms, with a small poll limit and nothing in flight: the wait
+    gives up, KDA_ERR_TIMEOUT is in the status word, no output is written, and
+    an ordinary call right after it on the same context matches the oracle."""
+    assert kda.device_status() == 0
+    x = kda_inputs.make_prefill(2, 128, 128, [130, 64], seed=61, device="cuda", S0_std=0.02)
+    o = torch.full((194, 2, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], cu_seqlens=x["cu_seqlens"],
+                  S0=x["S0"], o=o, pre=kda.TEST_STALL)
+    torch.cuda.synchronize()
+    assert kda.device_status() == kda.KDA_ERR_TIMEOUT
+    assert torch.isnan(o.float()).all()  # the CTAs returned before writing anything
+    assert kda.device_status() == 0      # read-and-reset cleared it
+    o, S_final, snaps, offs, _ = check_all(x, kda)
+
+
+def test_bad_slot_and_row_indices_are_skipped_and_reported(kda):
+    """Out-of-range slot / snapshot-row indices are checked on the device: the
+    row is skipped (no access outside the pool), KDA_ERR_SHAPE is recorded,
+    and every in-range row is still computed correctly."""
+    n, H, d = 4, 2, 64
+    x = kda_inputs.make_prefill(H, d, d, [1] * n, seed=62, device="cuda", S0_std=0.02)
+    pool = x["S0"].clone()
+    slots = torch.tensor([2, 7, -1, 0], dtype=torch.int32, device="cuda")  # 7, -1 are bad
+    before = pool.clone()
+    o = torch.full((n, H, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    kda.decode_step(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], pool, slots=slots, o=o)
+    torch.cuda.synchronize()
+    assert kda.device_status() == kda.KDA_ERR_SHAPE
+    assert torch.isnan(o[1].float()).all() and torch.isnan(o[2].float()).all()
+    assert torch.equal(pool[1], before[1]) and torch.equal(pool[3], before[3])
+    st = np.ascontiguousarray(f64(before[[2, 0]]))
+    o_ref = oracle.decode_step(*(f64(x[nm][[0, 3]]) for nm in ("q", "k", "v", "z", "beta")),
+                               f64(x["A"]), st)
+    assert o_err(f64(o[[0, 3]]), o_ref) <= O_TOL
+    assert s_err(f64(pool[[2, 0]]), st) <= DECODE_TOL
+    # snapshot restore: a row past the snapshots and a slot past the pool
+    snaps = torch.randn((3, H, d, d), device="cuda")
+    pool2 = torch.zeros((2, H, d, d), device="cuda")
+    kda.state_snapshot(snaps, torch.tensor([1, 3, 0], dtype=torch.int64, device="cuda"), pool2,
+                       torch.tensor([0, 1, 5], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert kda.device_status() == kda.KDA_ERR_SHAPE
+    assert torch.equal(pool2[0], snaps[1]) and torch.equal(pool2[1], torch.zeros_like(pool2[1]))
+    # multi-token decode through a bad slot: that sequence is skipped
+    y = kda_inputs.make_prefill(H, d, d, [3, 5], seed=63, device="cuda", S0_std=0.02)
+    pool3 = y["S0"].clone()
+    before3 = pool3.clone()
+    kda.decode_tokens(y["q"], y["k"], y["v"], y["z"], y["beta"], y["A"], pool3,
+                      torch.tensor([1, 9], dtype=torch.int32, device="cuda"), y["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert kda.device_status() == kda.KDA_ERR_SHAPE
+    assert torch.equal(pool3[0], before3[0])
+    ref = oracle_subset(dict(y, S0=before3[[1, 0]].contiguous()), [0], [0, 1], snapshots=False)
+    assert s_err(f64(pool3[1]), ref["S_final"][0]) <= S_TOL
+
+
+@pytest.mark.parametrize("workspace", [True, False])
+def test_malformed_cu_seqlens_and_snap_offsets_are_reported(kda, workspace):
+    """A decreasing cu_seqlens, or snap_offsets that do not match the lengths,
+    are caught on the device (two-pass and single-pass kernels alike): the
+    call touches nothing outside its arrays and records KDA_ERR_SHAPE; the
+    same call with the correct arrays then matches the oracle."""
+    lengths = [130, 64, 70]
+    x = kda_inputs.make_prefill(2, 128, 128, lengths, seed=64, device="cuda", S0_std=0.02)
+    total = x["k"].shape[0]
+    ws = (torch.empty(kda.workspace_bytes(3, total, 2, 128, 128), dtype=torch.uint8,
+                      device="cuda") if workspace else torch.empty(16, dtype=torch.uint8,
+                                                                   device="cuda"))
+    offs = kda.snapshot_offsets(lengths)
+    snaps = torch.zeros((int(offs[-1]), 2, 128, 128), device="cuda")
+    S_final = torch.zeros((3, 2, 128, 128), device="cuda")
+    args = [x[nm] for nm in ("q", "k", "v", "z", "beta", "A")]
+    bad_cu = torch.tensor([0, 150, 100, total], dtype=torch.int32, device="cuda")
+    kda.chunk_fwd(*args, cu_seqlens=bad_cu, S0=x["S0"], S_final=S_final, snaps=snaps,
+                  snap_offsets=offs, workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.device_status() == kda.KDA_ERR_SHAPE
+    bad_offs = torch.tensor([0, 2, 2, 5], dtype=torch.int64, device="cuda")  # seq 1 needs 1 row
+    kda.chunk_fwd(*args, cu_seqlens=x["cu_seqlens"], S0=x["S0"], S_final=S_final, snaps=snaps,
+                  snap_offsets=bad_offs, workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.device_status() == kda.KDA_ERR_SHAPE
+    o = kda.chunk_fwd(*args, cu_seqlens=x["cu_seqlens"], S0=x["S0"], S_final=S_final,
+                      snaps=snaps, snap_offsets=offs, workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    ref = oracle_subset(x, [0, 1, 2], [0, 1])
+    assert o_err(f64(o), ref["o"]) <= O_TOL
+    assert s_err(f64(S_final), ref["S_final"]) <= S_TOL
+    assert s_err(f64(snaps), ref["snaps"]) <= S_TOL
+
+
+def test_fp16_range_is_reported_not_silent(kda):
+    """The state and the chunk terms U, W pass through fp16 tensor-core
+    operands.  Values of |v| ~ 3e4 overflow that range: the call records
+    KDA_ERR_RANGE instead of returning silent infinities.  |v| ~ 300 (and S0
+    to match) stays inside it and matches the oracle."""
+    x = kda_inputs.make_prefill(2, 128, 128, [200, 64], seed=65, device="cuda", S0_std=0.02)
+    big = dict(x, v=(x["v"].float() * 3e4).to(torch.bfloat16))
+    n_seq = 2
+    S_final = torch.empty((n_seq, 2, 128, 128), device="cuda")
+    kda.chunk_fwd(big["q"], big["k"], big["v"], big["z"], big["beta"], big["A"],
+                  cu_seqlens=big["cu_seqlens"], S0=big["S0"], S_final=S_final)
+    torch.cuda.synchronize()
+    assert kda.device_status() & kda.KDA_ERR_RANGE
+    ok = dict(x, v=(x["v"].float() * 300).to(torch.bfloat16), S0=x["S0"] * 1.5e4)
+    check_all(ok, kda)

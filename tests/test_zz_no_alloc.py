@@ -48,15 +48,15 @@ def _s_err(a, b):
                  torch.linalg.vector_norm(b.double()))
 
 
-def _noalloc(kda, x, n_seq, S_final, snaps):
+def _noalloc(kda, x, n_seq, S_final, snaps, snap_offsets=None, expect=0):
     total, H, dk = x["k"].shape
     dv = x["v"].shape[2]
     o = torch.full((total, H, dv), float("nan"), dtype=torch.bfloat16, device="cuda")
     st = kda.lib().kda_chunk_fwd_noalloc(
         _ptr(x["q"]), _ptr(x["k"]), _ptr(x["v"]), _ptr(x["z"]), _ptr(x["beta"]), _ptr(x["A"]),
         -5.0, None, n_seq, total, H, dk, dv, 64, _ptr(x["S0"]), _ptr(o), _ptr(S_final),
-        _ptr(snaps), None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-    assert st == 0, f"kda_chunk_fwd_noalloc returned {st}"
+        _ptr(snaps), _ptr(snap_offsets), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == expect, f"kda_chunk_fwd_noalloc returned {st}"
     return o
 
 
@@ -87,11 +87,45 @@ def test_noalloc_matches_the_workspace_entry_point_twice(kda):
         f64 = kda_inputs.to_f64
         ref = oracle.prefill(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["z"]), f64(x["beta"]),
                              f64(x["A"]), cu_seqlens=x["cu_seqlens"].cpu().numpy().astype(np.int64),
-                             S0=f64(x["S0"]))
+                             S0=f64(x["S0"]), snapshots=True)
         assert _o_err(o_new, torch.from_numpy(ref["o"])) <= O_TOL
         assert _o_err(o_ref, torch.from_numpy(ref["o"])) <= O_TOL
-        assert _s_err(S_new, S_ref) <= S_TOL
-        assert _s_err(snaps_new, snaps_ref) <= S_TOL
+        # final states and snapshots of both entry points against the oracle
+        for S_gpu, sn_gpu in ((S_new, snaps_new), (S_ref, snaps_ref)):
+            assert _s_err(S_gpu.cpu(), torch.from_numpy(ref["S_final"])) <= S_TOL
+            assert _s_err(sn_gpu.cpu(), torch.from_numpy(ref["snaps"])) <= S_TOL
+
+
+def test_noalloc_with_snap_offsets_runs_without_scratch(kda):
+    """An equal-length 2^20-token call: without snap_offsets it would take the
+    segment scan (96 MiB of scratch at 2 heads: refused before anything
+    runs); with snap_offsets kda_chunk_fwd never takes the scan, so neither
+    does this entry point: it runs the single-pass kernel, needs no scratch,
+    and matches the oracle (every output, snapshot and the final state of
+    both heads, the oracle running segment by segment on its own state)."""
+    T, H = 1 << 20, 2
+    x = kda_inputs.make_prefill(H, 128, 128, [T], seed=33, device="cuda", S0_std=0.02)
+    S_final = torch.full((1, H, 128, 128), float("nan"), device="cuda")
+    snaps = torch.full((T // 64, H, 128, 128), float("nan"), device="cuda")
+    _noalloc(kda, x, 1, S_final, snaps, expect=KDA_ERR_WORKSPACE)
+    offs = torch.tensor([0, T // 64], dtype=torch.int64, device="cuda")
+    o = _noalloc(kda, x, 1, S_final, snaps, snap_offsets=offs)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    f64 = kda_inputs.to_f64
+    seg = 1 << 17
+    S = f64(x["S0"])
+    worst_o = worst_sn = 0.0
+    for a in range(0, T, seg):
+        sl = slice(a, a + seg)
+        ref = oracle.prefill(*(f64(x[n][sl]) for n in ("q", "k", "v", "z", "beta")), f64(x["A"]),
+                             S0=S, snapshots=True)
+        S = ref["S_final"]
+        worst_o = max(worst_o, _o_err(o[sl], torch.from_numpy(ref["o"])))
+        worst_sn = max(worst_sn, _s_err(snaps[a // 64:(a + seg) // 64].cpu(),
+                                        torch.from_numpy(ref["snaps"])))
+    assert worst_o <= O_TOL and worst_sn <= S_TOL
+    assert _s_err(S_final.cpu(), torch.from_numpy(S)) <= S_TOL
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(kda):

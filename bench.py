@@ -357,17 +357,31 @@ def prefill_buffers(kda, x, dev, with_ws=True):
     if with_ws:
         b["ws"] = torch.empty(max(kda.workspace_bytes(n_seq, total, H, dk, dv), 1),
                               dtype=torch.uint8, device=dev)
+    b["tiny_ws"] = torch.empty(16, dtype=torch.uint8, device=dev)  # too small: single pass
     return b
 
 
-def time_two_pass(kda, x, b, stream, steps, warmup, world, clock_gpu=None):
+def time_two_pass(kda, x, b, stream, steps, warmup, world, clock_gpu=None, single_pass=False):
     """Time `steps` prefill steps, each the two passes as split-phase calls
     (chunk preparation, then the state pass) with CUDA events around each on
     the launching stream; returns the per-pass mean times, the step time and
-    the clock summary when a GPU id is given."""
+    the clock summary when a GPU id is given.  single_pass: one call without
+    a workspace per step instead (the single-pass kernel; its time is
+    reported as the state pass, the preparation time as 0)."""
     import torch
 
     def step(e=None):
+        if single_pass:
+            if e is not None:
+                e[0].record(stream)
+                e[1].record(stream)
+            kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                          cu_seqlens=x["cu_seqlens"], S0=x.get("S0"), o=b["o"],
+                          S_final=b["S_final"], snaps=b["snaps"], snap_offsets=b["offs"],
+                          workspace=b["tiny_ws"], stream=stream)
+            if e is not None:
+                e[2].record(stream)
+            return
         if e is not None:
             e[0].record(stream)
         kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
@@ -471,8 +485,9 @@ def run_ours(args, rank, world, local):
 
     # the headline: the packed varlen prefill
     x = make_workload(WORKLOAD, dev)
-    b = prefill_buffers(kda, x, dev)
-    t = time_two_pass(kda, x, b, stream, args.steps, args.warmup, world, clock_gpu=gpu_id)
+    b = prefill_buffers(kda, x, dev, with_ws=not args.single_pass)
+    t = time_two_pass(kda, x, b, stream, args.steps, args.warmup, world, clock_gpu=gpu_id,
+                      single_pass=args.single_pass)
     n_tok = x["k"].shape[0]
     value = n_tok * args.steps * world / (t["elapsed_ms"] / 1e3)
     roofline = prefill_roofline(WORKLOAD, t, hbm_peak, tc_peak, peak_src,
@@ -485,7 +500,7 @@ def run_ours(args, rank, world, local):
         dts = time_oracle(cat, 1)
         cpu_baseline = {"value": n_s / dts[0], "unit": UNIT, "cores": oracle.num_threads(),
                         "kind": "oracle", "sample": sample_desc(WORKLOAD, args.cpu_tokens, n_s)}
-    e2e = None if args.no_e2e else run_e2e(args, x, b, stream, world)
+    e2e = None if (args.no_e2e or args.single_pass) else run_e2e(args, x, b, stream, world)
     del x, b
     torch.cuda.empty_cache()
 
@@ -493,6 +508,8 @@ def run_ours(args, rank, world, local):
     long_ctx = None if args.no_long else run_long(args, dev, stream, hbm_peak, peak_src, world)
     decode = None if args.no_decode else run_decode(args, dev, stream, hbm_peak, peak_src, world)
     tiny = None if args.no_tiny else run_tiny(args, dev, stream, world)
+    restore = None if args.no_restore else run_restore(args, dev, stream, hbm_peak, peak_src,
+                                                       world)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -501,8 +518,11 @@ def run_ours(args, rank, world, local):
                 "scaling": "weak", "vs_baseline": None, "dtype": kda_dtype(),
                 "data": "synthetic", "config": workload_config(WORKLOAD),
                 "clocks": t["clocks"], "roofline": roofline, "cpu_baseline": cpu_baseline,
-                "e2e": e2e, "gpu_launches": 3 * args.steps,
-                "mid": mid, "long_context": long_ctx, "decode": decode, "tiny": tiny}
+                "e2e": e2e, "gpu_launches": (1 if args.single_pass else 3) * args.steps,
+                "prefill_path": "single pass (no workspace)" if args.single_pass else
+                                "two passes (chunk preparation, state pass)",
+                "mid": mid, "long_context": long_ctx, "decode": decode, "tiny": tiny,
+                "restore": restore}
         print(json.dumps(line), flush=True)
 
 
@@ -703,8 +723,8 @@ def run_long(args, dev, stream, hbm_peak, peak_src, world):
     import kda_inputs
     import linear_attention_serving_chunk_gb300 as kda
     w = kda_inputs.WORKLOADS["long"]
-    B, H, T, dk, dv = w["B"], w["H"], w["T"], w["dk"], w["dv"]
-    x = kda_inputs.make_workload_prefill("long", device=dev)
+    B, H, T, dk, dv = w["B"], w["H"], args.long_len or w["T"], w["dk"], w["dv"]
+    x = kda_inputs.make_workload_prefill("long", device=dev, T=T)
     snaps = torch.empty((B * (T // 64), H, dk, dv), dtype=torch.float32, device=dev)
     S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
     o = torch.empty((B * T, H, dv), dtype=torch.bfloat16, device=dev)
@@ -738,6 +758,46 @@ def run_long(args, dev, stream, hbm_peak, peak_src, world):
                      "achieved": nbytes / (ms / 1e3) / 1e9,
                      "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, "unit": "GB/s",
                      "peak": hbm_peak, "peak_source": peak_src}}
+
+
+def run_restore(args, dev, stream, hbm_peak, peak_src, world):
+    """Prefix-cache restore (kda_state_snapshot): 512 x 32 chunk-boundary
+    states (dk = dv = 128, 1 GiB) gathered from a snapshot array into state
+    slots in a permuted order; a pure HBM copy, timed over --restore-reps
+    calls."""
+    import torch
+
+    import linear_attention_serving_chunk_gb300 as kda
+    n, H, d, rows = 512, 32, 128, 1024
+    snaps = torch.randn((rows, H, d, d), dtype=torch.float32, device=dev)
+    pool = torch.empty((n, H, d, d), dtype=torch.float32, device=dev)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(1005)
+    src = torch.randperm(rows, generator=g)[:n].to(torch.int64).to(dev)
+    dst = torch.randperm(n, generator=g).to(torch.int32).to(dev)
+    for _ in range(3):
+        kda.state_snapshot(snaps, src, pool, dst, stream=stream)
+    torch.cuda.synchronize()
+    reps = args.restore_reps
+    a = torch.cuda.Event(enable_timing=True)
+    bb = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        kda.state_snapshot(snaps, src, pool, dst, stream=stream)
+    bb.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(a.elapsed_time(bb), world) / reps
+    nbytes = 2 * n * H * d * d * 4
+    ok = bool(torch.equal(pool[dst[:4].long()], snaps[src[:4]]))
+    del snaps, pool
+    torch.cuda.empty_cache()
+    return {"value": n * world / (ms / 1e3), "unit": "states/s", "ms_per_call": ms,
+            "reps": reps, "workload": f"restore {n} x H={H} snapshot states, dk=dv={d}",
+            "copy_exact": ok,
+            "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
+                         "kernel": "snapshot_restore_kernel", "peak_source": peak_src}}
 
 
 def run_tiny(args, dev, stream, world):
@@ -790,6 +850,13 @@ def main(argv=None):
     ap.add_argument("--no-tiny", action="store_true", help="skip the tiny-prefill latency line")
     ap.add_argument("--long-steps", type=int, default=3)
     ap.add_argument("--tiny-reps", type=int, default=1000)
+    ap.add_argument("--no-restore", action="store_true", help="skip the snapshot-restore line")
+    ap.add_argument("--restore-reps", type=int, default=20)
+    ap.add_argument("--long-len", type=int, default=None,
+                    help="override T of the long-context line (small cases for profiling)")
+    ap.add_argument("--single-pass", action="store_true",
+                    help="run the headline prefill without a workspace (the single-pass "
+                         "kernel), for comparison and profiling")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=2048,
                     help="tokens per sequence in the cpu_baseline sample (one timed run)")

@@ -1,0 +1,886 @@
+// Chunk preparation of the two-pass tensor-core prefill: everything in a
+// chunk that does not depend on the state, for every (chunk, head) of the
+// batch at once, written as one record per (chunk, head) (kda_split.cuh) for
+// the sequential state pass.
+//
+// Algebra ("Kimi K3 Technical Report - Open Frontier Intelligence", sec. 2.1
+// chunkwise-parallel form, sec. 2.1.1 / Fig. 3 bounded decay), for one chunk
+// of 64 tokens r with per-step decays a_r = e^{g_r} (per key channel) and
+// inclusive cumulative log-decay G_r:
+//
+//   A_kk[r][i] = beta_r sum_c k_r k_i e^{G_r - G_i}    (i < r)
+//   P[r][i]    =        sum_c q_r k_i e^{G_r - G_i}    (i <= r)
+//   T = (I + A_kk)^{-1},  T' = T diag(beta),  Wk = T' (K e^G),  U = T' V
+//   record: [-Wk ; -Q e^G], K' = K e^{G_last - G}, U, -P, gamma = e^{G_last}
+//
+// Every causal tile is a dense matmul.  The chunk is cut into four 16-token
+// sub-tiles R.  With F_r the decay product from the start of r's sub-tile
+// through r, Lam_R the sub-tile's total and B_i = Lam_J / F_i the product
+// after i to the end of its sub-tile J:
+//
+//  - an off-diagonal tile (i in J < R <= r's sub-tile) factors as
+//      e^{G_r - G_i} = F_r * prod_{J<M<R} Lam_M * B_i,
+//    every factor <= 1: the tiles run on the tcgen05 tensor cores with fp16
+//    operands [k_r F_r ; q_r F_r] (B) and k_i B_i prod Lam (A, one stacked
+//    block of rows per R), fp32 accumulation in TMEM;
+//  - a diagonal tile (i, r in one sub-tile) needs e^{G_r - G_i} = F_r / F_i,
+//    whose second factor reaches e^{-16 gmin} = e^80 -- the lower bound
+//    gmin = -5 is what keeps it inside the 8-bit exponent range.  These four
+//    16 x 16 tiles run as warp-level tf32 MMAs (m16n8k8) whose fragments are
+//    exactly the elements each thread holds: no operand goes through shared
+//    memory.
+//
+// The element mapping follows the m16n8k8 fragment layout: warp w owns
+// sub-tile R = w / 2 and the key channels 64 (w % 2) .. + 63; lane (g, t)
+// owns tokens 16R + g and 16R + g + 8 and, for k-step s = 0..7, channels
+// 64 (w % 2) + 8s + 2t and + 1.  The running products along the tokens of a
+// sub-tile are shuffle scans over g.
+//
+// Per task (persistent CTAs, two per SM: 256 threads, < 110 KB of shared
+// memory, 256 TMEM columns each):
+//   TMA    q, k, z (one barrier), v (after the operand build)
+//   SIMT   gate, scans, sub-tile totals; then every operand: [KE ; QE] and
+//          the stacked Kc (fp16, shared memory), K e^G (bf16), and -Q e^G,
+//          K' (fp16, straight to the record); diagonal tiles by mma.sync
+//   MMA    off-diagonal A_kk / P tiles (M128 N128 K128, fp16)
+//   SIMT   A_kk to shared memory (fp32, transposed), -P to the record;
+//          T by diagonal-block column updates and (I - E + E^2 - E^3) D for
+//          the off-diagonal blocks; T' = T diag(beta) as bf16 hi | lo
+//   MMA    T'(K e^G) and T'V, each one M128 N128 K128 product with hi and lo
+//          concatenated along K (bf16)
+//   SIMT   -Wk and U (fp16) to the record
+// Every mbarrier wait is bounded; a wait that gives up records
+// KDA_ERR_TIMEOUT and the CTA stops cleanly.
+#include "kda_common.cuh"
+#include "kda_sm100.cuh"
+#include "kda_split.cuh"
+#include "kda_tc_common.cuh"
+
+namespace kda {
+
+namespace {
+
+using namespace sm100;
+using namespace tcx;
+
+constexpr int CP_THREADS = 256;
+
+// Shared-memory map (byte offsets from the 1024-aligned dynamic base).
+constexpr uint32_t SM_Q = 0;              // q tile [64 tok x 128] bf16, then v
+constexpr uint32_t SM_K = 16 * KiB;       // k tile, then T' = [hi | lo] (K-major)
+constexpr uint32_t SM_Z = 32 * KiB;       // z tile, then K e^G (bf16, MN-major)
+constexpr uint32_t SM_KQ = 48 * KiB;      // [KE ; QE] fp16 K-major, 128 rows; then scratch
+constexpr uint32_t SM_KC = 80 * KiB;      // stacked Kc fp16 K-major, 96 rows
+constexpr uint32_t KC_REGION = 12 * KiB;  // its two 64-channel regions
+// scratch of the triangular inverse, in the [KE ; QE] tile once the off-diagonal MMA is done
+constexpr uint32_t SM_AKK = SM_KQ;                     // fp32 [64][68]: A_kk transposed, [i][r]
+constexpr uint32_t SM_TD = SM_AKK + 64 * 68 * 4;       // fp32 [4][16][17]: diagonal blocks of T
+constexpr uint32_t SM_XS = SM_TD + 4 * 16 * 17 * 4;    // fp32 [10][16][17]: block products
+static_assert(SM_XS + 10 * 16 * 17 * 4 <= SM_KC, "inverse scratch overflows the KE/QE tile");
+constexpr uint32_t SM_MISC = 104 * KiB;
+constexpr uint32_t MS_BAR_QKZ = SM_MISC;          // mbarriers: q/k/z in, v in, MMA done
+constexpr uint32_t MS_BAR_V = SM_MISC + 8;
+constexpr uint32_t MS_BAR_MMA = SM_MISC + 16;
+constexpr uint32_t MS_TMEM = SM_MISC + 24;
+constexpr uint32_t MS_TASK = SM_MISC + 32;        // 3 task slots of 32 bytes
+constexpr uint32_t MS_BETA = SM_MISC + 128;       // [64] fp32
+constexpr uint32_t MS_LAM = SM_MISC + 384;        // [128 channels][4 sub-tiles] fp32
+constexpr uint32_t MS_NSQ = MS_LAM + 128 * 16;    // [64 tok][2 halves] (k.k, q.q) partial sums
+// The M = 128 Kc operand reads 128 rows of each region: its second region's
+// unused rows 96..127 end 28 KiB after SM_KC, so the allocation reaches there.
+constexpr uint32_t CP_SMEM_BYTES = SM_KC + KC_REGION + 16 * KiB;
+static_assert(MS_NSQ + 64 * 2 * 8 <= CP_SMEM_BYTES, "misc area");
+static_assert(CP_SMEM_BYTES <= 110 * KiB, "two CTAs per SM");
+
+constexpr uint32_t TILE = 16 * KiB;  // a [64 tok x 128] 2-byte tile (two 8 KiB regions)
+constexpr uint32_t TM_COLS = 256;
+constexpr uint32_t TM_WK = 0;        // off-diagonal A_kk/P, then T'(K e^G)
+constexpr uint32_t TM_U = 128;       // T'V
+
+constexpr uint32_t kWaitPolls = 1u << 24;
+constexpr int kTmaThread = 96;       // lane 0 of warp 3 (idle in both TMEM read-outs)
+constexpr int kTaskThread = 224;     // lane 0 of warp 7 (idle in both TMEM read-outs)
+
+constexpr uint32_t ID_OFF = idesc_mma(128, 128, kFmtF16, kFmtF16, 0, 0);   // K-major x K-major
+constexpr uint32_t ID_TPROD = idesc_mma(128, 128, kFmtBF16, kFmtBF16, 0, 1);
+
+struct CpParams {
+  const kda_bf16 *beta;
+  const float *A;
+  float gmin;
+  const int32_t *cu_seqlens;   // or NULL: equal lengths fixed_len
+  const int32_t *chunk_start;  // varlen: first chunk of each sequence, [n_seq + 1]
+  int64_t fixed_len;
+  int n_seq, H, h0, hg;        // heads h0 .. h0 + hg - 1 of H
+  unsigned pre;
+  uint8_t *rec;                // records [chunk][head in group]
+  int *status;
+};
+
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
+}
+
+// Raw bf16 global load kept where it is written (a prefetch the compiler must
+// not sink to its use).
+__device__ __forceinline__ unsigned short ldg_u16_pinned(const kda_bf16 *ptr) {
+  unsigned short raw;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(raw) : "l"(ptr));
+  return raw;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// exp(gmin * sigmoid(eA * z)) with c1 = -eA log2(e), c2 = gmin log2(e).
+__device__ __forceinline__ float fast_decay2(float c1, float c2, float z) {
+  return ex2_approx(c2 * rcp_approx(1.0f + ex2_approx(c1 * z)));
+}
+
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi, uint32_t &lo) {
+  hi = pack_bf16x2(a, b);
+  const float2 h = unpack_bf16x2(hi);
+  lo = pack_bf16x2(a - h.x, b - h.y);
+}
+
+__device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One warp: C[16x16] (two 16x8 fragments) += X[16x16] Y[16x16] in tf32, X and
+// Y fp32 in shared memory (row strides ldx, ldy); XT / YT: given transposed.
+template <bool XT = false, bool YT = false>
+__device__ __forceinline__ void warp_mma16(const float *X, int ldx, const float *Y, int ldy,
+                                           float (&c)[2][4], int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  auto xa = [&](int row, int col) { return XT ? X[col * ldx + row] : X[row * ldx + col]; };
+  auto yb = [&](int row, int col) { return YT ? Y[col * ldy + row] : Y[row * ldy + col]; };
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    const int k0 = 8 * ks;
+    const uint32_t a0 = tf32_rna(xa(g, k0 + t)), a1 = tf32_rna(xa(g + 8, k0 + t));
+    const uint32_t a2 = tf32_rna(xa(g, k0 + t + 4)), a3 = tf32_rna(xa(g + 8, k0 + t + 4));
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+      mma_m16n8k8_tf32(c[nt], a0, a1, a2, a3, tf32_rna(yb(k0 + t, 8 * nt + g)),
+                       tf32_rna(yb(k0 + t + 4, 8 * nt + g)));
+  }
+}
+
+// 4 x 4 transpose of 32-bit words across the four lanes t = lane & 3 of a
+// quad: lane t holds x[j] = W[j][t] and ends with x[j] = W[t][j].
+__device__ __forceinline__ void quad_transpose(uint32_t (&x)[4], int t) {
+  {
+    const bool hi = (t & 2) != 0;
+    const uint32_t s0 = hi ? x[0] : x[2], s1 = hi ? x[1] : x[3];
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, s0, 2);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+    if (hi) { x[0] = r0; x[1] = r1; } else { x[2] = r0; x[3] = r1; }
+  }
+  {
+    const bool odd = (t & 1) != 0;
+    const uint32_t s0 = odd ? x[0] : x[1], s1 = odd ? x[2] : x[3];
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+    if (odd) { x[0] = r0; x[2] = r1; } else { x[1] = r0; x[3] = r1; }
+  }
+}
+
+// Byte offset of the 16-byte chunk `ch` (8 two-byte elements) of row r in a
+// 128-byte-swizzled tile (one 64-element region).
+__device__ __forceinline__ uint32_t chunk_off(int r, int ch) {
+  return static_cast<uint32_t>(r) * 128u + (static_cast<uint32_t>(ch ^ (r & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(CP_THREADS, 2)
+chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
+                  const CpParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  const Smem S{smem, sb};
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if ((sb & 1023u) != 0) {  // the swizzled layouts need 1024-byte alignment
+    if (tid == 0) atomicOr(p.status, KDA_ERR_UNSUPPORTED);
+    return;
+  }
+  const int H = p.H;
+  const int64_t cps = p.cu_seqlens ? 0 : (p.fixed_len + 63) / 64;
+  const int64_t n_tasks =
+      (p.cu_seqlens ? static_cast<int64_t>(p.chunk_start[p.n_seq]) : p.n_seq * cps) * p.hg;
+  const int n_iter = n_tasks > static_cast<int64_t>(blockIdx.x)
+                         ? static_cast<int>((n_tasks - blockIdx.x + gridDim.x - 1) / gridDim.x)
+                         : 0;
+
+  // Task n of this CTA: global task blockIdx.x + n * gridDim.x = chunk-major,
+  // head-minor.  Resolved two tasks ahead into a three-slot ring by one thread
+  // of a warp that is idle at that point; a varlen chunk's sequence is found
+  // by walking chunk_start forward from the previous task's (consecutive
+  // tasks of a CTA are ~gridDim / hg chunks apart, so the walk is a step or
+  // two of dependent loads).
+  int cur_seq = 0;  // only meaningful in kTaskThread
+  auto put_task = [&](int n) {
+    const int64_t task = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
+    const int64_t c = task / p.hg;
+    int64_t sb0, se0, j;
+    if (p.cu_seqlens) {
+      while (cur_seq + 1 < p.n_seq && p.chunk_start[cur_seq + 1] <= c) ++cur_seq;
+      sb0 = p.cu_seqlens[cur_seq];
+      se0 = p.cu_seqlens[cur_seq + 1];
+      j = c - p.chunk_start[cur_seq];
+    } else {
+      const int64_t q = c / cps;
+      sb0 = q * p.fixed_len;
+      se0 = sb0 + p.fixed_len;
+      j = c - q * cps;
+    }
+    const int64_t t0 = sb0 + 64 * j;
+    const int hh = p.h0 + static_cast<int>(task % p.hg);
+    const uint32_t slot = sb + MS_TASK + 32u * static_cast<uint32_t>(n % 3);
+    S.u128(slot) = make_uint4(static_cast<uint32_t>(t0), static_cast<uint32_t>(t0 >> 32),
+                              static_cast<uint32_t>(min(static_cast<int64_t>(64), se0 - t0)),
+                              static_cast<uint32_t>(hh));
+    S.f32(slot + 16) = -__expf(p.A[hh]) * 1.4426950408889634f;
+  };
+  struct Task {
+    int64_t t0;
+    int L, h;
+    float dc1;
+  };
+  auto task_of = [&](int n) -> Task {
+    const uint32_t slot = sb + MS_TASK + 32u * static_cast<uint32_t>(n % 3);
+    const uint4 w = S.u128(slot);
+    return {static_cast<int64_t>((static_cast<uint64_t>(w.y) << 32) | w.x), static_cast<int>(w.z),
+            static_cast<int>(w.w), S.f32(slot + 16)};
+  };
+
+  const uint32_t bar_qkz = sb + MS_BAR_QKZ, bar_v = sb + MS_BAR_V, bar_mma = sb + MS_BAR_MMA;
+  if (tid == 0) {
+    mbar_init(bar_qkz, 1);
+    mbar_init(bar_v, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_z);
+    prefetch_tensormap(&tm_v);
+  }
+  if (tid == kTaskThread) {
+    if (n_iter > 0) put_task(0);
+    if (n_iter > 1) put_task(1);
+  }
+  if (warp == 0) {
+    tmem_alloc(sb + MS_TMEM, TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + MS_TMEM);
+
+  auto issue_qkz = [&](int n) {
+    const Task tk = task_of(n);
+    const int t0 = static_cast<int>(tk.t0);
+    mbar_expect_tx(bar_qkz, 3 * TILE);
+    tma_load_3d(sb + SM_Q, &tm_q, 0, tk.h, t0, bar_qkz);
+    tma_load_3d(sb + SM_Q + REG64, &tm_q, 64, tk.h, t0, bar_qkz);
+    tma_load_3d(sb + SM_K, &tm_k, 0, tk.h, t0, bar_qkz);
+    tma_load_3d(sb + SM_K + REG64, &tm_k, 64, tk.h, t0, bar_qkz);
+    tma_load_3d(sb + SM_Z, &tm_z, 0, tk.h, t0, bar_qkz);
+    tma_load_3d(sb + SM_Z + REG64, &tm_z, 64, tk.h, t0, bar_qkz);
+  };
+  auto issue_v = [&](int n) {
+    const Task tk = task_of(n);
+    mbar_expect_tx(bar_v, TILE);
+    tma_load_3d(sb + SM_Q, &tm_v, 0, tk.h, static_cast<int>(tk.t0), bar_v);
+    tma_load_3d(sb + SM_Q + REG64, &tm_v, 64, tk.h, static_cast<int>(tk.t0), bar_v);
+  };
+  if (tid == kTmaThread && n_iter > 0) issue_qkz(0);
+  bool qkz_pending = n_iter > 0, v_pending = false, mma_pending = false, aborted = false;
+  uint32_t mma_phase = 0;
+  float range_max = 0.f;
+
+  auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+    const bool ok = mbar_wait_bounded(bar, parity, kWaitPolls);
+    if (__syncthreads_or(ok ? 0 : 1)) {
+      if (tid == 0) atomicOr(p.status, KDA_ERR_TIMEOUT);
+      return false;
+    }
+    return true;
+  };
+  auto wait_mma = [&]() -> bool {
+    const bool ok = wait_all(bar_mma, mma_phase);
+    if (ok) {
+      mma_phase ^= 1u;
+      mma_pending = false;
+    }
+    tc_fence_after();
+    return ok;
+  };
+
+  // Element mapping (see the header): sub-tile R, channel half hc, fragment (g, t).
+  const int R = warp >> 1, hc = warp & 1, g = lane >> 2, t = lane & 3;
+  const int ra = 16 * R + g, rb = ra + 8;               // this thread's two tokens
+  const uint32_t reg = static_cast<uint32_t>(hc) * REG64;  // 64-channel region of a [64 x 128] tile
+  const float c2 = p.gmin * 1.4426950408889634f;
+  const bool l2n = (p.pre & KDA_PRE_L2NORM_QK) != 0;
+  const int quad = warp & 3;                            // TMEM lane quadrant of this warp
+  const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+
+  for (int n = 0; n < n_iter && !aborted; ++n) {
+    const Task tk = task_of(n);
+    const int L = tk.L, h = tk.h;
+    const int64_t task = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
+    uint8_t *rec = p.rec + static_cast<size_t>(task) * kRecBytes;
+    // this chunk's beta (raw bits, widened after the operand build)
+    unsigned short beta_raw = 0;
+    if (tid < 64 && tid < L) beta_raw = ldg_u16_pinned(p.beta + static_cast<size_t>(tk.t0 + tid) * H + h);
+
+    if (!wait_all(bar_qkz, n & 1)) { aborted = true; break; }
+    qkz_pending = false;
+
+    // ---- phase 1: gate, running products along the tokens, sub-tile totals --------------
+    // F[s][0..3] = (ra, c), (ra, c + 1), (rb, c), (rb, c + 1) for c = 64 hc + 8 s + 2 t.
+    float F[8][4];
+    const bool ina = ra < L, inb = rb < L;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const uint32_t off = reg + static_cast<uint32_t>(4 * t);
+      const float2 za = unpack_bf16x2(S.u32(sb + SM_Z + off + chunk_off(ra, s)));
+      const float2 zb = unpack_bf16x2(S.u32(sb + SM_Z + off + chunk_off(rb, s)));
+      float x[4] = {ina ? fast_decay2(tk.dc1, c2, za.x) : 1.f,
+                    ina ? fast_decay2(tk.dc1, c2, za.y) : 1.f,
+                    inb ? fast_decay2(tk.dc1, c2, zb.x) : 1.f,
+                    inb ? fast_decay2(tk.dc1, c2, zb.y) : 1.f};
+      // inclusive products over g (lanes 4 apart) for tokens ra and rb separately
+#pragma unroll
+      for (int d = 1; d < 8; d <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float y = __shfl_up_sync(0xffffffffu, x[e], 4 * d);
+          if (g >= d) x[e] *= y;
+        }
+      }
+      // tokens rb continue from the product of all eight ra tokens (held at g = 7)
+      const float ta0 = __shfl_sync(0xffffffffu, x[0], 28 + t);
+      const float ta1 = __shfl_sync(0xffffffffu, x[1], 28 + t);
+      x[2] *= ta0;
+      x[3] *= ta1;
+      F[s][0] = x[0];
+      F[s][1] = x[1];
+      F[s][2] = x[2];
+      F[s][3] = x[3];
+      if (g == 7) {  // the sub-tile's totals Lam_R of channels c, c + 1
+        const int c = 64 * hc + 8 * s + 2 * t;
+        S.f32(sb + MS_LAM + 16 * c + 4 * R) = x[2];
+        S.f32(sb + MS_LAM + 16 * (c + 1) + 4 * R) = x[3];
+      }
+    }
+    if (l2n) {
+      // sums of squares of this warp's 64 channels of tokens ra, rb (k and q)
+      float ska = 0.f, skb = 0.f, sqa = 0.f, sqb = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t off = reg + static_cast<uint32_t>(4 * t);
+        const float2 ka = unpack_bf16x2(S.u32(sb + SM_K + off + chunk_off(ra, s)));
+        const float2 kb = unpack_bf16x2(S.u32(sb + SM_K + off + chunk_off(rb, s)));
+        const float2 qa = unpack_bf16x2(S.u32(sb + SM_Q + off + chunk_off(ra, s)));
+        const float2 qb = unpack_bf16x2(S.u32(sb + SM_Q + off + chunk_off(rb, s)));
+        ska += ka.x * ka.x + ka.y * ka.y;
+        skb += kb.x * kb.x + kb.y * kb.y;
+        sqa += qa.x * qa.x + qa.y * qa.y;
+        sqb += qb.x * qb.x + qb.y * qb.y;
+      }
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        ska += __shfl_xor_sync(0xffffffffu, ska, o);
+        skb += __shfl_xor_sync(0xffffffffu, skb, o);
+        sqa += __shfl_xor_sync(0xffffffffu, sqa, o);
+        sqb += __shfl_xor_sync(0xffffffffu, sqb, o);
+      }
+      if (t == 0) {
+        S.u64(sb + MS_NSQ + 16 * ra + 8 * hc) = make_uint2(__float_as_uint(ska), __float_as_uint(sqa));
+        S.u64(sb + MS_NSQ + 16 * rb + 8 * hc) = make_uint2(__float_as_uint(skb), __float_as_uint(sqb));
+      }
+    }
+    __syncthreads();  // B1: totals (and norms) in; z is read out
+
+    // ---- phase 2: operands ------------------------------------------------------------------
+    float nka = 1.f, nkb = 1.f, nqa = 1.f, nqb = 1.f;  // 1 / ||row|| with the pre-op
+    if (l2n) {
+      const uint4 a = S.u128(sb + MS_NSQ + 16 * ra), b = S.u128(sb + MS_NSQ + 16 * rb);
+      const float kka = __uint_as_float(a.x) + __uint_as_float(a.z);
+      const float qqa = __uint_as_float(a.y) + __uint_as_float(a.w);
+      const float kkb = __uint_as_float(b.x) + __uint_as_float(b.z);
+      const float qqb = __uint_as_float(b.y) + __uint_as_float(b.w);
+      nka = kka > 0.f ? rsqrtf(kka) : 0.f;
+      nqa = qqa > 0.f ? rsqrtf(qqa) : 0.f;
+      nkb = kkb > 0.f ? rsqrtf(kkb) : 0.f;
+      nqb = qqb > 0.f ? rsqrtf(qqb) : 0.f;
+    }
+    if (!ina) { nka = 0.f; nqa = 0.f; }  // tokens past the chunk's end: zero rows
+    if (!inb) { nkb = 0.f; nqb = 0.f; }
+    float dacc[4][4];  // diagonal tile: n-tiles KE(ra), KE(rb), QE(ra), QE(rb)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dacc[i][e] = 0.f;
+    // record words to transpose across the quad: [0..1] -Q e^G rows ra / rb of
+    // chunks s & 3 ... ; filled for s = 4 u .. 4 u + 3 then stored
+    uint32_t wq_a[4], wq_b[4], wk_a[4], wk_b[4];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const int c = 64 * hc + 8 * s + 2 * t;
+      const uint32_t off = reg + static_cast<uint32_t>(4 * t);
+      float2 ka = unpack_bf16x2(S.u32(sb + SM_K + off + chunk_off(ra, s)));
+      float2 kb = unpack_bf16x2(S.u32(sb + SM_K + off + chunk_off(rb, s)));
+      float2 qa = unpack_bf16x2(S.u32(sb + SM_Q + off + chunk_off(ra, s)));
+      float2 qb = unpack_bf16x2(S.u32(sb + SM_Q + off + chunk_off(rb, s)));
+      ka.x *= nka; ka.y *= nka; kb.x *= nkb; kb.y *= nkb;
+      qa.x *= nqa; qa.y *= nqa; qb.x *= nqb; qb.y *= nqb;
+      // sub-tile totals of channels c, c + 1
+      const float4 l0 = *reinterpret_cast<const float4 *>(S.ptr(sb + MS_LAM + 16 * c));
+      const float4 l1 = *reinterpret_cast<const float4 *>(S.ptr(sb + MS_LAM + 16 * (c + 1)));
+      const float la0[4] = {l0.x, l0.y, l0.z, l0.w}, la1[4] = {l1.x, l1.y, l1.z, l1.w};
+      float pre0 = 1.f, pre1 = 1.f, post0 = 1.f, post1 = 1.f;  // prod_{M<R}, prod_{M>R}
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        if (m < R) { pre0 *= la0[m]; pre1 *= la1[m]; }
+        if (m > R) { post0 *= la0[m]; post1 *= la1[m]; }
+      }
+      const float lr0 = R == 0 ? la0[0] : R == 1 ? la0[1] : R == 2 ? la0[2] : la0[3];
+      const float lr1 = R == 0 ? la1[0] : R == 1 ? la1[1] : R == 2 ? la1[2] : la1[3];
+      const float fa0 = F[s][0], fa1 = F[s][1], fb0 = F[s][2], fb1 = F[s][3];
+      const float ia0 = rcp_approx(fa0), ia1 = rcp_approx(fa1);
+      const float ib0 = rcp_approx(fb0), ib1 = rcp_approx(fb1);
+      // KE = k F, QE = q F (<= 1): the off-diagonal B operand, rows tok / 64 + tok
+      const float kea0 = ka.x * fa0, kea1 = ka.y * fa1, keb0 = kb.x * fb0, keb1 = kb.y * fb1;
+      const float qea0 = qa.x * fa0, qea1 = qa.y * fa1, qeb0 = qb.x * fb0, qeb1 = qb.y * fb1;
+      const uint32_t kq = sb + SM_KQ + static_cast<uint32_t>(hc) * TILE + static_cast<uint32_t>(4 * t);
+      S.u32(kq + chunk_off(ra, s)) = pack_f16x2(kea0, kea1);
+      S.u32(kq + chunk_off(rb, s)) = pack_f16x2(keb0, keb1);
+      S.u32(kq + chunk_off(64 + ra, s)) = pack_f16x2(qea0, qea1);
+      S.u32(kq + chunk_off(64 + rb, s)) = pack_f16x2(qeb0, qeb1);
+      // K e^G = KE prod_{M<R} Lam (bf16, B operand of T'(K e^G)), over z
+      S.u32(sb + SM_Z + off + chunk_off(ra, s)) = pack_bf16x2(kea0 * pre0, kea1 * pre1);
+      S.u32(sb + SM_Z + off + chunk_off(rb, s)) = pack_bf16x2(keb0 * pre0, keb1 * pre1);
+      // -Q e^G and K' = k B prod_{M>R} Lam (record words; B = Lam_R / F)
+      const float ba0 = lr0 * ia0, ba1 = lr1 * ia1, bb0 = lr0 * ib0, bb1 = lr1 * ib1;
+      const uint32_t nq_a = pack_f16x2(-qea0 * pre0, -qea1 * pre1);
+      const uint32_t nq_b = pack_f16x2(-qeb0 * pre0, -qeb1 * pre1);
+      const uint32_t kp_a = pack_f16x2(ka.x * ba0 * post0, ka.y * ba1 * post1);
+      const uint32_t kp_b = pack_f16x2(kb.x * bb0 * post0, kb.y * bb1 * post1);
+      wq_a[s & 3] = nq_a; wq_b[s & 3] = nq_b; wk_a[s & 3] = kp_a; wk_b[s & 3] = kp_b;
+      if ((s & 3) == 3) {
+        // lanes t of the quad hold the four words of chunk s' for s' = 4u..4u+3;
+        // after the transpose lane t holds chunk 4u + t of both rows
+        quad_transpose(wq_a, t);
+        quad_transpose(wq_b, t);
+        quad_transpose(wk_a, t);
+        quad_transpose(wk_b, t);
+        const int ch = (s & 4) + t;  // chunk inside the 64-channel region
+        // A3 rows 64 + tok: two regions of 128 rows; KP: two regions of 64 rows
+        uint4 *a3a = reinterpret_cast<uint4 *>(rec + kRecA3 + hc * 16384 + chunk_off(64 + ra, ch));
+        uint4 *a3b = reinterpret_cast<uint4 *>(rec + kRecA3 + hc * 16384 + chunk_off(64 + rb, ch));
+        uint4 *kpa = reinterpret_cast<uint4 *>(rec + kRecKP + hc * 8192 + chunk_off(ra, ch));
+        uint4 *kpb = reinterpret_cast<uint4 *>(rec + kRecKP + hc * 8192 + chunk_off(rb, ch));
+        *a3a = make_uint4(wq_a[0], wq_a[1], wq_a[2], wq_a[3]);
+        *a3b = make_uint4(wq_b[0], wq_b[1], wq_b[2], wq_b[3]);
+        *kpa = make_uint4(wk_a[0], wk_a[1], wk_a[2], wk_a[3]);
+        *kpb = make_uint4(wk_b[0], wk_b[1], wk_b[2], wk_b[3]);
+      }
+      // Kc rows of the later sub-tiles R' > R: k B prod_{R<M<R'} Lam, stacked at
+      // rows 0 (R' = 1, 16 rows), 16 (R' = 2, 32 rows), 48 (R' = 3, 48 rows)
+      {
+        float m0 = 1.f, m1 = 1.f;
+#pragma unroll
+        for (int rp = 1; rp < 4; ++rp) {
+          if (rp > R) {
+            if (rp > R + 1) {
+              const float x0 = rp - 1 == 1 ? la0[1] : rp - 1 == 2 ? la0[2] : la0[3];
+              const float x1 = rp - 1 == 1 ? la1[1] : rp - 1 == 2 ? la1[2] : la1[3];
+              m0 *= x0;
+              m1 *= x1;
+            }
+            const int base = rp == 1 ? 0 : rp == 2 ? 16 : 48;
+            const uint32_t kc = sb + SM_KC + static_cast<uint32_t>(hc) * KC_REGION +
+                                static_cast<uint32_t>(4 * t);
+            S.u32(kc + chunk_off(base + ra, s)) = pack_f16x2(ka.x * ba0 * m0, ka.y * ba1 * m1);
+            S.u32(kc + chunk_off(base + rb, s)) = pack_f16x2(kb.x * bb0 * m0, kb.y * bb1 * m1);
+          }
+        }
+      }
+      // diagonal tile by mma.sync: A = k / F (rows ra, rb), B = [KE | QE] (tokens ra, rb)
+      {
+        const uint32_t a0 = tf32_rna(ka.x * ia0), a1 = tf32_rna(kb.x * ib0);
+        const uint32_t a2 = tf32_rna(ka.y * ia1), a3 = tf32_rna(kb.y * ib1);
+        mma_m16n8k8_tf32(dacc[0], a0, a1, a2, a3, tf32_rna(kea0), tf32_rna(kea1));
+        mma_m16n8k8_tf32(dacc[1], a0, a1, a2, a3, tf32_rna(keb0), tf32_rna(keb1));
+        mma_m16n8k8_tf32(dacc[2], a0, a1, a2, a3, tf32_rna(qea0), tf32_rna(qea1));
+        mma_m16n8k8_tf32(dacc[3], a0, a1, a2, a3, tf32_rna(qeb0), tf32_rna(qeb1));
+      }
+      // gamma = prod_M Lam_M per key channel (one writer per channel)
+      if (R == 0 && g == 0) {
+        float* gam = reinterpret_cast<float *>(rec + kRecG);
+        *reinterpret_cast<float2 *>(gam + c) =
+            make_float2(la0[0] * la0[1] * la0[2] * la0[3], la1[0] * la1[1] * la1[2] * la1[3]);
+      }
+    }
+    if (tid < 64) {  // this chunk's beta (logits through a sigmoid with the pre-op)
+      const float bn = __uint_as_float(static_cast<uint32_t>(beta_raw) << 16);
+      const float b = (p.pre & KDA_PRE_SIGMOID_BETA) ? 1.0f / (1.0f + __expf(-bn)) : bn;
+      S.f32(sb + MS_BETA + 4 * tid) = tid < L ? b : 0.f;
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();  // B2: operands in; q, k are read out
+
+    // ---- off-diagonal A_kk / P tiles on the tensor cores; v streams into the q tile --------
+    if (tid == 0) {
+      tc_fence_after();
+      issue_mma(tmem + TM_WK, sb + SM_KC, false, KC_REGION, sb + SM_KQ, false, TILE, 8, ID_OFF,
+                0);
+      mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    if (tid == kTmaThread) issue_v(n);
+    v_pending = true;
+    // T' tiles start at zero (the inverse writes the lower triangle only)
+    for (int x = tid; x < 1024; x += CP_THREADS) S.u128(sb + SM_K + 16 * x) = make_uint4(0, 0, 0, 0);
+    if (!wait_mma()) { aborted = true; break; }
+
+    // ---- read-outs: A_kk (transposed, fp32) to shared memory, -P to the record --------------
+    // TMEM lane m is stacked row m of Kc: sub-tile R' = 1 for m < 16, 2 for m < 48,
+    // 3 for m < 96 (lanes 96..127 carry nothing); its columns r of sub-tile R'
+    // hold A_kk / beta_r (KE part, columns 16 R' ..) and P (QE part, 64 + 16 R' ..).
+    if (quad < 3) {
+      const int m = quad * 32 + lane;
+      const int rp = m < 16 ? 1 : m < 48 ? 2 : 3;
+      const int i = m - (rp == 1 ? 0 : rp == 2 ? 16 : 48);
+      const int wbase = quad == 0 ? 16 : quad == 1 ? 32 : 48;  // the warp's 32-column window
+      const bool upper = (16 * rp - wbase) != 0;               // this lane's 16 in the upper half
+      float w[32];
+      tmem_ld32(t_lane + TM_WK + (warp < 4 ? 0 : 64) + wbase, w);
+      tmem_wait_ld();
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = upper ? w[16 + j] : w[j];
+      if (warp < 4) {  // A_kk[r][i] = beta_r D[i][r] into row i of the transposed tile
+        const uint32_t row = sb + SM_AKK + 4u * static_cast<uint32_t>(i * 68 + 16 * rp);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 b = *reinterpret_cast<const float4 *>(S.ptr(sb + MS_BETA + 4 * (16 * rp + 4 * j)));
+          S.u128(row + 16 * j) = make_uint4(
+              __float_as_uint(b.x * v[4 * j]), __float_as_uint(b.y * v[4 * j + 1]),
+              __float_as_uint(b.z * v[4 * j + 2]), __float_as_uint(b.w * v[4 * j + 3]));
+        }
+      } else {  // -P[r][i], r in sub-tile R' (all below the diagonal): record row i, chunks 2R', 2R'+1
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+          *reinterpret_cast<uint4 *>(rec + kRecP + chunk_off(i, 2 * rp + cc)) = make_uint4(
+              pack_f16x2(-v[8 * cc + 0], -v[8 * cc + 1]), pack_f16x2(-v[8 * cc + 2], -v[8 * cc + 3]),
+              pack_f16x2(-v[8 * cc + 4], -v[8 * cc + 5]), pack_f16x2(-v[8 * cc + 6], -v[8 * cc + 7]));
+      }
+    }
+    // diagonal tiles: the two channel halves' partial sums meet in the block scratch
+    float *xs = reinterpret_cast<float *>(S.ptr(sb + SM_XS));  // [4 R][16 values][32 lanes]
+    if (hc == 1) {
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) xs[(R * 16 + 4 * nt + e) * 32 + lane] = dacc[nt][e];
+    }
+    tc_fence_before();
+    __syncthreads();  // B3
+    if (hc == 0) {
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dacc[nt][e] += xs[(R * 16 + 4 * nt + e) * 32 + lane];
+      // fragment (nt, e): token i = ra (e < 2) or rb (e >= 2), token
+      // r = 16 R + 8 (nt & 1) + 2 t + (e & 1); nt < 2: A_kk / beta_r, nt >= 2: P
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = e < 2 ? ra : rb, r = 16 * R + 8 * nt + 2 * t + (e & 1);
+          S.f32(sb + SM_AKK + 4 * (i * 68 + r)) = S.f32(sb + MS_BETA + 4 * r) * dacc[nt][e];
+        }
+      // -P row i, chunk (16 R + 8 (nt - 2)) / 8: lanes t hold its words 2t..2t+1 -> transpose
+      uint32_t pw[4];
+      pw[0] = pack_f16x2(ra <= 16 * R + 2 * t ? -dacc[2][0] : 0.f, ra <= 16 * R + 2 * t + 1 ? -dacc[2][1] : 0.f);
+      pw[1] = pack_f16x2(rb <= 16 * R + 2 * t ? -dacc[2][2] : 0.f, rb <= 16 * R + 2 * t + 1 ? -dacc[2][3] : 0.f);
+      pw[2] = pack_f16x2(ra <= 16 * R + 8 + 2 * t ? -dacc[3][0] : 0.f,
+                         ra <= 16 * R + 9 + 2 * t ? -dacc[3][1] : 0.f);
+      pw[3] = pack_f16x2(rb <= 16 * R + 8 + 2 * t ? -dacc[3][2] : 0.f,
+                         rb <= 16 * R + 9 + 2 * t ? -dacc[3][3] : 0.f);
+      // word j of the quad is (row, chunk) = (ra, 2R), (rb, 2R), (ra, 2R + 1), (rb, 2R + 1)
+      quad_transpose(pw, t);
+      const int prow = (t & 1) ? rb : ra, pch = 2 * R + (t >> 1);
+      *reinterpret_cast<uint4 *>(rec + kRecP + chunk_off(prow, pch)) =
+          make_uint4(pw[0], pw[1], pw[2], pw[3]);
+    } else {
+      // -P is zero for i above r: rows ra, rb, chunks 0 .. 2R - 1 (the earlier sub-tiles)
+      for (int x = t; x < 4 * R; x += 4) {
+        const int prow = (x & 1) ? rb : ra, pch = x >> 1;
+        *reinterpret_cast<uint4 *>(rec + kRecP + chunk_off(prow, pch)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    __syncthreads();  // B4: A_kk complete
+
+    // ---- T = (I + A_kk)^{-1}: diagonal 16 x 16 blocks by column updates --------------------
+    // T' = T diag(beta) as bf16 hi (K columns 0..63) | lo (64..127) of the A tile at SM_K.
+    auto put_tp = [&](int r, int col, float v) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      const uint32_t o = sw128_off(r, col, REG64);
+      S.u16(sb + SM_K + o) = *reinterpret_cast<const unsigned short *>(&hi);
+      S.u16(sb + SM_K + REG64 + o) = *reinterpret_cast<const unsigned short *>(&lo);
+    };
+    {
+      // column jc of the inverse of diagonal block Rd: four lanes per column,
+      // lane rq holds rows rq, rq + 4, rq + 8, rq + 12; x[m] passed by shuffle
+      const int Rd = warp >> 1, jc = 8 * (warp & 1) + (lane >> 2), rq = lane & 3, o = 16 * Rd;
+      float x[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) x[k] = (rq + 4 * k == jc) ? 1.f : 0.f;
+#pragma unroll
+      for (int mm = 0; mm < 15; ++mm) {
+        const float xm = __shfl_sync(0xffffffffu, x[mm >> 2], (lane & ~3) | (mm & 3));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int r = rq + 4 * k;
+          if (r > mm) x[k] -= S.f32(sb + SM_AKK + 4 * ((o + mm) * 68 + o + r)) * xm;
+        }
+      }
+      const float bj = S.f32(sb + MS_BETA + 4 * (o + jc));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int r = rq + 4 * k;
+        S.f32(sb + SM_TD + 4 * ((Rd * 16 + r) * 17 + jc)) = x[k];
+        if (r >= jc) put_tp(o + r, o + jc, x[k] * bj);
+      }
+    }
+    __syncthreads();  // B5
+    // Off-diagonal blocks: with D = blockdiag(T_RR) and E = D A_off (E_RJ =
+    // T_RR A_RJ, strictly block-lower, E^4 = 0): T = (I - E + E^2 - E^3) D,
+    // block by block with N = I - E + E^2 - E^3:
+    //   N_10 = -E_10, N_21 = -E_21, N_32 = -E_32, N_20 = E_21 E_10 - E_20,
+    //   N_31 = E_32 E_21 - E_31, N_30 = E_31 E_10 - E_30 - E_32 N_20;  T_RJ = N_RJ T_JJ.
+    {
+      const float *akk = reinterpret_cast<const float *>(S.ptr(sb + SM_AKK));
+      const float *td = reinterpret_cast<const float *>(S.ptr(sb + SM_TD));
+      float *bs = reinterpret_cast<float *>(S.ptr(sb + SM_XS));  // 10 blocks of [16][17]
+      auto blk = [&](int i) { return bs + i * 16 * 17; };
+      auto tdiag = [&](int Rr) { return td + Rr * 16 * 17; };
+      auto put16 = [&](float *dst, const float (&c)[2][4], const float *sub) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int oo = (g + 8 * hh) * 17 + 8 * nt + 2 * t;
+            dst[oo] = c[nt][2 * hh] - (sub ? sub[oo] : 0.f);
+            dst[oo + 1] = c[nt][2 * hh + 1] - (sub ? sub[oo + 1] : 0.f);
+          }
+      };
+      auto put_t = [&](int Rr, int J, const float (&c)[2][4], float sgn) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int col = 16 * J + 8 * nt + 2 * t;
+          const float b0 = sgn * S.f32(sb + MS_BETA + 4 * col);
+          const float b1 = sgn * S.f32(sb + MS_BETA + 4 * (col + 1));
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t hi, lo;
+            split_bf16x2(c[nt][2 * hh] * b0, c[nt][2 * hh + 1] * b1, hi, lo);
+            const uint32_t o = sw128_off(16 * Rr + g + 8 * hh, col, REG64);
+            S.u32(sb + SM_K + o) = hi;
+            S.u32(sb + SM_K + REG64 + o) = lo;
+          }
+        }
+      };
+      float c[2][4];
+      auto zero = [&]() {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[e >> 1][e & 1] = c[e >> 1][2 + (e & 1)] = 0.f;
+      };
+      zero();
+      if (warp < 6) {  // level 1: E_RJ = T_RR A_RJ (A_kk stored transposed)
+        const int Rr = warp == 0 ? 1 : warp < 3 ? 2 : 3;
+        const int J = warp == 0 ? 0 : warp < 3 ? warp - 1 : warp - 3;
+        warp_mma16<false, true>(tdiag(Rr), 17, akk + (16 * J) * 68 + 16 * Rr, 68, c, lane);
+        put16(blk(warp), c, nullptr);
+      }
+      __syncthreads();
+      if (warp < 6) {  // level 2
+        zero();
+        switch (warp) {
+          case 0: warp_mma16(blk(0), 17, tdiag(0), 17, c, lane); put_t(1, 0, c, -1.f); break;
+          case 1: warp_mma16(blk(2), 17, tdiag(1), 17, c, lane); put_t(2, 1, c, -1.f); break;
+          case 2: warp_mma16(blk(5), 17, tdiag(2), 17, c, lane); put_t(3, 2, c, -1.f); break;
+          case 3: warp_mma16(blk(2), 17, blk(0), 17, c, lane); put16(blk(6), c, blk(1)); break;
+          case 4: warp_mma16(blk(5), 17, blk(2), 17, c, lane); put16(blk(7), c, blk(4)); break;
+          default: warp_mma16(blk(4), 17, blk(0), 17, c, lane); put16(blk(8), c, nullptr); break;
+        }
+      }
+      __syncthreads();
+      if (warp < 3) {  // level 3
+        zero();
+        switch (warp) {
+          case 0: warp_mma16(blk(6), 17, tdiag(0), 17, c, lane); put_t(2, 0, c, 1.f); break;
+          case 1: warp_mma16(blk(7), 17, tdiag(1), 17, c, lane); put_t(3, 1, c, 1.f); break;
+          default:
+            // N_30 = (E_31 E_10 - E_30) - E_32 N_20
+            warp_mma16(blk(5), 17, blk(6), 17, c, lane);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int oo = (g + 8 * hh) * 17 + 8 * nt + 2 * t;
+                blk(9)[oo] = (blk(8)[oo] - blk(3)[oo]) - c[nt][2 * hh];
+                blk(9)[oo + 1] = (blk(8)[oo + 1] - blk(3)[oo + 1]) - c[nt][2 * hh + 1];
+              }
+            break;
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {  // level 4: T_30 = N_30 T_00
+        zero();
+        warp_mma16(blk(9), 17, tdiag(0), 17, c, lane);
+        put_t(3, 0, c, 1.f);
+      }
+    }
+    fence_proxy_async();  // T' was written by the threads above
+    tc_fence_before();
+    {
+      const bool v_ok = mbar_wait_bounded(bar_v, n & 1, kWaitPolls);
+      if (__syncthreads_or(v_ok ? 0 : 1)) {
+        if (tid == 0) atomicOr(p.status, KDA_ERR_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      v_pending = false;
+    }
+
+    // ---- Wk = T'(K e^G) -> TMEM 0..127, U = T'V -> 128..255 (hi | lo along K) ---------------
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        // A: T' K-major, K-step ks in region ks / 4 (hi, then lo); B: MN-major
+        // rows 16 (ks % 4) .. of K e^G and of v (the same 64 tokens twice)
+        const uint32_t a_off = static_cast<uint32_t>(ks >> 2) * REG64 + static_cast<uint32_t>(ks & 3) * 32u;
+        const uint32_t b_off = static_cast<uint32_t>(ks & 3) * 2048u;
+        const uint64_t ad = sw128_desc(sb + SM_K, 16u, 1024u) + (a_off >> 4);
+        const uint64_t bk = sw128_desc(sb + SM_Z, REG64, 1024u) + (b_off >> 4);
+        const uint64_t bv = sw128_desc(sb + SM_Q, REG64, 1024u) + (b_off >> 4);
+        mma_f16(tmem + TM_WK, ad, bk, ID_TPROD, ks > 0 ? 1u : 0u);
+        mma_f16(tmem + TM_U, ad, bv, ID_TPROD, ks > 0 ? 1u : 0u);
+      }
+      mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    if (!wait_mma()) { aborted = true; break; }
+    // q, k, z, v tiles are all consumed: the next task's inputs can come in
+    if (tid == kTmaThread && n + 1 < n_iter) issue_qkz(n + 1);
+    qkz_pending = n + 1 < n_iter;
+
+    // ---- -Wk (lanes 0..63, columns 0..127) and U (columns 128..255) to the record ---------
+    // (warps 2, 3, 6, 7 reach no TMEM lane below 64: one of them resolves task n + 2)
+    if (tid == kTaskThread && n + 2 < n_iter) put_task(n + 2);
+    if (quad < 2) {
+      const int r = quad * 32 + lane;
+      const bool is_u = warp >= 4;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float v[32];
+        tmem_ld32(t_lane + (is_u ? TM_U : TM_WK) + 32 * q4, v);
+        tmem_wait_ld();
+        if (is_u) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) range_max = fmaxf(range_max, fabsf(v[j]));
+        }
+        const float sc = is_u ? 1.f : -1.f;
+        // columns 32 q4 .. + 31: region q4 / 2, chunks 4 (q4 & 1) .. + 3
+        uint8_t *base = is_u ? rec + kRecU + (q4 >> 1) * 8192 : rec + kRecA3 + (q4 >> 1) * 16384;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4 *>(base + chunk_off(r, 4 * (q4 & 1) + j)) = make_uint4(
+              pack_f16x2(sc * v[8 * j + 0], sc * v[8 * j + 1]), pack_f16x2(sc * v[8 * j + 2], sc * v[8 * j + 3]),
+              pack_f16x2(sc * v[8 * j + 4], sc * v[8 * j + 5]), pack_f16x2(sc * v[8 * j + 6], sc * v[8 * j + 7]));
+      }
+    }
+    tc_fence_before();
+    __syncthreads();  // the TMEM columns are read before the next task's MMAs
+  }
+
+  // Drain anything still in flight (bounded) before TMEM and shared memory go.
+  if (aborted && tid == 0) {
+    if (mma_pending) mbar_wait_bounded(bar_mma, mma_phase, kWaitPolls);
+    if (qkz_pending) mbar_wait_bounded(bar_qkz, 0, kWaitPolls) || mbar_wait_bounded(bar_qkz, 1, kWaitPolls);
+    if (v_pending) mbar_wait_bounded(bar_v, 0, kWaitPolls) || mbar_wait_bounded(bar_v, 1, kWaitPolls);
+  }
+  tc_fence_before();
+  if (__syncthreads_or(range_max > 65504.f ? 1 : 0) && tid == 0) atomicOr(p.status, KDA_ERR_RANGE);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TM_COLS);
+  }
+}
+
+bool make_map(CUtensorMap *m, const void *base, int64_t total, int H, int d) {
+  EncodeTiledFn fn = tensor_map_encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(total)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(d) * 2 * H};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Persistent grid: two CTAs per SM, each taking (chunk, head) tasks in turn.
+cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                              const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
+                              const int32_t *cu_seqlens, const int32_t *chunk_start, int n_seq,
+                              int64_t total_tokens, int64_t fixed_len, int H, int dk, int dv,
+                              int h0, int hg, int64_t max_tasks, uint8_t *rec, int *status,
+                              unsigned pre, int n_sms, cudaStream_t stream) {
+  CUtensorMap mq, mk, mz, mv;
+  if (!make_map(&mq, q, total_tokens, H, dk) || !make_map(&mk, k, total_tokens, H, dk) ||
+      !make_map(&mz, z, total_tokens, H, dk) || !make_map(&mv, v, total_tokens, H, dv))
+    return cudaErrorInvalidValue;
+  cudaError_t err = cudaFuncSetAttribute(chunk_prep_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(CP_SMEM_BYTES));
+  if (err != cudaSuccess) return err;
+  CpParams prm{beta, A, gmin, cu_seqlens, chunk_start, fixed_len, n_seq, H, h0, hg, pre, rec,
+               status};
+  const int64_t ctas = max_tasks < 2LL * n_sms ? max_tasks : 2LL * n_sms;
+  if (ctas <= 0) return cudaSuccess;
+  chunk_prep_kernel<<<static_cast<unsigned>(ctas), CP_THREADS, CP_SMEM_BYTES, stream>>>(
+      mq, mk, mz, mv, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

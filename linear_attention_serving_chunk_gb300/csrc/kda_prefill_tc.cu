@@ -81,14 +81,10 @@ constexpr uint32_t SM_TF = SM_AP + 64 * 68 * 4;   // fp32 [64][65] T
 constexpr uint32_t SM_TY = SM_AP + 34 * KiB;      // fp32 [10][16][17] block products
 constexpr uint32_t SM_SBF = SM_AP;                // [dk x dv] S in fp16, MN-major (after T')
 constexpr uint32_t SM_A5 = SM_AP + 48 * KiB;      // [128 x 64] MN-major: [X ; -P] (X unused)
-// T' = T diag(beta) as bf16 hi + lo, two [128 x 64] K-major tiles.  The
-// single pass: TP = [hi ; 0], TPL = [lo ; 0] (rows 64..127 of D1 carry -O).
-// Chunk preparation stacks the halves in M instead: TP = [hi ; lo] and
-// TPL = [lo ; hi], so one MMA gives both halves of T'K~ (and of T'V) and the
-// read-out adds them across the lane quadrants.
+// T' = T diag(beta) as bf16 hi + lo, two [128 x 64] K-major tiles:
+// TP = [hi ; 0], TPL = [lo ; 0] (rows 64..127 of D1 carry -O).
 constexpr uint32_t SM_TP = SM_AP + 64 * KiB;
 constexpr uint32_t SM_TPL = SM_AP + 80 * KiB;
-constexpr uint32_t SM_XCH = SM_AP;                // chunk preparation: [2][16 KiB] bf16 exchange of the lo halves
 constexpr uint32_t SM_WBF = SM_AP + 64 * KiB;     // [tok x dv] W in fp16 (after T' is used)
 
 constexpr uint32_t SM_MISC = 224 * KiB;
@@ -100,8 +96,7 @@ constexpr uint32_t MS_BAR_V = SM_MISC + 40;
 constexpr uint32_t MS_BETA = SM_MISC + 64;        // 64 fp32
 constexpr uint32_t MS_LAM = SM_MISC + 320;        // [4][128] fp32 sub-tile decay totals
 constexpr uint32_t MS_NRM = MS_LAM + 4 * TD * 4;  // [64][2] fp32 1/||k_r||, 1/||q_r|| (pre-op)
-constexpr uint32_t MS_TASK = MS_NRM + 64 * 8;     // chunk preparation: 3 x 32-byte task slots
-constexpr uint32_t TC_SMEM_BYTES = MS_TASK + 3 * 32;
+constexpr uint32_t TC_SMEM_BYTES = MS_NRM + 64 * 8;
 static_assert(SM_TF + 64 * 65 * 4 <= SM_TY, "T scratch overlaps");
 static_assert(SM_TY + 10 * 16 * 17 * 4 <= SM_A5, "block scratch overlaps A5");
 static_assert(TC_SMEM_BYTES <= 232448, "shared memory budget");
@@ -118,18 +113,11 @@ constexpr uint32_t TM_D1 = 128;   // U -> W (rows 0..63), -O (rows 64..127)
 constexpr uint32_t TM_S = 256;    // fp32 state S (row = key channel)
 
 constexpr uint32_t TM_COLS = 512;
-constexpr uint32_t TM_COLS_PREP = 256;  // chunk preparation: no state
 
 constexpr uint32_t kWaitPolls = 1u << 24;
-// TMA loads are issued by lane 0 of warp 4 (a warp with no output stores;
-// in chunk preparation only those of k and v), the MMAs by thread 0.
+// TMA loads are issued by lane 0 of warp 4 (a warp with no output stores),
+// the MMAs by thread 0.
 constexpr int kTmaThread = 128;
-// Chunk preparation: lane 0 of warps 4..7 each store one part of the record
-// (and later wait for its own bulk group); warps 12..15 build nothing in the
-// first operand pass, so one of them issues the next task's q / z loads and
-// another resolves the task after that.
-constexpr int kQzThread = 416;
-constexpr int kTaskThread = 480;
 
 // Instruction descriptors (fp32 accumulation).
 constexpr uint32_t ID_AP = idesc_mma(128, 64, kFmtTF32, kFmtTF32, 0, 0);      // A_kk / P
@@ -158,10 +146,7 @@ struct TcParams {
   int zero_v;       // 1: treat v as zero (U = 0) and do not read it
   int s0_identity;  // 1: start every chain from S0 = I (dk = dv) instead of S0
   unsigned pre;     // KDA_PRE_* input pre-ops (L2-normalise q, k; sigmoid of beta)
-  // chunk-preparation mode: records [chunk][head in group] of heads h0 .. h0 + hg - 1
-  uint8_t *rec;
-  const int32_t *chunk_start;  // varlen: first chunk of each sequence, [n_seq + 1]
-  int n_seq, h0, hg;
+  int n_seq;
 };
 
 // Round fp32 to tf32 (nearest, ties away from zero) on the integer ALU: add
@@ -237,11 +222,7 @@ __device__ __forceinline__ void warp_mma16(const float *X, int ldx, const float 
   }
 }
 
-// kPrep = false: one CTA per (sequence, head) chain, the whole chunk step.
-// kPrep = true (chunk preparation): persistent CTAs take (chunk, head) tasks
-// of the whole batch, run the state-independent part of the step and store
-// each chunk's record (kda_split.cuh) for the state pass.
-template <bool kPrep>
+// One CTA per (sequence, head) chain, the whole chunk step, chunks in order.
 __global__ void __launch_bounds__(TC_THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
@@ -259,89 +240,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
 
   int64_t t_begin = 0, t_end = 0;
-  int n_chunks = 0;      // iterations of this CTA
-  int64_t n_tasks = 0;   // chunk preparation: (chunk, head) tasks of the batch
-  const int64_t cps = (p.fixed_len + 63) / 64;  // chunks per sequence (equal lengths)
   bool shape_bad = false;  // a device-side index was malformed (KDA_ERR_SHAPE)
   int slot = s;
-  if constexpr (!kPrep) {
-    if (p.slots) {
-      slot = p.slots[s];
-      if (slot < 0 || slot >= p.n_slots) {  // nothing of this sequence is touched
-        if (tid == 0) atomicOr(p.status, KDA_ERR_SHAPE);
-        return;
-      }
+  if (p.slots) {
+    slot = p.slots[s];
+    if (slot < 0 || slot >= p.n_slots) {  // nothing of this sequence is touched
+      if (tid == 0) atomicOr(p.status, KDA_ERR_SHAPE);
+      return;
     }
-    if (p.cu_seqlens) {
-      if (!seq_range(p.cu_seqlens, s, p.total, t_begin, t_end)) shape_bad = true;
-    } else {
-      t_begin = static_cast<int64_t>(s) * p.fixed_len;
-      t_end = t_begin + p.fixed_len;
-    }
-    n_chunks = static_cast<int>((t_end - t_begin + 63) / 64);
-  } else {
-    n_tasks = (p.cu_seqlens ? static_cast<int64_t>(p.chunk_start[p.n_seq])
-                            : static_cast<int64_t>(p.n_seq) * cps) * p.hg;
-    n_chunks = n_tasks > static_cast<int64_t>(blockIdx.x)
-                   ? static_cast<int>((n_tasks - blockIdx.x + gridDim.x - 1) / gridDim.x)
-                   : 0;
   }
-  // Iteration n's chunk: first token, length, head.
+  if (p.cu_seqlens) {
+    if (!seq_range(p.cu_seqlens, s, p.total, t_begin, t_end)) shape_bad = true;
+  } else {
+    t_begin = static_cast<int64_t>(s) * p.fixed_len;
+    t_end = t_begin + p.fixed_len;
+  }
+  int n_chunks = static_cast<int>((t_end - t_begin + 63) / 64);  // iterations of this CTA
+  // Iteration n's chunk: first token and length.
   struct Task {
     int64_t t0;
     int L, h;
   };
-  auto task_at = [&](int n) -> Task {
-    if constexpr (!kPrep) {
-      const int64_t t0 = t_begin + 64LL * n;
-      return {t0, static_cast<int>(min(static_cast<int64_t>(64), t_end - t0)), h};
-    } else {
-      const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
-      const int64_t c = t / p.hg;
-      int64_t sb0, se0, j;
-      if (p.cu_seqlens) {
-        int lo = 0, hi = p.n_seq;  // the sequence q with chunk_start[q] <= c < chunk_start[q + 1]
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (p.chunk_start[mid] <= c) lo = mid; else hi = mid;
-        }
-        sb0 = p.cu_seqlens[lo];
-        se0 = p.cu_seqlens[lo + 1];
-        j = c - p.chunk_start[lo];
-      } else {
-        const int64_t q = c / cps;
-        sb0 = q * p.fixed_len;
-        se0 = sb0 + p.fixed_len;
-        j = c - q * cps;
-      }
-      const int64_t t0 = sb0 + 64 * j;
-      return {t0, static_cast<int>(min(static_cast<int64_t>(64), se0 - t0)),
-              p.h0 + static_cast<int>(t % p.hg)};
-    }
-  };
-  // Chunk preparation resolves its tasks ahead of use: task n sits in slot
-  // n % 3, written during iteration n - 2 by an idle thread (a varlen task
-  // takes a binary search over chunk_start and two cu_seqlens loads, a chain
-  // of dependent global loads that would stall whoever needs the task).
-  // A slot also carries the head's decay constant -e^{A_h} log2(e).
-  auto put_task = [&](int n) {
-    const Task tk = task_at(n);
-    const uint32_t slot = sb + MS_TASK + 32u * static_cast<uint32_t>(n % 3);
-    S.u128(slot) = make_uint4(static_cast<uint32_t>(tk.t0), static_cast<uint32_t>(tk.t0 >> 32),
-                              static_cast<uint32_t>(tk.L), static_cast<uint32_t>(tk.h));
-    S.f32(slot + 16) = -__expf(p.A[tk.h]) * 1.4426950408889634f;
-  };
   auto task_of = [&](int n) -> Task {
-    if constexpr (kPrep) {
-      const uint4 w = S.u128(sb + MS_TASK + 32u * static_cast<uint32_t>(n % 3));
-      return {static_cast<int64_t>((static_cast<uint64_t>(w.y) << 32) | w.x),
-              static_cast<int>(w.z), static_cast<int>(w.w)};
-    } else {
-      return task_at(n);
-    }
+    const int64_t t0 = t_begin + 64LL * n;
+    return {t0, static_cast<int>(min(static_cast<int64_t>(64), t_end - t0)), h};
   };
   int64_t snap_row = 0;
-  bool want_snaps = !kPrep && p.snaps != nullptr;
+  bool want_snaps = p.snaps != nullptr;
   if (want_snaps) {
     snap_row = p.snap_offsets ? snap_first_row(p.snap_offsets, s, p.n_seq, t_end - t_begin)
                               : static_cast<int64_t>(s) * (p.fixed_len / 64);
@@ -351,10 +276,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   }
   const float kLog2e = 1.4426950408889634f;
-  float dc1 = kPrep ? 0.f : -__expf(p.A[h]) * kLog2e;  // chunk preparation: per task
+  const float dc1 = -__expf(p.A[h]) * kLog2e;
   const float dc2 = p.gmin * kLog2e;
   const int DK = p.dk, DV = p.dv;
-  const size_t state_off = kPrep ? 0 : (static_cast<size_t>(slot) * H + h) * DK * DV;
+  const size_t state_off = (static_cast<size_t>(slot) * H + h) * DK * DV;
 
   const uint32_t bar_qz0 = sb + MS_BAR_QZ, bar_k = sb + MS_BAR_K, bar_v = sb + MS_BAR_V,
                  bar_mma = sb + MS_BAR_MMA;
@@ -371,14 +296,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     prefetch_tensormap(&tm_v);
   }
   if (warp == 1) {
-    tmem_alloc(sb + MS_TMEM, kPrep ? TM_COLS_PREP : TM_COLS);
+    tmem_alloc(sb + MS_TMEM, TM_COLS);
     tmem_relinquish();
-  }
-  if constexpr (kPrep) {
-    if (tid == 64) {
-      if (n_chunks > 0) put_task(0);
-      if (n_chunks > 1) put_task(1);
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -405,7 +324,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // Initial state -> TMEM (row trow, columns [32 q4, 32 q4 + 32)); rows and
   // columns beyond dk, dv are zero.
   const bool row_in = trow < DK, cols_in = 32 * q4 < DV;
-  if constexpr (!kPrep) {
+  {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
@@ -456,7 +375,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const Task tk = task_of(0);
     if (tid < tk.L) beta_raw = p.beta[static_cast<size_t>(tk.t0 + tid) * H + tk.h];
   }
-  const bool rec_thread = kPrep && lane == 0 && warp >= 4 && warp < 8;
   // A full chunk's snapshot is written from the next chunk's state read-out
   // (or after the last chunk): the row it goes to, or -1.
   int64_t snap_pending = -1;
@@ -518,15 +436,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const Task tk = task_of(n);
     const int64_t t0 = tk.t0;
     const int L = tk.L;
-    if constexpr (kPrep) dc1 = S.f32(sb + MS_TASK + 32u * static_cast<uint32_t>(n % 3) + 16);
     const uint32_t a3 = sb + SM_A3 + par * A3_BYTES;
     const uint32_t zb = sb + SM_ZB + par * TILE_BYTES;
 
     // Prefetch the next chunk's q and z into the other parity buffers.  (The
     // threads that last wrote those buffers fenced their generic-proxy
-    // writes before the barrier that ended the previous chunk.)  Chunk
-    // preparation issues it later, once the previous record has been read.
-    if (!kPrep && tid == kTmaThread && n + 1 < n_chunks) issue_qz(n + 1);
+    // writes before the barrier that ended the previous chunk.)
+    if (tid == kTmaThread && n + 1 < n_chunks) issue_qz(n + 1);
     if (n + 1 < n_chunks) qz_pending |= 1u << (par ^ 1);
     // beta of this chunk was loaded one chunk ahead (logits pass through a sigmoid)
     if (tid < 64) {
@@ -608,10 +524,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           beta_raw = ldg_u16_pinned(p.beta + static_cast<size_t>(nx.t0 + tid) * H + nx.h);
       }
     }
-    // Chunk preparation: the previous record's bulk stores must have read
-    // A3 / ZB [par ^ 1], A5 and the U tile before they are overwritten (the
-    // next task's q, z and the work region, both after the barrier below).
-    if (rec_thread) bulk_wait_read0();
     if (!wait_all(bar_k, n & 1)) { aborted = true; break; }  // also orders the Lam table
     k_pending = false;
     if (L < 64) {
@@ -701,10 +613,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const float f1_0 = colf(0, l1), f1_1 = colf(1, l1), f1_2 = colf(2, l1), f1_3 = colf(3, l1);
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
-        if constexpr (kPrep) {
-          if (pp == 0 && tid == kQzThread && n + 1 < n_chunks) issue_qz(n + 1);
-          if (pp == 0 && tid == kTaskThread && n + 2 < n_chunks) put_task(n + 2);
-        }
         if (2 * pp + 1 >= R) {
           // column factors of the two Khat blocks of this pass
           const float fa0 = pp ? f0_2 : f0_0, fa1 = pp ? f1_2 : f1_0;
@@ -828,18 +736,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     auto put_tp16 = [&](uint32_t off, unsigned short hi, unsigned short lo) {
       S.u16(sb + SM_TP + off) = hi;
       S.u16(sb + SM_TPL + off) = lo;
-      if constexpr (kPrep) {
-        S.u16(sb + SM_TP + 8 * KiB + off) = lo;
-        S.u16(sb + SM_TPL + 8 * KiB + off) = hi;
-      }
     };
     auto put_tp32 = [&](uint32_t off, uint32_t hi, uint32_t lo) {
       S.u32(sb + SM_TP + off) = hi;
       S.u32(sb + SM_TPL + off) = lo;
-      if constexpr (kPrep) {
-        S.u32(sb + SM_TP + 8 * KiB + off) = lo;
-        S.u32(sb + SM_TPL + 8 * KiB + off) = hi;
-      }
     };
     {
       // Column jc of the inverse of diagonal block Rd by column updates (once
@@ -990,27 +890,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
       tc_fence_after();
       // T'K~ and T'V interleaved K-step by K-step (independent accumulators)
-      if constexpr (kPrep) {
-        // [hi ; lo] K~ and [lo ; hi] V: the halves land in different lane quadrants
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // T' hi, then T' lo
+        const uint32_t tp = h ? sb + SM_TPL : sb + SM_TP;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          issue_mma_step(tmem + TM_AP, sb + SM_TP, false, REG128, a3, true, REG128, ks, ID_TPROD,
-                         ks > 0 ? 1u : 0u);
-          issue_mma_step(tmem + TM_D1, sb + SM_TPL, false, REG128, sb + SM_VB, true, REG64, ks,
-                         ID_TPROD, ks > 0 ? 1u : 0u);
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {  // T' hi, then T' lo
-          const uint32_t tp = h ? sb + SM_TPL : sb + SM_TP;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t acc = (h > 0 || ks > 0) ? 1u : 0u;
-            issue_mma_step(tmem + TM_AP, tp, false, REG128, a3, true, REG128, ks, ID_TPROD, acc);
-            if (!p.zero_v)
-              issue_mma_step(tmem + TM_D1, tp, false, REG128, sb + SM_VB, true, REG64, ks,
-                             ID_TPROD, acc);
-          }
+          const uint32_t acc = (h > 0 || ks > 0) ? 1u : 0u;
+          issue_mma_step(tmem + TM_AP, tp, false, REG128, a3, true, REG128, ks, ID_TPROD, acc);
+          if (!p.zero_v)
+            issue_mma_step(tmem + TM_D1, tp, false, REG128, sb + SM_VB, true, REG64, ks,
+                           ID_TPROD, acc);
         }
       }
       mma_commit(bar_mma);
@@ -1022,68 +911,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (n + 1 < n_chunks) v_pending = true;
     }
 
-    if constexpr (kPrep) {
-      // ---- the chunk's record: -Wk -> A3 rows 0..63, U -> fp16 tile, gamma; then
-      //      A3 (with -Q~), K' (ZB), -P (A5 rows 64..127) and U go out as bulk stores.
-      const int64_t task = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
-      uint8_t *rec = p.rec + static_cast<size_t>(task) * kRecBytes;
-      {
-        // Lanes 0..63 hold the hi half of T'K~ and the lo half of T'V, lanes
-        // 64..127 the other two.  Each quadrant pair passes its lo half (small:
-        // bf16 keeps it to ~2^-17 of the sum) through the exchange tile
-        // [16 column chunks][64 rows][8 bf16] and finishes one product:
-        // lanes 0..63 -Wk, lanes 64..127 U.
-        const int r = trow & 63;
-        const bool top = quad < 2;
-        float v[32], x[32];
-        tmem_ld32(t_lane + (top ? TM_D1 : TM_AP) + 32 * q4, x);
-        tmem_ld32(t_lane + (top ? TM_AP : TM_D1) + 32 * q4, v);
-        tmem_wait_ld();
-        const uint32_t xo = sb + SM_XCH + (top ? 16 * KiB : 0);  // lo of Wk at 0, of U at 16 KiB
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          S.u128(xo + static_cast<uint32_t>(((4 * q4 + j) * 64 + r) * 16)) =
-              make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]), pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
-                         pack_bf16x2(x[8 * j + 4], x[8 * j + 5]), pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
-        if (!top && q4 < 2) {  // warps 2, 3, 6, 7: gamma, one key channel per thread
-          const int c = (2 * q4 + quad - 2) * 32 + lane;
-          float gam = 1.f;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) gam *= S.f32(sb + MS_LAM + 4 * (m * TD + c));
-          reinterpret_cast<float *>(rec + kRecG)[c] = gam;
-        }
-        __syncthreads();
-        const uint32_t xi = sb + SM_XCH + (top ? 0 : 16 * KiB);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 w = S.u128(xi + static_cast<uint32_t>(((4 * q4 + j) * 64 + r) * 16));
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = unpack_bf16x2(ws[e]);
-            v[8 * j + 2 * e] += f.x;
-            v[8 * j + 2 * e + 1] += f.y;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) range_max = fmaxf(range_max, fabsf(v[j]));
-        if (top)
-          store_row32_f16(S, a3, r, q4, REG128, v, -1.f);
-        else
-          store_row32_f16(S, sb + SM_WBF, r, q4, REG64, v, 1.f);
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      __syncthreads();
-      if (rec_thread) {  // one bulk store per thread, issued side by side
-        if (warp == 4) bulk_s2g(rec + kRecA3, a3, 32 * KiB);
-        if (warp == 5) bulk_s2g(rec + kRecKP, zb, 16 * KiB);
-        if (warp == 6) bulk_s2g(rec + kRecU, sb + SM_WBF, 16 * KiB);
-        if (warp == 7) bulk_s2g(rec + kRecP, sb + SM_A5 + 8 * KiB, 8 * KiB);
-        bulk_commit();
-      }
-      continue;
-    } else {
 
     // -Wk -> A3 rows 0..63;  S (fp32, TMEM) -> fp16 S for the MMA, then S *= e^{G_last}.
     {
@@ -1196,10 +1023,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (L == 64) ++snap_row;
     tc_fence_before();
     __syncthreads();
-    }  // !kPrep
-  }
-  if constexpr (kPrep) {
-    if (rec_thread) bulk_wait0();  // the last record is out before the CTA ends
   }
 
   if (!aborted && (p.S_final || snap_pending >= 0)) {
@@ -1238,7 +1061,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (shape_bad && tid == 0) atomicOr(p.status, KDA_ERR_SHAPE);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kPrep ? TM_COLS_PREP : TM_COLS);
+    tmem_dealloc(tmem, TM_COLS);
   }
 }
 
@@ -1279,40 +1102,17 @@ cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
       !make_map(&mz, z, total_tokens, H, dk) ||
       !make_map(&mv, zero_v ? k : v, total_tokens, H, zero_v ? dk : dv))
     return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel<false>,
+  cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(TC_SMEM_BYTES));
   if (err != cudaSuccess) return err;
   TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, total_tokens, H, S0, o, S_final, snaps,
                snap_offsets, status, slots, n_slots, dk, dv, test_stall, zero_v, s0_identity,
-               pre, nullptr, nullptr, n_seq, 0, H};
+               pre, n_seq};
   const dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(n_seq));
-  prefill_tc_kernel<false><<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(mq, mk, mz, mv, prm);
+  prefill_tc_kernel<<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(mq, mk, mz, mv, prm);
   return cudaGetLastError();
 }
 
-cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
-                              const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
-                              const int32_t *cu_seqlens, const int32_t *chunk_start, int n_seq,
-                              int64_t total_tokens, int64_t fixed_len, int H, int dk, int dv,
-                              int h0, int hg, int64_t max_tasks, uint8_t *rec, int *status,
-                              unsigned pre, int n_ctas, cudaStream_t stream) {
-  CUtensorMap mq, mk, mz, mv;
-  if (!make_map(&mq, q, total_tokens, H, dk) || !make_map(&mk, k, total_tokens, H, dk) ||
-      !make_map(&mz, z, total_tokens, H, dk) || !make_map(&mv, v, total_tokens, H, dv))
-    return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(prefill_tc_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(TC_SMEM_BYTES));
-  if (err != cudaSuccess) return err;
-  TcParams prm{beta, A, gmin, cu_seqlens, fixed_len, total_tokens, H, nullptr, nullptr,
-               nullptr, nullptr, nullptr, status, nullptr, 0, dk, dv, 0, 0, 0, pre, rec,
-               chunk_start, n_seq, h0, hg};
-  const int64_t ctas = max_tasks < n_ctas ? max_tasks : n_ctas;
-  if (ctas <= 0) return cudaSuccess;
-  prefill_tc_kernel<true><<<static_cast<unsigned>(ctas), TC_THREADS, TC_SMEM_BYTES, stream>>>(
-      mq, mk, mz, mv, prm);
-  return cudaGetLastError();
-}
 
 }  // namespace kda

@@ -41,7 +41,6 @@ using namespace sm100;
 using namespace tcx;
 
 constexpr int SP_THREADS = 512;
-constexpr int TD = 128;
 constexpr int NC = 64;  // value columns of the state per CTA (two CTAs per chain)
 
 // One stage holds one record, with only this CTA's half of U:

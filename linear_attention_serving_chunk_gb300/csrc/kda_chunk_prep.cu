@@ -36,12 +36,13 @@
 // 64 (w % 2) + 8s + 2t and + 1.  The running products along the tokens of a
 // sub-tile are shuffle scans over g.
 //
-// Per task (persistent CTAs, two per SM: 256 threads, < 110 KB of shared
+// Per task (persistent CTAs, two per SM: 256 threads, 108 KB of shared
 // memory, 256 TMEM columns each):
-//   TMA    q, k, z (one barrier), v (after the operand build)
+//   TMA    z (prefetched while the previous chunk runs), q and k, v (after
+//          the operand build)
 //   SIMT   gate, scans, sub-tile totals; then every operand: [KE ; QE] and
-//          the stacked Kc (fp16, shared memory), K e^G (bf16), and -Q e^G,
-//          K' (fp16, straight to the record); diagonal tiles by mma.sync
+//          the stacked Kc (fp16, shared memory), K e^G (bf16, over k), and
+//          -Q e^G, K' (fp16, straight to the record); diagonal tiles by mma.sync
 //   MMA    off-diagonal A_kk / P tiles (M128 N128 K128, fp16)
 //   SIMT   A_kk to shared memory (fp32, transposed), -P to the record;
 //          T by diagonal-block column updates and (I - E + E^2 - E^3) D for
@@ -67,24 +68,30 @@ constexpr int CP_THREADS = 256;
 
 // Shared-memory map (byte offsets from the 1024-aligned dynamic base).
 constexpr uint32_t SM_Q = 0;              // q tile [64 tok x 128] bf16, then v
-constexpr uint32_t SM_K = 16 * KiB;       // k tile, then T' = [hi | lo] (K-major)
-constexpr uint32_t SM_Z = 32 * KiB;       // z tile, then K e^G (bf16, MN-major)
+constexpr uint32_t SM_K = 16 * KiB;       // k tile, rewritten in place as K e^G (bf16, MN-major)
+constexpr uint32_t SM_Z = 32 * KiB;       // z tile (the next chunk's once the scans have read it)
 constexpr uint32_t SM_KQ = 48 * KiB;      // [KE ; QE] fp16 K-major, 128 rows; then scratch
 constexpr uint32_t SM_KC = 80 * KiB;      // stacked Kc fp16 K-major, 96 rows
 constexpr uint32_t KC_REGION = 12 * KiB;  // its two 64-channel regions
+// T' = T diag(beta) as bf16 hi (K columns 0..63) | lo (64..127), K-major, in
+// the Kc tile once the off-diagonal MMA has read it.  Its M = 128 operand
+// reads rows 64..127 of each region too (they only feed unused rows of D):
+// those of the lo region end 24 KiB after SM_TP, inside the Kc tile.
+constexpr uint32_t SM_TP = SM_KC;
 // scratch of the triangular inverse, in the [KE ; QE] tile once the off-diagonal MMA is done
 constexpr uint32_t SM_AKK = SM_KQ;                     // fp32 [64][68]: A_kk transposed, [i][r]
 constexpr uint32_t SM_TD = SM_AKK + 64 * 68 * 4;       // fp32 [4][16][17]: diagonal blocks of T
 constexpr uint32_t SM_XS = SM_TD + 4 * 16 * 17 * 4;    // fp32 [10][16][17]: block products
 static_assert(SM_XS + 10 * 16 * 17 * 4 <= SM_KC, "inverse scratch overflows the KE/QE tile");
 constexpr uint32_t SM_MISC = 104 * KiB;
-constexpr uint32_t MS_BAR_QKZ = SM_MISC;          // mbarriers: q/k/z in, v in, MMA done
-constexpr uint32_t MS_BAR_V = SM_MISC + 8;
-constexpr uint32_t MS_BAR_MMA = SM_MISC + 16;
-constexpr uint32_t MS_TMEM = SM_MISC + 24;
-constexpr uint32_t MS_TASK = SM_MISC + 32;        // 3 task slots of 32 bytes
-constexpr uint32_t MS_BETA = SM_MISC + 128;       // [64] fp32
-constexpr uint32_t MS_LAM = SM_MISC + 384;        // [128 channels][4 sub-tiles] fp32
+constexpr uint32_t MS_BAR_Z = SM_MISC;            // mbarriers: z in, q/k in, v in, MMA done
+constexpr uint32_t MS_BAR_QK = SM_MISC + 8;
+constexpr uint32_t MS_BAR_V = SM_MISC + 16;
+constexpr uint32_t MS_BAR_MMA = SM_MISC + 24;
+constexpr uint32_t MS_TMEM = SM_MISC + 32;
+constexpr uint32_t MS_TASK = SM_MISC + 64;        // 3 task slots of 32 bytes
+constexpr uint32_t MS_BETA = SM_MISC + 160;       // [64] fp32
+constexpr uint32_t MS_LAM = SM_MISC + 416;        // [128 channels][4 sub-tiles] fp32
 constexpr uint32_t MS_NSQ = MS_LAM + 128 * 16;    // [64 tok][2 halves] (k.k, q.q) partial sums
 // The M = 128 Kc operand reads 128 rows of each region: its second region's
 // unused rows 96..127 end 28 KiB after SM_KC, so the allocation reaches there.
@@ -122,11 +129,14 @@ __device__ __forceinline__ uint32_t tf32_rna(float x) {
 }
 
 // Raw bf16 global load kept where it is written (a prefetch the compiler must
-// not sink to its use).
-__device__ __forceinline__ unsigned short ldg_u16_pinned(const kda_bf16 *ptr) {
-  unsigned short raw;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(raw) : "l"(ptr));
-  return raw;
+// not sink to its use), predicated inside the instruction: raw keeps its
+// value when `take` is 0, so no select waits for the load here.
+__device__ __forceinline__ void ldg_u16_prefetch(unsigned short &raw, const kda_bf16 *ptr,
+                                                 int take) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t@p ld.global.nc.u16 %0, [%1];\n\t}"
+      : "+h"(raw)
+      : "l"(ptr), "r"(take));
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -269,9 +279,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             static_cast<int>(w.w), S.f32(slot + 16)};
   };
 
-  const uint32_t bar_qkz = sb + MS_BAR_QKZ, bar_v = sb + MS_BAR_V, bar_mma = sb + MS_BAR_MMA;
+  const uint32_t bar_z = sb + MS_BAR_Z, bar_qk = sb + MS_BAR_QK, bar_v = sb + MS_BAR_V,
+                 bar_mma = sb + MS_BAR_MMA;
   if (tid == 0) {
-    mbar_init(bar_qkz, 1);
+    mbar_init(bar_z, 1);
+    mbar_init(bar_qk, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
     fence_mbar_init();
@@ -293,25 +305,33 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + MS_TMEM);
 
-  auto issue_qkz = [&](int n) {
+  // Loads: z on its own barrier (the next chunk's z comes in as soon as this
+  // chunk's scans have read it), q and k together (once this chunk's T'
+  // products are done), v once the operand build has read q.
+  auto load2 = [&](uint32_t dst, const CUtensorMap *map, int n, uint32_t bar) {
     const Task tk = task_of(n);
-    const int t0 = static_cast<int>(tk.t0);
-    mbar_expect_tx(bar_qkz, 3 * TILE);
-    tma_load_3d(sb + SM_Q, &tm_q, 0, tk.h, t0, bar_qkz);
-    tma_load_3d(sb + SM_Q + REG64, &tm_q, 64, tk.h, t0, bar_qkz);
-    tma_load_3d(sb + SM_K, &tm_k, 0, tk.h, t0, bar_qkz);
-    tma_load_3d(sb + SM_K + REG64, &tm_k, 64, tk.h, t0, bar_qkz);
-    tma_load_3d(sb + SM_Z, &tm_z, 0, tk.h, t0, bar_qkz);
-    tma_load_3d(sb + SM_Z + REG64, &tm_z, 64, tk.h, t0, bar_qkz);
+    tma_load_3d(dst, map, 0, tk.h, static_cast<int>(tk.t0), bar);
+    tma_load_3d(dst + REG64, map, 64, tk.h, static_cast<int>(tk.t0), bar);
+  };
+  auto issue_z = [&](int n) {
+    mbar_expect_tx(bar_z, TILE);
+    load2(sb + SM_Z, &tm_z, n, bar_z);
+  };
+  auto issue_qk = [&](int n) {
+    mbar_expect_tx(bar_qk, 2 * TILE);
+    load2(sb + SM_Q, &tm_q, n, bar_qk);
+    load2(sb + SM_K, &tm_k, n, bar_qk);
   };
   auto issue_v = [&](int n) {
-    const Task tk = task_of(n);
     mbar_expect_tx(bar_v, TILE);
-    tma_load_3d(sb + SM_Q, &tm_v, 0, tk.h, static_cast<int>(tk.t0), bar_v);
-    tma_load_3d(sb + SM_Q + REG64, &tm_v, 64, tk.h, static_cast<int>(tk.t0), bar_v);
+    load2(sb + SM_Q, &tm_v, n, bar_v);
   };
-  if (tid == kTmaThread && n_iter > 0) issue_qkz(0);
-  bool qkz_pending = n_iter > 0, v_pending = false, mma_pending = false, aborted = false;
+  if (tid == kTmaThread && n_iter > 0) {
+    issue_z(0);
+    issue_qk(0);
+  }
+  bool z_pending = n_iter > 0, qk_pending = n_iter > 0, v_pending = false;
+  bool mma_pending = false, aborted = false;
   uint32_t mma_phase = 0;
   float range_max = 0.f;
 
@@ -349,48 +369,65 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint8_t *rec = p.rec + static_cast<size_t>(task) * kRecBytes;
     // this chunk's beta (raw bits, widened after the operand build)
     unsigned short beta_raw = 0;
-    if (tid < 64 && tid < L) beta_raw = ldg_u16_pinned(p.beta + static_cast<size_t>(tk.t0 + tid) * H + h);
+    if (tid < 64)
+      ldg_u16_prefetch(beta_raw, p.beta + static_cast<size_t>(tk.t0 + min(tid, L - 1)) * H + h,
+                       tid < L);
 
-    if (!wait_all(bar_qkz, n & 1)) { aborted = true; break; }
-    qkz_pending = false;
+    if (!wait_all(bar_z, n & 1)) { aborted = true; break; }
+    z_pending = false;
 
     // ---- phase 1: gate, running products along the tokens, sub-tile totals --------------
     // F[s][0..3] = (ra, c), (ra, c + 1), (rb, c), (rb, c + 1) for c = 64 hc + 8 s + 2 t.
     float F[8][4];
     const bool ina = ra < L, inb = rb < L;
+    // four k-steps at a time: 16 independent gate values, then each scan round
+    // over all 16, so the shuffle and transcendental latencies overlap
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t off = reg + static_cast<uint32_t>(4 * t);
-      const float2 za = unpack_bf16x2(S.u32(sb + SM_Z + off + chunk_off(ra, s)));
-      const float2 zb = unpack_bf16x2(S.u32(sb + SM_Z + off + chunk_off(rb, s)));
-      float x[4] = {ina ? fast_decay2(tk.dc1, c2, za.x) : 1.f,
-                    ina ? fast_decay2(tk.dc1, c2, za.y) : 1.f,
-                    inb ? fast_decay2(tk.dc1, c2, zb.x) : 1.f,
-                    inb ? fast_decay2(tk.dc1, c2, zb.y) : 1.f};
+    for (int s0 = 0; s0 < 8; s0 += 4) {
+      float x[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t off = reg + static_cast<uint32_t>(4 * t);
+        const float2 za = unpack_bf16x2(S.u32(sb + SM_Z + off + chunk_off(ra, s0 + u)));
+        const float2 zb = unpack_bf16x2(S.u32(sb + SM_Z + off + chunk_off(rb, s0 + u)));
+        x[u][0] = ina ? fast_decay2(tk.dc1, c2, za.x) : 1.f;
+        x[u][1] = ina ? fast_decay2(tk.dc1, c2, za.y) : 1.f;
+        x[u][2] = inb ? fast_decay2(tk.dc1, c2, zb.x) : 1.f;
+        x[u][3] = inb ? fast_decay2(tk.dc1, c2, zb.y) : 1.f;
+      }
       // inclusive products over g (lanes 4 apart) for tokens ra and rb separately
 #pragma unroll
       for (int d = 1; d < 8; d <<= 1) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float y = __shfl_up_sync(0xffffffffu, x[e], 4 * d);
-          if (g >= d) x[e] *= y;
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float y = __shfl_up_sync(0xffffffffu, x[u][e], 4 * d);
+            if (g >= d) x[u][e] *= y;
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        // tokens rb continue from the product of all eight ra tokens (held at g = 7)
+        const float ta0 = __shfl_sync(0xffffffffu, x[u][0], 28 + t);
+        const float ta1 = __shfl_sync(0xffffffffu, x[u][1], 28 + t);
+        F[s0 + u][0] = x[u][0];
+        F[s0 + u][1] = x[u][1];
+        F[s0 + u][2] = x[u][2] * ta0;
+        F[s0 + u][3] = x[u][3] * ta1;
+        if (g == 7) {  // the sub-tile's totals Lam_R of channels c, c + 1
+          const int c = 64 * hc + 8 * (s0 + u) + 2 * t;
+          S.f32(sb + MS_LAM + 16 * c + 4 * R) = F[s0 + u][2];
+          S.f32(sb + MS_LAM + 16 * (c + 1) + 4 * R) = F[s0 + u][3];
         }
       }
-      // tokens rb continue from the product of all eight ra tokens (held at g = 7)
-      const float ta0 = __shfl_sync(0xffffffffu, x[0], 28 + t);
-      const float ta1 = __shfl_sync(0xffffffffu, x[1], 28 + t);
-      x[2] *= ta0;
-      x[3] *= ta1;
-      F[s][0] = x[0];
-      F[s][1] = x[1];
-      F[s][2] = x[2];
-      F[s][3] = x[3];
-      if (g == 7) {  // the sub-tile's totals Lam_R of channels c, c + 1
-        const int c = 64 * hc + 8 * s + 2 * t;
-        S.f32(sb + MS_LAM + 16 * c + 4 * R) = x[2];
-        S.f32(sb + MS_LAM + 16 * (c + 1) + 4 * R) = x[3];
-      }
     }
+    // q and k (loaded since the previous chunk's T' products); the barrier also
+    // ends every read of z: the next chunk's z may come in
+    if (!wait_all(bar_qk, n & 1)) { aborted = true; break; }
+    qk_pending = false;
+    if (tid == kTmaThread && n + 1 < n_iter) issue_z(n + 1);
+    z_pending = n + 1 < n_iter;
     if (l2n) {
       // sums of squares of this warp's 64 channels of tokens ra, rb (k and q)
       float ska = 0.f, skb = 0.f, sqa = 0.f, sqb = 0.f;
@@ -418,7 +455,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         S.u64(sb + MS_NSQ + 16 * rb + 8 * hc) = make_uint2(__float_as_uint(skb), __float_as_uint(sqb));
       }
     }
-    __syncthreads();  // B1: totals (and norms) in; z is read out
+    __syncthreads();  // B1: totals (and norms) in
 
     // ---- phase 2: operands ------------------------------------------------------------------
     float nka = 1.f, nkb = 1.f, nqa = 1.f, nqb = 1.f;  // 1 / ||row|| with the pre-op
@@ -440,9 +477,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int e = 0; e < 4; ++e) dacc[i][e] = 0.f;
-    // record words to transpose across the quad: [0..1] -Q e^G rows ra / rb of
-    // chunks s & 3 ... ; filled for s = 4 u .. 4 u + 3 then stored
-    uint32_t wq_a[4], wq_b[4], wk_a[4], wk_b[4];
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       const int c = 64 * hc + 8 * s + 2 * t;
@@ -451,8 +485,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float2 kb = unpack_bf16x2(S.u32(sb + SM_K + off + chunk_off(rb, s)));
       float2 qa = unpack_bf16x2(S.u32(sb + SM_Q + off + chunk_off(ra, s)));
       float2 qb = unpack_bf16x2(S.u32(sb + SM_Q + off + chunk_off(rb, s)));
-      ka.x *= nka; ka.y *= nka; kb.x *= nkb; kb.y *= nkb;
-      qa.x *= nqa; qa.y *= nqa; qb.x *= nqb; qb.y *= nqb;
+      if (l2n || !ina || !inb) {  // the pre-op's norms; zero rows past the chunk's end
+        ka.x *= nka; ka.y *= nka; kb.x *= nkb; kb.y *= nkb;
+        qa.x *= nqa; qa.y *= nqa; qb.x *= nqb; qb.y *= nqb;
+      }
       // sub-tile totals of channels c, c + 1
       const float4 l0 = *reinterpret_cast<const float4 *>(S.ptr(sb + MS_LAM + 16 * c));
       const float4 l1 = *reinterpret_cast<const float4 *>(S.ptr(sb + MS_LAM + 16 * (c + 1)));
@@ -476,33 +512,22 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       S.u32(kq + chunk_off(rb, s)) = pack_f16x2(keb0, keb1);
       S.u32(kq + chunk_off(64 + ra, s)) = pack_f16x2(qea0, qea1);
       S.u32(kq + chunk_off(64 + rb, s)) = pack_f16x2(qeb0, qeb1);
-      // K e^G = KE prod_{M<R} Lam (bf16, B operand of T'(K e^G)), over z
-      S.u32(sb + SM_Z + off + chunk_off(ra, s)) = pack_bf16x2(kea0 * pre0, kea1 * pre1);
-      S.u32(sb + SM_Z + off + chunk_off(rb, s)) = pack_bf16x2(keb0 * pre0, keb1 * pre1);
+      // K e^G = KE prod_{M<R} Lam (bf16, B operand of T'(K e^G)): each thread
+      // overwrites exactly the k elements it has just read
+      S.u32(sb + SM_K + off + chunk_off(ra, s)) = pack_bf16x2(kea0 * pre0, kea1 * pre1);
+      S.u32(sb + SM_K + off + chunk_off(rb, s)) = pack_bf16x2(keb0 * pre0, keb1 * pre1);
       // -Q e^G and K' = k B prod_{M>R} Lam (record words; B = Lam_R / F)
       const float ba0 = lr0 * ia0, ba1 = lr1 * ia1, bb0 = lr0 * ib0, bb1 = lr1 * ib1;
-      const uint32_t nq_a = pack_f16x2(-qea0 * pre0, -qea1 * pre1);
-      const uint32_t nq_b = pack_f16x2(-qeb0 * pre0, -qeb1 * pre1);
-      const uint32_t kp_a = pack_f16x2(ka.x * ba0 * post0, ka.y * ba1 * post1);
-      const uint32_t kp_b = pack_f16x2(kb.x * bb0 * post0, kb.y * bb1 * post1);
-      wq_a[s & 3] = nq_a; wq_b[s & 3] = nq_b; wk_a[s & 3] = kp_a; wk_b[s & 3] = kp_b;
-      if ((s & 3) == 3) {
-        // lanes t of the quad hold the four words of chunk s' for s' = 4u..4u+3;
-        // after the transpose lane t holds chunk 4u + t of both rows
-        quad_transpose(wq_a, t);
-        quad_transpose(wq_b, t);
-        quad_transpose(wk_a, t);
-        quad_transpose(wk_b, t);
-        const int ch = (s & 4) + t;  // chunk inside the 64-channel region
-        // A3 rows 64 + tok: two regions of 128 rows; KP: two regions of 64 rows
-        uint4 *a3a = reinterpret_cast<uint4 *>(rec + kRecA3 + hc * 16384 + chunk_off(64 + ra, ch));
-        uint4 *a3b = reinterpret_cast<uint4 *>(rec + kRecA3 + hc * 16384 + chunk_off(64 + rb, ch));
-        uint4 *kpa = reinterpret_cast<uint4 *>(rec + kRecKP + hc * 8192 + chunk_off(ra, ch));
-        uint4 *kpb = reinterpret_cast<uint4 *>(rec + kRecKP + hc * 8192 + chunk_off(rb, ch));
-        *a3a = make_uint4(wq_a[0], wq_a[1], wq_a[2], wq_a[3]);
-        *a3b = make_uint4(wq_b[0], wq_b[1], wq_b[2], wq_b[3]);
-        *kpa = make_uint4(wk_a[0], wk_a[1], wk_a[2], wk_a[3]);
-        *kpb = make_uint4(wk_b[0], wk_b[1], wk_b[2], wk_b[3]);
+      // record rows: -Q e^G in A3 rows 64 + tok (two regions of 128 rows), K'
+      // in KP (two regions of 64 rows); the four lanes t of a quad write one
+      // 16-byte chunk together
+      {
+        uint8_t *a3 = rec + kRecA3 + hc * 16384 + 4 * t;
+        uint8_t *kp = rec + kRecKP + hc * 8192 + 4 * t;
+        *reinterpret_cast<uint32_t *>(a3 + chunk_off(64 + ra, s)) = pack_f16x2(-qea0 * pre0, -qea1 * pre1);
+        *reinterpret_cast<uint32_t *>(a3 + chunk_off(64 + rb, s)) = pack_f16x2(-qeb0 * pre0, -qeb1 * pre1);
+        *reinterpret_cast<uint32_t *>(kp + chunk_off(ra, s)) = pack_f16x2(ka.x * ba0 * post0, ka.y * ba1 * post1);
+        *reinterpret_cast<uint32_t *>(kp + chunk_off(rb, s)) = pack_f16x2(kb.x * bb0 * post0, kb.y * bb1 * post1);
       }
       // Kc rows of the later sub-tiles R' > R: k B prod_{R<M<R'} Lam, stacked at
       // rows 0 (R' = 1, 16 rows), 16 (R' = 2, 32 rows), 48 (R' = 3, 48 rows)
@@ -560,9 +585,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mma_pending = true;
     if (tid == kTmaThread) issue_v(n);
     v_pending = true;
-    // T' tiles start at zero (the inverse writes the lower triangle only)
-    for (int x = tid; x < 1024; x += CP_THREADS) S.u128(sb + SM_K + 16 * x) = make_uint4(0, 0, 0, 0);
     if (!wait_mma()) { aborted = true; break; }
+    // the Kc tile is consumed: T' starts at zero there (the inverse writes the
+    // lower triangle only; the barriers below order these stores before it)
+    for (int x = tid; x < 1024; x += CP_THREADS) S.u128(sb + SM_TP + 16 * x) = make_uint4(0, 0, 0, 0);
 
     // ---- read-outs: A_kk (transposed, fp32) to shared memory, -P to the record --------------
     // TMEM lane m is stacked row m of Kc: sub-tile R' = 1 for m < 16, 2 for m < 48,
@@ -649,8 +675,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const __nv_bfloat16 hi = __float2bfloat16_rn(v);
       const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
       const uint32_t o = sw128_off(r, col, REG64);
-      S.u16(sb + SM_K + o) = *reinterpret_cast<const unsigned short *>(&hi);
-      S.u16(sb + SM_K + REG64 + o) = *reinterpret_cast<const unsigned short *>(&lo);
+      S.u16(sb + SM_TP + o) = *reinterpret_cast<const unsigned short *>(&hi);
+      S.u16(sb + SM_TP + REG64 + o) = *reinterpret_cast<const unsigned short *>(&lo);
     };
     {
       // column jc of the inverse of diagonal block Rd: four lanes per column,
@@ -709,8 +735,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             uint32_t hi, lo;
             split_bf16x2(c[nt][2 * hh] * b0, c[nt][2 * hh + 1] * b1, hi, lo);
             const uint32_t o = sw128_off(16 * Rr + g + 8 * hh, col, REG64);
-            S.u32(sb + SM_K + o) = hi;
-            S.u32(sb + SM_K + REG64 + o) = lo;
+            S.u32(sb + SM_TP + o) = hi;
+            S.u32(sb + SM_TP + REG64 + o) = lo;
           }
         }
       };
@@ -727,35 +753,35 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         put16(blk(warp), c, nullptr);
       }
       __syncthreads();
+      // One product call site per level (operands picked per warp), so the
+      // loop body stays small enough for the instruction caches.
       if (warp < 6) {  // level 2
         zero();
-        switch (warp) {
-          case 0: warp_mma16(blk(0), 17, tdiag(0), 17, c, lane); put_t(1, 0, c, -1.f); break;
-          case 1: warp_mma16(blk(2), 17, tdiag(1), 17, c, lane); put_t(2, 1, c, -1.f); break;
-          case 2: warp_mma16(blk(5), 17, tdiag(2), 17, c, lane); put_t(3, 2, c, -1.f); break;
-          case 3: warp_mma16(blk(2), 17, blk(0), 17, c, lane); put16(blk(6), c, blk(1)); break;
-          case 4: warp_mma16(blk(5), 17, blk(2), 17, c, lane); put16(blk(7), c, blk(4)); break;
-          default: warp_mma16(blk(4), 17, blk(0), 17, c, lane); put16(blk(8), c, nullptr); break;
-        }
+        const int xi = warp == 0 ? 0 : warp == 1 ? 2 : warp == 2 ? 5 : warp == 3 ? 2 : warp == 4 ? 5 : 4;
+        const float *Y = warp < 3 ? tdiag(warp) : blk(warp == 4 ? 2 : 0);
+        warp_mma16(blk(xi), 17, Y, 17, c, lane);
+        if (warp < 3)
+          put_t(warp + 1, warp, c, -1.f);  // T_10, T_21, T_32 = -E T_JJ
+        else                               // N_20 + E_20, N_31 + E_31, E_31 E_10
+          put16(blk(warp + 3), c, warp == 3 ? blk(1) : warp == 4 ? blk(4) : nullptr);
       }
       __syncthreads();
       if (warp < 3) {  // level 3
         zero();
-        switch (warp) {
-          case 0: warp_mma16(blk(6), 17, tdiag(0), 17, c, lane); put_t(2, 0, c, 1.f); break;
-          case 1: warp_mma16(blk(7), 17, tdiag(1), 17, c, lane); put_t(3, 1, c, 1.f); break;
-          default:
-            // N_30 = (E_31 E_10 - E_30) - E_32 N_20
-            warp_mma16(blk(5), 17, blk(6), 17, c, lane);
+        warp_mma16(blk(warp == 0 ? 6 : warp == 1 ? 7 : 5), 17, warp < 2 ? tdiag(warp) : blk(6), 17,
+                   c, lane);
+        if (warp < 2) {
+          put_t(warp + 2, warp, c, 1.f);  // T_20 = N_20 T_00, T_31 = N_31 T_11
+        } else {
+          // N_30 = (E_31 E_10 - E_30) - E_32 N_20
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const int oo = (g + 8 * hh) * 17 + 8 * nt + 2 * t;
-                blk(9)[oo] = (blk(8)[oo] - blk(3)[oo]) - c[nt][2 * hh];
-                blk(9)[oo + 1] = (blk(8)[oo + 1] - blk(3)[oo + 1]) - c[nt][2 * hh + 1];
-              }
-            break;
+            for (int hh = 0; hh < 2; ++hh) {
+              const int oo = (g + 8 * hh) * 17 + 8 * nt + 2 * t;
+              blk(9)[oo] = (blk(8)[oo] - blk(3)[oo]) - c[nt][2 * hh];
+              blk(9)[oo + 1] = (blk(8)[oo + 1] - blk(3)[oo + 1]) - c[nt][2 * hh + 1];
+            }
         }
       }
       __syncthreads();
@@ -786,8 +812,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // rows 16 (ks % 4) .. of K e^G and of v (the same 64 tokens twice)
         const uint32_t a_off = static_cast<uint32_t>(ks >> 2) * REG64 + static_cast<uint32_t>(ks & 3) * 32u;
         const uint32_t b_off = static_cast<uint32_t>(ks & 3) * 2048u;
-        const uint64_t ad = sw128_desc(sb + SM_K, 16u, 1024u) + (a_off >> 4);
-        const uint64_t bk = sw128_desc(sb + SM_Z, REG64, 1024u) + (b_off >> 4);
+        const uint64_t ad = sw128_desc(sb + SM_TP, 16u, 1024u) + (a_off >> 4);
+        const uint64_t bk = sw128_desc(sb + SM_K, REG64, 1024u) + (b_off >> 4);
         const uint64_t bv = sw128_desc(sb + SM_Q, REG64, 1024u) + (b_off >> 4);
         mma_f16(tmem + TM_WK, ad, bk, ID_TPROD, ks > 0 ? 1u : 0u);
         mma_f16(tmem + TM_U, ad, bv, ID_TPROD, ks > 0 ? 1u : 0u);
@@ -796,9 +822,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     mma_pending = true;
     if (!wait_mma()) { aborted = true; break; }
-    // q, k, z, v tiles are all consumed: the next task's inputs can come in
-    if (tid == kTmaThread && n + 1 < n_iter) issue_qkz(n + 1);
-    qkz_pending = n + 1 < n_iter;
+    // v (in the q tile) and K e^G (in the k tile) are consumed: the next task's q, k
+    if (tid == kTmaThread && n + 1 < n_iter) issue_qk(n + 1);
+    qk_pending = n + 1 < n_iter;
 
     // ---- -Wk (lanes 0..63, columns 0..127) and U (columns 128..255) to the record ---------
     // (warps 2, 3, 6, 7 reach no TMEM lane below 64: one of them resolves task n + 2)
@@ -832,7 +858,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // Drain anything still in flight (bounded) before TMEM and shared memory go.
   if (aborted && tid == 0) {
     if (mma_pending) mbar_wait_bounded(bar_mma, mma_phase, kWaitPolls);
-    if (qkz_pending) mbar_wait_bounded(bar_qkz, 0, kWaitPolls) || mbar_wait_bounded(bar_qkz, 1, kWaitPolls);
+    if (z_pending) mbar_wait_bounded(bar_z, 0, kWaitPolls) || mbar_wait_bounded(bar_z, 1, kWaitPolls);
+    if (qk_pending) mbar_wait_bounded(bar_qk, 0, kWaitPolls) || mbar_wait_bounded(bar_qk, 1, kWaitPolls);
     if (v_pending) mbar_wait_bounded(bar_v, 0, kWaitPolls) || mbar_wait_bounded(bar_v, 1, kWaitPolls);
   }
   tc_fence_before();

@@ -79,7 +79,20 @@ def state_bytes(token_heads, full_chunk_heads, seq_heads, dk, dv, s0=False):
 # reported only while the kernel's sources hash to the sha256 prefix recorded
 # with the capture (else the kernel has changed since: null).
 _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
-PROFILED_TRAFFIC = {}
+_TC_FILES = ("kda_tc_common.cuh", "kda_sm100.cuh", "kda_split.cuh", "kda_common.cuh")
+PROFILED_TRAFFIC = {
+    # varlen prefill, 4 sequences (70,412 tokens), H = 32: 35,264 tasks
+    "chunk_prep_kernel": (2.327288e9 + 2.569980e9, 35264, "e2154db5c221de03",
+                          ("kda_chunk_prep.cu",) + _TC_FILES),
+    "state_pass_kernel": (2.626993e9 + 2.841820e9, 35264, "745dd246d6a1a9a3",
+                          ("kda_state_pass.cu",) + _TC_FILES),
+    # decode, 512 sequences x H = 32: 16,384 (sequence, head) states
+    "kda_decode_step": (1.090571e9 + 1.017656e9, 16384, "41f489e39d35105f",
+                        ("kda_decode.cu", "kda_common.cuh")),
+    # restore, 512 x H = 32 states
+    "snapshot_restore_kernel": (1.073760e9 + 1.025011e9, 16384, "7acfbeb05332783a",
+                                ("kda_snapshot.cu", "kda_common.cuh")),
+}
 
 
 def profiled_traffic(kernel, tasks):
@@ -440,7 +453,7 @@ def prefill_roofline(name, t, hbm_peak, tc_peak, peak_src, s0):
     full_heads = sum(l // 64 for l in L) * H
     seq_heads = len(L) * H
     kernels = {
-        "prefill_tc_kernel<prep>": (t["prep_s"], prep_bytes(token_heads, dk, dv)),
+        "chunk_prep_kernel": (t["prep_s"], prep_bytes(token_heads, dk, dv)),
         "state_pass_kernel": (t["state_s"], state_bytes(token_heads, full_heads, seq_heads, dk,
                                                         dv, s0=s0)),
     }
@@ -797,6 +810,7 @@ def run_restore(args, dev, stream, hbm_peak, peak_src, world):
             "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9,
                          "peak": hbm_peak, "unit": "GB/s",
                          "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
+                         "traffic": profiled_traffic("snapshot_restore_kernel", n * H),
                          "kernel": "snapshot_restore_kernel", "peak_source": peak_src}}
 
 

@@ -825,11 +825,11 @@ def run_tiny(args, dev, stream, world):
     x = kda_inputs.make_workload_prefill("tiny", device=dev)
     b = prefill_buffers(kda, x, dev)
 
-    def call():
+    def call(st=stream):
         kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
                       cu_seqlens=x["cu_seqlens"], o=b["o"], S_final=b["S_final"],
                       snaps=b["snaps"], snap_offsets=b["offs"], workspace=b["ws"],
-                      stream=stream)
+                      stream=st)
 
     for _ in range(10):
         call()
@@ -843,11 +843,42 @@ def run_tiny(args, dev, stream, world):
     bb.record(stream)
     torch.cuda.synchronize()
     us = reduce_max(a.elapsed_time(bb), world) * 1e3 / reps
+    # the same call captured once in a CUDA graph and replayed: the GPU's own
+    # latency of the three launches, without the host's per-call work
+    # (argument checks, tensor-map encoding, the Python binding)
+    graph_us = None
+    try:
+        side = torch.cuda.Stream(device=dev)  # captures need a stream other than the default
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            call(side)
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            call(side)
+        torch.cuda.synchronize()
+        for _ in range(10):
+            g.replay()
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream(dev)
+        a.record(cur)
+        for _ in range(reps):
+            g.replay()
+        bb.record(cur)
+        torch.cuda.synchronize()
+        graph_us = reduce_max(a.elapsed_time(bb), world) * 1e3 / reps
+        del g
+    except RuntimeError as e:  # capture not possible here: report the host-issued figure only
+        graph_us = f"not captured: {e}"
+    if kda.device_status() != 0:
+        raise RuntimeError("device status word set during the tiny prefill")
     return {"latency_us": us, "unit": "us per call", "reps": reps,
+            "graph_replay_us": graph_us,
             "workload": workload_config("tiny")["workload"],
             "gpu_launches_per_call": 3,
             "note": "launch-bound: three kernels (chunk-start table, chunk preparation, state "
-                    "pass) per call, back to back on one stream"}
+                    "pass) per call, back to back on one stream; latency_us issues every call "
+                    "from Python, graph_replay_us replays it from a CUDA graph"}
 
 
 def main(argv=None):

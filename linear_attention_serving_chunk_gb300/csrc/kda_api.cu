@@ -42,7 +42,8 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               int64_t total_tokens, int H, int dk, int dv, int h0, int hg,
                               const float *S0, kda_bf16 *o, float *S_final, float *snaps,
                               const int64_t *snap_offsets, int *status, const int32_t *slots,
-                              int n_slots, int zero_u, int s0_identity, cudaStream_t stream);
+                              int n_slots, int zero_u, int s0_identity, float *S_final2,
+                              cudaStream_t stream);
 cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
                                int32_t *chunk_start, int *status, cudaStream_t stream);
 cudaError_t segment_combine_launch(const float *M, const float *N, const float *S0,
@@ -273,10 +274,11 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
     float *Mb = static_cast<float *>(workspace), *Nb = Mb + arr, *Ss = Nb + arr;
     if (workspace_bytes >= need + scan_records_bytes(n_seq, total_tokens, H)) {
       // On the two-pass kernels: every chunk's record once, then the state
-      // pass over the segments three times (N from zero, M from the identity
-      // with v = 0, the outputs from the true segment starts).  The records
-      // are laid out by global chunk, which is also what the segment view
-      // (n2 sequences of seg_len tokens) addresses.
+      // pass over the segments twice: N (from zero) and M (from the identity
+      // with v = 0) as the two chains of one paired pass, then the outputs
+      // from the true segment starts.  The records are laid out by global
+      // chunk, which is also what the segment view (n2 sequences of seg_len
+      // tokens) addresses.
       uint8_t *rec = static_cast<uint8_t *>(workspace) + need;
       const int64_t cps = (fixed_len + 63) / 64;
       cudaError_t err = chunk_prep_launch(q, k, v, z, beta, A, gmin, nullptr, nullptr, n_seq,
@@ -285,17 +287,13 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
       if (err == cudaSuccess)
         err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, dk, dv,
                                 0, H, nullptr, nullptr, Nb, nullptr, nullptr, status, nullptr, 0,
-                                0, 0, st);
-      if (err == cudaSuccess)
-        err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, dk, dv,
-                                0, H, nullptr, nullptr, Mb, nullptr, nullptr, status, nullptr, 0,
-                                1, 1, st);
+                                0, 0, Mb, st);
       if (err == cudaSuccess)
         err = segment_combine_launch(Mb, Nb, S0, Ss, S_final, n_seq, plan.n_segs, H, st);
       if (err == cudaSuccess)
         err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, dk, dv,
                                 0, H, Ss, o, nullptr, snaps, nullptr, status, nullptr, 0, 0, 0,
-                                st);
+                                nullptr, st);
       return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     }
     // 1. every segment from a zero state (N) and its transition from S0 = I with v = 0 (M)
@@ -343,7 +341,7 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
       if (err == cudaSuccess && run_state)
         err = state_pass_launch(rec, cu_seqlens, chunk_start, n_seq, fixed_len, total_tokens, H,
                                 dk, dv, h0, g, S0, o, S_final, snaps, snap_offsets, status,
-                                nullptr, 0, 0, 0, st);
+                                nullptr, 0, 0, 0, nullptr, st);
     }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }

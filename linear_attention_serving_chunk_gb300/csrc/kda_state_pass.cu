@@ -70,6 +70,15 @@ constexpr uint32_t kRecInBytes = 32 * KiB + 16 * KiB + 8 * KiB + 8 * KiB + 512;
 constexpr uint32_t TM_S = 0;    // fp32 state columns (row = key channel)
 constexpr uint32_t TM_D1 = NC;  // -Wk S (rows 0..63); -O (rows 64..127)
 constexpr uint32_t TM_COLS = 128;
+// The segment scan's paired pass (`dual`) carries a second chain through the
+// same records: the transition M (from the identity, v taken as zero) beside
+// N (from zero, with v).  Its fp16 copy of the state and its W take the
+// snapshot staging area (no snapshots in that pass), its TMEM columns follow.
+constexpr uint32_t SM_SBF2 = SM_SNAP;
+constexpr uint32_t SM_WBF2 = SM_SNAP + 16 * KiB;
+constexpr uint32_t TM_S2 = 128;
+constexpr uint32_t TM_D12 = 128 + NC;
+constexpr uint32_t TM_COLS_DUAL = 256;
 
 constexpr uint32_t kWaitPolls = 1u << 24;
 constexpr int kCopyThread = 128;  // issues the record copies
@@ -96,6 +105,9 @@ struct SpParams {
   int n_slots;
   int zero_u;       // 1: v taken as zero (W = -Wk S; U is not loaded)
   int s0_identity;  // 1: every chain starts from S0 = I (dk = dv)
+  float *S_final2;  // non-NULL: the paired pass -- chain 1 from zero with v
+                    // (final state to S_final), chain 2 from the identity with
+                    // v = 0 (final state to S_final2); no o, no snapshots
 };
 
 // One CTA per (sequence, head, half of the value columns): the columns of the
@@ -160,8 +172,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
+  const bool dual = p.S_final2 != nullptr;
+  const uint32_t tm_cols = dual ? TM_COLS_DUAL : TM_COLS;
   if (warp == 1) {
-    tmem_alloc(sb + MS_TMEM, TM_COLS);
+    tmem_alloc(sb + MS_TMEM, tm_cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -185,6 +199,11 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
              : (p.S0 && row_in) ? p.S0[state_off + static_cast<size_t>(trow) * DV + cq + j]
                                 : 0.f;
     tmem_st16(t_lane + TM_S + 16 * q4, v);
+    if (dual) {  // the transition chain starts from the identity
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = trow == cq + j ? 1.f : 0.f;
+      tmem_st16(t_lane + TM_S2 + 16 * q4, v);
+    }
     tmem_wait_st();
   }
 
@@ -252,6 +271,17 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = sv[j] * gam;
       tmem_st16(t_lane + TM_S + 16 * q4, v);
+      if (dual) {
+        float s2[16];
+        tmem_ld16(t_lane + TM_S2 + 16 * q4, s2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) range_max = fmaxf(range_max, fabsf(s2[j]));
+        store_row16_f16(S, sb + SM_SBF2, trow, q4, s2, 1.f);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) s2[j] *= gam;
+        tmem_st16(t_lane + TM_S2 + 16 * q4, s2);
+      }
     }
     if (tid == kCopyThread) bulk_wait_read0();  // the last snapshot's stores have read the tile
     fence_proxy_async();
@@ -268,6 +298,9 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     if (tid == 0) {
       tc_fence_after();
       issue_mma(tmem + TM_D1, st + ST_A3, false, REG128, sb + SM_SBF, true, REG128, 8, ID_KMN, 0);
+      if (dual)
+        issue_mma(tmem + TM_D12, st + ST_A3, false, REG128, sb + SM_SBF2, true, REG128, 8, ID_KMN,
+                  0);
       mma_commit(bar_mma);
     }
     mma_pending = true;
@@ -306,6 +339,13 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
 #pragma unroll
       for (int j = 0; j < 16; ++j) range_max = fmaxf(range_max, fabsf(v[j]));
       store_row16_f16(S, sb + SM_WBF, trow, q4, v, 1.f);
+      if (dual) {  // W of the transition chain: v = 0
+        tmem_ld16(t_lane + TM_D12 + 16 * q4, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) range_max = fmaxf(range_max, fabsf(v[j]));
+        store_row16_f16(S, sb + SM_WBF2, trow, q4, v, 1.f);
+      }
     }
     tmem_wait_st();  // the gamma-scaled state is in TMEM before S += K'^T W
     fence_proxy_async();
@@ -325,6 +365,9 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
         }
       } else {  // the segment scan's passes for N and M
         issue_mma(tmem + TM_S, st + ST_KP, true, REG64, sb + SM_WBF, true, REG64, 4, ID_MNMN, 1);
+        if (dual)
+          issue_mma(tmem + TM_S2, st + ST_KP, true, REG64, sb + SM_WBF2, true, REG64, 4, ID_MNMN,
+                    1);
       }
       mma_commit(bar_mma);
     }
@@ -378,6 +421,17 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
       for (int j = 0; j < 4; ++j)
         dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
+    if (dual) {
+      tmem_ld16(t_lane + TM_S2 + 16 * q4, v);
+      tmem_wait_ld();
+      if (row_in) {
+        float4 *dst = reinterpret_cast<float4 *>(p.S_final2 + state_off +
+                                                 static_cast<size_t>(trow) * DV + cq);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
+    }
     if (snap_pending >= 0 && row_in) {
       float4 *dst = reinterpret_cast<float4 *>(
           p.snaps + (static_cast<size_t>(snap_pending) * H + h) * DK * DV +
@@ -404,7 +458,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
   if (shape_bad && tid == 0) atomicOr(p.status, KDA_ERR_SHAPE);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TM_COLS);
+    tmem_dealloc(tmem, tm_cols);
   }
 }
 
@@ -415,7 +469,8 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               int64_t total_tokens, int H, int dk, int dv, int h0, int hg,
                               const float *S0, kda_bf16 *o, float *S_final, float *snaps,
                               const int64_t *snap_offsets, int *status, const int32_t *slots,
-                              int n_slots, int zero_u, int s0_identity, cudaStream_t stream) {
+                              int n_slots, int zero_u, int s0_identity, float *S_final2,
+                              cudaStream_t stream) {
   // Snapshots as a 3-D fp32 array [rows * H][dk][dv]; rows <= total_tokens / 64
   // (each snapshot follows a full chunk), which bounds the map's extent.  A
   // box is 32 value columns x dk key rows of one (row, head) state, so a
@@ -446,7 +501,8 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
   if (err != cudaSuccess) return err;
   SpParams prm{rec,     cu_seqlens, chunk_start, fixed_len, total_tokens, n_seq, H,
                h0,      hg,         dk,          dv,        S0,           o,     S_final,
-               snaps,   snap_offsets, status,    slots,     n_slots,      zero_u, s0_identity};
+               snaps,   snap_offsets, status,    slots,     n_slots,      zero_u, s0_identity,
+               S_final2};
   const dim3 grid(static_cast<unsigned>((dv / NC) * hg), static_cast<unsigned>(n_seq));
   state_pass_kernel<<<grid, SP_THREADS, smem, stream>>>(tm_snap, prm);
   return cudaGetLastError();

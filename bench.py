@@ -84,7 +84,7 @@ PROFILED_TRAFFIC = {
     # varlen prefill, 4 sequences (70,412 tokens), H = 32: 35,264 tasks
     "chunk_prep_kernel": (2.327288e9 + 2.569980e9, 35264, "e2154db5c221de03",
                           ("kda_chunk_prep.cu",) + _TC_FILES),
-    "state_pass_kernel": (2.626993e9 + 2.841820e9, 35264, "745dd246d6a1a9a3",
+    "state_pass_kernel": (2.626518e9 + 2.842087e9, 35264, "9ab40dfe1b1f5089",
                           ("kda_state_pass.cu",) + _TC_FILES),
     # decode, 512 sequences x H = 32: 16,384 (sequence, head) states
     "kda_decode_step": (1.090571e9 + 1.017656e9, 16384, "41f489e39d35105f",

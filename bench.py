@@ -716,7 +716,10 @@ def run_decode(args, dev, stream, hbm_peak, peak_src, world):
     per = statistics.mean(x.elapsed_time(y) for x, y in evs) / 1e3
     nbytes = decode_bytes(Bd * H, dk, dv)
     achieved = nbytes / per / 1e9
+    multi = run_decode_tokens(kda, pool, A, Bd, H, dk, dv, w["seed"], dev, stream, hbm_peak,
+                              world)
     return {"value": n_steps * world / (total_ms / 1e3), "unit": "steps/s",
+            "multi_token": multi,
             "tokens_per_s": Bd * n_steps * world / (total_ms / 1e3),
             "workload": f"kda decode {Bd} sequences x H={H}, dk=dv={dk}, fp32 state in place, "
                         f"{n_steps} chained steps with fresh inputs",
@@ -725,6 +728,45 @@ def run_decode(args, dev, stream, hbm_peak, peak_src, world):
                          "frac": achieved / hbm_peak,
                          "traffic": profiled_traffic("kda_decode_step", Bd * H),
                          "kernel": "kda_decode_step", "peak_source": peak_src}}
+
+
+def run_decode_tokens(kda, pool, A, Bd, H, dk, dv, seed, dev, stream, hbm_peak, world,
+                      tokens=4, reps=20):
+    """Speculative verification: `tokens` tokens per sequence on the same
+    512 x 32 resident states (kda_decode_tokens, commit = 0: every state is
+    read once, none is written), timed over `reps` calls."""
+    import torch
+
+    import kda_inputs
+    x = kda_inputs.make_prefill(H, dk, dv, [tokens] * Bd, seed + 7, device=dev)
+    slots = torch.arange(Bd, dtype=torch.int32, device=dev)
+    o = torch.empty((Bd * tokens, H, dv), dtype=torch.bfloat16, device=dev)
+
+    def call():
+        kda.decode_tokens(x["q"], x["k"], x["v"], x["z"], x["beta"], A, pool, slots,
+                          x["cu_seqlens"], commit=False, o=o, stream=stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(a.elapsed_time(b), world) / reps
+    # the state read once, the tokens' inputs and outputs
+    nbytes = Bd * H * (dk * dv * 4 + tokens * (2 * (3 * dk + 2 * dv) + 2))
+    return {"tokens_per_seq": tokens, "ms_per_call": ms, "unit": "tokens/s",
+            "value": Bd * tokens * world / (ms / 1e3),
+            "workload": f"kda_decode_tokens: {tokens} tokens on each of {Bd} x H={H} states, "
+                        f"dk=dv={dk}, commit = 0 (verify)",
+            "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
+                         "kernel": "decode_tokens_kernel"}}
 
 
 def run_long(args, dev, stream, hbm_peak, peak_src, world):

@@ -244,10 +244,13 @@ int kda_decode_step_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
 /*
  * kda_decode_tokens - several tokens per sequence on resident states: the
  * serving step for multi-token decode and speculative verification (the
- * chunkwise form of the report page, sec. 2.1, applied to short runs on the
+ * recurrence of the report page, sec. 2.1, applied to short runs on the
  * fixed-size running state).  Sequence b's tokens are rows [cu_seqlens[b],
  * cu_seqlens[b+1]) of q, k, v, z, beta (layouts as kda_chunk_fwd; any
- * lengths, chunked by 64); its state is slot slots[b] of state_pool
+ * lengths).  With at most 16 tokens per sequence on average the tokens are
+ * applied one after another to the state held on chip (each state read once
+ * and, with commit, written once); longer runs go through the chunkwise form
+ * (chunks of 64).  Its state is slot slots[b] of state_pool
  * [n_slots, H, dk, dv].  o receives every token's output.  With commit != 0
  * the state after the last token is written back to the slot (in place);
  * with commit == 0 the pool is left unchanged (verify without accepting).

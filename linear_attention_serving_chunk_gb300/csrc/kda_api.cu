@@ -19,6 +19,12 @@ cudaError_t decode_step_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_b
                                float gmin, float *pool, const int32_t *slots, int n_slots,
                                int n, int H, int dk, int dv, kda_bf16 *o, unsigned pre,
                                int *status, cudaStream_t stream);
+cudaError_t decode_tokens_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                                 const kda_bf16 *z, const kda_bf16 *beta, const float *A,
+                                 float gmin, float *pool, const int32_t *slots, int n_slots,
+                                 const int32_t *cu_seqlens, int n, int64_t total, int H, int dk,
+                                 int dv, kda_bf16 *o, unsigned pre, int commit, int *status,
+                                 cudaStream_t stream);
 cudaError_t snapshot_restore_launch(const float *snaps, int64_t n_rows, const int64_t *src_idx,
                                     float *pool, int n_slots, const int32_t *dst_slots, int n,
                                     int H, int dk, int dv, int *status, cudaStream_t stream);
@@ -140,6 +146,11 @@ bool gmin_ok(float gmin) { return isfinite(gmin) && gmin <= 0.f && gmin >= -5.5f
 bool pre_ok(unsigned pre) { return (pre & ~(KDA_PRE_L2NORM_QK | KDA_PRE_SIGMOID_BETA)) == 0; }
 
 constexpr unsigned kPassFlags = KDA_PASS_PREPARE | KDA_PASS_STATE;
+
+// kda_decode_tokens with at most this many tokens per sequence on average runs
+// the token-by-token kernel on the state in registers (one state read, one
+// write); longer runs take the chunked single-pass kernel.
+constexpr int64_t kDecodeTokensRun = 16;
 
 }  // namespace
 
@@ -400,6 +411,13 @@ int kda_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
   float *S_final = commit ? state_pool : nullptr;
   int *status = status_word();
   if (!status) return KDA_ERR_CUDA;
+  if (total_tokens <= kDecodeTokensRun * static_cast<int64_t>(n)) {
+    // short runs: the tokens one after another on the state in registers
+    const cudaError_t err =
+        decode_tokens_launch(q, k, v, z, beta, A, gmin, state_pool, slots, n_slots, cu_seqlens, n,
+                             total_tokens, H, dk, dv, o, pre, commit, status, st);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  }
   const cudaError_t err =
       prefill_tc_launch(q, k, v, z, beta, A, gmin, cu_seqlens, n, total_tokens, 0, H, dk, dv,
                         state_pool, o, S_final, nullptr, nullptr, status, 0, 0, slots, n_slots,

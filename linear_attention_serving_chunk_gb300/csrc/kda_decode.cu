@@ -135,6 +135,159 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
   }
 }
 
+// Several tokens per (sequence, head) on its resident state: the state is
+// read into registers once, the run's tokens are applied in order -- each one
+// exactly the step above -- and the state is written back once (only when
+// committing).  The tokens' inputs are staged in shared memory kTokBlock at a
+// time (with the pre-ops and the k.q / norm sums per token), so a token costs
+// two CTA barriers and no global round trip.
+constexpr int kTokBlock = 16;
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kDecodeThreads)
+decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ k,
+                     const kda_bf16 *__restrict__ v, const kda_bf16 *__restrict__ z,
+                     const kda_bf16 *__restrict__ beta, const float *__restrict__ A,
+                     float gmin, float *__restrict__ pool, const int32_t *__restrict__ slots,
+                     int n_slots, const int32_t *__restrict__ cu_seqlens, int64_t total, int H,
+                     kda_bf16 *__restrict__ o, unsigned pre, int commit,
+                     int *__restrict__ status) {
+  constexpr int TPR = DV / 4;
+  constexpr int RG = kDecodeThreads / TPR;
+  constexpr int RPT = DK / RG;
+  constexpr int NW = kDecodeThreads / 32;
+  static_assert(RPT * RG == DK && TPR * RG == kDecodeThreads, "decode tiling");
+
+  __shared__ float s_a[kTokBlock][DK], s_k[kTokBlock][DK], s_q[kTokBlock][DK];
+  __shared__ float s_v[kTokBlock][DV];
+  __shared__ float s_beta[kTokBlock], s_kq[kTokBlock];
+  __shared__ float s_red_p[RG][DV], s_red_u[RG][DV];
+  __shared__ float s_delta[DV];
+
+  const int row = blockIdx.x;  // b * H + h
+  const int b = row / H, h = row - b * H;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cg = tid % TPR, rg = tid / TPR;
+  const int slot = slots[b];
+  int64_t t_begin, t_end;
+  if (slot < 0 || slot >= n_slots || !seq_range(cu_seqlens, b, total, t_begin, t_end)) {
+    if (tid == 0) atomicOr(status, KDA_ERR_SHAPE);  // nothing of this sequence is touched
+    return;
+  }
+  if (t_end == t_begin) return;  // no token: the state stays as it is
+  float *S = pool + (static_cast<size_t>(slot) * H + h) * (DK * DV);
+  float4 s[RPT];
+#pragma unroll
+  for (int rr = 0; rr < RPT; ++rr)
+    s[rr] = __ldcs(reinterpret_cast<const float4 *>(S + (rg * RPT + rr) * DV) + cg);
+  const float eA = expf(A[h]);
+
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += kTokBlock) {
+    const int nt = static_cast<int>(min(static_cast<int64_t>(kTokBlock), t_end - t0));
+    __syncthreads();  // the previous block's tokens are done with the staging arrays
+    for (int x = tid; x < nt * DK; x += kDecodeThreads) {
+      const int j = x / DK, c = x - j * DK;
+      const size_t g = (static_cast<size_t>(t0 + j) * H + h) * DK + c;
+      s_k[j][c] = bf2f(k[g]);
+      s_q[j][c] = bf2f(q[g]);
+      s_a[j][c] = decay_factor(gmin, eA, bf2f(z[g]));
+    }
+    for (int x = tid; x < nt * DV; x += kDecodeThreads) {
+      const int j = x / DV, c = x - j * DV;
+      s_v[j][c] = bf2f(v[(static_cast<size_t>(t0 + j) * H + h) * DV + c]);
+    }
+    __syncthreads();
+    // per token (one warp each): the pre-op norms applied to k and q in place,
+    // then k.q; beta through the pre-op
+    for (int j = warp; j < nt; j += NW) {
+      float kk = 0.f, qq = 0.f;
+      if (pre & KDA_PRE_L2NORM_QK) {
+        for (int c = lane; c < DK; c += 32) {
+          kk += s_k[j][c] * s_k[j][c];
+          qq += s_q[j][c] * s_q[j][c];
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          kk += __shfl_xor_sync(0xffffffffu, kk, off);
+          qq += __shfl_xor_sync(0xffffffffu, qq, off);
+        }
+        const float ik = kk > 0.f ? rsqrtf(kk) : 0.f, iq = qq > 0.f ? rsqrtf(qq) : 0.f;
+        for (int c = lane; c < DK; c += 32) {
+          s_k[j][c] *= ik;
+          s_q[j][c] *= iq;
+        }
+        __syncwarp();
+      }
+      float kq = 0.f;
+      for (int c = lane; c < DK; c += 32) kq += s_k[j][c] * s_q[j][c];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+      if (lane == 0) {
+        float bt = bf2f(beta[static_cast<size_t>(t0 + j) * H + h]);
+        if (pre & KDA_PRE_SIGMOID_BETA) bt = 1.f / (1.f + __expf(-bt));
+        s_beta[j] = bt;
+        s_kq[j] = kq;
+      }
+    }
+    __syncthreads();
+    for (int j = 0; j < nt; ++j) {
+      float p[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int rr = 0; rr < RPT; ++rr) {
+        const int i = rg * RPT + rr;
+        const float a = s_a[j][i], kv = s_k[j][i], qv = s_q[j][i];
+        s[rr].x *= a; s[rr].y *= a; s[rr].z *= a; s[rr].w *= a;
+        p[0] += s[rr].x * kv; p[1] += s[rr].y * kv; p[2] += s[rr].z * kv; p[3] += s[rr].w * kv;
+        u[0] += s[rr].x * qv; u[1] += s[rr].y * qv; u[2] += s[rr].z * qv; u[3] += s[rr].w * qv;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        s_red_p[rg][cg * 4 + c] = p[c];
+        s_red_u[rg][cg * 4 + c] = u[c];
+      }
+      __syncthreads();
+      if (tid < DV) {
+        float pj = 0.f, uj = 0.f;
+#pragma unroll
+        for (int g = 0; g < RG; ++g) {
+          pj += s_red_p[g][tid];
+          uj += s_red_u[g][tid];
+        }
+        const float delta = s_beta[j] * (s_v[j][tid] - pj);
+        s_delta[tid] = delta;
+        o[(static_cast<size_t>(t0 + j) * H + h) * DV + tid] = f2bf(uj + s_kq[j] * delta);
+      }
+      __syncthreads();
+      const float d0 = s_delta[cg * 4 + 0], d1 = s_delta[cg * 4 + 1];
+      const float d2 = s_delta[cg * 4 + 2], d3 = s_delta[cg * 4 + 3];
+#pragma unroll
+      for (int rr = 0; rr < RPT; ++rr) {
+        const float kv = s_k[j][rg * RPT + rr];
+        s[rr].x += kv * d0; s[rr].y += kv * d1; s[rr].z += kv * d2; s[rr].w += kv * d3;
+      }
+    }
+  }
+  if (commit) {
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr)
+      __stcs(reinterpret_cast<float4 *>(S + (rg * RPT + rr) * DV) + cg, s[rr]);
+  }
+}
+
+template <int DK, int DV>
+cudaError_t launch_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                                 const kda_bf16 *z, const kda_bf16 *beta, const float *A,
+                                 float gmin, float *pool, const int32_t *slots, int n_slots,
+                                 const int32_t *cu_seqlens, int n, int64_t total, int H,
+                                 kda_bf16 *o, unsigned pre, int commit, int *status,
+                                 cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(n) * H;
+  decode_tokens_kernel<DK, DV><<<static_cast<unsigned>(rows), kDecodeThreads, 0, stream>>>(
+      q, k, v, z, beta, A, gmin, pool, slots, n_slots, cu_seqlens, total, H, o, pre, commit,
+      status);
+  return cudaGetLastError();
+}
+
 template <int DK, int DV>
 cudaError_t launch_decode(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                           const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
@@ -147,6 +300,25 @@ cudaError_t launch_decode(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *
 }
 
 }  // namespace
+
+cudaError_t decode_tokens_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
+                                 const kda_bf16 *z, const kda_bf16 *beta, const float *A,
+                                 float gmin, float *pool, const int32_t *slots, int n_slots,
+                                 const int32_t *cu_seqlens, int n, int64_t total, int H, int dk,
+                                 int dv, kda_bf16 *o, unsigned pre, int commit, int *status,
+                                 cudaStream_t stream) {
+#define KDA_DT(DK_, DV_)                                                                        \
+  if (dk == DK_ && dv == DV_)                                                                   \
+    return launch_decode_tokens<DK_, DV_>(q, k, v, z, beta, A, gmin, pool, slots, n_slots,     \
+                                          cu_seqlens, n, total, H, o, pre, commit, status,     \
+                                          stream);
+  KDA_DT(128, 128)
+  KDA_DT(64, 64)
+  KDA_DT(128, 64)
+  KDA_DT(64, 128)
+#undef KDA_DT
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t decode_step_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                                const kda_bf16 *z, const kda_bf16 *beta, const float *A,

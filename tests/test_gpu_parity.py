@@ -235,6 +235,61 @@ def test_decode_tokens_multi_token(kda, d):
     assert s_err(f64(pool[perm.long()]), ref["S_final"]) <= S_TOL
 
 
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (128, 64), (64, 128)])
+def test_decode_tokens_short_runs(kda, dk, dv):
+    """Short runs (at most 16 tokens per sequence on average) take the
+    token-by-token kernel on the state held on chip: empty runs, single
+    tokens, a run of exactly one 16-token block and one of 50 tokens (four
+    blocks); verify (commit=False) leaves the pool untouched, commit=True
+    stores the final states; both against the oracle."""
+    lengths = [1, 0, 3, 16, 2, 50, 1, 5, 0, 7]
+    n, H = len(lengths), 2
+    assert sum(lengths) <= 16 * n
+    x = kda_inputs.make_prefill(H, dk, dv, lengths, seed=29, device="cuda", S0_std=0.02)
+    perm = torch.tensor([3, 9, 0, 7, 5, 1, 8, 2, 6, 4], dtype=torch.int32, device="cuda")
+    pool = torch.zeros((n, H, dk, dv), device="cuda")
+    pool[perm.long()] = x["S0"]
+    before = pool.clone()
+    args = [x[nm] for nm in ("q", "k", "v", "z", "beta")] + [x["A"]]
+    o_v = kda.decode_tokens(*args, pool, perm, x["cu_seqlens"], commit=False)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    assert torch.equal(pool, before)
+    o_c = kda.decode_tokens(*args, pool, perm, x["cu_seqlens"], commit=True)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    assert torch.equal(o_v, o_c)
+    ref = oracle_subset(x, list(range(n)), [0, 1], snapshots=False)
+    assert o_err(f64(o_c), ref["o"]) <= O_TOL
+    assert s_err(f64(pool[perm.long()]), ref["S_final"]) <= S_TOL
+    # empty runs keep their states exactly
+    for b in (1, 8):
+        assert torch.equal(pool[int(perm[b])], before[int(perm[b])])
+
+
+def test_decode_tokens_short_runs_match_single_steps(kda):
+    """The token-by-token kernel does each token's step as kda_decode_step
+    does it: the same pool, run by run or token by token (the k.q sums are
+    added in another order, so equal to float rounding)."""
+    lengths = [4, 4, 4, 4]
+    n, H, d = 4, 2, 128
+    x = kda_inputs.make_prefill(H, d, d, lengths, seed=31, device="cuda", S0_std=0.02)
+    pool_a = x["S0"].clone()
+    pool_b = x["S0"].clone()
+    slots = torch.arange(n, dtype=torch.int32, device="cuda")
+    o_a = kda.decode_tokens(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], pool_a, slots,
+                            x["cu_seqlens"], commit=True)
+    o_b = torch.empty_like(o_a)
+    for t in range(4):
+        rows = torch.arange(n, device="cuda") * 4 + t
+        ob = kda.decode_step(x["q"][rows], x["k"][rows], x["v"][rows], x["z"][rows],
+                             x["beta"][rows], x["A"], pool_b)
+        o_b[rows] = ob
+    torch.cuda.synchronize()
+    assert s_err(f64(pool_a), f64(pool_b)) <= 1e-6
+    assert np.max(np.abs(f64(o_a) - f64(o_b))) <= 2.0 ** -7 * max(np.max(np.abs(f64(o_b))), 1e-30)
+
+
 def test_decode_1000_steps(kda):
     """512 x 32 resident states, 1000 chained steps with fresh inputs: all
     states are checked after steps 1 and 10, 256 seeded (sequence, head)

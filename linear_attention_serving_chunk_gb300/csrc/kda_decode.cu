@@ -137,10 +137,11 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
 
 // Several tokens per (sequence, head) on its resident state: the state is
 // read into registers once, the run's tokens are applied in order -- each one
-// exactly the step above -- and the state is written back once (only when
-// committing).  The tokens' inputs are staged in shared memory kTokBlock at a
-// time (with the pre-ops and the k.q / norm sums per token), so a token costs
-// two CTA barriers and no global round trip.
+// the step above -- and the state is written back once (only when
+// committing).  Warp w owns value columns [w DV/8, (w+1) DV/8); its lanes split
+// the key rows, so p = S^T k and u = S^T q are reduced by shuffles inside the
+// warp and a token needs no CTA barrier.  The tokens' inputs are staged in
+// shared memory kTokBlock at a time (with the pre-ops and k.q per token).
 constexpr int kTokBlock = 16;
 
 template <int DK, int DV>
@@ -152,22 +153,21 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
                      int n_slots, const int32_t *__restrict__ cu_seqlens, int64_t total, int H,
                      kda_bf16 *__restrict__ o, unsigned pre, int commit,
                      int *__restrict__ status) {
-  constexpr int TPR = DV / 4;
-  constexpr int RG = kDecodeThreads / TPR;
-  constexpr int RPT = DK / RG;
   constexpr int NW = kDecodeThreads / 32;
-  static_assert(RPT * RG == DK && TPR * RG == kDecodeThreads, "decode tiling");
+  constexpr int CQ = DV / (4 * NW);   // 4-column groups per warp
+  constexpr int RL = 32 / CQ;         // row groups per warp (lanes sharing columns)
+  constexpr int RPT = DK / RL;        // rows per lane
+  static_assert(CQ * RL == 32 && RPT * RL == DK && 4 * CQ * NW == DV, "decode tiling");
 
   __shared__ float s_a[kTokBlock][DK], s_k[kTokBlock][DK], s_q[kTokBlock][DK];
   __shared__ float s_v[kTokBlock][DV];
   __shared__ float s_beta[kTokBlock], s_kq[kTokBlock];
-  __shared__ float s_red_p[RG][DV], s_red_u[RG][DV];
-  __shared__ float s_delta[DV];
 
   const int row = blockIdx.x;  // b * H + h
   const int b = row / H, h = row - b * H;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int cg = tid % TPR, rg = tid / TPR;
+  const int cq = lane % CQ, rl = lane / CQ;
+  const int col = 4 * (warp * CQ + cq);  // this lane's first value column
   const int slot = slots[b];
   int64_t t_begin, t_end;
   if (slot < 0 || slot >= n_slots || !seq_range(cu_seqlens, b, total, t_begin, t_end)) {
@@ -176,10 +176,10 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
   }
   if (t_end == t_begin) return;  // no token: the state stays as it is
   float *S = pool + (static_cast<size_t>(slot) * H + h) * (DK * DV);
-  float4 s[RPT];
+  float4 s[RPT];  // rows rl * RPT + rr, columns col .. col + 3
 #pragma unroll
   for (int rr = 0; rr < RPT; ++rr)
-    s[rr] = __ldcs(reinterpret_cast<const float4 *>(S + (rg * RPT + rr) * DV) + cg);
+    s[rr] = __ldcs(reinterpret_cast<const float4 *>(S + (rl * RPT + rr) * DV + col));
   const float eA = expf(A[h]);
 
   for (int64_t t0 = t_begin; t0 < t_end; t0 += kTokBlock) {
@@ -200,8 +200,8 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
     // per token (one warp each): the pre-op norms applied to k and q in place,
     // then k.q; beta through the pre-op
     for (int j = warp; j < nt; j += NW) {
-      float kk = 0.f, qq = 0.f;
       if (pre & KDA_PRE_L2NORM_QK) {
+        float kk = 0.f, qq = 0.f;
         for (int c = lane; c < DK; c += 32) {
           kk += s_k[j][c] * s_k[j][c];
           qq += s_q[j][c] * s_q[j][c];
@@ -234,43 +234,43 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
       float p[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int rr = 0; rr < RPT; ++rr) {
-        const int i = rg * RPT + rr;
+        const int i = rl * RPT + rr;
         const float a = s_a[j][i], kv = s_k[j][i], qv = s_q[j][i];
         s[rr].x *= a; s[rr].y *= a; s[rr].z *= a; s[rr].w *= a;
         p[0] += s[rr].x * kv; p[1] += s[rr].y * kv; p[2] += s[rr].z * kv; p[3] += s[rr].w * kv;
         u[0] += s[rr].x * qv; u[1] += s[rr].y * qv; u[2] += s[rr].z * qv; u[3] += s[rr].w * qv;
       }
+      // sums over the warp's row groups (lanes CQ apart): every lane gets its columns' p, u
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        s_red_p[rg][cg * 4 + c] = p[c];
-        s_red_u[rg][cg * 4 + c] = u[c];
-      }
-      __syncthreads();
-      if (tid < DV) {
-        float pj = 0.f, uj = 0.f;
+      for (int off = CQ; off < 32; off <<= 1)
 #pragma unroll
-        for (int g = 0; g < RG; ++g) {
-          pj += s_red_p[g][tid];
-          uj += s_red_u[g][tid];
+        for (int c = 0; c < 4; ++c) {
+          p[c] += __shfl_xor_sync(0xffffffffu, p[c], off);
+          u[c] += __shfl_xor_sync(0xffffffffu, u[c], off);
         }
-        const float delta = s_beta[j] * (s_v[j][tid] - pj);
-        s_delta[tid] = delta;
-        o[(static_cast<size_t>(t0 + j) * H + h) * DV + tid] = f2bf(uj + s_kq[j] * delta);
+      const float bt = s_beta[j], kq = s_kq[j];
+      float d[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) d[c] = bt * (s_v[j][col + c] - p[c]);
+      if (rl == 0) {
+        uint2 w;
+        w.x = static_cast<uint32_t>(f2bf(u[0] + kq * d[0])) |
+              (static_cast<uint32_t>(f2bf(u[1] + kq * d[1])) << 16);
+        w.y = static_cast<uint32_t>(f2bf(u[2] + kq * d[2])) |
+              (static_cast<uint32_t>(f2bf(u[3] + kq * d[3])) << 16);
+        *reinterpret_cast<uint2 *>(o + (static_cast<size_t>(t0 + j) * H + h) * DV + col) = w;
       }
-      __syncthreads();
-      const float d0 = s_delta[cg * 4 + 0], d1 = s_delta[cg * 4 + 1];
-      const float d2 = s_delta[cg * 4 + 2], d3 = s_delta[cg * 4 + 3];
 #pragma unroll
       for (int rr = 0; rr < RPT; ++rr) {
-        const float kv = s_k[j][rg * RPT + rr];
-        s[rr].x += kv * d0; s[rr].y += kv * d1; s[rr].z += kv * d2; s[rr].w += kv * d3;
+        const float kv = s_k[j][rl * RPT + rr];
+        s[rr].x += kv * d[0]; s[rr].y += kv * d[1]; s[rr].z += kv * d[2]; s[rr].w += kv * d[3];
       }
     }
   }
   if (commit) {
 #pragma unroll
     for (int rr = 0; rr < RPT; ++rr)
-      __stcs(reinterpret_cast<float4 *>(S + (rg * RPT + rr) * DV) + cg, s[rr]);
+      __stcs(reinterpret_cast<float4 *>(S + (rl * RPT + rr) * DV + col), s[rr]);
   }
 }
 

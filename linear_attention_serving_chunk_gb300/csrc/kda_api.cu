@@ -411,7 +411,8 @@ int kda_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
   float *S_final = commit ? state_pool : nullptr;
   int *status = status_word();
   if (!status) return KDA_ERR_CUDA;
-  if (total_tokens <= kDecodeTokensRun * static_cast<int64_t>(n)) {
+  if (total_tokens <= kDecodeTokensRun * static_cast<int64_t>(n) &&
+      static_cast<int64_t>(n) * H <= 0x7fffffffLL) {  // one CTA per (sequence, head)
     // short runs: the tokens one after another on the state in registers
     const cudaError_t err =
         decode_tokens_launch(q, k, v, z, beta, A, gmin, state_pool, slots, n_slots, cu_seqlens, n,

@@ -39,7 +39,8 @@ cudaError_t prefill_tc_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
                               int test_stall, cudaStream_t stream);
 cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                               const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
-                              const int32_t *cu_seqlens, const int32_t *chunk_start, int n_seq,
+                              const int32_t *cu_seqlens, const int32_t *chunk_start,
+                              const int2 *chunk_info, int n_seq,
                               int64_t total_tokens, int64_t fixed_len, int H, int dk, int dv,
                               int h0, int hg, int64_t max_tasks, uint8_t *rec, int *status,
                               unsigned pre, int n_ctas, cudaStream_t stream);
@@ -51,7 +52,8 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               int n_slots, int zero_u, int s0_identity, float *S_final2,
                               cudaStream_t stream);
 cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
-                               int32_t *chunk_start, int *status, cudaStream_t stream);
+                               int32_t *chunk_start, int2 *chunk_info, int *status,
+                               cudaStream_t stream);
 cudaError_t segment_combine_launch(const float *M, const float *N, const float *S0,
                                    float *S_start, float *S_final, int n_seq, int n_segs, int H,
                                    cudaStream_t stream);
@@ -102,27 +104,35 @@ size_t scan_records_bytes(int n_seq, int64_t total_tokens, int H) {
 
 // Two-pass prefill: a chunk-preparation pass over every
 // (chunk, head) of a group of hg heads, then the state pass over that group's
-// chains.  Workspace: the varlen chunk-start table (1 KiB granules), then one
+// chains.  Workspace: the varlen tables (the chunk start of every sequence,
+// then the first token and length of every chunk; 1 KiB granules), then one
 // record per (chunk, head of the group).  The chunk count is bounded by
 // ceil(total / 64) + n_seq, which covers any split of the tokens.
 constexpr size_t kRecordBytes = 73 * 1024;  // kRecBytes of kda_split.cuh
-
-size_t split_table_bytes(int n_seq) {
-  return ((static_cast<size_t>(n_seq) + 1) * sizeof(int32_t) + 1023) / 1024 * 1024;
-}
 
 int64_t split_max_chunks(int n_seq, int64_t total_tokens) {
   return (total_tokens + 63) / 64 + n_seq;
 }
 
+size_t round_kib(size_t b) { return (b + 1023) / 1024 * 1024; }
+
+size_t chunk_start_bytes(int n_seq) {
+  return round_kib((static_cast<size_t>(n_seq) + 1) * sizeof(int32_t));
+}
+
+size_t split_table_bytes(int n_seq, int64_t total_tokens) {
+  return chunk_start_bytes(n_seq) +
+         round_kib(static_cast<size_t>(split_max_chunks(n_seq, total_tokens)) * sizeof(int2));
+}
+
 size_t split_workspace_bytes(int n_seq, int64_t total_tokens, int hg) {
-  return split_table_bytes(n_seq) +
+  return split_table_bytes(n_seq, total_tokens) +
          static_cast<size_t>(split_max_chunks(n_seq, total_tokens)) * hg * kRecordBytes;
 }
 
 // Largest head group whose records fit in `bytes` (0: none fits).
 int split_heads(int n_seq, int64_t total_tokens, int H, size_t bytes) {
-  const size_t table = split_table_bytes(n_seq);
+  const size_t table = split_table_bytes(n_seq, total_tokens);
   if (bytes <= table) return 0;
   const size_t per_head =
       static_cast<size_t>(split_max_chunks(n_seq, total_tokens)) * kRecordBytes;
@@ -292,7 +302,7 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
       // tokens) addresses.
       uint8_t *rec = static_cast<uint8_t *>(workspace) + need;
       const int64_t cps = (fixed_len + 63) / 64;
-      cudaError_t err = chunk_prep_launch(q, k, v, z, beta, A, gmin, nullptr, nullptr, n_seq,
+      cudaError_t err = chunk_prep_launch(q, k, v, z, beta, A, gmin, nullptr, nullptr, nullptr, n_seq,
                                           total_tokens, fixed_len, H, dk, dv, 0, H,
                                           n_seq * cps * H, rec, status, ops, kSMs, st);
       if (err == cudaSuccess)
@@ -333,20 +343,23 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
     // two passes per group of hg heads: chunk preparation, then the state pass
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *chunk_start = nullptr;
+    int2 *chunk_info = nullptr;
     err = cudaSuccess;
     const bool run_prep = passes != KDA_PASS_STATE, run_state = passes != KDA_PASS_PREPARE;
     if (cu_seqlens) {
       chunk_start = reinterpret_cast<int32_t *>(ws);
-      if (run_prep) err = chunk_start_launch(cu_seqlens, n_seq, total_tokens, chunk_start, status,
-                                             st);
+      chunk_info = reinterpret_cast<int2 *>(ws + chunk_start_bytes(n_seq));
+      if (run_prep)
+        err = chunk_start_launch(cu_seqlens, n_seq, total_tokens, chunk_start, chunk_info, status,
+                                 st);
     }
-    uint8_t *rec = ws + split_table_bytes(n_seq);
+    uint8_t *rec = ws + split_table_bytes(n_seq, total_tokens);
     const int64_t max_chunks = cu_seqlens ? split_max_chunks(n_seq, total_tokens)
                                           : static_cast<int64_t>(n_seq) * ((fixed_len + 63) / 64);
     for (int h0 = 0; h0 < H && err == cudaSuccess; h0 += hg) {
       const int g = H - h0 < hg ? H - h0 : hg;
       if (run_prep)
-        err = chunk_prep_launch(q, k, v, z, beta, A, gmin, cu_seqlens, chunk_start, n_seq,
+        err = chunk_prep_launch(q, k, v, z, beta, A, gmin, cu_seqlens, chunk_start, chunk_info, n_seq,
                                 total_tokens, fixed_len, H, dk, dv, h0, g, max_chunks * g, rec,
                                 status, ops, kSMs, st);
       if (err == cudaSuccess && run_state)

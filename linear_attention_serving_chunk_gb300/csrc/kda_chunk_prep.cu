@@ -117,6 +117,7 @@ struct CpParams {
   float gmin;
   const int32_t *cu_seqlens;   // or NULL: equal lengths fixed_len
   const int32_t *chunk_start;  // varlen: first chunk of each sequence, [n_seq + 1]
+  const int2 *chunk_info;      // varlen: first token and length of every chunk
   int64_t fixed_len;
   int n_seq, H, h0, hg;        // heads h0 .. h0 + hg - 1 of H
   unsigned pre;
@@ -239,32 +240,25 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   // Task n of this CTA: global task blockIdx.x + n * gridDim.x = chunk-major,
   // head-minor.  Resolved two tasks ahead into a three-slot ring by one thread
-  // of a warp that is idle at that point; a varlen chunk's sequence is found
-  // by walking chunk_start forward from the previous task's (consecutive
-  // tasks of a CTA are ~gridDim / hg chunks apart, so the walk is a step or
-  // two of dependent loads).
-  int cur_seq = 0;  // only meaningful in kTaskThread
+  // of a warp that is idle at that point; a varlen chunk's first token and
+  // length come from the chunk table (one load, beside that of A).
   auto put_task = [&](int n) {
     const int64_t task = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
     const int64_t c = task / p.hg;
-    int64_t sb0, se0, j;
+    const int hh = p.h0 + static_cast<int>(task % p.hg);
+    int64_t t0, L;
     if (p.cu_seqlens) {
-      while (cur_seq + 1 < p.n_seq && p.chunk_start[cur_seq + 1] <= c) ++cur_seq;
-      sb0 = p.cu_seqlens[cur_seq];
-      se0 = p.cu_seqlens[cur_seq + 1];
-      j = c - p.chunk_start[cur_seq];
+      const int2 ci = p.chunk_info[c];
+      t0 = ci.x;
+      L = ci.y;
     } else {
       const int64_t q = c / cps;
-      sb0 = q * p.fixed_len;
-      se0 = sb0 + p.fixed_len;
-      j = c - q * cps;
+      t0 = q * p.fixed_len + 64 * (c - q * cps);
+      L = min(static_cast<int64_t>(64), (q + 1) * p.fixed_len - t0);
     }
-    const int64_t t0 = sb0 + 64 * j;
-    const int hh = p.h0 + static_cast<int>(task % p.hg);
     const uint32_t slot = sb + MS_TASK + 32u * static_cast<uint32_t>(n % 3);
     S.u128(slot) = make_uint4(static_cast<uint32_t>(t0), static_cast<uint32_t>(t0 >> 32),
-                              static_cast<uint32_t>(min(static_cast<int64_t>(64), se0 - t0)),
-                              static_cast<uint32_t>(hh));
+                              static_cast<uint32_t>(L), static_cast<uint32_t>(hh));
     S.f32(slot + 16) = -__expf(p.A[hh]) * 1.4426950408889634f;
   };
   struct Task {
@@ -889,10 +883,11 @@ bool make_map(CUtensorMap *m, const void *base, int64_t total, int H, int d) {
 // Persistent grid: two CTAs per SM, each taking (chunk, head) tasks in turn.
 cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
                               const kda_bf16 *z, const kda_bf16 *beta, const float *A, float gmin,
-                              const int32_t *cu_seqlens, const int32_t *chunk_start, int n_seq,
-                              int64_t total_tokens, int64_t fixed_len, int H, int dk, int dv,
-                              int h0, int hg, int64_t max_tasks, uint8_t *rec, int *status,
-                              unsigned pre, int n_sms, cudaStream_t stream) {
+                              const int32_t *cu_seqlens, const int32_t *chunk_start,
+                              const int2 *chunk_info, int n_seq, int64_t total_tokens,
+                              int64_t fixed_len, int H, int dk, int dv, int h0, int hg,
+                              int64_t max_tasks, uint8_t *rec, int *status, unsigned pre,
+                              int n_sms, cudaStream_t stream) {
   CUtensorMap mq, mk, mz, mv;
   if (!make_map(&mq, q, total_tokens, H, dk) || !make_map(&mk, k, total_tokens, H, dk) ||
       !make_map(&mz, z, total_tokens, H, dk) || !make_map(&mv, v, total_tokens, H, dv))
@@ -901,8 +896,8 @@ cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(CP_SMEM_BYTES));
   if (err != cudaSuccess) return err;
-  CpParams prm{beta, A, gmin, cu_seqlens, chunk_start, fixed_len, n_seq, H, h0, hg, pre, rec,
-               status};
+  CpParams prm{beta, A, gmin, cu_seqlens, chunk_start, chunk_info, fixed_len, n_seq, H, h0,
+               hg, pre, rec, status};
   const int64_t ctas = max_tasks < 2LL * n_sms ? max_tasks : 2LL * n_sms;
   if (ctas <= 0) return cudaSuccess;
   chunk_prep_kernel<<<static_cast<unsigned>(ctas), CP_THREADS, CP_SMEM_BYTES, stream>>>(

@@ -519,9 +519,12 @@ namespace {
 // checked on the way (cu[0] = 0, non-decreasing, cu[n_seq] = total): if any
 // entry is malformed the whole table is set to zero (no chunk-preparation
 // task, no record read by the state pass) and KDA_ERR_SHAPE is recorded.
+// Then, for every global chunk c of the batch, chunk_info[c] = (first token,
+// tokens in the chunk): the chunk preparation resolves a task with one load.
 __global__ void __launch_bounds__(1024) chunk_start_kernel(const int32_t *__restrict__ cu,
                                                            int n_seq, int64_t total,
                                                            int32_t *__restrict__ chunk_start,
+                                                           int2 *__restrict__ chunk_info,
                                                            int *status) {
   __shared__ int32_t warp_sum[32];
   __shared__ int32_t carry;
@@ -565,15 +568,30 @@ __global__ void __launch_bounds__(1024) chunk_start_kernel(const int32_t *__rest
   if (__syncthreads_or(bad)) {
     for (int i = tid; i <= n_seq; i += 1024) chunk_start[i] = 0;
     if (tid == 0) atomicOr(status, KDA_ERR_SHAPE);
+    return;
+  }
+  // chunk c belongs to the last sequence s with chunk_start[s] <= c (an empty
+  // sequence shares its start with the next one; the search skips it)
+  const int32_t chunks = chunk_start[n_seq];
+  for (int32_t c = tid; c < chunks; c += 1024) {
+    int lo = 0, hi = n_seq - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (chunk_start[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    const int32_t j = c - chunk_start[lo];
+    const int32_t t0 = cu[lo] + 64 * j;
+    chunk_info[c] = make_int2(t0, min(64, cu[lo + 1] - t0));
   }
 }
 
 }  // namespace
 
 cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
-                               int32_t *chunk_start, int *status, cudaStream_t stream) {
+                               int32_t *chunk_start, int2 *chunk_info, int *status,
+                               cudaStream_t stream) {
   chunk_start_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, n_seq, total_tokens, chunk_start,
-                                             status);
+                                             chunk_info, status);
   return cudaGetLastError();
 }
 

@@ -152,18 +152,27 @@ def test_workspace_query_is_pure_host(L):
 REC = 73 * 1024  # one (chunk, head) record of the two-pass prefill
 
 
+def table(n_seq, total):
+    """The varlen tables ahead of the records: the chunk start of every
+    sequence (int32 [n_seq + 1]) and the first token and length of every chunk
+    (int32 x 2 per chunk, for up to ceil(T/64) + n_seq chunks), each rounded up
+    to 1 KiB."""
+    kib = lambda b: (b + 1023) // 1024 * 1024
+    return kib((n_seq + 1) * 4) + kib(((total + 63) // 64 + n_seq) * 8)
+
+
 @pytest.mark.parametrize("n_seq,total,H,dk,dv,chunk,expect", [
     # the bench workload: two passes, records of every head for ceil(T/64) + n_seq
-    # chunks after a 1 KiB chunk-start table
-    (4, 4 * 8192, 16, 128, 128, 64, 1024 + (512 + 4) * 16 * REC),
+    # chunks after the tables
+    (4, 4 * 8192, 16, 128, 128, 64, table(4, 4 * 8192) + (512 + 4) * 16 * REC),
     # one 2^20-token sequence, 16 heads: the segment scan (64 segments of 16,384
     # tokens: three [64, 16, 128, 128] fp32 arrays) plus every chunk's record
     (1, 1 << 20, 16, 128, 128, 64, 3 * 64 * 16 * 128 * 128 * 4 + (1 << 14) * 16 * REC),
     # too short for four segments of at least 4096 tokens: two passes
-    (1, 8192, 4, 128, 128, 64, 1024 + (128 + 1) * 4 * REC),
+    (1, 8192, 4, 128, 128, 64, table(1, 8192) + (128 + 1) * 4 * REC),
     # 64-channel heads run the same two passes (records keep the 128-channel tiles)
-    (1, 256, 2, 64, 64, 64, 1024 + (4 + 1) * 2 * REC),
-    (3, 300, 2, 128, 64, 64, 1024 + (5 + 3) * 2 * REC),
+    (1, 256, 2, 64, 64, 64, table(1, 256) + (4 + 1) * 2 * REC),
+    (3, 300, 2, 128, 64, 64, table(3, 300) + (5 + 3) * 2 * REC),
     # only chunk = 64 exists
     (4, 4 * 8192, 16, 128, 128, 32, 0),
 ])

@@ -585,7 +585,8 @@ def test_two_pass_in_head_groups(kda, heads_per_group):
     lengths = [300, 130, 64, 1]
     x = kda_inputs.make_prefill(H, 128, 128, lengths, seed=54, device="cuda", S0_std=0.02)
     n, total = len(lengths), x["k"].shape[0]
-    table = ((n + 1) * 4 + 1023) // 1024 * 1024
+    kib = lambda b: (b + 1023) // 1024 * 1024
+    table = kib((n + 1) * 4) + kib(((total + 63) // 64 + n) * 8)  # chunk starts, chunk table
     per_head = ((total + 63) // 64 + n) * 73 * 1024
     assert kda.workspace_bytes(n, total, H, 128, 128) == table + H * per_head
     ws = torch.empty(table + heads_per_group * per_head, dtype=torch.uint8, device="cuda")

@@ -89,6 +89,9 @@ PROFILED_TRAFFIC = {
     # decode, 512 sequences x H = 32: 16,384 (sequence, head) states
     "kda_decode_step": (1.090571e9 + 1.017656e9, 16384, "41f489e39d35105f",
                         ("kda_decode.cu", "kda_common.cuh")),
+    # verify: 4 tokens on each of 512 x H = 32 states (commit = 0)
+    "decode_tokens_kernel": (1.141138e9 + 6.22336e6, 16384, "f693894b0151293e",
+                             ("kda_decode.cu", "kda_common.cuh")),
     # restore, 512 x H = 32 states
     "snapshot_restore_kernel": (1.073760e9 + 1.025011e9, 16384, "7acfbeb05332783a",
                                 ("kda_snapshot.cu", "kda_common.cuh")),
@@ -766,6 +769,7 @@ def run_decode_tokens(kda, pool, A, Bd, H, dk, dv, seed, dev, stream, hbm_peak, 
             "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9,
                          "peak": hbm_peak, "unit": "GB/s",
                          "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
+                         "traffic": profiled_traffic("decode_tokens_kernel", Bd * H),
                          "kernel": "decode_tokens_kernel"}}
 
 

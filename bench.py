@@ -82,12 +82,12 @@ _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
 _TC_FILES = ("kda_tc_common.cuh", "kda_sm100.cuh", "kda_split.cuh", "kda_common.cuh")
 PROFILED_TRAFFIC = {
     # varlen prefill, 4 sequences (70,412 tokens), H = 32: 35,264 tasks
-    "chunk_prep_kernel": (2.327288e9 + 2.569980e9, 35264, "e2154db5c221de03",
+    "chunk_prep_kernel": (2.328897e9 + 2.569476e9, 35264, "fb93ba4d94096531",
                           ("kda_chunk_prep.cu",) + _TC_FILES),
-    "state_pass_kernel": (2.626518e9 + 2.842087e9, 35264, "9ab40dfe1b1f5089",
+    "state_pass_kernel": (2.626862e9 + 2.843645e9, 35264, "9436ef8b90144c54",
                           ("kda_state_pass.cu",) + _TC_FILES),
     # decode, 512 sequences x H = 32: 16,384 (sequence, head) states
-    "kda_decode_step": (1.090571e9 + 1.017656e9, 16384, "41f489e39d35105f",
+    "kda_decode_step": (1.090570e9 + 1.017794e9, 16384, "f693894b0151293e",
                         ("kda_decode.cu", "kda_common.cuh")),
     # verify: 4 tokens on each of 512 x H = 32 states (commit = 0)
     "decode_tokens_kernel": (1.141138e9 + 6.22336e6, 16384, "f693894b0151293e",

@@ -45,8 +45,9 @@
 //          -Q e^G, K' (fp16, straight to the record); diagonal tiles by mma.sync
 //   MMA    off-diagonal A_kk / P tiles (M128 N128 K128, fp16)
 //   SIMT   A_kk to shared memory (fp32, transposed), -P to the record;
-//          T by diagonal-block column updates and (I - E + E^2 - E^3) D for
-//          the off-diagonal blocks; T' = T diag(beta) as bf16 hi | lo
+//          T by diagonal-block column updates, then block forward
+//          substitution for the off-diagonal blocks in three levels of
+//          16 x 16 products; T' = T diag(beta) as bf16 hi | lo
 //   MMA    T'(K e^G) and T'V, each one M128 N128 K128 product with hi and lo
 //          concatenated along K (bf16)
 //   SIMT   -Wk and U (fp16) to the record
@@ -83,6 +84,7 @@ constexpr uint32_t SM_AKK = SM_KQ;                     // fp32 [64][68]: A_kk tr
 constexpr uint32_t SM_TD = SM_AKK + 64 * 68 * 4;       // fp32 [4][16][17]: diagonal blocks of T
 constexpr uint32_t SM_XS = SM_TD + 4 * 16 * 17 * 4;    // fp32 [10][16][17]: block products
 static_assert(SM_XS + 10 * 16 * 17 * 4 <= SM_KC, "inverse scratch overflows the KE/QE tile");
+static_assert(6 * 16 * 17 * 4 <= 64 * 68 * 4, "level-2 blocks overflow the A_kk tile");
 constexpr uint32_t SM_MISC = 104 * KiB;
 constexpr uint32_t MS_BAR_Z = SM_MISC;            // mbarriers: z in, q/k in, v in, MMA done
 constexpr uint32_t MS_BAR_QK = SM_MISC + 8;
@@ -698,22 +700,30 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     __syncthreads();  // B5
     // Off-diagonal blocks: with D = blockdiag(T_RR) and E = D A_off (E_RJ =
-    // T_RR A_RJ, strictly block-lower, E^4 = 0): T = (I - E + E^2 - E^3) D,
-    // block by block with N = I - E + E^2 - E^3:
-    //   N_10 = -E_10, N_21 = -E_21, N_32 = -E_32, N_20 = E_21 E_10 - E_20,
-    //   N_31 = E_32 E_21 - E_31, N_30 = E_31 E_10 - E_30 - E_32 N_20;  T_RJ = N_RJ T_JJ.
+    // T_RR A_RJ, strictly block-lower, E^4 = 0), block forward substitution
+    // T_RJ = -sum_{J<=M<R} E_RM T_MJ in three dependent levels, with
+    // Y_RJ = E_RJ T_JJ and N_31 = E_32 E_21 - E_31:
+    //   level 1: E_RJ (six blocks);
+    //   level 2: T_10 = -Y_10, T_21 = -Y_21, T_32 = -Y_32; Y_20, Y_31, Y_30, N_31;
+    //   level 3: T_20 = E_21 Y_10 - Y_20, T_31 = E_32 Y_21 - Y_31,
+    //            T_30 = E_32 Y_20 - N_31 Y_10 - Y_30.
     {
       const float *akk = reinterpret_cast<const float *>(S.ptr(sb + SM_AKK));
       const float *td = reinterpret_cast<const float *>(S.ptr(sb + SM_TD));
-      float *bs = reinterpret_cast<float *>(S.ptr(sb + SM_XS));  // 10 blocks of [16][17]
+      float *bs = reinterpret_cast<float *>(S.ptr(sb + SM_XS));  // E_RJ: 6 blocks of [16][17]
+      // level 2 results, in the A_kk tile (read for the last time by level 1)
+      float *ys = reinterpret_cast<float *>(S.ptr(sb + SM_AKK));
       auto blk = [&](int i) { return bs + i * 16 * 17; };
+      auto yblk = [&](int i) { return ys + i * 16 * 17; };
       auto tdiag = [&](int Rr) { return td + Rr * 16 * 17; };
+      // fragment element (nt, hh, e) of a 16 x 16 block: row g + 8 hh, column 8 nt + 2 t + e
+      auto frag_off = [&](int nt, int hh) { return (g + 8 * hh) * 17 + 8 * nt + 2 * t; };
       auto put16 = [&](float *dst, const float (&c)[2][4], const float *sub) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            const int oo = (g + 8 * hh) * 17 + 8 * nt + 2 * t;
+            const int oo = frag_off(nt, hh);
             dst[oo] = c[nt][2 * hh] - (sub ? sub[oo] : 0.f);
             dst[oo + 1] = c[nt][2 * hh + 1] - (sub ? sub[oo + 1] : 0.f);
           }
@@ -735,54 +745,48 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
       };
       float c[2][4];
-      auto zero = [&]() {
+      auto zero = [&](float (&x)[2][4]) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) c[e >> 1][e & 1] = c[e >> 1][2 + (e & 1)] = 0.f;
+        for (int e = 0; e < 4; ++e) x[e >> 1][e & 1] = x[e >> 1][2 + (e & 1)] = 0.f;
       };
-      zero();
+      zero(c);
       if (warp < 6) {  // level 1: E_RJ = T_RR A_RJ (A_kk stored transposed)
         const int Rr = warp == 0 ? 1 : warp < 3 ? 2 : 3;
         const int J = warp == 0 ? 0 : warp < 3 ? warp - 1 : warp - 3;
         warp_mma16<false, true>(tdiag(Rr), 17, akk + (16 * J) * 68 + 16 * Rr, 68, c, lane);
-        put16(blk(warp), c, nullptr);
+        put16(blk(warp), c, nullptr);  // blocks E_10, E_20, E_21, E_30, E_31, E_32
       }
       __syncthreads();
       // One product call site per level (operands picked per warp), so the
       // loop body stays small enough for the instruction caches.
-      if (warp < 6) {  // level 2
-        zero();
-        const int xi = warp == 0 ? 0 : warp == 1 ? 2 : warp == 2 ? 5 : warp == 3 ? 2 : warp == 4 ? 5 : 4;
-        const float *Y = warp < 3 ? tdiag(warp) : blk(warp == 4 ? 2 : 0);
+      if (warp < 7) {  // level 2: Y_10, Y_21, Y_32, Y_20, Y_31, Y_30, E_32 E_21
+        zero(c);
+        const int xi = warp == 0 ? 0 : warp == 1 ? 2 : warp == 2 ? 5 : warp == 3 ? 1 : warp == 4 ? 4
+                     : warp == 5 ? 3 : 5;
+        const float *Y = warp == 6 ? blk(2)
+                                   : tdiag(warp == 1 || warp == 4 ? 1 : warp == 2 ? 2 : 0);
         warp_mma16(blk(xi), 17, Y, 17, c, lane);
-        if (warp < 3)
-          put_t(warp + 1, warp, c, -1.f);  // T_10, T_21, T_32 = -E T_JJ
-        else                               // N_20 + E_20, N_31 + E_31, E_31 E_10
-          put16(blk(warp + 3), c, warp == 3 ? blk(1) : warp == 4 ? blk(4) : nullptr);
+        if (warp < 3) put_t(warp + 1, warp, c, -1.f);  // T_10, T_21, T_32
+        // kept for level 3: Y_10, Y_21, Y_20, Y_31, Y_30 in slots 0..4, N_31 in slot 5
+        if (warp != 2) put16(yblk(warp < 2 ? warp : warp - 1), c, warp == 6 ? blk(4) : nullptr);
       }
       __syncthreads();
-      if (warp < 3) {  // level 3
-        zero();
-        warp_mma16(blk(warp == 0 ? 6 : warp == 1 ? 7 : 5), 17, warp < 2 ? tdiag(warp) : blk(6), 17,
-                   c, lane);
-        if (warp < 2) {
-          put_t(warp + 2, warp, c, 1.f);  // T_20 = N_20 T_00, T_31 = N_31 T_11
-        } else {
-          // N_30 = (E_31 E_10 - E_30) - E_32 N_20
+      if (warp < 3) {  // level 3: T_20, T_31, T_30
+        zero(c);
+        warp_mma16(blk(warp == 0 ? 2 : 5), 17, yblk(warp), 17, c, lane);
+        const float *ysub = yblk(warp == 0 ? 2 : warp == 1 ? 3 : 4);
+        float c2[2][4];
+        zero(c2);
+        if (warp == 2) warp_mma16(yblk(5), 17, yblk(0), 17, c2, lane);  // N_31 Y_10
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int oo = (g + 8 * hh) * 17 + 8 * nt + 2 * t;
-              blk(9)[oo] = (blk(8)[oo] - blk(3)[oo]) - c[nt][2 * hh];
-              blk(9)[oo + 1] = (blk(8)[oo + 1] - blk(3)[oo + 1]) - c[nt][2 * hh + 1];
-            }
-        }
-      }
-      __syncthreads();
-      if (warp == 0) {  // level 4: T_30 = N_30 T_00
-        zero();
-        warp_mma16(blk(9), 17, tdiag(0), 17, c, lane);
-        put_t(3, 0, c, 1.f);
+          for (int hh = 0; hh < 2; ++hh) {
+            const int oo = frag_off(nt, hh);
+            c[nt][2 * hh] -= c2[nt][2 * hh] + ysub[oo];
+            c[nt][2 * hh + 1] -= c2[nt][2 * hh + 1] + ysub[oo + 1];
+          }
+        put_t(warp == 0 ? 2 : 3, warp == 1 ? 1 : 0, c, 1.f);
       }
     }
     fence_proxy_async();  // T' was written by the threads above

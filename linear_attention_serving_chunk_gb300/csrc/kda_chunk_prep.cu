@@ -41,14 +41,14 @@
 //   TMA    z (prefetched while the previous chunk runs), q and k, v (after
 //          the operand build)
 //   SIMT   gate, scans, sub-tile totals; then every operand: [KE ; QE] and
-//          the stacked Kc (fp16, shared memory), K e^G (bf16, over k), and
+//          the stacked Kc (fp16, shared memory), -K e^G (bf16, over k), and
 //          -Q e^G, K' (fp16, straight to the record); diagonal tiles by mma.sync
 //   MMA    off-diagonal A_kk / P tiles (M128 N128 K128, fp16)
 //   SIMT   A_kk to shared memory (fp32, transposed), -P to the record;
 //          T by diagonal-block column updates, then block forward
 //          substitution for the off-diagonal blocks in three levels of
 //          16 x 16 products; T' = T diag(beta) as bf16 hi | lo
-//   MMA    T'(K e^G) and T'V, each one M128 N128 K128 product with hi and lo
+//   MMA    T'(-K e^G) and T'V, each one M128 N128 K128 product with hi and lo
 //          concatenated along K (bf16)
 //   SIMT   -Wk and U (fp16) to the record
 // Every mbarrier wait is bounded; a wait that gives up records
@@ -69,7 +69,7 @@ constexpr int CP_THREADS = 256;
 
 // Shared-memory map (byte offsets from the 1024-aligned dynamic base).
 constexpr uint32_t SM_Q = 0;              // q tile [64 tok x 128] bf16, then v
-constexpr uint32_t SM_K = 16 * KiB;       // k tile, rewritten in place as K e^G (bf16, MN-major)
+constexpr uint32_t SM_K = 16 * KiB;       // k tile, rewritten in place as -K e^G (bf16, MN-major)
 constexpr uint32_t SM_Z = 32 * KiB;       // z tile (the next chunk's once the scans have read it)
 constexpr uint32_t SM_KQ = 48 * KiB;      // [KE ; QE] fp16 K-major, 128 rows; then scratch
 constexpr uint32_t SM_KC = 80 * KiB;      // stacked Kc fp16 K-major, 96 rows
@@ -103,7 +103,7 @@ static_assert(CP_SMEM_BYTES <= 110 * KiB, "two CTAs per SM");
 
 constexpr uint32_t TILE = 16 * KiB;  // a [64 tok x 128] 2-byte tile (two 8 KiB regions)
 constexpr uint32_t TM_COLS = 256;
-constexpr uint32_t TM_WK = 0;        // off-diagonal A_kk/P, then T'(K e^G)
+constexpr uint32_t TM_WK = 0;        // off-diagonal A_kk/P, then T'(-K e^G) = -Wk
 constexpr uint32_t TM_U = 128;       // T'V
 
 constexpr uint32_t kWaitPolls = 1u << 24;
@@ -508,10 +508,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       S.u32(kq + chunk_off(rb, s)) = pack_f16x2(keb0, keb1);
       S.u32(kq + chunk_off(64 + ra, s)) = pack_f16x2(qea0, qea1);
       S.u32(kq + chunk_off(64 + rb, s)) = pack_f16x2(qeb0, qeb1);
-      // K e^G = KE prod_{M<R} Lam (bf16, B operand of T'(K e^G)): each thread
-      // overwrites exactly the k elements it has just read
-      S.u32(sb + SM_K + off + chunk_off(ra, s)) = pack_bf16x2(kea0 * pre0, kea1 * pre1);
-      S.u32(sb + SM_K + off + chunk_off(rb, s)) = pack_bf16x2(keb0 * pre0, keb1 * pre1);
+      // -K e^G = -KE prod_{M<R} Lam (bf16, B operand of T'(-K e^G) = -Wk, the
+      // record's sign): each thread overwrites exactly the k elements it has just read
+      S.u32(sb + SM_K + off + chunk_off(ra, s)) = pack_bf16x2(-kea0 * pre0, -kea1 * pre1);
+      S.u32(sb + SM_K + off + chunk_off(rb, s)) = pack_bf16x2(-keb0 * pre0, -keb1 * pre1);
       // -Q e^G and K' = k B prod_{M>R} Lam (record words; B = Lam_R / F)
       const float ba0 = lr0 * ia0, ba1 = lr1 * ia1, bb0 = lr0 * ib0, bb1 = lr1 * ib1;
       // record rows: -Q e^G in A3 rows 64 + tok (two regions of 128 rows), K'
@@ -801,13 +801,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       v_pending = false;
     }
 
-    // ---- Wk = T'(K e^G) -> TMEM 0..127, U = T'V -> 128..255 (hi | lo along K) ---------------
+    // ---- -Wk = T'(-K e^G) -> TMEM 0..127, U = T'V -> 128..255 (hi | lo along K) -------------
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         // A: T' K-major, K-step ks in region ks / 4 (hi, then lo); B: MN-major
-        // rows 16 (ks % 4) .. of K e^G and of v (the same 64 tokens twice)
+        // rows 16 (ks % 4) .. of -K e^G and of v (the same 64 tokens twice)
         const uint32_t a_off = static_cast<uint32_t>(ks >> 2) * REG64 + static_cast<uint32_t>(ks & 3) * 32u;
         const uint32_t b_off = static_cast<uint32_t>(ks & 3) * 2048u;
         const uint64_t ad = sw128_desc(sb + SM_TP, 16u, 1024u) + (a_off >> 4);
@@ -820,7 +820,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     mma_pending = true;
     if (!wait_mma()) { aborted = true; break; }
-    // v (in the q tile) and K e^G (in the k tile) are consumed: the next task's q, k
+    // v (in the q tile) and -K e^G (in the k tile) are consumed: the next task's q, k
     if (tid == kTmaThread && n + 1 < n_iter) issue_qk(n + 1);
     qk_pending = n + 1 < n_iter;
 
@@ -830,23 +830,26 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (quad < 2) {
       const int r = quad * 32 + lane;
       const bool is_u = warp >= 4;
+      // two 32-column loads per wait: columns 64 h .. + 63 are region h
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float v[32];
-        tmem_ld32(t_lane + (is_u ? TM_U : TM_WK) + 32 * q4, v);
+      for (int h = 0; h < 2; ++h) {
+        float v[2][32];
+        tmem_ld32(t_lane + (is_u ? TM_U : TM_WK) + 64 * h, v[0]);
+        tmem_ld32(t_lane + (is_u ? TM_U : TM_WK) + 64 * h + 32, v[1]);
         tmem_wait_ld();
         if (is_u) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) range_max = fmaxf(range_max, fabsf(v[j]));
+          for (int j = 0; j < 32; ++j)
+            range_max = fmaxf(range_max, fmaxf(fabsf(v[0][j]), fabsf(v[1][j])));
         }
-        const float sc = is_u ? 1.f : -1.f;
-        // columns 32 q4 .. + 31: region q4 / 2, chunks 4 (q4 & 1) .. + 3
-        uint8_t *base = is_u ? rec + kRecU + (q4 >> 1) * 8192 : rec + kRecA3 + (q4 >> 1) * 16384;
+        uint8_t *base = is_u ? rec + kRecU + h * 8192 : rec + kRecA3 + h * 16384;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4 *>(base + chunk_off(r, 4 * (q4 & 1) + j)) = make_uint4(
-              pack_f16x2(sc * v[8 * j + 0], sc * v[8 * j + 1]), pack_f16x2(sc * v[8 * j + 2], sc * v[8 * j + 3]),
-              pack_f16x2(sc * v[8 * j + 4], sc * v[8 * j + 5]), pack_f16x2(sc * v[8 * j + 6], sc * v[8 * j + 7]));
+        for (int hq = 0; hq < 2; ++hq)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(base + chunk_off(r, 4 * hq + j)) = make_uint4(
+                pack_f16x2(v[hq][8 * j + 0], v[hq][8 * j + 1]), pack_f16x2(v[hq][8 * j + 2], v[hq][8 * j + 3]),
+                pack_f16x2(v[hq][8 * j + 4], v[hq][8 * j + 5]), pack_f16x2(v[hq][8 * j + 6], v[hq][8 * j + 7]));
       }
     }
     tc_fence_before();

@@ -135,7 +135,8 @@ int kda_version(void);
  *    The value returned holds the records of all heads for up to
  *    ceil(total_tokens / 64) + n_seq chunks (any split of the tokens), plus
  *    small tables (each sequence's first chunk, each chunk's first token and
- *    length; 1 KiB granules).  A smaller workspace makes the call run the heads in
+ *    length, and the order in which the state pass takes the sequences:
+ *    longest first; 1 KiB granules).  A smaller workspace makes the call run the heads in
  *    groups; one too small for a single head's records, or none, makes it
  *    run the single-pass kernel instead.  Either way the results are the same
  *    up to rounding.

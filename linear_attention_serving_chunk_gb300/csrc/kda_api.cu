@@ -50,10 +50,10 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               const float *S0, kda_bf16 *o, float *S_final, float *snaps,
                               const int64_t *snap_offsets, int *status, const int32_t *slots,
                               int n_slots, int zero_u, int s0_identity, float *S_final2,
-                              cudaStream_t stream);
+                              const int32_t *order, cudaStream_t stream);
 cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
-                               int32_t *chunk_start, int2 *chunk_info, int *status,
-                               cudaStream_t stream);
+                               int32_t *chunk_start, int2 *chunk_info, int32_t *order,
+                               int *status, cudaStream_t stream);
 cudaError_t segment_combine_launch(const float *M, const float *N, const float *S0,
                                    float *S_start, float *S_final, int n_seq, int n_segs, int H,
                                    cudaStream_t stream);
@@ -120,9 +120,14 @@ size_t chunk_start_bytes(int n_seq) {
   return round_kib((static_cast<size_t>(n_seq) + 1) * sizeof(int32_t));
 }
 
+size_t chunk_info_bytes(int n_seq, int64_t total_tokens) {
+  return round_kib(static_cast<size_t>(split_max_chunks(n_seq, total_tokens)) * sizeof(int2));
+}
+
+// [chunk_start | chunk_info | state-pass order of the sequences], then the records
 size_t split_table_bytes(int n_seq, int64_t total_tokens) {
-  return chunk_start_bytes(n_seq) +
-         round_kib(static_cast<size_t>(split_max_chunks(n_seq, total_tokens)) * sizeof(int2));
+  return chunk_start_bytes(n_seq) + chunk_info_bytes(n_seq, total_tokens) +
+         round_kib(static_cast<size_t>(n_seq) * sizeof(int32_t));
 }
 
 size_t split_workspace_bytes(int n_seq, int64_t total_tokens, int hg) {
@@ -308,13 +313,13 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
       if (err == cudaSuccess)
         err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, dk, dv,
                                 0, H, nullptr, nullptr, Nb, nullptr, nullptr, status, nullptr, 0,
-                                0, 0, Mb, st);
+                                0, 0, Mb, nullptr, st);
       if (err == cudaSuccess)
         err = segment_combine_launch(Mb, Nb, S0, Ss, S_final, n_seq, plan.n_segs, H, st);
       if (err == cudaSuccess)
         err = state_pass_launch(rec, nullptr, nullptr, n2, plan.seg_len, total_tokens, H, dk, dv,
                                 0, H, Ss, o, nullptr, snaps, nullptr, status, nullptr, 0, 0, 0,
-                                nullptr, st);
+                                nullptr, nullptr, st);
       return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     }
     // 1. every segment from a zero state (N) and its transition from S0 = I with v = 0 (M)
@@ -342,16 +347,18 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
   if (hg > 0) {
     // two passes per group of hg heads: chunk preparation, then the state pass
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    int32_t *chunk_start = nullptr;
+    int32_t *chunk_start = nullptr, *order = nullptr;
     int2 *chunk_info = nullptr;
     err = cudaSuccess;
     const bool run_prep = passes != KDA_PASS_STATE, run_state = passes != KDA_PASS_PREPARE;
     if (cu_seqlens) {
       chunk_start = reinterpret_cast<int32_t *>(ws);
       chunk_info = reinterpret_cast<int2 *>(ws + chunk_start_bytes(n_seq));
+      order = reinterpret_cast<int32_t *>(ws + chunk_start_bytes(n_seq) +
+                                          chunk_info_bytes(n_seq, total_tokens));
       if (run_prep)
-        err = chunk_start_launch(cu_seqlens, n_seq, total_tokens, chunk_start, chunk_info, status,
-                                 st);
+        err = chunk_start_launch(cu_seqlens, n_seq, total_tokens, chunk_start, chunk_info, order,
+                                 status, st);
     }
     uint8_t *rec = ws + split_table_bytes(n_seq, total_tokens);
     const int64_t max_chunks = cu_seqlens ? split_max_chunks(n_seq, total_tokens)
@@ -365,7 +372,7 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
       if (err == cudaSuccess && run_state)
         err = state_pass_launch(rec, cu_seqlens, chunk_start, n_seq, fixed_len, total_tokens, H,
                                 dk, dv, h0, g, S0, o, S_final, snaps, snap_offsets, status,
-                                nullptr, 0, 0, 0, nullptr, st);
+                                nullptr, 0, 0, 0, nullptr, order, st);
     }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }

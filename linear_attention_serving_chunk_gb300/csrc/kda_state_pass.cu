@@ -108,6 +108,7 @@ struct SpParams {
   float *S_final2;  // non-NULL: the paired pass -- chain 1 from zero with v
                     // (final state to S_final), chain 2 from the identity with
                     // v = 0 (final state to S_final2); no o, no snapshots
+  const int32_t *order;  // varlen: the sequence of each grid row (longest first), or NULL
 };
 
 // One CTA per (sequence, head, half of the value columns): the columns of the
@@ -123,7 +124,17 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     return;
   }
   const int halves = p.dv / NC;  // CTAs per chain
-  const int hh = blockIdx.x / halves, half = blockIdx.x - hh * halves, s = blockIdx.y;
+  const int hh = blockIdx.x / halves, half = blockIdx.x - hh * halves;
+  // grid rows in the chunk table's order, longest sequences first, so that the
+  // long chains do not start in the last wave
+  int s = blockIdx.y;
+  if (p.order) {
+    s = p.order[blockIdx.y];
+    if (s < 0 || s >= p.n_seq) {
+      if (tid == 0) atomicOr(p.status, KDA_ERR_SHAPE);
+      return;
+    }
+  }
   const int H = p.H, h = p.h0 + hh;
   const int DK = p.dk, DV = p.dv;
   const int col0 = NC * half;
@@ -470,7 +481,7 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                               const float *S0, kda_bf16 *o, float *S_final, float *snaps,
                               const int64_t *snap_offsets, int *status, const int32_t *slots,
                               int n_slots, int zero_u, int s0_identity, float *S_final2,
-                              cudaStream_t stream) {
+                              const int32_t *order, cudaStream_t stream) {
   // Snapshots as a 3-D fp32 array [rows * H][dk][dv]; rows <= total_tokens / 64
   // (each snapshot follows a full chunk), which bounds the map's extent.  A
   // box is 32 value columns x dk key rows of one (row, head) state, so a
@@ -502,7 +513,7 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
   SpParams prm{rec,     cu_seqlens, chunk_start, fixed_len, total_tokens, n_seq, H,
                h0,      hg,         dk,          dv,        S0,           o,     S_final,
                snaps,   snap_offsets, status,    slots,     n_slots,      zero_u, s0_identity,
-               S_final2};
+               S_final2, order};
   const dim3 grid(static_cast<unsigned>((dv / NC) * hg), static_cast<unsigned>(n_seq));
   state_pass_kernel<<<grid, SP_THREADS, smem, stream>>>(tm_snap, prm);
   return cudaGetLastError();
@@ -521,11 +532,17 @@ namespace {
 // task, no record read by the state pass) and KDA_ERR_SHAPE is recorded.
 // Then, for every global chunk c of the batch, chunk_info[c] = (first token,
 // tokens in the chunk): the chunk preparation resolves a task with one load.
+// Sequences ranked by chunk count up to this many; beyond it the state pass
+// takes them in batch order (its tail is then short against the whole pass).
+constexpr int kOrderMax = 512;
+
 __global__ void __launch_bounds__(1024) chunk_start_kernel(const int32_t *__restrict__ cu,
                                                            int n_seq, int64_t total,
                                                            int32_t *__restrict__ chunk_start,
                                                            int2 *__restrict__ chunk_info,
+                                                           int32_t *__restrict__ order,
                                                            int *status) {
+  __shared__ int32_t cnt[kOrderMax];
   __shared__ int32_t warp_sum[32];
   __shared__ int32_t carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -567,8 +584,25 @@ __global__ void __launch_bounds__(1024) chunk_start_kernel(const int32_t *__rest
   if (tid == 0) chunk_start[n_seq] = carry;
   if (__syncthreads_or(bad)) {
     for (int i = tid; i <= n_seq; i += 1024) chunk_start[i] = 0;
+    for (int i = tid; i < n_seq; i += 1024) order[i] = i;
     if (tid == 0) atomicOr(status, KDA_ERR_SHAPE);
     return;
+  }
+  // state-pass order: descending chunk count, ties in batch order (a permutation)
+  if (n_seq <= kOrderMax) {
+    for (int i = tid; i < n_seq; i += 1024) cnt[i] = chunk_start[i + 1] - chunk_start[i];
+    __syncthreads();
+    for (int i = tid; i < n_seq; i += 1024) {
+      const int ci = cnt[i];
+      int rank = 0;
+      for (int j = 0; j < n_seq; ++j) {
+        const int cj = cnt[j];
+        rank += (cj > ci || (cj == ci && j < i)) ? 1 : 0;
+      }
+      order[rank] = i;
+    }
+  } else {
+    for (int i = tid; i < n_seq; i += 1024) order[i] = i;
   }
   // chunk c belongs to the last sequence s with chunk_start[s] <= c (an empty
   // sequence shares its start with the next one; the search skips it)
@@ -588,10 +622,10 @@ __global__ void __launch_bounds__(1024) chunk_start_kernel(const int32_t *__rest
 }  // namespace
 
 cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
-                               int32_t *chunk_start, int2 *chunk_info, int *status,
-                               cudaStream_t stream) {
+                               int32_t *chunk_start, int2 *chunk_info, int32_t *order,
+                               int *status, cudaStream_t stream) {
   chunk_start_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, n_seq, total_tokens, chunk_start,
-                                             chunk_info, status);
+                                             chunk_info, order, status);
   return cudaGetLastError();
 }
 

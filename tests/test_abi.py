@@ -154,11 +154,11 @@ REC = 73 * 1024  # one (chunk, head) record of the two-pass prefill
 
 def table(n_seq, total):
     """The varlen tables ahead of the records: the chunk start of every
-    sequence (int32 [n_seq + 1]) and the first token and length of every chunk
-    (int32 x 2 per chunk, for up to ceil(T/64) + n_seq chunks), each rounded up
-    to 1 KiB."""
+    sequence (int32 [n_seq + 1]), the first token and length of every chunk
+    (int32 x 2 per chunk, for up to ceil(T/64) + n_seq chunks) and the state
+    pass's order of the sequences (int32 [n_seq]), each rounded up to 1 KiB."""
     kib = lambda b: (b + 1023) // 1024 * 1024
-    return kib((n_seq + 1) * 4) + kib(((total + 63) // 64 + n_seq) * 8)
+    return kib((n_seq + 1) * 4) + kib(((total + 63) // 64 + n_seq) * 8) + kib(n_seq * 4)
 
 
 @pytest.mark.parametrize("n_seq,total,H,dk,dv,chunk,expect", [

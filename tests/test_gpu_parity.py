@@ -351,6 +351,18 @@ def test_ragged_lengths(kda, dk, dv):
     assert torch.equal(S_final[0], x["S0"][0])
 
 
+@pytest.mark.parametrize("n", [512, 600])
+def test_many_sequences_and_the_state_pass_order(kda, n):
+    """The chunk table ranks up to 512 sequences longest first for the state
+    pass (ties in batch order) and leaves more in batch order.  Lengths with
+    many ties, empty and exact-chunk sequences: every sequence must be taken
+    exactly once (a missed one leaves NaN outputs, a doubled one races)."""
+    rng = np.random.default_rng(77 + n)
+    lengths = rng.choice([0, 1, 63, 64, 65, 130, 257, 700], size=n).tolist()
+    x = kda_inputs.make_prefill(2, 128, 128, lengths, seed=12 + n, device="cuda", S0_std=0.02)
+    check_all(x, kda)
+
+
 def test_zero_initial_state_and_no_optional_outputs(kda):
     x = kda_inputs.make_prefill(2, 64, 64, [150, 77], seed=12, device="cuda")
     o = kda.chunk_fwd(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
@@ -586,7 +598,7 @@ def test_two_pass_in_head_groups(kda, heads_per_group):
     x = kda_inputs.make_prefill(H, 128, 128, lengths, seed=54, device="cuda", S0_std=0.02)
     n, total = len(lengths), x["k"].shape[0]
     kib = lambda b: (b + 1023) // 1024 * 1024
-    table = kib((n + 1) * 4) + kib(((total + 63) // 64 + n) * 8)  # chunk starts, chunk table
+    table = kib((n + 1) * 4) + kib(((total + 63) // 64 + n) * 8) + kib(n * 4)  # starts, chunks, order
     per_head = ((total + 63) // 64 + n) * 73 * 1024
     assert kda.workspace_bytes(n, total, H, 128, 128) == table + H * per_head
     ws = torch.empty(table + heads_per_group * per_head, dtype=torch.uint8, device="cuda")

@@ -142,7 +142,13 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
 // the key rows, so p = S^T k and u = S^T q are reduced by shuffles inside the
 // warp and a token needs no CTA barrier.  The tokens' inputs are staged in
 // shared memory kTokBlock at a time (with the pre-ops and k.q per token).
+// A lane reads the decay, k and q of its RPT rows as float4s; each row group
+// is padded to an odd number of 16-byte units, so the row groups of a warp
+// fall on distinct banks and the loads are conflict-free.
 constexpr int kTokBlock = 16;
+
+// Padded length of a row group of RPT key channels in the staging arrays.
+constexpr int tok_row_stride(int rpt) { return ((rpt / 4 + 1) & 1) ? rpt + 4 : rpt + 8; }
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(kDecodeThreads)
@@ -158,9 +164,14 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
   constexpr int RL = 32 / CQ;         // row groups per warp (lanes sharing columns)
   constexpr int RPT = DK / RL;        // rows per lane
   static_assert(CQ * RL == 32 && RPT * RL == DK && 4 * CQ * NW == DV, "decode tiling");
+  constexpr int RPS = tok_row_stride(RPT);  // row group stride (floats)
+  constexpr int KS = RL * RPS;              // one token's padded key channels
+  static_assert(RPT % 4 == 0 && ((RPS / 4) & 1) == 1, "float4 rows, odd 16-byte stride");
+  // key channel c of a token at c / RPT * RPS + c % RPT
+  auto kidx = [](int c) { return c / RPT * RPS + c % RPT; };
 
-  __shared__ float s_a[kTokBlock][DK], s_k[kTokBlock][DK], s_q[kTokBlock][DK];
-  __shared__ float s_v[kTokBlock][DV];
+  __shared__ __align__(16) float s_a[kTokBlock][KS], s_k[kTokBlock][KS], s_q[kTokBlock][KS];
+  __shared__ __align__(16) float s_v[kTokBlock][DV];
   __shared__ float s_beta[kTokBlock], s_kq[kTokBlock];
 
   const int row = blockIdx.x;  // b * H + h
@@ -176,10 +187,15 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
   }
   if (t_end == t_begin) return;  // no token: the state stays as it is
   float *S = pool + (static_cast<size_t>(slot) * H + h) * (DK * DV);
-  float4 s[RPT];  // rows rl * RPT + rr, columns col .. col + 3
+  // rows rl * RPT + rr, columns col, col + 1 (sl) and col + 2, col + 3 (sh):
+  // column pairs for the packed fp32x2 arithmetic
+  float2 sl[RPT], sh[RPT];
 #pragma unroll
-  for (int rr = 0; rr < RPT; ++rr)
-    s[rr] = __ldcs(reinterpret_cast<const float4 *>(S + (rl * RPT + rr) * DV + col));
+  for (int rr = 0; rr < RPT; ++rr) {
+    const float4 t = __ldcs(reinterpret_cast<const float4 *>(S + (rl * RPT + rr) * DV + col));
+    sl[rr] = make_float2(t.x, t.y);
+    sh[rr] = make_float2(t.z, t.w);
+  }
   const float eA = expf(A[h]);
 
   for (int64_t t0 = t_begin; t0 < t_end; t0 += kTokBlock) {
@@ -188,9 +204,10 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
     for (int x = tid; x < nt * DK; x += kDecodeThreads) {
       const int j = x / DK, c = x - j * DK;
       const size_t g = (static_cast<size_t>(t0 + j) * H + h) * DK + c;
-      s_k[j][c] = bf2f(k[g]);
-      s_q[j][c] = bf2f(q[g]);
-      s_a[j][c] = decay_factor(gmin, eA, bf2f(z[g]));
+      const int ci = kidx(c);
+      s_k[j][ci] = bf2f(k[g]);
+      s_q[j][ci] = bf2f(q[g]);
+      s_a[j][ci] = decay_factor(gmin, eA, bf2f(z[g]));
     }
     for (int x = tid; x < nt * DV; x += kDecodeThreads) {
       const int j = x / DV, c = x - j * DV;
@@ -203,8 +220,9 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
       if (pre & KDA_PRE_L2NORM_QK) {
         float kk = 0.f, qq = 0.f;
         for (int c = lane; c < DK; c += 32) {
-          kk += s_k[j][c] * s_k[j][c];
-          qq += s_q[j][c] * s_q[j][c];
+          const int ci = kidx(c);
+          kk += s_k[j][ci] * s_k[j][ci];
+          qq += s_q[j][ci] * s_q[j][ci];
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -213,13 +231,14 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
         }
         const float ik = kk > 0.f ? rsqrtf(kk) : 0.f, iq = qq > 0.f ? rsqrtf(qq) : 0.f;
         for (int c = lane; c < DK; c += 32) {
-          s_k[j][c] *= ik;
-          s_q[j][c] *= iq;
+          const int ci = kidx(c);
+          s_k[j][ci] *= ik;
+          s_q[j][ci] *= iq;
         }
         __syncwarp();
       }
       float kq = 0.f;
-      for (int c = lane; c < DK; c += 32) kq += s_k[j][c] * s_q[j][c];
+      for (int c = lane; c < DK; c += 32) kq += s_k[j][kidx(c)] * s_q[j][kidx(c)];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
       if (lane == 0) {
@@ -231,46 +250,70 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
     }
     __syncthreads();
     for (int j = 0; j < nt; ++j) {
-      float p[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 pl = make_float2(0.f, 0.f), ph = pl, ul = pl, uh = pl;  // p, u of the 4 columns
+      float kr[RPT];  // this lane's k rows, kept for the update
 #pragma unroll
-      for (int rr = 0; rr < RPT; ++rr) {
-        const int i = rl * RPT + rr;
-        const float a = s_a[j][i], kv = s_k[j][i], qv = s_q[j][i];
-        s[rr].x *= a; s[rr].y *= a; s[rr].z *= a; s[rr].w *= a;
-        p[0] += s[rr].x * kv; p[1] += s[rr].y * kv; p[2] += s[rr].z * kv; p[3] += s[rr].w * kv;
-        u[0] += s[rr].x * qv; u[1] += s[rr].y * qv; u[2] += s[rr].z * qv; u[3] += s[rr].w * qv;
+      for (int m = 0; m < RPT / 4; ++m) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(&s_a[j][rl * RPS + 4 * m]);
+        const float4 k4 = *reinterpret_cast<const float4 *>(&s_k[j][rl * RPS + 4 * m]);
+        const float4 q4 = *reinterpret_cast<const float4 *>(&s_q[j][rl * RPS + 4 * m]);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv4[4] = {k4.x, k4.y, k4.z, k4.w},
+                    qv4[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int rr = 4 * m + e;
+          kr[rr] = kv4[e];
+          const float2 a2 = make_float2(av[e], av[e]), k2 = make_float2(kv4[e], kv4[e]),
+                       q2 = make_float2(qv4[e], qv4[e]);
+          sl[rr] = __fmul2_rn(sl[rr], a2);
+          sh[rr] = __fmul2_rn(sh[rr], a2);
+          pl = __ffma2_rn(sl[rr], k2, pl);
+          ph = __ffma2_rn(sh[rr], k2, ph);
+          ul = __ffma2_rn(sl[rr], q2, ul);
+          uh = __ffma2_rn(sh[rr], q2, uh);
+        }
       }
       // sums over the warp's row groups (lanes CQ apart): every lane gets its columns' p, u
 #pragma unroll
-      for (int off = CQ; off < 32; off <<= 1)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          p[c] += __shfl_xor_sync(0xffffffffu, p[c], off);
-          u[c] += __shfl_xor_sync(0xffffffffu, u[c], off);
-        }
+      for (int off = CQ; off < 32; off <<= 1) {
+        const float2 rpl = make_float2(__shfl_xor_sync(0xffffffffu, pl.x, off),
+                                       __shfl_xor_sync(0xffffffffu, pl.y, off));
+        const float2 rph = make_float2(__shfl_xor_sync(0xffffffffu, ph.x, off),
+                                       __shfl_xor_sync(0xffffffffu, ph.y, off));
+        const float2 rul = make_float2(__shfl_xor_sync(0xffffffffu, ul.x, off),
+                                       __shfl_xor_sync(0xffffffffu, ul.y, off));
+        const float2 ruh = make_float2(__shfl_xor_sync(0xffffffffu, uh.x, off),
+                                       __shfl_xor_sync(0xffffffffu, uh.y, off));
+        pl = __fadd2_rn(pl, rpl);
+        ph = __fadd2_rn(ph, rph);
+        ul = __fadd2_rn(ul, rul);
+        uh = __fadd2_rn(uh, ruh);
+      }
       const float bt = s_beta[j], kq = s_kq[j];
-      float d[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) d[c] = bt * (s_v[j][col + c] - p[c]);
+      const float4 v4 = *reinterpret_cast<const float4 *>(&s_v[j][col]);
+      const float2 dl = make_float2(bt * (v4.x - pl.x), bt * (v4.y - pl.y));
+      const float2 dh = make_float2(bt * (v4.z - ph.x), bt * (v4.w - ph.y));
       if (rl == 0) {
         uint2 w;
-        w.x = static_cast<uint32_t>(f2bf(u[0] + kq * d[0])) |
-              (static_cast<uint32_t>(f2bf(u[1] + kq * d[1])) << 16);
-        w.y = static_cast<uint32_t>(f2bf(u[2] + kq * d[2])) |
-              (static_cast<uint32_t>(f2bf(u[3] + kq * d[3])) << 16);
+        w.x = static_cast<uint32_t>(f2bf(ul.x + kq * dl.x)) |
+              (static_cast<uint32_t>(f2bf(ul.y + kq * dl.y)) << 16);
+        w.y = static_cast<uint32_t>(f2bf(uh.x + kq * dh.x)) |
+              (static_cast<uint32_t>(f2bf(uh.y + kq * dh.y)) << 16);
         *reinterpret_cast<uint2 *>(o + (static_cast<size_t>(t0 + j) * H + h) * DV + col) = w;
       }
 #pragma unroll
       for (int rr = 0; rr < RPT; ++rr) {
-        const float kv = s_k[j][rl * RPT + rr];
-        s[rr].x += kv * d[0]; s[rr].y += kv * d[1]; s[rr].z += kv * d[2]; s[rr].w += kv * d[3];
+        const float2 k2 = make_float2(kr[rr], kr[rr]);
+        sl[rr] = __ffma2_rn(k2, dl, sl[rr]);
+        sh[rr] = __ffma2_rn(k2, dh, sh[rr]);
       }
     }
   }
   if (commit) {
 #pragma unroll
     for (int rr = 0; rr < RPT; ++rr)
-      __stcs(reinterpret_cast<float4 *>(S + (rl * RPT + rr) * DV + col), s[rr]);
+      __stcs(reinterpret_cast<float4 *>(S + (rl * RPT + rr) * DV + col),
+             make_float4(sl[rr].x, sl[rr].y, sh[rr].x, sh[rr].y));
   }
 }
 

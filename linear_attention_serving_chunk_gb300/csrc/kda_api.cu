@@ -24,7 +24,7 @@ cudaError_t decode_tokens_launch(const kda_bf16 *q, const kda_bf16 *k, const kda
                                  float gmin, float *pool, const int32_t *slots, int n_slots,
                                  const int32_t *cu_seqlens, int n, int64_t total, int H, int dk,
                                  int dv, kda_bf16 *o, unsigned pre, int commit, int *status,
-                                 cudaStream_t stream);
+                                 int n_sms, cudaStream_t stream);
 cudaError_t snapshot_restore_launch(const float *snaps, int64_t n_rows, const int64_t *src_idx,
                                     float *pool, int n_slots, const int32_t *dst_slots, int n,
                                     int H, int dk, int dv, int *status, cudaStream_t stream);
@@ -432,11 +432,11 @@ int kda_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
   int *status = status_word();
   if (!status) return KDA_ERR_CUDA;
   if (total_tokens <= kDecodeTokensRun * static_cast<int64_t>(n) &&
-      static_cast<int64_t>(n) * H <= 0x7fffffffLL) {  // one CTA per (sequence, head)
+      static_cast<int64_t>(n_slots) * H <= 0x7fffffffLL) {
     // short runs: the tokens one after another on the state in registers
     const cudaError_t err =
         decode_tokens_launch(q, k, v, z, beta, A, gmin, state_pool, slots, n_slots, cu_seqlens, n,
-                             total_tokens, H, dk, dv, o, pre, commit, status, st);
+                             total_tokens, H, dk, dv, o, pre, commit, status, kSMs, st);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }
   const cudaError_t err =

@@ -13,6 +13,7 @@
 // write, so the state crosses HBM exactly twice.  Rows of S are read and
 // written as 16-byte vectors, one 512-byte row per warp instruction (dv=128).
 #include "kda_common.cuh"
+#include "kda_tc_common.cuh"
 
 namespace kda {
 
@@ -140,82 +141,146 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
 // the step above -- and the state is written back once (only when
 // committing).  Warp w owns value columns [w DV/8, (w+1) DV/8); its lanes split
 // the key rows, so p = S^T k and u = S^T q are reduced by shuffles inside the
-// warp and a token needs no CTA barrier.  The tokens' inputs are staged in
-// shared memory kTokBlock at a time (with the pre-ops and k.q per token).
-// A lane reads the decay, k and q of its RPT rows as float4s; each row group
-// is padded to an odd number of 16-byte units, so the row groups of a warp
-// fall on distinct banks and the loads are conflict-free.
-constexpr int kTokBlock = 16;
+// warp and a token needs no barrier.  The tokens' inputs are staged in shared
+// memory kTokBlock at a time (with the pre-ops and k.q per token); each row
+// group of the staging arrays is padded to an odd number of 16-byte units, so
+// a lane's float4 reads of the decay, k and q of its rows are conflict-free.
+// The arithmetic is packed fp32x2 over column pairs.
+//
+// Persistent CTAs, two per SM, each walking its (sequence, head) rows.  While
+// a CTA applies one row's tokens from registers, the next row's state comes
+// in by TMA (DV / 32 boxes of 32 columns x DK rows, 128-byte swizzle, on one
+// mbarrier) and the raw bf16 k, q, z, v rows of its first kTokBlock tokens by
+// asynchronous copies: the state read overlaps the arithmetic instead of
+// preceding it.  Lane row group rl holds the state rows rl + RL rr, so the
+// swizzle puts a warp's row groups on distinct banks when the state moves
+// into registers.  Later blocks of a long run are loaded directly.  Every
+// mbarrier wait is bounded; one that gives up records KDA_ERR_TIMEOUT, waits
+// (bounded) for the copy in flight and stops the CTA.
+constexpr int kTokBlock = 8;
+constexpr int kTokCtasPerSm = 2;
+constexpr uint32_t kTokPolls = 1u << 24;
 
 // Padded length of a row group of RPT key channels in the staging arrays.
 constexpr int tok_row_stride(int rpt) { return ((rpt / 4 + 1) & 1) ? rpt + 4 : rpt + 8; }
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(kDecodeThreads)
-decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ k,
+struct TokTiling {
+  static constexpr int NW = kDecodeThreads / 32;
+  static constexpr int CQ = DV / (4 * NW);  // 4-column groups per warp
+  static constexpr int RL = 32 / CQ;        // row groups per warp (lanes sharing columns)
+  static constexpr int RPT = DK / RL;       // rows per lane
+  static constexpr int RPS = tok_row_stride(RPT);  // row group stride (floats)
+  static constexpr int KS = RL * RPS;              // one token's padded key channels
+  static constexpr int TOKB = (3 * DK + DV) * 2;   // raw k, q, z, v of one token (bytes)
+  static constexpr uint32_t SS = 0;                                   // next state, DV / 32 boxes
+  static constexpr uint32_t RAW = SS + DK * DV * 4;                   // raw token rows
+  static constexpr uint32_t STG = RAW + kTokBlock * TOKB;             // fp32 staging
+  // (plus 1 KiB to align the swizzled boxes to 1024 bytes)
+  static constexpr uint32_t BYTES =
+      1024 + STG + (3 * kTokBlock * KS + kTokBlock * DV + 2 * kTokBlock) * 4;
+  static_assert(CQ * RL == 32 && RPT * RL == DK && 4 * CQ * NW == DV, "decode tiling");
+  static_assert(RPT % 4 == 0 && ((RPS / 4) & 1) == 1, "float4 rows, odd 16-byte stride");
+  static_assert(DV % 32 == 0 && (DK * 128) % 1024 == 0, "whole 128-byte-swizzled boxes");
+  static_assert(TOKB % 16 == 0 && STG % 16 == 0, "16-byte pieces");
+};
+
+struct TokRow {  // one (sequence, head) row of the work
+  int64_t t0;    // first token
+  int L;         // tokens (0: nothing to do, or a rejected row)
+  int slot, h;
+  bool bad;      // slot or cu_seqlens out of range
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kDecodeThreads, kTokCtasPerSm)
+decode_tokens_kernel(const __grid_constant__ CUtensorMap tm_state,
+                     const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ k,
                      const kda_bf16 *__restrict__ v, const kda_bf16 *__restrict__ z,
                      const kda_bf16 *__restrict__ beta, const float *__restrict__ A,
                      float gmin, float *__restrict__ pool, const int32_t *__restrict__ slots,
                      int n_slots, const int32_t *__restrict__ cu_seqlens, int64_t total, int H,
-                     kda_bf16 *__restrict__ o, unsigned pre, int commit,
+                     int64_t rows, kda_bf16 *__restrict__ o, unsigned pre, int commit,
                      int *__restrict__ status) {
-  constexpr int NW = kDecodeThreads / 32;
-  constexpr int CQ = DV / (4 * NW);   // 4-column groups per warp
-  constexpr int RL = 32 / CQ;         // row groups per warp (lanes sharing columns)
-  constexpr int RPT = DK / RL;        // rows per lane
-  static_assert(CQ * RL == 32 && RPT * RL == DK && 4 * CQ * NW == DV, "decode tiling");
-  constexpr int RPS = tok_row_stride(RPT);  // row group stride (floats)
-  constexpr int KS = RL * RPS;              // one token's padded key channels
-  static_assert(RPT % 4 == 0 && ((RPS / 4) & 1) == 1, "float4 rows, odd 16-byte stride");
-  // key channel c of a token at c / RPT * RPS + c % RPT
-  auto kidx = [](int c) { return c / RPT * RPS + c % RPT; };
+  using T = TokTiling<DK, DV>;
+  constexpr int NW = T::NW, CQ = T::CQ, RL = T::RL, RPT = T::RPT, RPS = T::RPS, KS = T::KS;
+  // key channel c = rl + RL rr of a token at rl RPS + rr
+  auto kidx = [](int c) { return c % RL * RPS + c / RL; };
+  extern __shared__ __align__(16) uint8_t tsm_raw[];
+  __shared__ __align__(8) uint64_t load_bar;
+  uint8_t *tsm = tsm_raw + ((1024u - (sm100::smem_u32(tsm_raw) & 1023u)) & 1023u);
+  float(*s_a)[KS] = reinterpret_cast<float(*)[KS]>(tsm + T::STG);
+  float(*s_k)[KS] = s_a + kTokBlock;
+  float(*s_q)[KS] = s_k + kTokBlock;
+  float(*s_v)[DV] = reinterpret_cast<float(*)[DV]>(s_q + kTokBlock);
+  float *s_beta = reinterpret_cast<float *>(s_v + kTokBlock), *s_kq = s_beta + kTokBlock;
 
-  __shared__ __align__(16) float s_a[kTokBlock][KS], s_k[kTokBlock][KS], s_q[kTokBlock][KS];
-  __shared__ __align__(16) float s_v[kTokBlock][DV];
-  __shared__ float s_beta[kTokBlock], s_kq[kTokBlock];
-
-  const int row = blockIdx.x;  // b * H + h
-  const int b = row / H, h = row - b * H;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cq = lane % CQ, rl = lane / CQ;
   const int col = 4 * (warp * CQ + cq);  // this lane's first value column
-  const int slot = slots[b];
-  int64_t t_begin, t_end;
-  if (slot < 0 || slot >= n_slots || !seq_range(cu_seqlens, b, total, t_begin, t_end)) {
-    if (tid == 0) atomicOr(status, KDA_ERR_SHAPE);  // nothing of this sequence is touched
-    return;
+  const uint32_t sbase = sm100::smem_u32(tsm), bar = sm100::smem_u32(&load_bar);
+  if (tid == 0) {
+    sm100::mbar_init(bar, 1);
+    sm100::fence_mbar_init();
+    sm100::prefetch_tensormap(&tm_state);
   }
-  if (t_end == t_begin) return;  // no token: the state stays as it is
-  float *S = pool + (static_cast<size_t>(slot) * H + h) * (DK * DV);
-  // rows rl * RPT + rr, columns col, col + 1 (sl) and col + 2, col + 3 (sh):
-  // column pairs for the packed fp32x2 arithmetic
-  float2 sl[RPT], sh[RPT];
-#pragma unroll
-  for (int rr = 0; rr < RPT; ++rr) {
-    const float4 t = __ldcs(reinterpret_cast<const float4 *>(S + (rl * RPT + rr) * DV + col));
-    sl[rr] = make_float2(t.x, t.y);
-    sh[rr] = make_float2(t.z, t.w);
-  }
-  const float eA = expf(A[h]);
+  __syncthreads();
 
-  for (int64_t t0 = t_begin; t0 < t_end; t0 += kTokBlock) {
-    const int nt = static_cast<int>(min(static_cast<int64_t>(kTokBlock), t_end - t0));
-    __syncthreads();  // the previous block's tokens are done with the staging arrays
-    for (int x = tid; x < nt * DK; x += kDecodeThreads) {
-      const int j = x / DK, c = x - j * DK;
-      const size_t g = (static_cast<size_t>(t0 + j) * H + h) * DK + c;
-      const int ci = kidx(c);
-      s_k[j][ci] = bf2f(k[g]);
-      s_q[j][ci] = bf2f(q[g]);
-      s_a[j][ci] = decay_factor(gmin, eA, bf2f(z[g]));
+  auto row_of = [&](int64_t r) -> TokRow {
+    TokRow w{0, 0, 0, 0, false};
+    if (r >= rows) return w;
+    const int b = static_cast<int>(r / H);
+    w.h = static_cast<int>(r - static_cast<int64_t>(b) * H);
+    w.slot = slots[b];
+    int64_t e = 0;
+    if (w.slot < 0 || w.slot >= n_slots || !seq_range(cu_seqlens, b, total, w.t0, e)) {
+      w.bad = true;
+      return w;
     }
-    for (int x = tid; x < nt * DV; x += kDecodeThreads) {
-      const int j = x / DV, c = x - j * DV;
-      s_v[j][c] = bf2f(v[(static_cast<size_t>(t0 + j) * H + h) * DV + c]);
+    w.L = static_cast<int>(e - w.t0);
+    return w;
+  };
+  // the state of row w (TMA) and its first block's raw token rows; beta of
+  // those tokens into a register of threads 0 .. nt - 1
+  float beta_next = 0.f;
+  auto prefetch = [&](const TokRow &w) {
+    if (w.L == 0) return;
+    if (tid == 0) {
+      sm100::fence_proxy_async();
+      sm100::mbar_expect_tx(bar, DK * DV * 4);
+      const int st = w.slot * H + w.h;  // < 2^31, checked by the launch
+#pragma unroll
+      for (int b = 0; b < DV / 32; ++b)
+        sm100::tma_load_3d(sbase + T::SS + b * DK * 128, &tm_state, 32 * b, 0, st, bar);
     }
+    const int nt = min(w.L, kTokBlock);
+    constexpr int P = T::TOKB / 16;  // 16-byte pieces per token
+    for (int x = tid; x < nt * P; x += kDecodeThreads) {
+      const int j = x / P, ob = (x - j * P) * 16;  // byte offset in the token's raw rows
+      const size_t tok = static_cast<size_t>(w.t0 + j) * H + w.h;
+      const uint8_t *src =
+          ob < 2 * DK   ? reinterpret_cast<const uint8_t *>(k + tok * DK) + ob
+          : ob < 4 * DK ? reinterpret_cast<const uint8_t *>(q + tok * DK) + (ob - 2 * DK)
+          : ob < 6 * DK ? reinterpret_cast<const uint8_t *>(z + tok * DK) + (ob - 4 * DK)
+                        : reinterpret_cast<const uint8_t *>(v + tok * DV) + (ob - 6 * DK);
+      cp_async16(sbase + T::RAW + j * T::TOKB + ob, src);
+    }
+    cp_async_commit();
+    if (tid < nt) beta_next = bf2f(beta[static_cast<size_t>(w.t0 + tid) * H + w.h]);
+  };
+  // the pre-op norms, k.q and beta of tokens 0 .. nt - 1 of the staging area
+  auto token_scalars = [&](int nt) {
     __syncthreads();
-    // per token (one warp each): the pre-op norms applied to k and q in place,
-    // then k.q; beta through the pre-op
     for (int j = warp; j < nt; j += NW) {
       if (pre & KDA_PRE_L2NORM_QK) {
         float kk = 0.f, qq = 0.f;
@@ -241,80 +306,161 @@ decode_tokens_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict_
       for (int c = lane; c < DK; c += 32) kq += s_k[j][kidx(c)] * s_q[j][kidx(c)];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-      if (lane == 0) {
-        float bt = bf2f(beta[static_cast<size_t>(t0 + j) * H + h]);
-        if (pre & KDA_PRE_SIGMOID_BETA) bt = 1.f / (1.f + __expf(-bt));
-        s_beta[j] = bt;
-        s_kq[j] = kq;
-      }
+      if (lane == 0) s_kq[j] = kq;
     }
+    if (tid < nt)
+      s_beta[tid] = (pre & KDA_PRE_SIGMOID_BETA) ? 1.f / (1.f + __expf(-beta_next)) : beta_next;
     __syncthreads();
-    for (int j = 0; j < nt; ++j) {
-      float2 pl = make_float2(0.f, 0.f), ph = pl, ul = pl, uh = pl;  // p, u of the 4 columns
-      float kr[RPT];  // this lane's k rows, kept for the update
+  };
+
+  const int64_t stride = gridDim.x;
+  uint32_t phase = 0;
+  TokRow cur = row_of(blockIdx.x);
+  TokRow nxt = row_of(blockIdx.x + stride);
+  prefetch(cur);
+  for (int64_t r = blockIdx.x; r < rows; r += stride) {
+    const TokRow after = row_of(r + 2 * stride);  // used one row later: its latency is hidden
+    if (cur.bad && tid == 0) atomicOr(status, KDA_ERR_SHAPE);  // nothing of it is touched
+    const int L = cur.L;
+    float2 sl[RPT], sh[RPT];  // rows rl + RL rr; columns col, col + 1 (sl) and + 2, + 3 (sh)
+    if (L > 0) {
+      const bool ok = sm100::mbar_wait_bounded(bar, phase, kTokPolls);
+      phase ^= 1u;
+      cp_async_wait_all();
+      if (__syncthreads_or(ok ? 0 : 1)) {  // also: every thread's raw token pieces are in
+        if (tid == 0) {
+          atomicOr(status, KDA_ERR_TIMEOUT);
+          sm100::mbar_wait_bounded(bar, phase ^ 1u, kTokPolls);  // the copy in flight
+        }
+        return;
+      }
+      {
+        const int b = col >> 5, chunk = (col & 31) >> 2;
 #pragma unroll
-      for (int m = 0; m < RPT / 4; ++m) {
-        const float4 a4 = *reinterpret_cast<const float4 *>(&s_a[j][rl * RPS + 4 * m]);
-        const float4 k4 = *reinterpret_cast<const float4 *>(&s_k[j][rl * RPS + 4 * m]);
-        const float4 q4 = *reinterpret_cast<const float4 *>(&s_q[j][rl * RPS + 4 * m]);
-        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv4[4] = {k4.x, k4.y, k4.z, k4.w},
-                    qv4[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int rr = 4 * m + e;
-          kr[rr] = kv4[e];
-          const float2 a2 = make_float2(av[e], av[e]), k2 = make_float2(kv4[e], kv4[e]),
-                       q2 = make_float2(qv4[e], qv4[e]);
-          sl[rr] = __fmul2_rn(sl[rr], a2);
-          sh[rr] = __fmul2_rn(sh[rr], a2);
-          pl = __ffma2_rn(sl[rr], k2, pl);
-          ph = __ffma2_rn(sh[rr], k2, ph);
-          ul = __ffma2_rn(sl[rr], q2, ul);
-          uh = __ffma2_rn(sh[rr], q2, uh);
+        for (int rr = 0; rr < RPT; ++rr) {
+          const int r = rl + RL * rr;
+          const float4 t = *reinterpret_cast<const float4 *>(
+              tsm + T::SS + b * DK * 128 + r * 128 + ((chunk ^ (r & 7)) << 4));
+          sl[rr] = make_float2(t.x, t.y);
+          sh[rr] = make_float2(t.z, t.w);
         }
       }
-      // sums over the warp's row groups (lanes CQ apart): every lane gets its columns' p, u
-#pragma unroll
-      for (int off = CQ; off < 32; off <<= 1) {
-        const float2 rpl = make_float2(__shfl_xor_sync(0xffffffffu, pl.x, off),
-                                       __shfl_xor_sync(0xffffffffu, pl.y, off));
-        const float2 rph = make_float2(__shfl_xor_sync(0xffffffffu, ph.x, off),
-                                       __shfl_xor_sync(0xffffffffu, ph.y, off));
-        const float2 rul = make_float2(__shfl_xor_sync(0xffffffffu, ul.x, off),
-                                       __shfl_xor_sync(0xffffffffu, ul.y, off));
-        const float2 ruh = make_float2(__shfl_xor_sync(0xffffffffu, uh.x, off),
-                                       __shfl_xor_sync(0xffffffffu, uh.y, off));
-        pl = __fadd2_rn(pl, rpl);
-        ph = __fadd2_rn(ph, rph);
-        ul = __fadd2_rn(ul, rul);
-        uh = __fadd2_rn(uh, ruh);
+      // the first block's tokens: raw bf16 -> fp32 staging (decay through the gate)
+      const int nt = min(L, kTokBlock);
+      const float eA = expf(A[cur.h]);
+      for (int x = tid; x < nt * DK; x += kDecodeThreads) {
+        const int j = x / DK, c = x - j * DK;
+        const kda_bf16 *raw = reinterpret_cast<const kda_bf16 *>(tsm + T::RAW + j * T::TOKB);
+        const int ci = kidx(c);
+        s_k[j][ci] = bf2f(raw[c]);
+        s_q[j][ci] = bf2f(raw[DK + c]);
+        s_a[j][ci] = decay_factor(gmin, eA, bf2f(raw[2 * DK + c]));
       }
-      const float bt = s_beta[j], kq = s_kq[j];
-      const float4 v4 = *reinterpret_cast<const float4 *>(&s_v[j][col]);
-      const float2 dl = make_float2(bt * (v4.x - pl.x), bt * (v4.y - pl.y));
-      const float2 dh = make_float2(bt * (v4.z - ph.x), bt * (v4.w - ph.y));
-      if (rl == 0) {
-        uint2 w;
-        w.x = static_cast<uint32_t>(f2bf(ul.x + kq * dl.x)) |
-              (static_cast<uint32_t>(f2bf(ul.y + kq * dl.y)) << 16);
-        w.y = static_cast<uint32_t>(f2bf(uh.x + kq * dh.x)) |
-              (static_cast<uint32_t>(f2bf(uh.y + kq * dh.y)) << 16);
-        *reinterpret_cast<uint2 *>(o + (static_cast<size_t>(t0 + j) * H + h) * DV + col) = w;
+      for (int x = tid; x < nt * DV; x += kDecodeThreads) {
+        const int j = x / DV, c = x - j * DV;
+        s_v[j][c] = bf2f(reinterpret_cast<const kda_bf16 *>(tsm + T::RAW + j * T::TOKB)[3 * DK + c]);
       }
+      token_scalars(nt);  // its barriers also end every read of the raw rows
+    }
+    // the next row's state and tokens come in while this row's tokens are applied
+    prefetch(nxt);
+
+    for (int64_t t0 = cur.t0; t0 < cur.t0 + L; t0 += kTokBlock) {
+      const int nt = static_cast<int>(min(static_cast<int64_t>(kTokBlock), cur.t0 + L - t0));
+      if (t0 != cur.t0) {  // a long run's later block: straight from global memory
+        __syncthreads();   // the previous block's tokens are done with the staging area
+        const float eA = expf(A[cur.h]);
+        for (int x = tid; x < nt * DK; x += kDecodeThreads) {
+          const int j = x / DK, c = x - j * DK;
+          const size_t g = (static_cast<size_t>(t0 + j) * H + cur.h) * DK + c;
+          const int ci = kidx(c);
+          s_k[j][ci] = bf2f(k[g]);
+          s_q[j][ci] = bf2f(q[g]);
+          s_a[j][ci] = decay_factor(gmin, eA, bf2f(z[g]));
+        }
+        for (int x = tid; x < nt * DV; x += kDecodeThreads) {
+          const int j = x / DV, c = x - j * DV;
+          s_v[j][c] = bf2f(v[(static_cast<size_t>(t0 + j) * H + cur.h) * DV + c]);
+        }
+        const float keep = beta_next;  // threads 0 .. 7 hold the next row's beta
+        if (tid < nt) beta_next = bf2f(beta[static_cast<size_t>(t0 + tid) * H + cur.h]);
+        token_scalars(nt);
+        beta_next = keep;
+      }
+      for (int j = 0; j < nt; ++j) {
+        float2 pl = make_float2(0.f, 0.f), ph = pl, ul = pl, uh = pl;  // p, u of the 4 columns
 #pragma unroll
-      for (int rr = 0; rr < RPT; ++rr) {
-        const float2 k2 = make_float2(kr[rr], kr[rr]);
-        sl[rr] = __ffma2_rn(k2, dl, sl[rr]);
-        sh[rr] = __ffma2_rn(k2, dh, sh[rr]);
+        for (int m = 0; m < RPT / 4; ++m) {
+          const float4 a4 = *reinterpret_cast<const float4 *>(&s_a[j][rl * RPS + 4 * m]);
+          const float4 k4 = *reinterpret_cast<const float4 *>(&s_k[j][rl * RPS + 4 * m]);
+          const float4 q4 = *reinterpret_cast<const float4 *>(&s_q[j][rl * RPS + 4 * m]);
+          const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv4[4] = {k4.x, k4.y, k4.z, k4.w},
+                      qv4[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int rr = 4 * m + e;
+            const float2 a2 = make_float2(av[e], av[e]), k2 = make_float2(kv4[e], kv4[e]),
+                         q2 = make_float2(qv4[e], qv4[e]);
+            sl[rr] = __fmul2_rn(sl[rr], a2);
+            sh[rr] = __fmul2_rn(sh[rr], a2);
+            pl = __ffma2_rn(sl[rr], k2, pl);
+            ph = __ffma2_rn(sh[rr], k2, ph);
+            ul = __ffma2_rn(sl[rr], q2, ul);
+            uh = __ffma2_rn(sh[rr], q2, uh);
+          }
+        }
+        // sums over the warp's row groups (lanes CQ apart): every lane gets its columns' p, u
+#pragma unroll
+        for (int off = CQ; off < 32; off <<= 1) {
+          const float2 rpl = make_float2(__shfl_xor_sync(0xffffffffu, pl.x, off),
+                                         __shfl_xor_sync(0xffffffffu, pl.y, off));
+          const float2 rph = make_float2(__shfl_xor_sync(0xffffffffu, ph.x, off),
+                                         __shfl_xor_sync(0xffffffffu, ph.y, off));
+          const float2 rul = make_float2(__shfl_xor_sync(0xffffffffu, ul.x, off),
+                                         __shfl_xor_sync(0xffffffffu, ul.y, off));
+          const float2 ruh = make_float2(__shfl_xor_sync(0xffffffffu, uh.x, off),
+                                         __shfl_xor_sync(0xffffffffu, uh.y, off));
+          pl = __fadd2_rn(pl, rpl);
+          ph = __fadd2_rn(ph, rph);
+          ul = __fadd2_rn(ul, rul);
+          uh = __fadd2_rn(uh, ruh);
+        }
+        const float bt = s_beta[j], kq = s_kq[j];
+        const float4 v4 = *reinterpret_cast<const float4 *>(&s_v[j][col]);
+        const float2 dl = make_float2(bt * (v4.x - pl.x), bt * (v4.y - pl.y));
+        const float2 dh = make_float2(bt * (v4.z - ph.x), bt * (v4.w - ph.y));
+        if (rl == 0) {
+          uint2 w;
+          w.x = static_cast<uint32_t>(f2bf(ul.x + kq * dl.x)) |
+                (static_cast<uint32_t>(f2bf(ul.y + kq * dl.y)) << 16);
+          w.y = static_cast<uint32_t>(f2bf(uh.x + kq * dh.x)) |
+                (static_cast<uint32_t>(f2bf(uh.y + kq * dh.y)) << 16);
+          *reinterpret_cast<uint2 *>(o + (static_cast<size_t>(t0 + j) * H + cur.h) * DV + col) = w;
+        }
+#pragma unroll
+        for (int m = 0; m < RPT / 4; ++m) {
+          const float4 k4 = *reinterpret_cast<const float4 *>(&s_k[j][rl * RPS + 4 * m]);
+          const float kv4[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 k2 = make_float2(kv4[e], kv4[e]);
+            sl[4 * m + e] = __ffma2_rn(k2, dl, sl[4 * m + e]);
+            sh[4 * m + e] = __ffma2_rn(k2, dh, sh[4 * m + e]);
+          }
+        }
       }
     }
-  }
-  if (commit) {
+    if (L > 0 && commit) {
+      float *S = pool + (static_cast<size_t>(cur.slot) * H + cur.h) * (DK * DV);
 #pragma unroll
-    for (int rr = 0; rr < RPT; ++rr)
-      __stcs(reinterpret_cast<float4 *>(S + (rl * RPT + rr) * DV + col),
-             make_float4(sl[rr].x, sl[rr].y, sh[rr].x, sh[rr].y));
+      for (int rr = 0; rr < RPT; ++rr)
+        __stcs(reinterpret_cast<float4 *>(S + (rl + RL * rr) * DV + col),
+               make_float4(sl[rr].x, sl[rr].y, sh[rr].x, sh[rr].y));
+    }
+    cur = nxt;
+    nxt = after;
   }
+  cp_async_wait_all();  // nothing may still be arriving when the CTA's shared memory goes
 }
 
 template <int DK, int DV>
@@ -322,12 +468,34 @@ cudaError_t launch_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda
                                  const kda_bf16 *z, const kda_bf16 *beta, const float *A,
                                  float gmin, float *pool, const int32_t *slots, int n_slots,
                                  const int32_t *cu_seqlens, int n, int64_t total, int H,
-                                 kda_bf16 *o, unsigned pre, int commit, int *status,
+                                 kda_bf16 *o, unsigned pre, int commit, int *status, int n_sms,
                                  cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(n) * H;
-  decode_tokens_kernel<DK, DV><<<static_cast<unsigned>(rows), kDecodeThreads, 0, stream>>>(
-      q, k, v, z, beta, A, gmin, pool, slots, n_slots, cu_seqlens, total, H, o, pre, commit,
-      status);
+  const int64_t states = static_cast<int64_t>(n_slots) * H;  // TMA coordinates are 32-bit
+  if (states <= 0 || states > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const tcx::EncodeTiledFn encode = tcx::tensor_map_encoder();
+  if (!encode) return cudaErrorInvalidValue;
+  CUtensorMap tm_state;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(DV), static_cast<cuuint64_t>(DK),
+                              static_cast<cuuint64_t>(states)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(DV) * 4,
+                                 static_cast<cuuint64_t>(DK) * DV * 4};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(DK), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (encode(&tm_state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, pool, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const int64_t slots_max = static_cast<int64_t>(kTokCtasPerSm) * n_sms;
+  const int64_t ctas = rows < slots_max ? rows : slots_max;
+  if (ctas <= 0) return cudaSuccess;
+  const int smem = static_cast<int>(TokTiling<DK, DV>::BYTES);
+  cudaError_t err = cudaFuncSetAttribute(decode_tokens_kernel<DK, DV>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  decode_tokens_kernel<DK, DV><<<static_cast<unsigned>(ctas), kDecodeThreads, smem, stream>>>(
+      tm_state, q, k, v, z, beta, A, gmin, pool, slots, n_slots, cu_seqlens, total, H, rows, o,
+      pre, commit, status);
   return cudaGetLastError();
 }
 
@@ -349,12 +517,12 @@ cudaError_t decode_tokens_launch(const kda_bf16 *q, const kda_bf16 *k, const kda
                                  float gmin, float *pool, const int32_t *slots, int n_slots,
                                  const int32_t *cu_seqlens, int n, int64_t total, int H, int dk,
                                  int dv, kda_bf16 *o, unsigned pre, int commit, int *status,
-                                 cudaStream_t stream) {
+                                 int n_sms, cudaStream_t stream) {
 #define KDA_DT(DK_, DV_)                                                                        \
   if (dk == DK_ && dv == DV_)                                                                   \
     return launch_decode_tokens<DK_, DV_>(q, k, v, z, beta, A, gmin, pool, slots, n_slots,     \
                                           cu_seqlens, n, total, H, o, pre, commit, status,     \
-                                          stream);
+                                          n_sms, stream);
   KDA_DT(128, 128)
   KDA_DT(64, 64)
   KDA_DT(128, 64)

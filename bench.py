@@ -82,16 +82,17 @@ _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
 _TC_FILES = ("kda_tc_common.cuh", "kda_sm100.cuh", "kda_split.cuh", "kda_common.cuh")
 PROFILED_TRAFFIC = {
     # varlen prefill, 4 sequences (70,412 tokens), H = 32: 35,264 tasks
-    "chunk_prep_kernel": (2.328897e9 + 2.569476e9, 35264, "fb93ba4d94096531",
+    "chunk_prep_kernel": (2.324024e9 + 2.569180e9, 35264, "2a9151fc334afa72",
                           ("kda_chunk_prep.cu",) + _TC_FILES),
-    "state_pass_kernel": (2.626862e9 + 2.843645e9, 35264, "9436ef8b90144c54",
+    "state_pass_kernel": (2.626483e9 + 2.844175e9, 35264, "a5543806be39f2ea",
                           ("kda_state_pass.cu",) + _TC_FILES),
     # decode, 512 sequences x H = 32: 16,384 (sequence, head) states
-    "kda_decode_step": (1.090570e9 + 1.017794e9, 16384, "f693894b0151293e",
-                        ("kda_decode.cu", "kda_common.cuh")),
+    "kda_decode_step": (1.090588e9 + 1.017627e9, 16384, "627e6d5d92c7e4b1",
+                        ("kda_decode.cu", "kda_common.cuh", "kda_tc_common.cuh", "kda_sm100.cuh")),
     # verify: 4 tokens on each of 512 x H = 32 states (commit = 0)
-    "decode_tokens_kernel": (1.141138e9 + 6.22336e6, 16384, "f693894b0151293e",
-                             ("kda_decode.cu", "kda_common.cuh")),
+    "decode_tokens_kernel": (1.141094e9 + 1.8558976e7, 16384, "627e6d5d92c7e4b1",
+                             ("kda_decode.cu", "kda_common.cuh", "kda_tc_common.cuh",
+                              "kda_sm100.cuh")),
     # restore, 512 x H = 32 states
     "snapshot_restore_kernel": (1.073760e9 + 1.025011e9, 16384, "7acfbeb05332783a",
                                 ("kda_snapshot.cu", "kda_common.cuh")),

@@ -239,9 +239,10 @@ def test_decode_tokens_multi_token(kda, d):
 def test_decode_tokens_short_runs(kda, dk, dv):
     """Short runs (at most 16 tokens per sequence on average) take the
     token-by-token kernel on the state held on chip: empty runs, single
-    tokens, a run of exactly one 16-token block and one of 50 tokens (four
-    blocks); verify (commit=False) leaves the pool untouched, commit=True
-    stores the final states; both against the oracle."""
+    tokens, a run of 16 tokens (two 8-token blocks) and one of 50 tokens
+    (seven blocks, the later ones loaded directly); verify (commit=False)
+    leaves the pool untouched, commit=True stores the final states; both
+    against the oracle."""
     lengths = [1, 0, 3, 16, 2, 50, 1, 5, 0, 7]
     n, H = len(lengths), 2
     assert sum(lengths) <= 16 * n
@@ -264,6 +265,67 @@ def test_decode_tokens_short_runs(kda, dk, dv):
     assert s_err(f64(pool[perm.long()]), ref["S_final"]) <= S_TOL
     # empty runs keep their states exactly
     for b in (1, 8):
+        assert torch.equal(pool[int(perm[b])], before[int(perm[b])])
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (128, 64), (64, 128)])
+def test_decode_tokens_many_rows_per_cta(kda, dk, dv):
+    """More (sequence, head) rows than the token kernel's persistent CTAs (two
+    per SM): each CTA takes several rows in turn, the next row's state and
+    tokens prefetched while the current row's tokens run.  Runs of 0 to 20
+    tokens (a run's later 8-token blocks loaded directly), permuted slots;
+    verify and commit against the oracle, empty runs untouched."""
+    rng = np.random.default_rng(37)
+    n, H = 200, 4  # 800 rows
+    lengths = rng.choice([0, 1, 2, 4, 7, 8, 9, 12, 16, 20], size=n).tolist()
+    assert sum(lengths) <= 16 * n
+    x = kda_inputs.make_prefill(H, dk, dv, lengths, seed=41, device="cuda", S0_std=0.02)
+    perm = torch.from_numpy(rng.permutation(n).astype(np.int32)).to("cuda")
+    pool = torch.zeros((n, H, dk, dv), device="cuda")
+    pool[perm.long()] = x["S0"]
+    before = pool.clone()
+    args = [x[nm] for nm in ("q", "k", "v", "z", "beta")] + [x["A"]]
+    o_v = kda.decode_tokens(*args, pool, perm, x["cu_seqlens"], commit=False)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    assert torch.equal(pool, before)
+    o_c = kda.decode_tokens(*args, pool, perm, x["cu_seqlens"], commit=True)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    assert torch.equal(o_v, o_c)
+    ref = oracle_subset(x, list(range(n)), list(range(H)), snapshots=False)
+    assert o_err(f64(o_c), ref["o"]) <= O_TOL
+    assert s_err(f64(pool[perm.long()]), ref["S_final"]) <= S_TOL
+    for b in range(n):
+        if lengths[b] == 0:
+            assert torch.equal(pool[int(perm[b])], before[int(perm[b])])
+
+
+def test_decode_tokens_bad_slots_among_many_rows(kda):
+    """Rejected rows (slots out of range) between valid ones of the same
+    persistent CTA: they are skipped and reported, the prefetching of the rows
+    around them is unaffected, and pool slots nobody names stay as they were."""
+    rng = np.random.default_rng(43)
+    n, H, d = 160, 4, 128  # 640 rows
+    lengths = rng.integers(1, 13, size=n).tolist()
+    x = kda_inputs.make_prefill(H, d, d, lengths, seed=47, device="cuda", S0_std=0.02)
+    perm = rng.permutation(n).astype(np.int32)
+    bad = [5, 77, 151]
+    slots_np = perm.copy()
+    slots_np[bad] = [-1, n, 10 ** 6]
+    slots = torch.from_numpy(slots_np).to("cuda")
+    pool = torch.zeros((n, H, d, d), device="cuda")
+    pool[torch.from_numpy(perm).long().to("cuda")] = x["S0"]
+    before = pool.clone()
+    args = [x[nm] for nm in ("q", "k", "v", "z", "beta")] + [x["A"]]
+    kda.decode_tokens(*args, pool, slots, x["cu_seqlens"], commit=True)
+    torch.cuda.synchronize()
+    assert kda.device_status() == kda.KDA_ERR_SHAPE
+    good = [b for b in range(n) if b not in bad]
+    ref = oracle_subset(x, good, list(range(H)), snapshots=False)
+    got = f64(pool[torch.from_numpy(perm[good]).long().to("cuda")])
+    assert s_err(got, ref["S_final"]) <= S_TOL
+    for b in bad:  # the slots the rejected sequences would have used are untouched
         assert torch.equal(pool[int(perm[b])], before[int(perm[b])])
 
 

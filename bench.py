@@ -79,7 +79,7 @@ def state_bytes(token_heads, full_chunk_heads, seq_heads, dk, dv, s0=False):
 # reported only while the kernel's sources hash to the sha256 prefix recorded
 # with the capture (else the kernel has changed since: null).
 _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
-_TC_FILES = ("kda_tc_common.cuh", "kda_sm100.cuh", "kda_split.cuh", "kda_common.cuh")
+_TC_FILES = ("kda_tc_common.cuh", "kda_sm100.cuh", "kda_split.cuh", "kda_common.cuh", "kda_pdl.cuh")
 PROFILED_TRAFFIC = {
     # varlen prefill, 4 sequences (70,412 tokens), H = 32: 35,264 tasks
     "chunk_prep_kernel": (2.324024e9 + 2.569180e9, 35264, "2a9151fc334afa72",

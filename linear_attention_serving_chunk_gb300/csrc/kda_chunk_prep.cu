@@ -54,6 +54,7 @@
 // Every mbarrier wait is bounded; a wait that gives up records
 // KDA_ERR_TIMEOUT and the CTA stops cleanly.
 #include "kda_common.cuh"
+#include "kda_pdl.cuh"
 #include "kda_sm100.cuh"
 #include "kda_split.cuh"
 #include "kda_tc_common.cuh"
@@ -232,6 +233,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) atomicOr(p.status, KDA_ERR_UNSUPPORTED);
     return;
   }
+  // a dependent launch: the inputs, the chunk table and the workspace (the
+  // previous head group's state pass reads it) are only touched from here on
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int H = p.H;
   const int64_t cps = p.cu_seqlens ? 0 : (p.fixed_len + 63) / 64;
   const int64_t n_tasks =
@@ -907,9 +912,8 @@ cudaError_t chunk_prep_launch(const kda_bf16 *q, const kda_bf16 *k, const kda_bf
                hg, pre, rec, status};
   const int64_t ctas = max_tasks < 2LL * n_sms ? max_tasks : 2LL * n_sms;
   if (ctas <= 0) return cudaSuccess;
-  chunk_prep_kernel<<<static_cast<unsigned>(ctas), CP_THREADS, CP_SMEM_BYTES, stream>>>(
-      mq, mk, mz, mv, prm);
-  return cudaGetLastError();
+  return launch_pdl(chunk_prep_kernel, dim3(static_cast<unsigned>(ctas)), dim3(CP_THREADS),
+                    CP_SMEM_BYTES, stream, mq, mk, mz, mv, prm);
 }
 
 }  // namespace kda

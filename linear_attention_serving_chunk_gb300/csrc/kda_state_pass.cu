@@ -29,6 +29,7 @@
 #include <string.h>
 
 #include "kda_common.cuh"
+#include "kda_pdl.cuh"
 #include "kda_sm100.cuh"
 #include "kda_split.cuh"
 #include "kda_tc_common.cuh"
@@ -123,6 +124,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap tm_snap, const SpParams p)
     if (tid == 0) atomicOr(p.status, KDA_ERR_UNSUPPORTED);
     return;
   }
+  grid_dependency_wait();  // the records, tables and S0 of the kernels before
   const int halves = p.dv / NC;  // CTAs per chain
   const int hh = blockIdx.x / halves, half = blockIdx.x - hh * halves;
   // grid rows in the chunk table's order, longest sequences first, so that the
@@ -515,8 +517,7 @@ cudaError_t state_pass_launch(const uint8_t *rec, const int32_t *cu_seqlens,
                snaps,   snap_offsets, status,    slots,     n_slots,      zero_u, s0_identity,
                S_final2, order};
   const dim3 grid(static_cast<unsigned>((dv / NC) * hg), static_cast<unsigned>(n_seq));
-  state_pass_kernel<<<grid, SP_THREADS, smem, stream>>>(tm_snap, prm);
-  return cudaGetLastError();
+  return launch_pdl(state_pass_kernel, grid, dim3(SP_THREADS), smem, stream, tm_snap, prm);
 }
 
 }  // namespace kda
@@ -543,6 +544,8 @@ __global__ void __launch_bounds__(1024) chunk_start_kernel(const int32_t *__rest
                                                            int32_t *__restrict__ order,
                                                            int *status) {
   __shared__ int32_t cnt[kOrderMax];
+  grid_dependency_wait();
+  grid_launch_dependents();  // the chunk preparation may set up meanwhile
   __shared__ int32_t warp_sum[32];
   __shared__ int32_t carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -624,9 +627,8 @@ __global__ void __launch_bounds__(1024) chunk_start_kernel(const int32_t *__rest
 cudaError_t chunk_start_launch(const int32_t *cu_seqlens, int n_seq, int64_t total_tokens,
                                int32_t *chunk_start, int2 *chunk_info, int32_t *order,
                                int *status, cudaStream_t stream) {
-  chunk_start_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, n_seq, total_tokens, chunk_start,
-                                             chunk_info, order, status);
-  return cudaGetLastError();
+  return launch_pdl(chunk_start_kernel, dim3(1), dim3(1024), 0, stream, cu_seqlens, n_seq,
+                    total_tokens, chunk_start, chunk_info, order, status);
 }
 
 }  // namespace kda

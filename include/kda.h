@@ -259,7 +259,8 @@ int kda_decode_step_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
  * Slots must be distinct; a slot outside [0, n_slots) is skipped on the
  * device and recorded as KDA_ERR_SHAPE.  cu_seqlens (int32 [n + 1]) and
  * slots (int32 [n]) are device arrays.  pre: KDA_PRE_* input pre-ops (0 =
- * none).
+ * none).  The short-run kernel's copy waits are bounded: one that gives up
+ * records KDA_ERR_TIMEOUT in the device status word.
  *   Errors: KDA_ERR_NULL, _SHAPE, _ALIGN, _UNSUPPORTED, _CUDA.
  */
 int kda_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,

@@ -94,7 +94,7 @@ constexpr uint32_t MS_BAR_MMA = SM_MISC + 24;
 constexpr uint32_t MS_TMEM = SM_MISC + 32;
 constexpr uint32_t MS_TASK = SM_MISC + 64;        // 3 task slots of 32 bytes
 constexpr uint32_t MS_BETA = SM_MISC + 160;       // [64] fp32
-constexpr uint32_t MS_LAM = SM_MISC + 416;        // [128 channels][4 sub-tiles] fp32
+constexpr uint32_t MS_LAM = SM_MISC + 416;        // [64 channel pairs][4 sub-tiles][2] fp32
 constexpr uint32_t MS_NSQ = MS_LAM + 128 * 16;    // [64 tok][2 halves] (k.k, q.q) partial sums
 // The M = 128 Kc operand reads 128 rows of each region: its second region's
 // unused rows 96..127 end 28 KiB after SM_KC, so the allocation reaches there.
@@ -416,10 +416,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         F[s0 + u][1] = x[u][1];
         F[s0 + u][2] = x[u][2] * ta0;
         F[s0 + u][3] = x[u][3] * ta1;
-        if (g == 7) {  // the sub-tile's totals Lam_R of channels c, c + 1
+        if (g == 7) {  // the sub-tile's totals Lam_R of channels c, c + 1, as one pair
           const int c = 64 * hc + 8 * (s0 + u) + 2 * t;
-          S.f32(sb + MS_LAM + 16 * c + 4 * R) = F[s0 + u][2];
-          S.f32(sb + MS_LAM + 16 * (c + 1) + 4 * R) = F[s0 + u][3];
+          S.u64(sb + MS_LAM + 32 * (c >> 1) + 8 * R) =
+              make_uint2(__float_as_uint(F[s0 + u][2]), __float_as_uint(F[s0 + u][3]));
         }
       }
     }
@@ -478,6 +478,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int e = 0; e < 4; ++e) dacc[i][e] = 0.f;
+    // channel pairs (c, c + 1) in packed fp32x2 arithmetic: every factor below is
+    // per channel, so the pairs need no duplication
+    auto mul2 = [](float2 a, float2 b) { return __fmul2_rn(a, b); };
+    const float2 nk2a = make_float2(nka, nka), nk2b = make_float2(nkb, nkb);
+    const float2 nq2a = make_float2(nqa, nqa), nq2b = make_float2(nqb, nqb);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       const int c = 64 * hc + 8 * s + 2 * t;
@@ -487,84 +492,86 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float2 qa = unpack_bf16x2(S.u32(sb + SM_Q + off + chunk_off(ra, s)));
       float2 qb = unpack_bf16x2(S.u32(sb + SM_Q + off + chunk_off(rb, s)));
       if (l2n || !ina || !inb) {  // the pre-op's norms; zero rows past the chunk's end
-        ka.x *= nka; ka.y *= nka; kb.x *= nkb; kb.y *= nkb;
-        qa.x *= nqa; qa.y *= nqa; qb.x *= nqb; qb.y *= nqb;
+        ka = mul2(ka, nk2a);
+        kb = mul2(kb, nk2b);
+        qa = mul2(qa, nq2a);
+        qb = mul2(qb, nq2b);
       }
-      // sub-tile totals of channels c, c + 1
-      const float4 l0 = *reinterpret_cast<const float4 *>(S.ptr(sb + MS_LAM + 16 * c));
-      const float4 l1 = *reinterpret_cast<const float4 *>(S.ptr(sb + MS_LAM + 16 * (c + 1)));
-      const float la0[4] = {l0.x, l0.y, l0.z, l0.w}, la1[4] = {l1.x, l1.y, l1.z, l1.w};
-      float pre0 = 1.f, pre1 = 1.f, post0 = 1.f, post1 = 1.f;  // prod_{M<R}, prod_{M>R}
+      // sub-tile totals Lam_M of channels c, c + 1 (pairs)
+      const float4 l01 = *reinterpret_cast<const float4 *>(S.ptr(sb + MS_LAM + 32 * (c >> 1)));
+      const float4 l23 = *reinterpret_cast<const float4 *>(S.ptr(sb + MS_LAM + 32 * (c >> 1) + 16));
+      const float2 lam[4] = {make_float2(l01.x, l01.y), make_float2(l01.z, l01.w),
+                             make_float2(l23.x, l23.y), make_float2(l23.z, l23.w)};
+      float2 pre = make_float2(1.f, 1.f), post = pre;  // prod_{M<R}, prod_{M>R}
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        if (m < R) { pre0 *= la0[m]; pre1 *= la1[m]; }
-        if (m > R) { post0 *= la0[m]; post1 *= la1[m]; }
+        if (m < R) pre = mul2(pre, lam[m]);
+        if (m > R) post = mul2(post, lam[m]);
       }
-      const float lr0 = R == 0 ? la0[0] : R == 1 ? la0[1] : R == 2 ? la0[2] : la0[3];
-      const float lr1 = R == 0 ? la1[0] : R == 1 ? la1[1] : R == 2 ? la1[2] : la1[3];
-      const float fa0 = F[s][0], fa1 = F[s][1], fb0 = F[s][2], fb1 = F[s][3];
-      const float ia0 = rcp_approx(fa0), ia1 = rcp_approx(fa1);
-      const float ib0 = rcp_approx(fb0), ib1 = rcp_approx(fb1);
+      const float2 lr = R == 0 ? lam[0] : R == 1 ? lam[1] : R == 2 ? lam[2] : lam[3];
+      const float2 fa = make_float2(F[s][0], F[s][1]), fb = make_float2(F[s][2], F[s][3]);
+      const float2 ia = make_float2(rcp_approx(fa.x), rcp_approx(fa.y));
+      const float2 ib = make_float2(rcp_approx(fb.x), rcp_approx(fb.y));
       // KE = k F, QE = q F (<= 1): the off-diagonal B operand, rows tok / 64 + tok
-      const float kea0 = ka.x * fa0, kea1 = ka.y * fa1, keb0 = kb.x * fb0, keb1 = kb.y * fb1;
-      const float qea0 = qa.x * fa0, qea1 = qa.y * fa1, qeb0 = qb.x * fb0, qeb1 = qb.y * fb1;
+      const float2 kea = mul2(ka, fa), keb = mul2(kb, fb), qea = mul2(qa, fa), qeb = mul2(qb, fb);
       const uint32_t kq = sb + SM_KQ + static_cast<uint32_t>(hc) * TILE + static_cast<uint32_t>(4 * t);
-      S.u32(kq + chunk_off(ra, s)) = pack_f16x2(kea0, kea1);
-      S.u32(kq + chunk_off(rb, s)) = pack_f16x2(keb0, keb1);
-      S.u32(kq + chunk_off(64 + ra, s)) = pack_f16x2(qea0, qea1);
-      S.u32(kq + chunk_off(64 + rb, s)) = pack_f16x2(qeb0, qeb1);
+      S.u32(kq + chunk_off(ra, s)) = pack_f16x2(kea.x, kea.y);
+      S.u32(kq + chunk_off(rb, s)) = pack_f16x2(keb.x, keb.y);
+      S.u32(kq + chunk_off(64 + ra, s)) = pack_f16x2(qea.x, qea.y);
+      S.u32(kq + chunk_off(64 + rb, s)) = pack_f16x2(qeb.x, qeb.y);
       // -K e^G = -KE prod_{M<R} Lam (bf16, B operand of T'(-K e^G) = -Wk, the
       // record's sign): each thread overwrites exactly the k elements it has just read
-      S.u32(sb + SM_K + off + chunk_off(ra, s)) = pack_bf16x2(-kea0 * pre0, -kea1 * pre1);
-      S.u32(sb + SM_K + off + chunk_off(rb, s)) = pack_bf16x2(-keb0 * pre0, -keb1 * pre1);
+      const float2 npre = make_float2(-pre.x, -pre.y);
+      const float2 nka2 = mul2(kea, npre), nkb2 = mul2(keb, npre);
+      S.u32(sb + SM_K + off + chunk_off(ra, s)) = pack_bf16x2(nka2.x, nka2.y);
+      S.u32(sb + SM_K + off + chunk_off(rb, s)) = pack_bf16x2(nkb2.x, nkb2.y);
       // -Q e^G and K' = k B prod_{M>R} Lam (record words; B = Lam_R / F)
-      const float ba0 = lr0 * ia0, ba1 = lr1 * ia1, bb0 = lr0 * ib0, bb1 = lr1 * ib1;
+      const float2 ba = mul2(lr, ia), bb = mul2(lr, ib);
+      const float2 kba = mul2(ka, ba), kbb = mul2(kb, bb);
       // record rows: -Q e^G in A3 rows 64 + tok (two regions of 128 rows), K'
       // in KP (two regions of 64 rows); the four lanes t of a quad write one
       // 16-byte chunk together
       {
         uint8_t *a3 = rec + kRecA3 + hc * 16384 + 4 * t;
         uint8_t *kp = rec + kRecKP + hc * 8192 + 4 * t;
-        *reinterpret_cast<uint32_t *>(a3 + chunk_off(64 + ra, s)) = pack_f16x2(-qea0 * pre0, -qea1 * pre1);
-        *reinterpret_cast<uint32_t *>(a3 + chunk_off(64 + rb, s)) = pack_f16x2(-qeb0 * pre0, -qeb1 * pre1);
-        *reinterpret_cast<uint32_t *>(kp + chunk_off(ra, s)) = pack_f16x2(ka.x * ba0 * post0, ka.y * ba1 * post1);
-        *reinterpret_cast<uint32_t *>(kp + chunk_off(rb, s)) = pack_f16x2(kb.x * bb0 * post0, kb.y * bb1 * post1);
+        const float2 nqa2 = mul2(qea, npre), nqb2 = mul2(qeb, npre);
+        const float2 kpa = mul2(kba, post), kpb = mul2(kbb, post);
+        *reinterpret_cast<uint32_t *>(a3 + chunk_off(64 + ra, s)) = pack_f16x2(nqa2.x, nqa2.y);
+        *reinterpret_cast<uint32_t *>(a3 + chunk_off(64 + rb, s)) = pack_f16x2(nqb2.x, nqb2.y);
+        *reinterpret_cast<uint32_t *>(kp + chunk_off(ra, s)) = pack_f16x2(kpa.x, kpa.y);
+        *reinterpret_cast<uint32_t *>(kp + chunk_off(rb, s)) = pack_f16x2(kpb.x, kpb.y);
       }
       // Kc rows of the later sub-tiles R' > R: k B prod_{R<M<R'} Lam, stacked at
       // rows 0 (R' = 1, 16 rows), 16 (R' = 2, 32 rows), 48 (R' = 3, 48 rows)
       {
-        float m0 = 1.f, m1 = 1.f;
+        float2 mm = make_float2(1.f, 1.f);
 #pragma unroll
         for (int rp = 1; rp < 4; ++rp) {
           if (rp > R) {
-            if (rp > R + 1) {
-              const float x0 = rp - 1 == 1 ? la0[1] : rp - 1 == 2 ? la0[2] : la0[3];
-              const float x1 = rp - 1 == 1 ? la1[1] : rp - 1 == 2 ? la1[2] : la1[3];
-              m0 *= x0;
-              m1 *= x1;
-            }
+            if (rp > R + 1) mm = mul2(mm, rp - 1 == 1 ? lam[1] : rp - 1 == 2 ? lam[2] : lam[3]);
             const int base = rp == 1 ? 0 : rp == 2 ? 16 : 48;
             const uint32_t kc = sb + SM_KC + static_cast<uint32_t>(hc) * KC_REGION +
                                 static_cast<uint32_t>(4 * t);
-            S.u32(kc + chunk_off(base + ra, s)) = pack_f16x2(ka.x * ba0 * m0, ka.y * ba1 * m1);
-            S.u32(kc + chunk_off(base + rb, s)) = pack_f16x2(kb.x * bb0 * m0, kb.y * bb1 * m1);
+            const float2 xa = mul2(kba, mm), xb = mul2(kbb, mm);
+            S.u32(kc + chunk_off(base + ra, s)) = pack_f16x2(xa.x, xa.y);
+            S.u32(kc + chunk_off(base + rb, s)) = pack_f16x2(xb.x, xb.y);
           }
         }
       }
       // diagonal tile by mma.sync: A = k / F (rows ra, rb), B = [KE | QE] (tokens ra, rb)
       {
-        const uint32_t a0 = tf32_rna(ka.x * ia0), a1 = tf32_rna(kb.x * ib0);
-        const uint32_t a2 = tf32_rna(ka.y * ia1), a3 = tf32_rna(kb.y * ib1);
-        mma_m16n8k8_tf32(dacc[0], a0, a1, a2, a3, tf32_rna(kea0), tf32_rna(kea1));
-        mma_m16n8k8_tf32(dacc[1], a0, a1, a2, a3, tf32_rna(keb0), tf32_rna(keb1));
-        mma_m16n8k8_tf32(dacc[2], a0, a1, a2, a3, tf32_rna(qea0), tf32_rna(qea1));
-        mma_m16n8k8_tf32(dacc[3], a0, a1, a2, a3, tf32_rna(qeb0), tf32_rna(qeb1));
+        const float2 kia = mul2(ka, ia), kib = mul2(kb, ib);
+        const uint32_t a0 = tf32_rna(kia.x), a1 = tf32_rna(kib.x);
+        const uint32_t a2 = tf32_rna(kia.y), a3 = tf32_rna(kib.y);
+        mma_m16n8k8_tf32(dacc[0], a0, a1, a2, a3, tf32_rna(kea.x), tf32_rna(kea.y));
+        mma_m16n8k8_tf32(dacc[1], a0, a1, a2, a3, tf32_rna(keb.x), tf32_rna(keb.y));
+        mma_m16n8k8_tf32(dacc[2], a0, a1, a2, a3, tf32_rna(qea.x), tf32_rna(qea.y));
+        mma_m16n8k8_tf32(dacc[3], a0, a1, a2, a3, tf32_rna(qeb.x), tf32_rna(qeb.y));
       }
       // gamma = prod_M Lam_M per key channel (one writer per channel)
       if (R == 0 && g == 0) {
         float* gam = reinterpret_cast<float *>(rec + kRecG);
-        *reinterpret_cast<float2 *>(gam + c) =
-            make_float2(la0[0] * la0[1] * la0[2] * la0[3], la1[0] * la1[1] * la1[2] * la1[3]);
+        *reinterpret_cast<float2 *>(gam + c) = mul2(mul2(lam[0], lam[1]), mul2(lam[2], lam[3]));
       }
     }
     if (tid < 64) {  // this chunk's beta (logits through a sigmoid with the pre-op)

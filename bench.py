@@ -77,14 +77,15 @@ def state_bytes(token_heads, full_chunk_heads, seq_heads, dk, dv, s0=False):
 # the ncu captures summarised under profiles/, per (chunk, head) task of the
 # captured launch, scaled here by the tasks of the timed launch.  They are
 # reported only while the kernel's sources hash to the sha256 prefix recorded
-# with the capture (else the kernel has changed since: null).
+# with the capture (else the kernel has changed since: null).  A change to the
+# sources' comments alone updates the recorded prefix without a new capture.
 _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
 _TC_FILES = ("kda_tc_common.cuh", "kda_sm100.cuh", "kda_split.cuh", "kda_common.cuh", "kda_pdl.cuh")
 PROFILED_TRAFFIC = {
     # varlen prefill, 4 sequences (70,412 tokens), H = 32: 35,264 tasks
-    "chunk_prep_kernel": (2.325763e9 + 2.569389e9, 35264, "987edc614c1c28fd",
+    "chunk_prep_kernel": (2.325763e9 + 2.569389e9, 35264, "6cbc58f518fa86b4",
                           ("kda_chunk_prep.cu",) + _TC_FILES),
-    "state_pass_kernel": (2.626630e9 + 2.843281e9, 35264, "724694903b5d1f14",
+    "state_pass_kernel": (2.626630e9 + 2.843281e9, 35264, "2282604758755b95",
                           ("kda_state_pass.cu",) + _TC_FILES),
     # decode, 512 sequences x H = 32: 16,384 (sequence, head) states
     "kda_decode_step": (1.090588e9 + 1.017627e9, 16384, "627e6d5d92c7e4b1",

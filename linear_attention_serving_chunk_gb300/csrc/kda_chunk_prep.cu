@@ -40,8 +40,9 @@
 // memory, 256 TMEM columns each):
 //   TMA    z (prefetched while the previous chunk runs), q and k, v (after
 //          the operand build)
-//   SIMT   gate, scans, sub-tile totals; then every operand: [KE ; QE] and
-//          the stacked Kc (fp16, shared memory), -K e^G (bf16, over k), and
+//   SIMT   gate, scans, sub-tile totals; then every operand (packed fp32x2
+//          arithmetic over each thread's channel pairs): [KE ; QE] and the
+//          stacked Kc (fp16, shared memory), -K e^G (bf16, over k), and
 //          -Q e^G, K' (fp16, straight to the record); diagonal tiles by mma.sync
 //   MMA    off-diagonal A_kk / P tiles (M128 N128 K128, fp16)
 //   SIMT   A_kk to shared memory (fp32, transposed), -P to the record;

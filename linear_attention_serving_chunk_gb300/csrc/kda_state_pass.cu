@@ -26,6 +26,11 @@
 //
 // Heads of 64 key channels carry zero state rows 64..127 (their records hold
 // zero key channels); heads of 64 value channels run one CTA per chain.
+// Packed batches are taken longest chain first (the chunk-table kernel's order
+// table), so that no long chain starts in the last wave.  The chunk table, the
+// chunk preparation and this pass are programmatic dependent launches: each
+// waits on the device for the grids before it, and the next one's launch
+// overlaps its run.
 #include <string.h>
 
 #include "kda_common.cuh"

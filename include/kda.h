@@ -202,9 +202,10 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
  * takes the segment-parallel scan (an equal-length batch with few long
  * chains: kda_chunk_fwd_workspace_bytes() then gives the scan's size) it
  * uses a fixed scratch array of KDA_NOALLOC_WORKSPACE_BYTES in device memory
- * that the library holds on every GPU that loads it; calls needing more
- * return KDA_ERR_WORKSPACE before launching anything.  Every other call runs
- * the single-pass kernel, which needs no scratch.  The first call on a device
+ * that the library holds on every GPU that loads it; a scan needing more
+ * runs on the single-pass kernel instead (same results up to rounding, less
+ * parallel).  Every other call runs the single-pass kernel, which needs no
+ * scratch.  The first call on a device
  * looks up the array's device address (with that device current); make it
  * before any stream capture.  All calls share the array: calls that overlap
  * on the GPU race.  Allocates nothing.

@@ -105,8 +105,8 @@ size_t scan_records_bytes(int n_seq, int64_t total_tokens, int H) {
 // Two-pass prefill: a chunk-preparation pass over every
 // (chunk, head) of a group of hg heads, then the state pass over that group's
 // chains.  Workspace: the varlen tables (the chunk start of every sequence,
-// then the first token and length of every chunk; 1 KiB granules), then one
-// record per (chunk, head of the group).  The chunk count is bounded by
+// the first token and length of every chunk, the state pass's order of the
+// sequences; 1 KiB granules), then one record per (chunk, head of the group).  The chunk count is bounded by
 // ceil(total / 64) + n_seq, which covers any split of the tokens.
 constexpr size_t kRecordBytes = 73 * 1024;  // kRecBytes of kda_split.cuh
 
@@ -229,12 +229,20 @@ int kda_chunk_fwd(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const
                           workspace_bytes, stream);
 }
 
-int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *z,
-                     const kda_bf16 *beta, const float *A, float gmin,
-                     const int32_t *cu_seqlens, int n_seq, int64_t total_tokens, int H, int dk,
-                     int dv, int chunk, unsigned pre, const float *S0, kda_bf16 *o,
-                     float *S_final, float *snaps, const int64_t *snap_offsets, void *workspace,
-                     size_t workspace_bytes, kda_stream_t stream) {
+}  // extern "C"
+
+namespace kda {
+
+// kda_chunk_fwd_ex; allow_scan = false runs a call that would take the
+// segment-parallel scan on the single-pass kernel instead (which needs no
+// scratch): the allocation-free entry point's fallback when its fixed scratch
+// is too small for the scan.
+int chunk_fwd_run(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *z,
+                  const kda_bf16 *beta, const float *A, float gmin, const int32_t *cu_seqlens,
+                  int n_seq, int64_t total_tokens, int H, int dk, int dv, int chunk, unsigned pre,
+                  const float *S0, kda_bf16 *o, float *S_final, float *snaps,
+                  const int64_t *snap_offsets, void *workspace, size_t workspace_bytes,
+                  kda_stream_t stream, bool allow_scan) {
   if (n_seq < 0 || total_tokens < 0 || H <= 0 || H > 65535) return KDA_ERR_SHAPE;
   const unsigned passes = pre & kPassFlags;
   const bool stall = (pre & KDA_TEST_STALL) != 0;
@@ -266,8 +274,8 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
       return KDA_ERR_WORKSPACE;
   }
   size_t need = 0;
-  const bool scan = chunk_fwd_takes_scan(pre, cu_seqlens, snap_offsets, n_seq, total_tokens, H,
-                                         dk, dv, chunk, &need);
+  const bool scan = allow_scan && chunk_fwd_takes_scan(pre, cu_seqlens, snap_offsets, n_seq,
+                                                       total_tokens, H, dk, dv, chunk, &need);
   if (scan) {
     if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KDA_ERR_ALIGN;
@@ -380,6 +388,21 @@ int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, co
                           dk, dv, S0, o, S_final, snaps, snap_offsets, status, 0, 0, nullptr,
                           n_seq, ops, 0, st);
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace kda
+
+extern "C" {
+
+int kda_chunk_fwd_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *z,
+                     const kda_bf16 *beta, const float *A, float gmin,
+                     const int32_t *cu_seqlens, int n_seq, int64_t total_tokens, int H, int dk,
+                     int dv, int chunk, unsigned pre, const float *S0, kda_bf16 *o,
+                     float *S_final, float *snaps, const int64_t *snap_offsets, void *workspace,
+                     size_t workspace_bytes, kda_stream_t stream) {
+  return kda::chunk_fwd_run(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, total_tokens, H, dk,
+                            dv, chunk, pre, S0, o, S_final, snaps, snap_offsets, workspace,
+                            workspace_bytes, stream, true);
 }
 
 int kda_decode_step(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *z,

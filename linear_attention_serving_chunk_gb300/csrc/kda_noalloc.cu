@@ -32,6 +32,12 @@ namespace kda {
 bool chunk_fwd_takes_scan(unsigned pre, const int32_t *cu_seqlens, const int64_t *snap_offsets,
                           int n_seq, int64_t total_tokens, int H, int dk, int dv, int chunk,
                           size_t *scan_bytes);
+int chunk_fwd_run(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *z,
+                  const kda_bf16 *beta, const float *A, float gmin, const int32_t *cu_seqlens,
+                  int n_seq, int64_t total_tokens, int H, int dk, int dv, int chunk, unsigned pre,
+                  const float *S0, kda_bf16 *o, float *S_final, float *snaps,
+                  const int64_t *snap_offsets, void *workspace, size_t workspace_bytes,
+                  kda_stream_t stream, bool allow_scan);
 
 namespace {
 
@@ -67,17 +73,20 @@ extern "C" int kda_chunk_fwd_noalloc(const kda_bf16 *q, const kda_bf16 *k, const
                                      const int64_t *snap_offsets, kda_stream_t stream) {
   // Only the segment-parallel scan needs scratch, and whether a call takes it
   // is decided by the same rule kda_chunk_fwd applies; every other call gets
-  // no workspace and so runs the single-pass kernel, which needs none.
+  // no workspace and so runs the single-pass kernel, which needs none.  A scan
+  // whose scratch does not fit the fixed array runs on the single-pass kernel
+  // too (the same results up to rounding, without the scan's parallelism).
   size_t need = 0;
   if (!kda::chunk_fwd_takes_scan(0u, cu_seqlens, snap_offsets, n_seq, total_tokens, H, dk, dv,
                                  chunk, &need))
     need = 0;
-  if (need > KDA_NOALLOC_WORKSPACE_BYTES) return KDA_ERR_WORKSPACE;
+  const bool scan = need > 0 && need <= KDA_NOALLOC_WORKSPACE_BYTES;
   void *ws = nullptr;
-  if (need > 0) {
+  if (scan) {
     ws = kda::noalloc_workspace();
     if (!ws) return KDA_ERR_CUDA;
   }
-  return kda_chunk_fwd(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, total_tokens, H, dk, dv,
-                       chunk, S0, o, S_final, snaps, snap_offsets, ws, need, stream);
+  return kda::chunk_fwd_run(q, k, v, z, beta, A, gmin, cu_seqlens, n_seq, total_tokens, H, dk,
+                            dv, chunk, 0u, S0, o, S_final, snaps, snap_offsets, ws,
+                            scan ? need : 0, stream, scan);
 }

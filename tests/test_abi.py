@@ -194,14 +194,14 @@ def test_python_binding_fails_loudly_without_cuda_tensors(L):
 
 def test_noalloc_scratch_decision_matches_chunk_fwd(L):
     """kda_chunk_fwd_noalloc needs its fixed scratch only where kda_chunk_fwd
-    would take the segment scan.  One 2^20-token sequence with 16 heads and
-    snapshots: without snap_offsets the scan needs 192 MiB (refused with
-    KDA_ERR_WORKSPACE before anything is touched); with snap_offsets the call
-    runs the single-pass kernel, so it passes the scratch check and stops at
-    the next host check here (a misaligned o: KDA_ERR_ALIGN), launching
-    nothing."""
+    would take the segment scan, and a scan beyond that scratch falls back to
+    the single-pass kernel instead of being refused.  One 2^20-token sequence
+    with 16 heads and snapshots: without snap_offsets the scan would need
+    192 MiB; with snap_offsets kda_chunk_fwd takes no scan.  Either way the call
+    passes the scratch decision and stops at the next host check here (a
+    misaligned o: KDA_ERR_ALIGN), launching nothing."""
     fake = ctypes.c_void_p(0x10000)
     bad_o = ctypes.c_void_p(0x10008)
     common = [fake] * 6 + [-5.0, None, 1, 1 << 20, 16, 128, 128, 64, None]
-    assert L.kda_chunk_fwd_noalloc(*common, fake, None, fake, None, None) == 5
+    assert L.kda_chunk_fwd_noalloc(*common, bad_o, None, fake, None, None) == 3
     assert L.kda_chunk_fwd_noalloc(*common, bad_o, None, fake, fake, None) == 3

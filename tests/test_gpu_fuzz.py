@@ -57,7 +57,7 @@ def ref_of(x, use_S0):
                           snapshots=True)
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_prefill_configuration(kda, seed):
     c = draw(9000 + seed)
     x = kda_inputs.make_prefill(c["H"], c["dk"], c["dv"], c["lengths"], seed=9100 + seed,
@@ -91,7 +91,7 @@ def test_random_prefill_configuration(kda, seed):
         assert s_err(f64(snaps[:rows]), ref["snaps"]) <= S_TOL, c
 
 
-@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("seed", range(12))
 def test_random_decode_tokens(kda, seed):
     """Random runs on random slots: short runs (the token kernel) and long
     ones (the chunked path), verify then commit."""

@@ -579,6 +579,17 @@ def host_mem_available():
     return avail
 
 
+def host_fits_all_ranks(nbytes, world, avail=None):
+    """True on every rank when each node has nbytes of host memory for each of
+    its ranks (LOCAL_WORLD_SIZE), else False on every rank: a line with
+    barriers is then run by all ranks or by none."""
+    if avail is None:
+        avail = host_mem_available()
+    local_ranks = max(1, int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
+    short = avail is not None and nbytes * local_ranks > avail
+    return reduce_max(1.0 if short else 0.0, world) == 0.0
+
+
 def run_e2e(args, x, b, stream, world):
     """The same step through the public API with host buffers: every step copies
     its inputs from pinned host memory to the device, runs kda_chunk_fwd
@@ -597,12 +608,11 @@ def run_e2e(args, x, b, stream, world):
     names_in = ("q", "k", "v", "z", "beta", "A", "cu_seqlens", "S0")
     h2d = sum(x[n].numel() * x[n].element_size() for n in names_in)
     d2h = sum(b[n].numel() * b[n].element_size() for n in ("o", "S_final"))
-    avail = host_mem_available()
-    if avail is not None and 2 * (h2d + d2h) > avail:
+    if not host_fits_all_ranks(2 * (h2d + d2h), world):
         return {"value": None, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "skipped": f"needs {(h2d + d2h) / 1e9:.1f} GB of pinned host memory, "
-                           f"{avail / 1e9:.1f} GB available"}
+                "skipped": f"needs {(h2d + d2h) / 1e9:.1f} GB of pinned host memory per rank, "
+                           "more than some node has for all of its ranks"}
     host_in = {n: x[n].cpu().pin_memory() for n in names_in}
     host_out = {n: torch.empty_like(b[n], device="cpu").pin_memory() for n in ("o", "S_final")}
     slots = [{"in": {n: x[n] for n in names_in}, "out": {"o": b["o"], "S_final": b["S_final"]}},

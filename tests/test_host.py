@@ -86,6 +86,35 @@ def _rank_main(rank, world, port, q):
     dist.destroy_process_group()
 
 
+def _fits_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), LOCAL_WORLD_SIZE=str(world))
+    r, w, lr = bench.dist_setup(world)
+    bench.init_pg(w)
+    # 10 GB per rank, two ranks on the node: rank 0's node has 30 GB, rank 1's 15 GB
+    both = bench.host_fits_all_ranks(10e9, w, avail=30e9 if r == 0 else 15e9)
+    roomy = bench.host_fits_all_ranks(10e9, w, avail=30e9)
+    q.put((r, both, roomy))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_end_to_end_line_runs_on_all_ranks_or_none_gloo_world_size_2():
+    """The end-to-end line pins host buffers on every rank and has barriers:
+    one rank short of host memory makes every rank skip it, none hangs."""
+    ctx = torch.multiprocessing.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_fits_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    assert res == [(0, False, True), (1, False, True)]
+
+
 def test_max_over_ranks_gloo_world_size_2():
     ctx = torch.multiprocessing.get_context("spawn")
     q = ctx.Queue()

@@ -649,6 +649,7 @@ def run_e2e(args, x, b, stream, world):
     for i in range(2):  # warm-up: both slots once
         e2e_step(i)
     torch.cuda.synchronize()
+    link = host_link(slots[0], host_in, host_out, names_in, s_in, s_out, h2d, d2h)
     e2e_steps = max(2, min(args.steps, 10))
     barrier(world)
     a = torch.cuda.Event(enable_timing=True)
@@ -667,9 +668,37 @@ def run_e2e(args, x, b, stream, world):
            "ms_per_step": e2e_ms / e2e_steps,
            "d2h": "o and final states; the chunk snapshots are computed every step and stay in "
                   "device memory (the prefix cache)",
-           "pipelined": "2 buffer slots; copies in and out on their own streams, compute on 1"}
+           "pipelined": "2 buffer slots; copies in and out on their own streams, compute on 1",
+           "link": link}
     del host_in, host_out, slots
     return out
+
+
+def host_link(slot, host_in, host_out, names_in, s_in, s_out, h2d, d2h):
+    """The host link as this run sees it, just before the end-to-end region:
+    one step's inputs copied in alone, then its outputs copied out alone, each
+    timed with CUDA events on its copy stream.  floor_ms = the slower of the
+    two directions, the least an end-to-end step can take; on a machine shared
+    with other jobs this link's bandwidth is not constant from run to run."""
+    import torch
+
+    def timed(stream, copies):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for dst, src in copies:
+                dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    t_in = timed(s_in, [(slot["in"][n], host_in[n]) for n in names_in])
+    t_out = timed(s_out, [(host_out[n], slot["out"][n]) for n in ("o", "S_final")])
+    return {"h2d_gbs": h2d / t_in / 1e6, "d2h_gbs": d2h / t_out / 1e6,
+            "floor_ms": max(t_in, t_out),
+            "how": "one step's inputs in alone, then its outputs out alone, CUDA events"}
 
 
 def kda_dtype():

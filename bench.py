@@ -88,10 +88,10 @@ PROFILED_TRAFFIC = {
     "state_pass_kernel": (2.626630e9 + 2.843281e9, 35264, "2282604758755b95",
                           ("kda_state_pass.cu",) + _TC_FILES),
     # decode, 512 sequences x H = 32: 16,384 (sequence, head) states
-    "kda_decode_step": (1.090588e9 + 1.017627e9, 16384, "627e6d5d92c7e4b1",
+    "kda_decode_step": (1.090611e9 + 1.017599e9, 16384, "850844e37b9a8a6f",
                         ("kda_decode.cu", "kda_common.cuh", "kda_tc_common.cuh", "kda_sm100.cuh")),
     # verify: 4 tokens on each of 512 x H = 32 states (commit = 0)
-    "decode_tokens_kernel": (1.141094e9 + 1.8558976e7, 16384, "627e6d5d92c7e4b1",
+    "decode_tokens_kernel": (1.141108e9 + 1.8478080e7, 16384, "850844e37b9a8a6f",
                              ("kda_decode.cu", "kda_common.cuh", "kda_tc_common.cuh",
                               "kda_sm100.cuh")),
     # restore, 512 x H = 32 states

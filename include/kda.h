@@ -294,11 +294,38 @@ int kda_state_snapshot(const float *snaps, int64_t n_rows, const int64_t *src_id
  * hanging), KDA_ERR_SHAPE (a malformed cu_seqlens / snap_offsets entry or an
  * out-of-range slot or row index, skipped), KDA_ERR_RANGE (an fp16 operand
  * overflowed).  The word is one per device and sticky: every call on the
- * device ORs into it until it is reset, so calls running on different
- * streams are not told apart.  This call synchronises the device.  Returns
- * KDA_OK, the recorded code(s) OR-ed together, or KDA_ERR_CUDA.
+ * device that runs on a stream with no word of its own (kda_stream_status_bind)
+ * ORs into it until it is reset, so such calls on different streams are not
+ * told apart.  This call synchronises the device.  Returns KDA_OK, the
+ * recorded code(s) OR-ed together, or KDA_ERR_CUDA.
  */
 int kda_device_status(int reset);
+
+/*
+ * kda_stream_status_bind - give a stream a status word of its own.  From this
+ * call on, every library call issued on `stream` has its kernels OR their
+ * device-side codes (the ones kda_device_status lists) into *device_word
+ * instead of the device word; calls on other streams are unaffected.
+ * device_word: one int in device memory (4-byte aligned), owned by the
+ * caller, zeroed by the caller before first use and valid until it is
+ * unbound; the library never allocates or frees it.  A call on the stream
+ * captured into a CUDA graph keeps the word bound at capture time.
+ * device_word == NULL removes the stream's binding (a no-op if it has none);
+ * binding again replaces the word.  Host-side only: nothing is enqueued and
+ * nothing synchronises.  Thread-safe.  At most 64 streams are bound at once.
+ * Returns KDA_OK, KDA_ERR_ALIGN (a misaligned word) or KDA_ERR_SHAPE (64
+ * streams are already bound).
+ */
+int kda_stream_status_bind(kda_stream_t stream, int *device_word);
+
+/*
+ * kda_stream_status - read (and with reset != 0, clear) the word bound to
+ * `stream`: a copy ordered after the work already issued on that stream,
+ * then a synchronisation of that stream only.  Returns KDA_OK, the recorded
+ * code(s) OR-ed together, KDA_ERR_NULL (no word is bound to the stream) or
+ * KDA_ERR_CUDA.
+ */
+int kda_stream_status(kda_stream_t stream, int reset);
 
 #ifdef __cplusplus
 }

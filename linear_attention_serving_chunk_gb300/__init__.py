@@ -38,6 +38,7 @@ KDA_OK = 0
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_ALIGN",
                 4: "KDA_ERR_UNSUPPORTED", 5: "KDA_ERR_WORKSPACE", 6: "KDA_ERR_CUDA",
                 7: "KDA_ERR_TIMEOUT", 8: "KDA_ERR_RANGE"}
+KDA_ERR_NULL = 1
 KDA_ERR_SHAPE = 2
 KDA_ERR_TIMEOUT = 7
 KDA_ERR_RANGE = 8
@@ -45,7 +46,7 @@ KDA_ERR_RANGE = 8
 EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_bytes",
             "kda_chunk_fwd", "kda_decode_step", "kda_state_snapshot", "kda_device_status",
             "kda_chunk_fwd_noalloc", "kda_decode_tokens", "kda_chunk_fwd_ex",
-            "kda_decode_step_ex")
+            "kda_decode_step_ex", "kda_stream_status_bind", "kda_stream_status")
 
 _lib = None
 
@@ -94,6 +95,10 @@ def lib():
         L.kda_state_snapshot.argtypes = [P, I64, P, P, I, P, I, I, I, I, P]
         L.kda_device_status.restype = I
         L.kda_device_status.argtypes = [I]
+        L.kda_stream_status_bind.restype = I
+        L.kda_stream_status_bind.argtypes = [P, P]
+        L.kda_stream_status.restype = I
+        L.kda_stream_status.argtypes = [P, I]
         _lib = L
     return _lib
 
@@ -285,3 +290,20 @@ def state_snapshot(snaps, src_idx, state_pool, dst_slots, stream=None):
 def device_status(reset=True):
     """Read (and clear) the device status word; synchronises the device."""
     return int(lib().kda_device_status(1 if reset else 0))
+
+
+def stream_status_bind(word, stream=None):
+    """Give `stream` (default: the current stream) a status word of its own:
+    `word`, a zeroed one-element int32 CUDA tensor that the caller keeps
+    alive while it is bound, or None to remove the binding."""
+    if word is not None:
+        _check(word, "word", torch.int32, (1,))
+    _raise_on("kda_stream_status_bind", lib().kda_stream_status_bind(_stream(stream), _ptr(word)))
+
+
+def stream_status(stream=None, reset=True):
+    """Read (and clear) the word bound to `stream`; synchronises that stream only."""
+    st = int(lib().kda_stream_status(_stream(stream), 1 if reset else 0))
+    if st == KDA_ERR_NULL:
+        raise KDAError("kda_stream_status", st)
+    return st

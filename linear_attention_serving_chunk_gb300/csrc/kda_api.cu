@@ -4,6 +4,8 @@
 // (except kda_device_status, which says so).
 #include <math.h>
 
+#include <mutex>
+
 #include "kda_common.cuh"
 
 namespace kda {
@@ -145,7 +147,29 @@ int split_heads(int n_seq, int64_t total_tokens, int H, size_t bytes) {
   return static_cast<int>(hg < static_cast<size_t>(H) ? hg : static_cast<size_t>(H));
 }
 
-int *status_word() {
+// Per-stream status words.  A caller that binds a device int to a stream has
+// every call on that stream record into it instead of the device word: calls
+// on different streams are told apart, and the caller can read its word with
+// a copy ordered on its own stream, without synchronising the device.
+constexpr int kMaxStatusBindings = 64;
+struct StatusBinding {
+  cudaStream_t stream;
+  int *word;
+};
+std::mutex g_bind_mu;
+StatusBinding g_bind[kMaxStatusBindings];
+int g_n_bind = 0;
+
+int *bound_status_word(cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_bind_mu);
+  for (int i = 0; i < g_n_bind; ++i)
+    if (g_bind[i].stream == st) return g_bind[i].word;
+  return nullptr;
+}
+
+// The word the kernels of a call on stream st record into.
+int *status_word(cudaStream_t st) {
+  if (int *w = bound_status_word(st)) return w;
   void *p = nullptr;
   return cudaGetSymbolAddress(&p, g_status) == cudaSuccess ? static_cast<int *>(p) : nullptr;
 }
@@ -282,7 +306,7 @@ int chunk_fwd_run(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v, const
   }
   // every host-side check is done: from here on the call launches work
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int *status = status_word();
+  int *status = status_word(st);
   if (!status) return KDA_ERR_CUDA;
   if (stall) {  // test hook: the single-pass kernel gives up on an unarmed wait
     const cudaError_t err = prefill_tc_launch(
@@ -426,7 +450,7 @@ int kda_decode_step_ex(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
   const void *ptrs[] = {q, k, v, z, beta, A, state_pool, slots, o};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_ALIGN;
-  int *status = status_word();
+  int *status = status_word(reinterpret_cast<cudaStream_t>(stream));
   if (!status) return KDA_ERR_CUDA;
   const cudaError_t err = decode_step_launch(q, k, v, z, beta, A, gmin, state_pool, slots,
                                              n_slots, n, H, dk, dv, o, pre, status,
@@ -452,7 +476,7 @@ int kda_decode_tokens(const kda_bf16 *q, const kda_bf16 *k, const kda_bf16 *v,
   if (!prefill_tc_supported(dk, dv, total_tokens)) return KDA_ERR_SHAPE;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   float *S_final = commit ? state_pool : nullptr;
-  int *status = status_word();
+  int *status = status_word(st);
   if (!status) return KDA_ERR_CUDA;
   if (total_tokens <= kDecodeTokensRun * static_cast<int64_t>(n) &&
       static_cast<int64_t>(n_slots) * H <= 0x7fffffffLL) {
@@ -479,12 +503,42 @@ int kda_state_snapshot(const float *snaps, int64_t n_rows, const int64_t *src_id
   const void *ptrs[] = {snaps, src_idx, state_pool, dst_slots};
   for (const void *p : ptrs)
     if (!aligned16(p)) return KDA_ERR_ALIGN;
-  int *status = status_word();
+  int *status = status_word(reinterpret_cast<cudaStream_t>(stream));
   if (!status) return KDA_ERR_CUDA;
   const cudaError_t err =
       snapshot_restore_launch(snaps, n_rows, src_idx, state_pool, n_slots, dst_slots, n, H, dk,
                               dv, status, reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_stream_status_bind(kda_stream_t stream, int *device_word) {
+  if (device_word && (reinterpret_cast<uintptr_t>(device_word) & 3u)) return KDA_ERR_ALIGN;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_bind_mu);
+  for (int i = 0; i < g_n_bind; ++i)
+    if (g_bind[i].stream == st) {
+      if (device_word)
+        g_bind[i].word = device_word;
+      else
+        g_bind[i] = g_bind[--g_n_bind];
+      return KDA_OK;
+    }
+  if (!device_word) return KDA_OK;  // nothing was bound: nothing to undo
+  if (g_n_bind == kMaxStatusBindings) return KDA_ERR_SHAPE;
+  g_bind[g_n_bind++] = StatusBinding{st, device_word};
+  return KDA_OK;
+}
+
+int kda_stream_status(kda_stream_t stream, int reset) {
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int *w = bound_status_word(st);
+  if (!w) return KDA_ERR_NULL;
+  int value = 0;
+  if (cudaMemcpyAsync(&value, w, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (reset && cudaMemsetAsync(w, 0, sizeof(int), st) != cudaSuccess) return KDA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_CUDA;
+  return value == 0 ? KDA_OK : value;
 }
 
 int kda_device_status(int reset) {

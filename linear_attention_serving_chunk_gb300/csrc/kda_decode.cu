@@ -142,10 +142,10 @@ decode_step_kernel(const kda_bf16 *__restrict__ q, const kda_bf16 *__restrict__ 
 // committing).  Warp w owns value columns [w DV/8, (w+1) DV/8); its lanes split
 // the key rows, so p = S^T k and u = S^T q are reduced by shuffles inside the
 // warp and a token needs no barrier.  The tokens' inputs are staged in shared
-// memory kTokBlock at a time (with the pre-ops and k.q per token); each row
-// group of the staging arrays is padded to an odd number of 16-byte units, so
-// a lane's float4 reads of the decay, k and q of its rows are conflict-free.
-// The arithmetic is packed fp32x2 over column pairs.
+// memory kTokBlock at a time (with the pre-ops and k.q per token, two warps a
+// token); each row group of the staging arrays is padded to an odd number of
+// 16-byte units, so a lane's float4 reads of the decay, k and q of its rows are
+// conflict-free.  The arithmetic is packed fp32x2 over column pairs.
 //
 // Persistent CTAs, two per SM, each walking its (sequence, head) rows.  While
 // a CTA applies one row's tokens from registers, the next row's state comes
@@ -202,6 +202,31 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// N (2 or 4) consecutive bf16 values from a 2N-byte-aligned address (shared or global)
+template <int N>
+__device__ __forceinline__ void load_bf16_row(const kda_bf16 *p, float (&out)[N]) {
+  static_assert(N == 2 || N == 4, "2 or 4 channels a lane");
+  uint32_t w[N / 2];
+  if constexpr (N == 4) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    w[0] = u.x;
+    w[1] = u.y;
+  } else {
+    w[0] = *reinterpret_cast<const uint32_t *>(p);
+  }
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    out[2 * i] = __uint_as_float(w[i] << 16);
+    out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
 template <int DK, int DV>
 __global__ void __launch_bounds__(kDecodeThreads, kTokCtasPerSm)
 decode_tokens_kernel(const __grid_constant__ CUtensorMap tm_state,
@@ -239,8 +264,9 @@ decode_tokens_kernel(const __grid_constant__ CUtensorMap tm_state,
   auto row_of = [&](int64_t r) -> TokRow {
     TokRow w{0, 0, 0, 0, false};
     if (r >= rows) return w;
-    const int b = static_cast<int>(r / H);
-    w.h = static_cast<int>(r - static_cast<int64_t>(b) * H);
+    const uint32_t r32 = static_cast<uint32_t>(r);  // rows = n H < 2^32
+    const int b = static_cast<int>(r32 / static_cast<uint32_t>(H));
+    w.h = static_cast<int>(r32 - static_cast<uint32_t>(b) * static_cast<uint32_t>(H));
     w.slot = slots[b];
     int64_t e = 0;
     if (w.slot < 0 || w.slot >= n_slots || !seq_range(cu_seqlens, b, total, w.t0, e)) {
@@ -278,35 +304,70 @@ decode_tokens_kernel(const __grid_constant__ CUtensorMap tm_state,
     cp_async_commit();
     if (tid < nt) beta_next = bf2f(beta[static_cast<size_t>(w.t0 + tid) * H + w.h]);
   };
-  // the pre-op norms, k.q and beta of tokens 0 .. nt - 1 of the staging area
-  auto token_scalars = [&](int nt) {
-    __syncthreads();
-    for (int j = warp; j < nt; j += NW) {
-      if (pre & KDA_PRE_L2NORM_QK) {
-        float kk = 0.f, qq = 0.f;
-        for (int c = lane; c < DK; c += 32) {
-          const int ci = kidx(c);
-          kk += s_k[j][ci] * s_k[j][ci];
-          qq += s_q[j][ci] * s_q[j][ci];
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          kk += __shfl_xor_sync(0xffffffffu, kk, off);
-          qq += __shfl_xor_sync(0xffffffffu, qq, off);
-        }
-        const float ik = kk > 0.f ? rsqrtf(kk) : 0.f, iq = qq > 0.f ? rsqrtf(qq) : 0.f;
-        for (int c = lane; c < DK; c += 32) {
-          const int ci = kidx(c);
-          s_k[j][ci] *= ik;
-          s_q[j][ci] *= iq;
-        }
-        __syncwarp();
+  // Tokens 0 .. nt - 1 of a block into the fp32 staging area, from their bf16
+  // rows: the raw rows in shared memory for a row's first block, global memory
+  // for later ones.  Two warps per token, each lane on DK / 32 consecutive
+  // channels: one warp takes k and q (the pre-op norms and k.q, reduced in the
+  // warp), the other the decay of z and v.  Thread j < nt holds token j's beta.
+  // The closing barrier also ends every read of the raw rows.
+  auto stage = [&](int nt, bool from_raw, int64_t t0, int h) {
+    constexpr int CK = DK / 32, CV = DV / 32;
+    for (int t = warp; t < 2 * nt; t += NW) {
+      const int j = t >> 1;
+      const kda_bf16 *kr, *qr, *zr, *vr;
+      if (from_raw) {
+        kr = reinterpret_cast<const kda_bf16 *>(tsm + T::RAW + j * T::TOKB);
+        qr = kr + DK;
+        zr = kr + 2 * DK;
+        vr = kr + 3 * DK;
+      } else {
+        const size_t tok = static_cast<size_t>(t0 + j) * H + h;
+        kr = k + tok * DK;
+        qr = q + tok * DK;
+        zr = z + tok * DK;
+        vr = v + tok * DV;
       }
-      float kq = 0.f;
-      for (int c = lane; c < DK; c += 32) kq += s_k[j][kidx(c)] * s_q[j][kidx(c)];
+      if ((t & 1) == 0) {
+        float kv[CK], qv[CK];
+        load_bf16_row<CK>(kr + CK * lane, kv);
+        load_bf16_row<CK>(qr + CK * lane, qv);
+        if (pre & KDA_PRE_L2NORM_QK) {
+          float kk = 0.f, qq = 0.f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-      if (lane == 0) s_kq[j] = kq;
+          for (int e = 0; e < CK; ++e) {
+            kk += kv[e] * kv[e];
+            qq += qv[e] * qv[e];
+          }
+          kk = warp_sum(kk);
+          qq = warp_sum(qq);
+          const float ik = kk > 0.f ? rsqrtf(kk) : 0.f, iq = qq > 0.f ? rsqrtf(qq) : 0.f;
+#pragma unroll
+          for (int e = 0; e < CK; ++e) {
+            kv[e] *= ik;
+            qv[e] *= iq;
+          }
+        }
+        float kq = 0.f;
+#pragma unroll
+        for (int e = 0; e < CK; ++e) kq += kv[e] * qv[e];
+        kq = warp_sum(kq);
+#pragma unroll
+        for (int e = 0; e < CK; ++e) {
+          const int ci = kidx(CK * lane + e);
+          s_k[j][ci] = kv[e];
+          s_q[j][ci] = qv[e];
+        }
+        if (lane == 0) s_kq[j] = kq;
+      } else {
+        const float eA = expf(A[h]);
+        float zv[CK], vv[CV];
+        load_bf16_row<CK>(zr + CK * lane, zv);
+        load_bf16_row<CV>(vr + CV * lane, vv);
+#pragma unroll
+        for (int e = 0; e < CK; ++e) s_a[j][kidx(CK * lane + e)] = decay_factor(gmin, eA, zv[e]);
+#pragma unroll
+        for (int e = 0; e < CV; ++e) s_v[j][CV * lane + e] = vv[e];
+      }
     }
     if (tid < nt)
       s_beta[tid] = (pre & KDA_PRE_SIGMOID_BETA) ? 1.f / (1.f + __expf(-beta_next)) : beta_next;
@@ -345,22 +406,7 @@ decode_tokens_kernel(const __grid_constant__ CUtensorMap tm_state,
           sh[rr] = make_float2(t.z, t.w);
         }
       }
-      // the first block's tokens: raw bf16 -> fp32 staging (decay through the gate)
-      const int nt = min(L, kTokBlock);
-      const float eA = expf(A[cur.h]);
-      for (int x = tid; x < nt * DK; x += kDecodeThreads) {
-        const int j = x / DK, c = x - j * DK;
-        const kda_bf16 *raw = reinterpret_cast<const kda_bf16 *>(tsm + T::RAW + j * T::TOKB);
-        const int ci = kidx(c);
-        s_k[j][ci] = bf2f(raw[c]);
-        s_q[j][ci] = bf2f(raw[DK + c]);
-        s_a[j][ci] = decay_factor(gmin, eA, bf2f(raw[2 * DK + c]));
-      }
-      for (int x = tid; x < nt * DV; x += kDecodeThreads) {
-        const int j = x / DV, c = x - j * DV;
-        s_v[j][c] = bf2f(reinterpret_cast<const kda_bf16 *>(tsm + T::RAW + j * T::TOKB)[3 * DK + c]);
-      }
-      token_scalars(nt);  // its barriers also end every read of the raw rows
+      stage(min(L, kTokBlock), true, cur.t0, cur.h);  // the first block's tokens
     }
     // the next row's state and tokens come in while this row's tokens are applied
     prefetch(nxt);
@@ -369,22 +415,9 @@ decode_tokens_kernel(const __grid_constant__ CUtensorMap tm_state,
       const int nt = static_cast<int>(min(static_cast<int64_t>(kTokBlock), cur.t0 + L - t0));
       if (t0 != cur.t0) {  // a long run's later block: straight from global memory
         __syncthreads();   // the previous block's tokens are done with the staging area
-        const float eA = expf(A[cur.h]);
-        for (int x = tid; x < nt * DK; x += kDecodeThreads) {
-          const int j = x / DK, c = x - j * DK;
-          const size_t g = (static_cast<size_t>(t0 + j) * H + cur.h) * DK + c;
-          const int ci = kidx(c);
-          s_k[j][ci] = bf2f(k[g]);
-          s_q[j][ci] = bf2f(q[g]);
-          s_a[j][ci] = decay_factor(gmin, eA, bf2f(z[g]));
-        }
-        for (int x = tid; x < nt * DV; x += kDecodeThreads) {
-          const int j = x / DV, c = x - j * DV;
-          s_v[j][c] = bf2f(v[(static_cast<size_t>(t0 + j) * H + cur.h) * DV + c]);
-        }
         const float keep = beta_next;  // threads 0 .. 7 hold the next row's beta
         if (tid < nt) beta_next = bf2f(beta[static_cast<size_t>(t0 + tid) * H + cur.h]);
-        token_scalars(nt);
+        stage(nt, false, t0, cur.h);
         beta_next = keep;
       }
       for (int j = 0; j < nt; ++j) {

@@ -45,6 +45,29 @@ def test_status_strings_and_version(L):
     assert L.kda_status_string(99) == b"unknown status"
 
 
+def test_stream_status_binding_table(L):
+    """kda_stream_status_bind is host-side bookkeeping (nothing is enqueued, so
+    the pointers below are never dereferenced): a misaligned word is refused,
+    64 streams can be bound and a 65th cannot, binding again replaces the word,
+    unbinding frees a place and is a no-op for an unbound stream, and reading
+    an unbound stream's word is KDA_ERR_NULL."""
+    word = ctypes.c_void_p(0x20000)
+    streams = [ctypes.c_void_p(0x1000 + 16 * i) for i in range(65)]
+    try:
+        assert L.kda_stream_status_bind(streams[0], ctypes.c_void_p(0x20002)) == 3
+        for s in streams[:64]:
+            assert L.kda_stream_status_bind(s, word) == 0
+        assert L.kda_stream_status_bind(streams[64], word) == 2
+        assert L.kda_stream_status_bind(streams[3], ctypes.c_void_p(0x20004)) == 0
+        assert L.kda_stream_status_bind(streams[3], None) == 0
+        assert L.kda_stream_status_bind(streams[64], word) == 0
+        assert L.kda_stream_status_bind(streams[3], None) == 0
+        assert L.kda_stream_status(streams[3], 0) == 1
+    finally:
+        for s in streams:
+            L.kda_stream_status_bind(s, None)
+
+
 def _chunk_args(**kw):
     fake = ctypes.c_void_p(0x10000)  # never dereferenced: every call below is rejected first
     args = dict(q=fake, k=fake, v=fake, z=fake, beta=fake, A=fake, gmin=-5.0, cu=None, n_seq=1,

@@ -737,6 +737,53 @@ def test_bad_slot_and_row_indices_are_skipped_and_reported(kda):
     assert s_err(f64(pool3[1]), ref["S_final"][0]) <= S_TOL
 
 
+def test_stream_status_words_tell_streams_apart(kda):
+    """Two streams with a status word each (kda_stream_status_bind): a bad slot
+    in a call on one stream and a timed-out wait in a call on the other are
+    recorded in their own words; the device word and the other stream's word
+    stay clear; after unbinding, the device word takes the codes again."""
+    assert kda.device_status() == 0
+    n, H, d = 4, 2, 64
+    x = kda_inputs.make_prefill(H, d, d, [1] * n, seed=64, device="cuda", S0_std=0.02)
+    y = kda_inputs.make_prefill(2, 128, 128, [130, 64], seed=61, device="cuda", S0_std=0.02)
+    s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
+    w_a = torch.zeros(1, dtype=torch.int32, device="cuda")
+    w_b = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    kda.stream_status_bind(w_a, s_a)
+    kda.stream_status_bind(w_b, s_b)
+    try:
+        pool = x["S0"].clone()
+        before = pool.clone()
+        slots = torch.tensor([2, 7, -1, 0], dtype=torch.int32, device="cuda")  # 7, -1 are bad
+        o_b = torch.full((194, 2, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+        kda.decode_step(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], pool, slots=slots,
+                        stream=s_a)
+        kda.chunk_fwd(y["q"], y["k"], y["v"], y["z"], y["beta"], y["A"],
+                      cu_seqlens=y["cu_seqlens"], S0=y["S0"], o=o_b, pre=kda.TEST_STALL,
+                      stream=s_b)
+        assert kda.stream_status(s_a) == kda.KDA_ERR_SHAPE
+        assert kda.stream_status(s_b) == kda.KDA_ERR_TIMEOUT
+        assert kda.stream_status(s_a) == 0 and kda.stream_status(s_b) == 0  # read and reset
+        assert torch.isnan(o_b.float()).all()
+        assert torch.equal(pool[1], before[1]) and torch.equal(pool[3], before[3])
+        assert kda.device_status() == 0  # nothing reached the device word
+    finally:
+        kda.stream_status_bind(None, s_a)
+        kda.stream_status_bind(None, s_b)
+    with pytest.raises(kda.KDAError):
+        kda.stream_status(s_a)  # no word is bound any more
+    pool = x["S0"].clone()
+    slots = torch.tensor([2, 7, -1, 0], dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    kda.decode_step(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], pool, slots=slots,
+                    stream=s_a)
+    s_a.synchronize()
+    assert kda.device_status() == kda.KDA_ERR_SHAPE
+    assert int(w_a.item()) == 0
+
+
 @pytest.mark.parametrize("workspace", [True, False])
 def test_malformed_cu_seqlens_and_snap_offsets_are_reported(kda, workspace):
     """A decreasing cu_seqlens, or snap_offsets that do not match the lengths,

@@ -82,10 +82,10 @@ def state_bytes(token_heads, full_chunk_heads, seq_heads, dk, dv, s0=False):
 _CSRC = os.path.join(ROOT, "linear_attention_serving_chunk_gb300", "csrc")
 _TC_FILES = ("kda_tc_common.cuh", "kda_sm100.cuh", "kda_split.cuh", "kda_common.cuh", "kda_pdl.cuh")
 PROFILED_TRAFFIC = {
-    # varlen prefill, 4 sequences (70,412 tokens), H = 32: 35,264 tasks
-    "chunk_prep_kernel": (2.325763e9 + 2.569389e9, 35264, "6cbc58f518fa86b4",
+    # the full varlen prefill step (64 sequences, 1,012,452 tokens, H = 32): 507,168 tasks
+    "chunk_prep_kernel": (33.747327744e9 + 37.643570432e9, 507168, "6cbc58f518fa86b4",
                           ("kda_chunk_prep.cu",) + _TC_FILES),
-    "state_pass_kernel": (2.626630e9 + 2.843281e9, 35264, "2282604758755b95",
+    "state_pass_kernel": (37.787850240e9 + 41.482227200e9, 507168, "2282604758755b95",
                           ("kda_state_pass.cu",) + _TC_FILES),
     # decode, 512 sequences x H = 32: 16,384 (sequence, head) states
     "kda_decode_step": (1.090611e9 + 1.017599e9, 16384, "850844e37b9a8a6f",

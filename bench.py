@@ -590,6 +590,16 @@ def host_fits_all_ranks(nbytes, world, avail=None):
     return reduce_max(1.0 if short else 0.0, world) == 0.0
 
 
+def agreed_capture(ms, err, world):
+    """A graph-replay time agreed on by every rank: (the maximum over ranks,
+    None) when every rank captured its graph (ms not None), else (None, the
+    reason: this rank's own error, or "on another rank").  Collective: every
+    rank calls it exactly once, whether its own capture worked or not."""
+    if reduce_max(1.0 if ms is None else 0.0, world) == 0.0:
+        return reduce_max(ms, world), None
+    return None, (err if ms is None else "on another rank")
+
+
 def run_e2e(args, x, b, stream, world):
     """The same step through the public API with host buffers: every step copies
     its inputs from pinned host memory to the device, runs kda_chunk_fwd
@@ -766,7 +776,7 @@ def run_decode(args, dev, stream, hbm_peak, peak_src, world):
     # the same chained steps captured in one CUDA graph, replayed once untimed
     # and once timed (the first replay uploads the graph).  No collective runs
     # inside the try: whether every rank captured is agreed on after it.
-    graph_ms, graph_err = None, "on another rank"
+    graph_ms, graph_err = None, None
     try:
         side = torch.cuda.Stream(device=dev)  # captures need a stream other than the default
         graph = torch.cuda.CUDAGraph()
@@ -787,8 +797,8 @@ def run_decode(args, dev, stream, hbm_peak, peak_src, world):
         del graph
     except RuntimeError as e:  # capture not possible here: the issued figure only
         graph_err = str(e)
-    if reduce_max(1.0 if graph_ms is None else 0.0, world) == 0.0:
-        graph_ms = reduce_max(graph_ms, world)
+    graph_ms, graph_err = agreed_capture(graph_ms, graph_err, world)
+    if graph_ms is not None:
         graph_line = {"value": n_steps * world / (graph_ms / 1e3), "unit": "steps/s",
                       "ms_per_step": graph_ms / n_steps,
                       "how": f"the {n_steps} steps captured in one CUDA graph, replayed once"}
@@ -969,7 +979,7 @@ def run_tiny(args, dev, stream, world):
     # latency of the three launches, without the host's per-call work
     # (argument checks, tensor-map encoding, the Python binding)
     # (no collective inside the try: whether every rank captured is agreed on after it)
-    graph_ms, graph_err = None, "on another rank"
+    graph_ms, graph_err = None, None
     try:
         side = torch.cuda.Stream(device=dev)  # captures need a stream other than the default
         side.wait_stream(stream)
@@ -993,10 +1003,8 @@ def run_tiny(args, dev, stream, world):
         del g
     except RuntimeError as e:  # capture not possible here: report the host-issued figure only
         graph_err = str(e)
-    if reduce_max(1.0 if graph_ms is None else 0.0, world) == 0.0:
-        graph_us = reduce_max(graph_ms, world) * 1e3 / reps
-    else:
-        graph_us = f"not captured: {graph_err}"
+    graph_ms, graph_err = agreed_capture(graph_ms, graph_err, world)
+    graph_us = graph_ms * 1e3 / reps if graph_ms is not None else f"not captured: {graph_err}"
     if kda.device_status() != 0:
         raise RuntimeError("device status word set during the tiny prefill")
     return {"latency_us": us, "unit": "us per call", "reps": reps,

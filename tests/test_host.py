@@ -115,6 +115,38 @@ def test_end_to_end_line_runs_on_all_ranks_or_none_gloo_world_size_2():
     assert res == [(0, False, True), (1, False, True)]
 
 
+def _capture_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), LOCAL_WORLD_SIZE=str(world))
+    r, w, lr = bench.dist_setup(world)
+    bench.init_pg(w)
+    # rank 1's capture fails in the first round; both capture in the second
+    first = bench.agreed_capture(None if r == 1 else 5.0, "no capture" if r == 1 else None, w)
+    second = bench.agreed_capture(4.0 + r, None, w)
+    q.put((r, first, second))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_graph_capture_is_agreed_on_by_all_ranks_gloo_world_size_2():
+    """A rank whose CUDA-graph capture fails makes every rank report the
+    graph figure as not captured (with the reason: its own, or 'on another
+    rank'), and none waits in a collective the other skipped; when all
+    capture, every rank gets the maximum."""
+    ctx = torch.multiprocessing.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_capture_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    assert res == [(0, (None, "on another rank"), (5.0, None)),
+                   (1, (None, "no capture"), (5.0, None))]
+
+
 def test_max_over_ranks_gloo_world_size_2():
     ctx = torch.multiprocessing.get_context("spawn")
     q = ctx.Queue()

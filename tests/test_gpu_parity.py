@@ -784,6 +784,41 @@ def test_stream_status_words_tell_streams_apart(kda):
     assert int(w_a.item()) == 0
 
 
+def test_stream_status_word_is_kept_by_a_captured_graph(kda):
+    """A call captured into a CUDA graph on a stream with its own status word
+    records into that word at every replay, also after the stream was unbound
+    (the word bound at capture time is part of the graph)."""
+    assert kda.device_status() == 0
+    n, H, d = 4, 2, 64
+    x = kda_inputs.make_prefill(H, d, d, [1] * n, seed=65, device="cuda", S0_std=0.02)
+    pool = x["S0"].clone()
+    slots = torch.tensor([2, 7, -1, 0], dtype=torch.int32, device="cuda")  # 7, -1 are bad
+    o = torch.empty((n, H, d), dtype=torch.bfloat16, device="cuda")
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # one uncaptured call first, on the same stream
+        kda.decode_step(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], pool, slots=slots,
+                        o=o, stream=side)
+    side.synchronize()
+    assert kda.device_status() == kda.KDA_ERR_SHAPE
+    kda.stream_status_bind(word, side)
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            kda.decode_step(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], pool,
+                            slots=slots, o=o, stream=side)
+    finally:
+        kda.stream_status_bind(None, side)
+    torch.cuda.synchronize()
+    assert int(word.item()) == 0  # capturing runs nothing
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(word.item()) == kda.KDA_ERR_SHAPE
+    assert kda.device_status() == 0
+    del g
+
+
 @pytest.mark.parametrize("workspace", [True, False])
 def test_malformed_cu_seqlens_and_snap_offsets_are_reported(kda, workspace):
     """A decreasing cu_seqlens, or snap_offsets that do not match the lengths,
